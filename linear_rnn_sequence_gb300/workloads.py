@@ -1,0 +1,107 @@
+"""Seeded synthetic workloads for kernelized linear attention.
+
+This module only draws random inputs.  It holds none of the method's
+arithmetic, so both the CUDA path's tests and the fp64 oracle can use it
+without sharing any computation.
+
+Recipe (one ``torch.Generator`` per workload): q, then k, then v are drawn
+in that order as iid N(0, 1) float32 tensors of the full ``[B, H, N, d]`` /
+``[B, H, N, dv]`` shape, multiplied by ``scale`` in float32, then cast to the
+workload's input dtype (bf16 by round-to-nearest-even).  The decode workload
+draws its prefill (unscaled) from a generator seeded ``seed`` and its per-step
+q, k, v (scaled by 1/sqrt(d)) from a second generator seeded ``seed + 1``,
+step after step, q then k then v.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    mode: str            # "causal" | "noncausal" | "decode"
+    B: int
+    H: int
+    N: int               # sequence length (decode: prefill length)
+    d: int
+    dv: int
+    dtype: torch.dtype   # input dtype of q, k, v
+    scale: float         # multiplier applied to the N(0,1) draws
+    seed: int = 0
+    eps: float = 1e-6
+    steps: int = 0       # decode steps
+    step_scale: float = 1.0
+
+    @property
+    def BH(self) -> int:
+        return self.B * self.H
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    # fp32 causal, small enough for the oracle in well under a second.
+    "causal_fp32_b1h2n256d32": Workload("causal_fp32_b1h2n256d32", "causal", 1, 2, 256, 32, 32,
+                                        torch.float32, 1.0),
+    # non-causal bf16.
+    "noncausal_bf16_b4h8n4096d64": Workload("noncausal_bf16_b4h8n4096d64", "noncausal", 4, 8,
+                                            4096, 64, 64, torch.bfloat16, 1.0 / math.sqrt(64)),
+    # causal chunkwise, training / prefill shape.
+    "causal_bf16_b8h16n8192d128": Workload("causal_bf16_b8h16n8192d128", "causal", 8, 16, 8192,
+                                           128, 128, torch.bfloat16, 1.0 / math.sqrt(128)),
+    # long-context causal.
+    "causal_bf16_b1h32n131072d64": Workload("causal_bf16_b1h32n131072d64", "causal", 1, 32,
+                                            131072, 64, 64, torch.bfloat16, 1.0 / math.sqrt(64)),
+    # recurrent decode from a 1024-token prefill.
+    "decode_bf16_b256h32d128": Workload("decode_bf16_b256h32d128", "decode", 256, 32, 1024, 128,
+                                        128, torch.bfloat16, 1.0, steps=4096,
+                                        step_scale=1.0 / math.sqrt(128)),
+}
+
+
+def _draw(gen: torch.Generator, shape, scale: float, dtype: torch.dtype, device) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=gen.device)
+    if scale != 1.0:
+        x = x * torch.tensor(scale, dtype=torch.float32, device=x.device)
+    return x.to(dtype).to(device)
+
+
+def make_qkv(w: Workload, device="cpu", gen_device="cpu"):
+    """Draw (q, k, v) for a causal / non-causal workload, or the decode prefill.
+
+    ``gen_device`` picks the generator's device; the same seed on a different
+    generator device gives different (but equally seeded) numbers, so a test
+    must compare against the oracle on the tensors this returns.
+    """
+    g = torch.Generator(device=gen_device)
+    g.manual_seed(w.seed)
+    q = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    k = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    v = _draw(g, (w.B, w.H, w.N, w.dv), w.scale, w.dtype, device)
+    return q, k, v
+
+
+def decode_step_generator(w: Workload, gen_device="cpu") -> torch.Generator:
+    g = torch.Generator(device=gen_device)
+    g.manual_seed(w.seed + 1)
+    return g
+
+
+def next_decode_inputs(w: Workload, g: torch.Generator, device=None):
+    """Draw one decode step's (q, k, v): [B, H, d], [B, H, d], [B, H, dv]."""
+    device = device if device is not None else g.device
+    q = _draw(g, (w.B, w.H, w.d), w.step_scale, w.dtype, device)
+    k = _draw(g, (w.B, w.H, w.d), w.step_scale, w.dtype, device)
+    v = _draw(g, (w.B, w.H, w.dv), w.step_scale, w.dtype, device)
+    return q, k, v
+
+
+def random_qkv(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="cpu"):
+    """Ad-hoc seeded draw with the same recipe (for edge-case tests)."""
+    w = Workload("adhoc", "causal", B, H, N, d, dv, dtype, scale, seed)
+    return make_qkv(w, device=device)

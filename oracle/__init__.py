@@ -1,0 +1,194 @@
+"""fp64 CPU oracle for elu(x)+1 kernelized linear attention.
+
+TEST INFRASTRUCTURE ONLY.  The product path (the CUDA library and its Python
+binding) never imports this package; only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` do.  The C source
+``linattn_oracle.c`` shares nothing with the CUDA sources.
+
+Each function widens its inputs to float64 numpy arrays and calls the plain
+C loops in ``linattn_oracle.c``:
+
+* ``phi(x)``                       -- elu(x) + 1 ("Linear Attention/es",
+  "Mapas de características"; "Linear Transformer", "La función ELU + 1").
+* ``causal_recurrent(q, k, v)``    -- token-by-token recurrent form
+  ("Linear Attention/es", "Forma recurrente e inferencia autorregresiva").
+* ``noncausal(q, k, v)``           -- matrix form with S, z summed over the
+  whole sequence ("Linear Attention/es", "Reformulación con núcleos").
+* ``quadratic(q, k, v, causal)``   -- brute-force pairwise form (first
+  equality of the same equation), O(N^2).
+* ``causal_chunked(q, k, v, C)``   -- blockwise form ("Linear Attention/es",
+  "Entrenamiento: forma paralela").
+* ``decode_step(q, k, v, S, z)``   -- one recurrent step on a stored state.
+
+Shapes: q, k ``[..., N, d]``; v ``[..., N, dv]``; leading dims are flattened
+into independent heads.  States: S ``[..., d, dv]``, z ``[..., d]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "linattn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liblinattn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math) into oracle/_build."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.POINTER(ctypes.c_double)
+    i, dbl = ctypes.c_int, ctypes.c_double
+    lib.oracle_phi.argtypes = [P, P, ctypes.c_long]
+    lib.oracle_phi.restype = None
+    lib.oracle_causal_recurrent.argtypes = [P, P, P, P, i, i, i, i, dbl, P, P, P, P, i]
+    lib.oracle_causal_recurrent.restype = i
+    lib.oracle_noncausal.argtypes = [P, P, P, P, i, i, i, i, dbl, P, P, i]
+    lib.oracle_noncausal.restype = i
+    lib.oracle_quadratic.argtypes = [P, P, P, P, i, i, i, i, dbl, i, i]
+    lib.oracle_quadratic.restype = i
+    lib.oracle_causal_chunked.argtypes = [P, P, P, P, i, i, i, i, dbl, i, P, P, P, P, i]
+    lib.oracle_causal_chunked.restype = i
+    lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, i, i, i, dbl, i]
+    lib.oracle_decode_step.restype = i
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _f64(x) -> np.ndarray:
+    """Widen any array-like (numpy, or a CPU torch tensor via numpy()) to C-contiguous f64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _split(q, k, v):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.shape != k.shape or q.shape[:-1] != v.shape[:-1] or q.ndim < 2:
+        raise ValueError(f"bad shapes q{q.shape} k{k.shape} v{v.shape}")
+    lead = q.shape[:-2]
+    N, d, dv = q.shape[-2], q.shape[-1], v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    return q, k, v, lead, BH, N, d, dv
+
+
+def phi(x) -> np.ndarray:
+    x = _f64(x)
+    out = np.empty_like(x)
+    _load().oracle_phi(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def causal_recurrent(q, k, v, eps: float = 1e-6, S_in=None, z_in=None,
+                     return_state: bool = False, nthreads: int | None = None):
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    y = np.empty(lead + (N, dv))
+    S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
+    z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
+    S = np.empty(lead + (d, dv)) if return_state else None
+    z = np.empty(lead + (d,)) if return_state else None
+    rc = _load().oracle_causal_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                         float(eps), _ptr(S_in), _ptr(z_in), _ptr(S), _ptr(z),
+                                         nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_causal_recurrent failed")
+    return (y, S, z) if return_state else y
+
+
+def noncausal(q, k, v, eps: float = 1e-6, return_state: bool = False,
+              nthreads: int | None = None):
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    y = np.empty(lead + (N, dv))
+    S = np.empty(lead + (d, dv)) if return_state else None
+    z = np.empty(lead + (d,)) if return_state else None
+    rc = _load().oracle_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv, float(eps),
+                                  _ptr(S), _ptr(z), nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_noncausal failed")
+    return (y, S, z) if return_state else y
+
+
+def quadratic(q, k, v, causal: bool = True, eps: float = 1e-6, nthreads: int | None = None):
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    y = np.empty(lead + (N, dv))
+    rc = _load().oracle_quadratic(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv, float(eps),
+                                  1 if causal else 0, nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_quadratic failed")
+    return y
+
+
+def causal_chunked(q, k, v, chunk: int, eps: float = 1e-6, S_in=None, z_in=None,
+                   return_state: bool = False, nthreads: int | None = None):
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    y = np.empty(lead + (N, dv))
+    S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
+    z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
+    S = np.empty(lead + (d, dv)) if return_state else None
+    z = np.empty(lead + (d,)) if return_state else None
+    rc = _load().oracle_causal_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                       float(eps), int(chunk), _ptr(S_in), _ptr(z_in), _ptr(S),
+                                       _ptr(z), nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_causal_chunked failed")
+    return (y, S, z) if return_state else y
+
+
+def decode_step(q, k, v, S, z, eps: float = 1e-6, nthreads: int | None = None):
+    """One decode step.  q, k: [..., d]; v: [..., dv]; S: [..., d, dv]; z: [..., d].
+
+    Returns (y, S_new, z_new); the inputs are not modified.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    S = _f64(S).copy()
+    z = _f64(z).copy()
+    lead = q.shape[:-1]
+    d, dv = q.shape[-1], v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    if S.shape != lead + (d, dv) or z.shape != lead + (d,):
+        raise ValueError("state shape mismatch")
+    y = np.empty(lead + (dv,))
+    rc = _load().oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z),
+                                    BH, d, dv, float(eps), nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_decode_step failed")
+    return y, S, z

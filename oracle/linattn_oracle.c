@@ -1,0 +1,317 @@
+/*
+ * linattn_oracle.c -- fp64 CPU oracle for elu(x)+1 kernelized linear attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * Every routine is the plain definition from the pages, written out in
+ * double precision with straightforward loops (no blocking, no fusion, no
+ * reordering beyond what the definition states).  Citations name the page
+ * and the section / equation each step follows:
+ *
+ *   [P1] "Linear Attention/es" (marovi.ai)
+ *        - "Reformulación con núcleos", eq. y_i = phi(q_i)^T S / phi(q_i)^T z
+ *          with S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j).
+ *        - "Mapas de características", phi(x) = elu(x) + 1.
+ *        - "Forma recurrente e inferencia autorregresiva", S_t = S_{t-1} +
+ *          phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t), y_t = phi(q_t)^T S_t /
+ *          phi(q_t)^T z_t.
+ *        - "Entrenamiento: forma paralela", blockwise form: masked
+ *          intra-block pairs plus an inter-block linear state update.
+ *   [P2] "Linear Transformer (Transformers are RNNs)" (visibilidadia.com)
+ *        - "La función ELU + 1": ELU(x) = x for x > 0, e^x - 1 for x <= 0.
+ *        - "La formulación recurrente paso a paso": S_t, z_t, o_t.
+ *        - The worked PyTorch examples divide by the denominator clamped
+ *          from below by eps (clamp_min), which is what max(den, eps) is.
+ *
+ * Layouts (all row-major, contiguous, fp64):
+ *   q, k : [BH][N][d]      v, y : [BH][N][dv]
+ *   S    : [BH][d][dv]     z    : [BH][d]
+ * BH is batch*heads; heads are independent and are split across threads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* [P1] "Mapas de características": phi(x) = elu(x) + 1, with
+ * [P2] "La función ELU + 1": ELU(x) = x (x > 0), e^x - 1 (x <= 0).  The same
+ * section simplifies the sum to phi(x) = x + 1 (x > 0), e^x (x <= 0); that
+ * form is used because it is exact in double precision and keeps phi > 0
+ * (the section stresses positivity), whereas (e^x - 1) + 1 rounds e^x away
+ * once e^x < 2^-53.                                                         */
+static double phi(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
+
+/* Denominator clamp used by the pages' examples: max(den, eps). */
+static double clamp_den(double den, double eps) { return den < eps ? eps : den; }
+
+void oracle_phi(const double *x, double *out, long n)
+{
+    for (long i = 0; i < n; ++i) out[i] = phi(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Per-head work items and a tiny pthread pool over heads.                  */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int kind;              /* 0 recurrent causal, 1 non-causal, 2 quadratic, 3 chunked */
+    const double *q, *k, *v;
+    double *y;
+    const double *S_in, *z_in; /* nullable: zero state */
+    double *S_out, *z_out;     /* nullable */
+    int BH, N, d, dv, causal, chunk;
+    double eps;
+    int h_begin, h_end;
+} job_t;
+
+/* [P1] "Forma recurrente ..." / [P2] "La formulación recurrente paso a paso":
+ * for t = 1..N: S += phi(k_t) v_t^T, z += phi(k_t) (update first), then
+ * y_t = phi(q_t)^T S / max(phi(q_t)^T z, eps).                            */
+static void head_recurrent(const job_t *J, int h)
+{
+    const int N = J->N, d = J->d, dv = J->dv;
+    const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
+    const double *v = J->v + (long)h * N * dv;
+    double *y = J->y + (long)h * N * dv;
+    double *S = calloc((size_t)d * dv, sizeof(double));
+    double *z = calloc((size_t)d, sizeof(double));
+    double *fk = malloc(sizeof(double) * d), *fq = malloc(sizeof(double) * d);
+    if (J->S_in) memcpy(S, J->S_in + (long)h * d * dv, sizeof(double) * d * dv);
+    if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
+    for (int t = 0; t < N; ++t) {
+        for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) {
+            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];
+            z[a] += fk[a];
+        }
+        for (int a = 0; a < d; ++a) fq[a] = phi(q[(long)t * d + a]);
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += fq[a] * z[a];
+        den = clamp_den(den, J->eps);
+        for (int b = 0; b < dv; ++b) {
+            double num = 0.0;
+            for (int a = 0; a < d; ++a) num += fq[a] * S[(long)a * dv + b];
+            y[(long)t * dv + b] = num / den;
+        }
+    }
+    if (J->S_out) memcpy(J->S_out + (long)h * d * dv, S, sizeof(double) * d * dv);
+    if (J->z_out) memcpy(J->z_out + (long)h * d, z, sizeof(double) * d);
+    free(S); free(z); free(fk); free(fq);
+}
+
+/* [P1] "Reformulación con núcleos": S = sum_j phi(k_j) v_j^T and
+ * z = sum_j phi(k_j) over the whole sequence, then for every query
+ * y_i = phi(q_i)^T S / max(phi(q_i)^T z, eps).                             */
+static void head_noncausal(const job_t *J, int h)
+{
+    const int N = J->N, d = J->d, dv = J->dv;
+    const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
+    const double *v = J->v + (long)h * N * dv;
+    double *y = J->y + (long)h * N * dv;
+    double *S = calloc((size_t)d * dv, sizeof(double));
+    double *z = calloc((size_t)d, sizeof(double));
+    double *f = malloc(sizeof(double) * d);
+    for (int j = 0; j < N; ++j) {
+        for (int a = 0; a < d; ++a) f[a] = phi(k[(long)j * d + a]);
+        for (int a = 0; a < d; ++a) {
+            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += f[a] * v[(long)j * dv + b];
+            z[a] += f[a];
+        }
+    }
+    for (int i = 0; i < N; ++i) {
+        for (int a = 0; a < d; ++a) f[a] = phi(q[(long)i * d + a]);
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += f[a] * z[a];
+        den = clamp_den(den, J->eps);
+        for (int b = 0; b < dv; ++b) {
+            double num = 0.0;
+            for (int a = 0; a < d; ++a) num += f[a] * S[(long)a * dv + b];
+            y[(long)i * dv + b] = num / den;
+        }
+    }
+    if (J->S_out) memcpy(J->S_out + (long)h * d * dv, S, sizeof(double) * d * dv);
+    if (J->z_out) memcpy(J->z_out + (long)h * d, z, sizeof(double) * d);
+    free(S); free(z); free(f);
+}
+
+/* [P1] "Reformulación con núcleos", first equality, evaluated pair by pair:
+ * y_i = sum_j w_ij v_j / max(sum_j w_ij, eps), w_ij = phi(q_i)^T phi(k_j),
+ * over j <= i (causal) or all j.  O(N^2 d): brute force for small cases.   */
+static void head_quadratic(const job_t *J, int h)
+{
+    const int N = J->N, d = J->d, dv = J->dv;
+    const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
+    const double *v = J->v + (long)h * N * dv;
+    double *y = J->y + (long)h * N * dv;
+    double *num = malloc(sizeof(double) * dv);
+    for (int i = 0; i < N; ++i) {
+        const int jmax = J->causal ? i : N - 1;
+        double den = 0.0;
+        for (int b = 0; b < dv; ++b) num[b] = 0.0;
+        for (int j = 0; j <= jmax; ++j) {
+            double w = 0.0;
+            for (int a = 0; a < d; ++a) w += phi(q[(long)i * d + a]) * phi(k[(long)j * d + a]);
+            den += w;
+            for (int b = 0; b < dv; ++b) num[b] += w * v[(long)j * dv + b];
+        }
+        den = clamp_den(den, J->eps);
+        for (int b = 0; b < dv; ++b) y[(long)i * dv + b] = num[b] / den;
+    }
+    free(num);
+}
+
+/* [P1] "Entrenamiento: forma paralela": split the sequence into blocks of C
+ * tokens.  Inside block c the output combines the masked pairwise term over
+ * the block (j <= i, both in c) with the linear term phi(q_i)^T S_prev over
+ * all earlier blocks; after the block, S_prev += sum_{j in c} phi(k_j) v_j^T
+ * and z_prev += sum_{j in c} phi(k_j).                                      */
+static void head_chunked(const job_t *J, int h)
+{
+    const int N = J->N, d = J->d, dv = J->dv, C = J->chunk;
+    const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
+    const double *v = J->v + (long)h * N * dv;
+    double *y = J->y + (long)h * N * dv;
+    double *S = calloc((size_t)d * dv, sizeof(double));
+    double *z = calloc((size_t)d, sizeof(double));
+    double *fq = malloc(sizeof(double) * (size_t)C * d);
+    double *fk = malloc(sizeof(double) * (size_t)C * d);
+    double *num = malloc(sizeof(double) * dv);
+    if (J->S_in) memcpy(S, J->S_in + (long)h * d * dv, sizeof(double) * d * dv);
+    if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
+    for (int c0 = 0; c0 < N; c0 += C) {
+        const int L = (N - c0) < C ? (N - c0) : C;
+        for (int i = 0; i < L; ++i)
+            for (int a = 0; a < d; ++a) {
+                fq[(long)i * d + a] = phi(q[(long)(c0 + i) * d + a]);
+                fk[(long)i * d + a] = phi(k[(long)(c0 + i) * d + a]);
+            }
+        for (int i = 0; i < L; ++i) {
+            /* inter-block: phi(q_i)^T S_prev and phi(q_i)^T z_prev */
+            double den = 0.0;
+            for (int a = 0; a < d; ++a) den += fq[(long)i * d + a] * z[a];
+            for (int b = 0; b < dv; ++b) {
+                double s = 0.0;
+                for (int a = 0; a < d; ++a) s += fq[(long)i * d + a] * S[(long)a * dv + b];
+                num[b] = s;
+            }
+            /* intra-block: masked pairs j <= i inside the block */
+            for (int j = 0; j <= i; ++j) {
+                double w = 0.0;
+                for (int a = 0; a < d; ++a) w += fq[(long)i * d + a] * fk[(long)j * d + a];
+                den += w;
+                for (int b = 0; b < dv; ++b) num[b] += w * v[(long)(c0 + j) * dv + b];
+            }
+            den = clamp_den(den, J->eps);
+            for (int b = 0; b < dv; ++b) y[(long)(c0 + i) * dv + b] = num[b] / den;
+        }
+        /* state update after the block */
+        for (int j = 0; j < L; ++j)
+            for (int a = 0; a < d; ++a) {
+                for (int b = 0; b < dv; ++b)
+                    S[(long)a * dv + b] += fk[(long)j * d + a] * v[(long)(c0 + j) * dv + b];
+                z[a] += fk[(long)j * d + a];
+            }
+    }
+    if (J->S_out) memcpy(J->S_out + (long)h * d * dv, S, sizeof(double) * d * dv);
+    if (J->z_out) memcpy(J->z_out + (long)h * d, z, sizeof(double) * d);
+    free(S); free(z); free(fq); free(fk); free(num);
+}
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    for (int h = J->h_begin; h < J->h_end; ++h) {
+        switch (J->kind) {
+        case 0: head_recurrent(J, h); break;
+        case 1: head_noncausal(J, h); break;
+        case 2: head_quadratic(J, h); break;
+        default: head_chunked(J, h); break;
+        }
+    }
+    return NULL;
+}
+
+static int run_jobs(job_t base, int nthreads)
+{
+    if (base.BH < 0 || base.N < 0 || base.d <= 0 || base.dv <= 0) return 1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > base.BH) nthreads = base.BH > 0 ? base.BH : 1;
+    job_t *jobs = malloc(sizeof(job_t) * nthreads);
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].h_begin = (int)((long)base.BH * t / nthreads);
+        jobs[t].h_end = (int)((long)base.BH * (t + 1) / nthreads);
+    }
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, worker, &jobs[t]) == 0) ++started;
+        else worker(&jobs[t]); /* fall back to running it on this thread */
+    worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    free(jobs); free(th);
+    return 0;
+}
+
+/* Causal, recurrent (token by token).  S_in/z_in may be NULL (zero state);
+ * S_out/z_out may be NULL.  Returns 0 on success.                          */
+int oracle_causal_recurrent(const double *q, const double *k, const double *v, double *y,
+                            int BH, int N, int d, int dv, double eps,
+                            const double *S_in, const double *z_in,
+                            double *S_out, double *z_out, int nthreads)
+{
+    job_t J = {0};
+    J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S_in; J.z_in = z_in;
+    J.S_out = S_out; J.z_out = z_out; J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    return run_jobs(J, nthreads);
+}
+
+/* Non-causal matrix form.  S_out/z_out (the full-sequence sums) may be NULL. */
+int oracle_noncausal(const double *q, const double *k, const double *v, double *y,
+                     int BH, int N, int d, int dv, double eps,
+                     double *S_out, double *z_out, int nthreads)
+{
+    job_t J = {0};
+    J.kind = 1; J.q = q; J.k = k; J.v = v; J.y = y; J.S_out = S_out; J.z_out = z_out;
+    J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    return run_jobs(J, nthreads);
+}
+
+/* Brute-force pairwise form; causal != 0 restricts to j <= i. */
+int oracle_quadratic(const double *q, const double *k, const double *v, double *y,
+                     int BH, int N, int d, int dv, double eps, int causal, int nthreads)
+{
+    job_t J = {0};
+    J.kind = 2; J.q = q; J.k = k; J.v = v; J.y = y; J.BH = BH; J.N = N; J.d = d; J.dv = dv;
+    J.eps = eps; J.causal = causal;
+    return run_jobs(J, nthreads);
+}
+
+/* Blockwise causal form with block length `chunk` (>= 1). */
+int oracle_causal_chunked(const double *q, const double *k, const double *v, double *y,
+                          int BH, int N, int d, int dv, double eps, int chunk,
+                          const double *S_in, const double *z_in,
+                          double *S_out, double *z_out, int nthreads)
+{
+    if (chunk < 1) return 1;
+    job_t J = {0};
+    J.kind = 3; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S_in; J.z_in = z_in;
+    J.S_out = S_out; J.z_out = z_out; J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    J.chunk = chunk;
+    return run_jobs(J, nthreads);
+}
+
+/* One recurrent decode step per head on a stored state (in place):
+ * S += phi(k) v^T, z += phi(k), then y = phi(q)^T S / max(phi(q)^T z, eps).
+ * q, k: [BH][d]; v, y: [BH][dv]; S: [BH][d][dv]; z: [BH][d].               */
+int oracle_decode_step(const double *q, const double *k, const double *v, double *y,
+                       double *S, double *z, int BH, int d, int dv, double eps, int nthreads)
+{
+    /* A decode step is the recurrent form with N = 1 continuing from (S, z). */
+    job_t J = {0};
+    J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S; J.z_in = z;
+    J.S_out = S; J.z_out = z; J.BH = BH; J.N = 1; J.d = d; J.dv = dv; J.eps = eps;
+    return run_jobs(J, nthreads);
+}

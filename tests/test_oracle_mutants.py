@@ -1,0 +1,102 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check a pin catches each.
+
+Each mutant is a textual edit of a copy of ``oracle/linattn_oracle.c``,
+compiled to a temporary library and swapped in for the real one.  The pins
+run here are the hand-derived golden cases, the numpy brute force and the
+chunked-vs-recurrent agreement from ``test_oracle.py``.
+"""
+import ctypes
+import json
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(__file__)
+SRC = os.path.join(os.path.dirname(HERE), "oracle", "linattn_oracle.c")
+
+MUTANTS = {
+    "phi_drops_plus_one": ("x > 0.0 ? x + 1.0 : exp(x)", "x > 0.0 ? x : exp(x)"),
+    "phi_exp_branch_minus_one": ("x > 0.0 ? x + 1.0 : exp(x)", "x > 0.0 ? x + 1.0 : exp(x) - 1.0"),
+    "eps_added_not_clamped": ("return den < eps ? eps : den;", "return den + eps;"),
+    "recurrent_wrong_v_index": ("S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];",
+                                "S[(long)a * dv + b] += fk[a] * v[(long)t * dv + 0];"),
+    "recurrent_z_counts_tokens": ("            z[a] += fk[a];\n        }\n        for (int a = 0; a < d; ++a) fq[a]",
+                                  "            z[a] += 1.0;\n        }\n        for (int a = 0; a < d; ++a) fq[a]"),
+    "chunked_strict_mask": ("for (int j = 0; j <= i; ++j) {", "for (int j = 0; j < i; ++j) {"),
+    "quadratic_exclusive": ("const int jmax = J->causal ? i : N - 1;", "const int jmax = J->causal ? i - 1 : N - 1;"),
+    "noncausal_transposed_state": ("for (int a = 0; a < d; ++a) num += f[a] * S[(long)a * dv + b];",
+                                   "for (int a = 0; a < d; ++a) num += f[a] * S[(long)b * dv + a];"),
+}
+
+
+def _phi_np(x):
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def _brute(q, k, v, causal):
+    fq, fk = _phi_np(q), _phi_np(k)
+    N = q.shape[0]
+    y = np.zeros((N, v.shape[1]))
+    for i in range(N):
+        j = i + 1 if causal else N
+        w = fk[:j] @ fq[i]
+        y[i] = (w @ v[:j]) / max(w.sum(), 1e-6)
+    return y
+
+
+def _pins_pass() -> bool:
+    """True if every pin passes with the currently loaded oracle."""
+    with open(os.path.join(HERE, "golden", "hand_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q, k, v = (np.array(c[x], dtype=np.float64) for x in ("q", "k", "v"))
+        want = np.array(c["y"])
+        if c["mode"] == "causal":
+            outs = [oracle.causal_recurrent(q, k, v, eps=c["eps"]),
+                    oracle.quadratic(q, k, v, True, eps=c["eps"]),
+                    oracle.causal_chunked(q, k, v, 2, eps=c["eps"])]
+        else:
+            outs = [oracle.noncausal(q, k, v, eps=c["eps"]),
+                    oracle.quadratic(q, k, v, False, eps=c["eps"])]
+        for y in outs:
+            if not np.allclose(y, want, rtol=1e-12, atol=1e-300):
+                return False
+    r = np.random.default_rng(5)
+    q, k, v = (r.standard_normal((40, n)) for n in (4, 4, 3))
+    if not np.allclose(oracle.causal_recurrent(q, k, v), _brute(q, k, v, True), rtol=1e-11):
+        return False
+    if not np.allclose(oracle.noncausal(q, k, v), _brute(q, k, v, False), rtol=1e-11):
+        return False
+    if not np.allclose(oracle.quadratic(q, k, v, True), _brute(q, k, v, True), rtol=1e-11):
+        return False
+    if not np.allclose(oracle.causal_chunked(q, k, v, 7), oracle.causal_recurrent(q, k, v),
+                       rtol=1e-11):
+        return False
+    return True
+
+
+def test_unmutated_oracle_passes_pins():
+    assert _pins_pass()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c = tmp_path / "mut.c"
+    so = tmp_path / "libmut.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", str(c), "-o",
+                    str(so), "-lm"], check=True)
+    saved = oracle._lib
+    oracle._lib = oracle._bind(ctypes.CDLL(str(so)))
+    try:
+        assert not _pins_pass(), f"mutant {name} survived every pin"
+    finally:
+        oracle._lib = saved

@@ -1,0 +1,481 @@
+"""Benchmark: elu+1 kernelized linear attention on GB300.
+
+Headline step: one causal chunkwise forward (la_forward_causal) over the
+B=8, H=16, N=8192, d=dv=128 bf16 workload (tokens = B*N positions, all heads).
+Each extra mode (non-causal B4 H8 N4096 d64, long causal B1 H32 N131072 d64,
+recurrent decode B256 H32 d128) is timed the same way and reported under
+"modes" with its own roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (weak
+scaling, no data-path collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_rnn_sequence_gb300.workloads import WORKLOADS, Workload, make_qkv  # noqa: E402
+
+METRIC = "causal linear-attn tokens/s & TFLOP/s on 1 GB300, % roofline; decode tokens/s"
+HEADLINE = "causal_bf16_b8h16n8192d128"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic counts (per token-head; decode: per head-step)
+# ----------------------------------------------------------------------------
+def esize(dt):
+    return 2 if dt == torch.bfloat16 else 4
+
+
+def alg_flops_per_token_head(d, dv):
+    # state update 2*d*dv, query 2*d*dv, z update d, phi(q).z 2d, divide dv
+    return 4 * d * dv + 3 * d + dv
+
+
+def alg_bytes_per_token_head(w: Workload):
+    return (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4  # q, k, v read; y (fp32) written
+
+
+def decode_bytes_per_head_step(w: Workload):
+    return 2 * (w.d * w.dv + w.d) * 4 + (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing
+# ----------------------------------------------------------------------------
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = str(local_rank)
+        if vis:
+            parts = [p.strip() for p in vis.split(",")]
+            if local_rank < len(parts) and parts[local_rank].isdigit():
+                idx = parts[local_rank]
+        self.idx = idx
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.idx, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# timing helpers
+# ----------------------------------------------------------------------------
+def flush_l2(buf):
+    buf.zero_()
+
+
+def time_steps(fn, steps, warmup, world, flush=None):
+    """Run `warmup` untimed steps, then exactly `steps` timed steps.
+
+    Returns (total_ms (max over ranks), per-step kernel ms list from events on
+    the launching stream).  If `flush` is given it runs between timed steps,
+    outside the per-step event pairs.
+    """
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    per = [a.elapsed_time(b) for a, b in ev]
+    total = sum(per) if flush is not None else t_start.elapsed_time(t_end)
+    return max_over_ranks(total, world), per
+
+
+def roofline(bytes_per_launch, flops_per_launch, launch_ms, peaks, peak_kind, traffic=None):
+    t = launch_ms * 1e-3
+    gbs = bytes_per_launch / t / 1e9
+    tflops = flops_per_launch / t / 1e12
+    t_bytes = bytes_per_launch / (peaks["hbm_gbs"] * 1e9)
+    t_flops = flops_per_launch / (peaks["bf16_tflops"] * 1e12)
+    if t_bytes >= t_flops:
+        r = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": gbs / peaks["hbm_gbs"]}
+    else:
+        r = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
+    r["traffic"] = traffic
+    r["peak_source"] = peak_kind
+    r["roof_fraction"] = max(t_bytes, t_flops) / t  # slower of the two roofs / measured time
+    return r
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle as it stands, on a bounded sample
+# ----------------------------------------------------------------------------
+def cpu_baseline(w: Workload, budget_s=12.0):
+    import oracle
+    cores = oracle.default_threads()
+    sample = w.with_(B=1)
+    q, k, v = make_qkv(sample)
+    done_tokens, t0 = 0, time.perf_counter()
+    reps = 0
+    while True:
+        oracle.causal_recurrent(q, k, v, eps=w.eps, nthreads=cores)
+        reps += 1
+        done_tokens += sample.N  # one batch row: N positions with all H heads
+        if time.perf_counter() - t0 >= budget_s or reps >= 8:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done_tokens / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x (B=1, H={w.H}, N={w.N}, d={w.d}, dv={w.dv}) recurrent fp64, "
+                      f"{el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from linear_rnn_sequence_gb300 import linattn as la
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+    w = WORKLOADS[HEADLINE]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    need = la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype)
+    ws = la.alloc_workspace(need, dev)
+
+    def step():
+        la.forward_causal(q, k, v, eps=w.eps, out=y, workspace=ws)
+
+    with ClockSampler(local) as clk:
+        total_ms, per = time_steps(step, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    T = w.B * w.H * w.N
+    tokens = w.B * w.N
+    ms_per_step = total_ms / args.steps
+    value = world * tokens / (ms_per_step * 1e-3)
+    launch_ms = sum(per) / len(per)
+    bytes_launch = T * alg_bytes_per_token_head(w)
+    flops_launch = T * alg_flops_per_token_head(w.d, w.dv)
+    traffic = load_traffic(HEADLINE)
+    roof = roofline(bytes_launch, flops_launch, launch_ms, peaks, peak_kind, traffic)
+    status = la.workspace_status(ws)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": path_dtype(w), "data": "synthetic (seeded iid N(0,1)/sqrt(d), bf16)",
+        "config": {"workload": HEADLINE, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dv": w.dv,
+                   "input_dtype": "bf16", "output_dtype": "f32", "eps": w.eps,
+                   "l2": "inputs larger than L2 (1.07 GB of q,k,v per step)",
+                   "parallelism": f"replica x{world}"},
+        "tflops": world * flops_launch / (ms_per_step * 1e-3) / 1e12,
+        "roofline": roof,
+        "gpu_launches": args.steps * launches_per_call("causal", w),
+        "clocks": clocks,
+        "run_status": la.status_string(status),
+    }
+    del q, k, v, y
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        out["e2e"] = e2e_causal(w, dev, world, args)
+    if not args.no_modes:
+        out["modes"] = run_modes(args, world, dev, peaks, peak_kind)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w)
+    return out
+
+
+def path_dtype(w):
+    from linear_rnn_sequence_gb300 import linattn as la
+    tc = la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 0
+    return "bf16" if (tc and w.dtype == torch.bfloat16) else "f32"
+
+
+def launches_per_call(mode, w):
+    """Kernels of ours that one call launches (the launch list under ncu agrees)."""
+    from linear_rnn_sequence_gb300 import linattn as la
+    if mode == "causal":
+        return 1
+    if mode == "noncausal":
+        return 2
+    return 1
+
+
+def load_traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if one matches the current kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f).get(name)
+    except Exception:
+        return None
+
+
+def e2e_causal(w, dev, world, args):
+    """Same metric through the public API with pinned host buffers: H2D of q,k,v,
+    la_forward_causal, D2H of y, all inside the timed region."""
+    from linear_rnn_sequence_gb300 import linattn as la
+    qh, kh, vh = (t.pin_memory() for t in make_qkv(w.with_(B=1), device="cpu"))
+    # one batch row per transfer keeps pinned memory modest; replicate to B rows
+    qh = qh.expand(w.B, -1, -1, -1).contiguous().pin_memory()
+    kh = kh.expand(w.B, -1, -1, -1).contiguous().pin_memory()
+    vh = vh.expand(w.B, -1, -1, -1).contiguous().pin_memory()
+    yh = torch.empty(w.B, w.H, w.N, w.dv, dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+    yd = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    need = la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype)
+    ws = la.alloc_workspace(need, dev)
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        la.forward_causal(qd, kd, vd, eps=w.eps, out=yd, workspace=ws)
+        yh.copy_(yd, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    total_ms, _ = time_steps(step, steps, 2, world)
+    ms = total_ms / steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = yh.numel() * yh.element_size()
+    return {"value": world * w.B * w.N / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_modes(args, world, dev, peaks, peak_kind):
+    from linear_rnn_sequence_gb300 import linattn as la
+    modes = {}
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    steps = max(3, min(args.steps, 20))
+
+    # non-causal: inputs fit in L2, so flush L2 between timed launches
+    w = WORKLOADS["noncausal_bf16_b4h8n4096d64"]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    ws = la.alloc_workspace(la.noncausal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv), dev)
+    total, per = time_steps(lambda: la.forward_noncausal(q, k, v, out=y, workspace=ws), steps,
+                            args.warmup, world, flush=lambda: flush_l2(flush_buf))
+    T = w.BH * w.N
+    ms = sum(per) / len(per)
+    modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+                     "l2": "flushed between launches (256 MB write)",
+                     "roofline": roofline(T * alg_bytes_per_token_head(w),
+                                          T * alg_flops_per_token_head(w.d, w.dv), ms, peaks,
+                                          peak_kind, load_traffic(w.name))}
+    del q, k, v, y, ws
+
+    # long causal
+    w = WORKLOADS["causal_bf16_b1h32n131072d64"]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    ws = la.alloc_workspace(la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+    total, per = time_steps(lambda: la.forward_causal(q, k, v, out=y, workspace=ws), steps,
+                            args.warmup, world)
+    T = w.BH * w.N
+    ms = sum(per) / len(per)
+    modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+                     "l2": "inputs larger than L2",
+                     "roofline": roofline(T * alg_bytes_per_token_head(w),
+                                          T * alg_flops_per_token_head(w.d, w.dv), ms, peaks,
+                                          peak_kind, load_traffic(w.name))}
+    del q, k, v, y, ws
+    torch.cuda.empty_cache()
+
+    # decode: state from a 1024-token prefill, then timed steps (state > L2)
+    w = WORKLOADS["decode_bf16_b256h32d128"]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    _, S, z = la.forward_causal(q, k, v, return_state=True)
+    del q, k, v
+    torch.cuda.empty_cache()
+    nsteps = 256
+    g = torch.Generator(device=dev).manual_seed(w.seed + 1)
+    sc = torch.tensor(w.step_scale, device=dev)
+    qs = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    ks = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    vs = (torch.randn(nsteps, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
+    yd = torch.empty(w.B, w.H, w.dv, device=dev)
+    it = [0]
+
+    def dstep():
+        i = it[0] % nsteps
+        it[0] += 1
+        la.decode_step(qs[i], ks[i], vs[i], S, z, eps=w.eps, out=yd)
+
+    total, per = time_steps(dstep, nsteps, args.warmup, world)
+    ms = total / nsteps
+    heads = w.BH
+    modes[w.name] = {"tokens_per_s": world * w.B / (ms * 1e-3), "ms_per_step": ms,
+                     "steps_timed": nsteps, "l2": "state (512 MB) larger than L2",
+                     "roofline": roofline(heads * decode_bytes_per_head_step(w),
+                                          heads * alg_flops_per_token_head(w.d, w.dv),
+                                          sum(per) / len(per), peaks, peak_kind,
+                                          load_traffic(w.name))}
+    return modes
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle, as it stands, on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    w = WORKLOADS[HEADLINE]
+    cores = oracle.default_threads()
+    sample = w.with_(B=1, N=1024)   # one batch row, first 1024 positions, all heads
+    q, k, v = make_qkv(sample)
+    for _ in range(args.warmup):
+        oracle.causal_recurrent(q[:, :, :64], k[:, :, :64], v[:, :, :64], nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.causal_recurrent(q, k, v, eps=w.eps, nthreads=cores)
+    el = time.perf_counter() - t0
+    value = args.steps * sample.N / el
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: B=1, H={w.H}, N={sample.N}, d={w.d} "
+                                       f"recurrent fp64"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-modes", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * linattn.h -- C ABI of liblinattn.so: elu(x)+1 kernelized linear attention
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The method ("Linear Attention/es", section "Reformulación con núcleos"):
+ *
+ *     y_i = phi(q_i)^T S / max(phi(q_i)^T z, eps),
+ *     S   = sum_j phi(k_j) v_j^T  (d x dv),   z = sum_j phi(k_j)  (d),
+ *     phi(x) = elu(x) + 1 = x + 1 (x > 0), e^x (x <= 0)
+ *
+ * ("Mapas de características"; "Linear Transformer (Transformers are RNNs)",
+ * section "La función ELU + 1").  The sums run over all j (non-causal) or over
+ * j <= i (causal: "Forma recurrente e inferencia autorregresiva", where the
+ * state is updated with token i before it is read).  The denominator is
+ * clamped from below by eps, as the worked PyTorch examples on the "Linear
+ * Transformer" page do with clamp_min.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Pointers   All tensor pointers are DEVICE pointers (cudaMalloc'd or
+ *             equivalent) owned by the caller.  The library allocates no
+ *             device memory and keeps no state between calls except a small
+ *             host-side cache of TMA tensor maps (none outlives the process).
+ *  Layout     Contiguous row-major:
+ *               q, k : [B][H][N][d]   (decode: [B][H][d])   dtype `dt`
+ *               v    : [B][H][N][dv]  (decode: [B][H][dv])  dtype `dt`
+ *               y    : [B][H][N][dv]  (decode: [B][H][dv])  float32
+ *               S    : [B][H][d][dv]  float32,  z : [B][H][d] float32
+ *             q, k, v and y must be 16-byte aligned; S and z 16-byte aligned.
+ *  Output     y is float32 for both input dtypes.  (A bfloat16 output could
+ *             not meet the stated accuracy: rounding y alone to bf16 moves the
+ *             largest early-token outputs by up to 2^-9 of their size, far more
+ *             than 2e-2 of the RMS of y for long causal sequences.)
+ *  Sizes      B, H >= 1; N >= 0 (N = 0 is a no-op that still writes the
+ *             final state when asked); d, dv in {32, 64, 128}.  Other d / dv
+ *             return LA_ERR_UNSUPPORTED.  B*H*N*max(d,dv) must fit in 2^31.
+ *  eps        must be finite and > 0, else LA_ERR_INVALID_ARG.
+ *  Streams    `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ *             work is enqueued asynchronously; the call returns after the
+ *             launches.  Launch failures return LA_ERR_CUDA.
+ *  Aliasing   y must not alias q, k, v, S or z.  S_in may equal S_out and
+ *             z_in may equal z_out (read fully before written per head).
+ *  Errors     Argument checks happen on the host before anything is
+ *             launched; on any error nothing is enqueued.  The only error a
+ *             kernel can raise at run time is a bounded wait that ran out
+ *             (LA_ERR_TIMEOUT), recorded in the workspace and reported by
+ *             la_workspace_status().
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, bad eps */
+    LA_ERR_UNSUPPORTED = 2,   /* d or dv outside {32, 64, 128}, unknown dtype  */
+    LA_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed           */
+    LA_ERR_TIMEOUT = 4,       /* a bounded inter-CTA wait ran out (see above)  */
+    LA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required    */
+} la_status;
+
+typedef enum {
+    LA_DTYPE_F32 = 0,         /* float32 q, k, v                               */
+    LA_DTYPE_BF16 = 1         /* bfloat16 q, k, v                              */
+} la_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+LA_API const char *la_status_string(la_status s);
+
+/* Library version string, e.g. "linattn 0.1 sm_103a". */
+LA_API const char *la_version(void);
+
+/*
+ * Workspace size in bytes for la_forward_causal with these sizes (0 when the
+ * chosen kernels need none).  The workspace holds the per-segment states of
+ * the sequence-axis prefix scan ("Entrenamiento: forma paralela": prefix
+ * sums over blocks) plus a small header; it must be device memory, 256-byte
+ * aligned, and may be reused by later calls on the same stream.
+ */
+LA_API size_t la_causal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt);
+
+/* Workspace size for la_forward_noncausal (the split-N partial sums of S, z). */
+LA_API size_t la_noncausal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt);
+
+/*
+ * Causal forward ("Linear Attention/es", "Forma recurrente e inferencia
+ * autorregresiva" for the definition, computed blockwise as in
+ * "Entrenamiento: forma paralela"):
+ *   for each (b, h) and t = 0..N-1:
+ *     S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ *     y_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps)
+ * starting from (S_in, z_in), or from zero when both are NULL (one NULL and
+ * one not is LA_ERR_INVALID_ARG).  When S_out / z_out are non-NULL the final
+ * (S_N, z_N) is written there (both or neither).
+ */
+LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, float *y,
+                            int B, int H, int N, int d, int dv, la_dtype dt, float eps,
+                            const float *S_in, const float *z_in,
+                            float *S_out, float *z_out,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Non-causal forward ("Linear Attention/es", "Reformulación con núcleos"):
+ *   S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j) over all N tokens, then
+ *   y_i = phi(q_i)^T S / max(phi(q_i)^T z, eps) for every i.
+ * S_out / z_out (both or neither) receive S and z.  N must be >= 1.
+ */
+LA_API la_status la_forward_noncausal(const void *q, const void *k, const void *v, float *y,
+                               int B, int H, int N, int d, int dv, la_dtype dt, float eps,
+                               float *S_out, float *z_out,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One recurrent decode step per (b, h), in place on the state ("Forma
+ * recurrente e inferencia autorregresiva"; constant memory, no growing
+ * cache):  S += phi(k) v^T,  z += phi(k),  y = phi(q)^T S / max(phi(q)^T z, eps).
+ * q, k: [B][H][d]; v: [B][H][dv]; y: [B][H][dv] float32; S, z float32 in/out.
+ */
+LA_API la_status la_decode_step(const void *q, const void *k, const void *v, float *y,
+                         float *S, float *z, int B, int H, int d, int dv, la_dtype dt,
+                         float eps, void *stream);
+
+/*
+ * Synchronise `stream` and report the run-time status recorded in a
+ * workspace by the last call that used it: LA_OK, or LA_ERR_TIMEOUT when one
+ * of its bounded waits ran out (its outputs are then undefined).  The next
+ * call that uses the workspace clears the record.
+ */
+LA_API la_status la_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Test hook (host side only, process-wide, not thread-safe): when
+ * skip_publish_segment >= 0, the causal scan's CTA for that segment index
+ * never publishes its state, so its successor's bounded wait runs out;
+ * wait_limit_ns bounds every inter-CTA wait (<= 0 restores the default of
+ * about one second).  Pass (-1, 0) to turn the hook off.  Nothing faults,
+ * traps or hangs: the waiter records LA_ERR_TIMEOUT and returns.
+ */
+LA_API void la_debug_set_scan_fault(int skip_publish_segment, long long wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

@@ -1,0 +1,191 @@
+// api.cu -- the extern "C" entry points of liblinattn.so (declared in
+// include/linattn.h): argument checks on the host, then dispatch to the
+// kernels.  Nothing here computes attention; every step runs in the kernels.
+#include <cmath>
+#include <cstring>
+
+#include "la_internal.h"
+
+namespace la {
+
+DebugFault &debug_fault() {
+    static DebugFault f;
+    return f;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int x) { return x == 32 || x == 64 || x == 128; }
+
+// [p, p+n) and [q, q+m) overlap?
+bool overlap(const void *p, size_t n, const void *q, size_t m) {
+    if (!p || !q || n == 0 || m == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+size_t esize(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
+
+la_status check_common(const void *q, const void *k, const void *v, const float *y, int B, int H,
+                       long N, int d, int dv, la_dtype dt, float eps) {
+    if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || N < 0) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(d) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
+    const long long elems = (long long)B * H * (N > 0 ? N : 1) * (d > dv ? d : dv);
+    if (elems >= (1LL << 31)) return LA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !y) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y)) return LA_ERR_INVALID_ARG;
+    const size_t es = esize(dt), T = (size_t)B * H * (N > 0 ? N : 0);
+    const size_t ybytes = T * dv * 4;
+    if (overlap(y, ybytes, q, T * d * es) || overlap(y, ybytes, k, T * d * es) ||
+        overlap(y, ybytes, v, T * dv * es))
+        return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+la_status check_state(const float *S, const float *z, bool required) {
+    if ((S == nullptr) != (z == nullptr)) return LA_ERR_INVALID_ARG;
+    if (required && !S) return LA_ERR_INVALID_ARG;
+    if (S && (!aligned16(S) || !aligned16(z))) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+la_status check_ws(void *ws, size_t have, size_t need) {
+    if (need == 0) return LA_OK;
+    if (!ws || have < need) return LA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LA_ERR_WORKSPACE;
+    return LA_OK;
+}
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+size_t causal_ws(int B, int H, int N, int d, int dv, la_dtype dt) {
+    FwdArgs a{};
+    a.B = B; a.H = H; a.N = N; a.d = d; a.dv = dv; a.dt = dt;
+    if (B < 1 || H < 1 || N < 0 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    if (causal_tc_supported(a)) return causal_tc_workspace(B * H, N, d, dv);
+    return 0;
+}
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+const char *la_status_string(la_status s) {
+    switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+const char *la_version(void) { return "linattn 0.1 sm_103a"; }
+
+size_t la_causal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
+    return causal_ws(B, H, N, d, dv, dt);
+}
+
+size_t la_noncausal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
+    (void)dt;
+    if (B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    return noncausal_simt_workspace(B * H, N, d, dv);
+}
+
+la_status la_forward_causal(const void *q, const void *k, const void *v, float *y, int B, int H,
+                            int N, int d, int dv, la_dtype dt, float eps, const float *S_in,
+                            const float *z_in, float *S_out, float *z_out, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
+    if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
+    const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
+    if (overlap(y, T * dv * 4, S_in, sb) || overlap(y, T * dv * 4, z_in, zb) ||
+        overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = causal_ws(B, H, N, d, dv, dt);
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {  // no tokens: the final state is the initial state
+        if (S_out) {
+            cudaError_t e = cudaSuccess;
+            if (!S_in) e = cudaMemsetAsync(S_out, 0, sb, s);
+            else if (S_in != S_out)
+                e = cudaMemcpyAsync(S_out, S_in, sb, cudaMemcpyDeviceToDevice, s);
+            if (e == cudaSuccess) {
+                if (!z_in) e = cudaMemsetAsync(z_out, 0, zb, s);
+                else if (z_in != z_out)
+                    e = cudaMemcpyAsync(z_out, z_in, zb, cudaMemcpyDeviceToDevice, s);
+            }
+            return from_cuda(e);
+        }
+        return LA_OK;
+    }
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out,
+              workspace, workspace_bytes, s};
+    if (need > 0) {
+        cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s);
+        if (e != cudaSuccess) return LA_ERR_CUDA;
+    }
+    if (causal_tc_supported(a)) return from_cuda(launch_causal_tc(a));
+    return from_cuda(launch_causal_simt(a));
+}
+
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, float *y, int B,
+                               int H, int N, int d, int dv, la_dtype dt, float eps, float *S_out,
+                               float *z_out, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (N < 1) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
+    const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
+    if (overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = la_noncausal_workspace_bytes(B, H, N, d, dv, dt);
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, nullptr, nullptr, S_out, z_out,
+              workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+    return from_cuda(launch_noncausal_simt(a));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, float *y, float *S,
+                         float *z, int B, int H, int d, int dv, la_dtype dt, float eps,
+                         void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, 1, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if ((st = check_state(S, z, true)) != LA_OK) return st;
+    const size_t yb = (size_t)B * H * dv * 4, sb = (size_t)B * H * d * dv * 4,
+                 zb = (size_t)B * H * d * 4;
+    if (overlap(y, yb, S, sb) || overlap(y, yb, z, zb) || overlap(S, sb, z, zb))
+        return LA_ERR_INVALID_ARG;
+    DecodeArgs a{q, k, v, y, S, z, B, H, d, dv, dt, eps, static_cast<cudaStream_t>(stream)};
+    return from_cuda(launch_decode_simt(a));
+}
+
+la_status la_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return LA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LA_ERR_CUDA;
+    WsHeader h;
+    if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return h.error == 0 ? LA_OK : static_cast<la_status>(h.error);
+}
+
+void la_debug_set_scan_fault(int skip_publish_segment, long long wait_limit_ns) {
+    debug_fault().skip_publish_segment = skip_publish_segment;
+    debug_fault().wait_limit_ns = wait_limit_ns;
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+// decode.cu -- one recurrent decode step per head, in place on the fp32 state.
+//
+// "Linear Attention/es", "Forma recurrente e inferencia autorregresiva":
+//   S <- S + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T S / max(phi(q)^T z, eps)
+// (update first, then read, as in "La formulación recurrente paso a paso").
+//
+// The step is bound by HBM: per head it reads and writes d*dv*4 bytes of S
+// and does 2*d*dv FMAs.  One CTA of 8 warps owns one head.  Warp w owns the
+// d/8 rows [w*d/8, (w+1)*d/8) of S; lane l owns the dv/32 contiguous columns
+// starting at l*dv/32, so each warp moves whole 128..512-byte rows with 4..16
+// byte vector accesses.  All of a warp's row loads are issued before any is
+// used to keep d/8 * dv*4/ (32 lanes) bytes per lane in flight.  The dot
+// products over d are finished with a per-warp partial in shared memory
+// (columns) and a warp-shuffle reduction (the denominator).
+#include "la_device.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+template <int VEC> struct FVec;
+template <> struct FVec<1> {
+    float x[1];
+    __device__ __forceinline__ void load(const float *p) { x[0] = __ldcs(p); }
+    __device__ __forceinline__ void store(float *p) const { __stcs(p, x[0]); }
+};
+template <> struct FVec<2> {
+    float x[2];
+    __device__ __forceinline__ void load(const float *p) {
+        float2 t = __ldcs(reinterpret_cast<const float2 *>(p));
+        x[0] = t.x; x[1] = t.y;
+    }
+    __device__ __forceinline__ void store(float *p) const {
+        __stcs(reinterpret_cast<float2 *>(p), make_float2(x[0], x[1]));
+    }
+};
+template <> struct FVec<4> {
+    float x[4];
+    __device__ __forceinline__ void load(const float *p) {
+        float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    }
+    __device__ __forceinline__ void store(float *p) const {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
+    }
+};
+
+constexpr int kDecodeWarps = 8;
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                   float *__restrict__ y, float *__restrict__ S, float *__restrict__ z, float eps)
+{
+    constexpr int NW = kDecodeWarps;
+    constexpr int RPW = D / NW;   // rows of S per warp
+    constexpr int VEC = DV / 32;  // columns per lane
+    static_assert(RPW >= 1 && VEC >= 1, "unsupported size");
+    __shared__ float fq_s[D], fk_s[D], v_s[DV];
+    __shared__ float ypart[NW][DV];
+    __shared__ float dpart[NW];
+
+    const int head = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long qk_off = (long)head * D, v_off = (long)head * DV;
+    float *Sh = S + (long)head * D * DV;
+
+    // Issue the state loads first: they are the whole cost of the step.
+    FVec<VEC> s[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) s[r].load(Sh + (long)(warp * RPW + r) * DV + lane * VEC);
+
+    // phi(q), phi(k), v to shared; z update and the denominator phi(q)^T z_new.
+    float dp = 0.f;
+    for (int i = tid; i < D; i += NW * 32) {
+        const float fq = phi_f(to_f(q[qk_off + i]));
+        const float fk = phi_f(to_f(k[qk_off + i]));
+        fq_s[i] = fq;
+        fk_s[i] = fk;
+        const float zn = z[qk_off + i] + fk;
+        z[qk_off + i] = zn;
+        dp = fmaf(fq, zn, dp);
+    }
+    for (int i = tid; i < DV; i += NW * 32) v_s[i] = to_f(v[v_off + i]);
+    dp = warp_sum(dp);
+    if (lane == 0) dpart[warp] = dp;
+    __syncthreads();
+
+    float vv[VEC], acc[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) { vv[c] = v_s[lane * VEC + c]; acc[c] = 0.f; }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int a = warp * RPW + r;
+        const float fk = fk_s[a], fq = fq_s[a];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            const float sn = fmaf(fk, vv[c], s[r].x[c]);
+            s[r].x[c] = sn;
+            acc[c] = fmaf(fq, sn, acc[c]);
+        }
+        s[r].store(Sh + (long)a * DV + lane * VEC);
+    }
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) ypart[warp][lane * VEC + c] = acc[c];
+    __syncthreads();
+
+    if (tid < DV) {
+        float den = 0.f, num = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) { den += dpart[w]; num += ypart[w][tid]; }
+        y[v_off + tid] = num / fmaxf(den, eps);
+    }
+}
+
+template <int D, int DV>
+cudaError_t launch_dv(const DecodeArgs &a) {
+    const int grid = a.B * a.H;
+    if (a.dt == LA_DTYPE_BF16)
+        decode_step_kernel<D, DV, __nv_bfloat16><<<grid, kDecodeWarps * 32, 0, a.stream>>>(
+            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v,
+            a.y, a.S, a.z, a.eps);
+    else
+        decode_step_kernel<D, DV, float><<<grid, kDecodeWarps * 32, 0, a.stream>>>(
+            (const float *)a.q, (const float *)a.k, (const float *)a.v, a.y, a.S, a.z, a.eps);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeArgs &a) {
+    switch (a.dv) {
+    case 32: return launch_dv<D, 32>(a);
+    case 64: return launch_dv<D, 64>(a);
+    case 128: return launch_dv<D, 128>(a);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeArgs &a) {
+    switch (a.d) {
+    case 32: return launch_d<32>(a);
+    case 64: return launch_d<64>(a);
+    case 128: return launch_d<128>(a);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace la

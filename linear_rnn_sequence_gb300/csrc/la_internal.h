@@ -1,0 +1,65 @@
+// la_internal.h -- internal declarations shared by the CUDA translation units
+// of liblinattn.so.  Not part of the public ABI (that is include/linattn.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "linattn.h"
+
+namespace la {
+
+// Everything a forward launch needs; pointers are device pointers.
+struct FwdArgs {
+    const void *q, *k, *v;
+    float *y;
+    int B, H, N, d, dv;
+    la_dtype dt;
+    float eps;
+    const float *S_in, *z_in;   // nullable (zero initial state)
+    float *S_out, *z_out;       // nullable
+    void *ws;                   // workspace (may be null when none is needed)
+    size_t ws_bytes;
+    cudaStream_t stream;
+    int BH() const { return B * H; }
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    float *y, *S, *z;
+    int B, H, d, dv;
+    la_dtype dt;
+    float eps;
+    cudaStream_t stream;
+};
+
+// Workspace header written at the start of every workspace (256 bytes).
+struct WsHeader {
+    unsigned int error;         // 0 = ok, else an la_status value (LA_ERR_TIMEOUT)
+    unsigned int error_where;   // diagnostic: which segment gave up
+    unsigned int ticket;        // dynamic segment ticket counter
+    unsigned int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
+
+// Process-wide test hook state (see la_debug_set_scan_fault).
+struct DebugFault {
+    int skip_publish_segment = -1;
+    long long wait_limit_ns = 0;
+};
+DebugFault &debug_fault();
+
+// ---- launchers (return cudaSuccess or the launch error) ------------------
+cudaError_t launch_decode_simt(const DecodeArgs &a);
+cudaError_t launch_causal_simt(const FwdArgs &a);
+size_t noncausal_simt_workspace(int BH, int N, int d, int dv);
+cudaError_t launch_noncausal_simt(const FwdArgs &a);
+
+// tcgen05 / TMA path (bf16 inputs, d and dv in {64, 128}).
+bool causal_tc_supported(const FwdArgs &a);
+size_t causal_tc_workspace(int BH, int N, int d, int dv);
+cudaError_t launch_causal_tc(const FwdArgs &a);
+
+}  // namespace la

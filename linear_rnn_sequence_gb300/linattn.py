@@ -1,0 +1,212 @@
+"""ctypes binding of liblinattn.so (C ABI: include/linattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C entry points.  Tensors must be contiguous CUDA tensors;
+outputs and workspaces are allocated here with torch (the library allocates
+nothing).  There is no CPU fallback: a missing or unbuildable library raises.
+
+Names follow the C ABI:
+
+* ``forward_causal``    -> ``la_forward_causal``
+* ``forward_noncausal`` -> ``la_forward_noncausal``
+* ``decode_step``       -> ``la_decode_step``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
+LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load (building first if the sources are newer) and return the ctypes library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _build.is_stale():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"liblinattn.so missing at {_build.LIB}")
+            L = ctypes.CDLL(_build.LIB)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.la_status_string.argtypes = [i]
+            L.la_status_string.restype = ctypes.c_char_p
+            L.la_version.argtypes = []
+            L.la_version.restype = ctypes.c_char_p
+            L.la_causal_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            L.la_causal_workspace_bytes.restype = sz
+            L.la_noncausal_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            L.la_noncausal_workspace_bytes.restype = sz
+            L.la_forward_causal.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp,
+                                            vp, sz, vp]
+            L.la_forward_causal.restype = i
+            L.la_forward_noncausal.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
+                                               sz, vp]
+            L.la_forward_noncausal.restype = i
+            L.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            L.la_decode_step.restype = i
+            L.la_workspace_status.argtypes = [vp, sz, vp]
+            L.la_workspace_status.restype = i
+            L.la_debug_set_scan_fault.argtypes = [i, ctypes.c_longlong]
+            L.la_debug_set_scan_fault.restype = None
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().la_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().la_version().decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return LA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return LA_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors (no CPU fallback)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _raise(st: int, where: str):
+    if st != LA_OK:
+        raise LinAttnError(st, where)
+
+
+def causal_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(lib().la_causal_workspace_bytes(B, H, N, d, dv, code))
+
+
+def noncausal_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(lib().la_noncausal_workspace_bytes(B, H, N, d, dv, code))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_state=False,
+                   out=None, S_out=None, z_out=None, workspace=None, stream=None):
+    """Causal elu+1 linear attention.  q, k: [B,H,N,d]; v: [B,H,N,dv] (bf16 or fp32).
+
+    Returns y [B,H,N,dv] float32 (and the final (S, z) when ``return_state``).
+    """
+    _check_cuda(q, k, v, S_in, z_in, out, S_out, z_out, workspace)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = int(lib().la_causal_workspace_bytes(B, H, N, d, dv, dt))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().la_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                 float(eps), _ptr(S_in), _ptr(z_in), _ptr(S_out), _ptr(z_out),
+                                 _ptr(workspace), wbytes, _stream_handle(stream, q.device))
+    _raise(st, "la_forward_causal")
+    return (y, S_out, z_out) if return_state else y
+
+
+def forward_noncausal(q, k, v, eps: float = 1e-6, return_state=False, out=None, S_out=None,
+                      z_out=None, workspace=None, stream=None):
+    """Non-causal elu+1 linear attention.  Returns y [B,H,N,dv] float32 (+ S, z)."""
+    _check_cuda(q, k, v, out, S_out, z_out, workspace)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = int(lib().la_noncausal_workspace_bytes(B, H, N, d, dv, dt))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().la_forward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                    float(eps), _ptr(S_out), _ptr(z_out), _ptr(workspace), wbytes,
+                                    _stream_handle(stream, q.device))
+    _raise(st, "la_forward_noncausal")
+    return (y, S_out, z_out) if return_state else y
+
+
+def decode_step(q, k, v, S, z, eps: float = 1e-6, out=None, stream=None):
+    """One decode step in place on (S, z).  q, k: [B,H,d]; v: [B,H,dv]; returns y [B,H,dv] fp32."""
+    _check_cuda(q, k, v, S, z, out)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if S.dtype != torch.float32 or z.dtype != torch.float32:
+        raise TypeError("state must be float32")
+    if S.shape != (B, H, d, dv) or z.shape != (B, H, d):
+        raise ValueError("state shape mismatch")
+    y = out if out is not None else torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    st = lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), B, H, d, dv,
+                              dt, float(eps), _stream_handle(stream, q.device))
+    _raise(st, "la_decode_step")
+    return y
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Synchronise and return the run-time status recorded in ``workspace``."""
+    if workspace is None:
+        return LA_OK
+    return int(lib().la_workspace_status(_ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_handle(stream, workspace.device)))
+
+
+def set_scan_fault(skip_publish_segment: int = -1, wait_limit_ns: int = 0) -> None:
+    """Test hook: see la_debug_set_scan_fault in include/linattn.h."""
+    lib().la_debug_set_scan_fault(int(skip_publish_segment), int(wait_limit_ns))

@@ -1,0 +1,133 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, and
+exports every entry point include/linattn.h declares; host-side argument
+validation rejects bad calls before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from linear_rnn_sequence_gb300 import _build
+from linear_rnn_sequence_gb300 import linattn as la
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "linattn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LA_API\s+[\w\s\*]*?\b(la_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("la_forward_causal", "la_forward_noncausal", "la_decode_step",
+              "la_causal_workspace_bytes", "la_noncausal_workspace_bytes", "la_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = la.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r"\bT (la_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_build_targets_sm103a_only():
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_header_compiles_as_c():
+    src = '#include "linattn.h"\nint main(void){ return (int)LA_OK; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-", "-o", "/dev/null"], input=src, text=True,
+                       capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings_and_version():
+    assert la.status_string(la.LA_OK) == "LA_OK"
+    assert la.status_string(la.LA_ERR_TIMEOUT) == "LA_ERR_TIMEOUT"
+    assert la.status_string(99) == "LA_ERR_UNKNOWN"
+    assert "sm_103a" in la.version()
+
+
+def test_workspace_sizes():
+    L = la.lib()
+    assert L.la_noncausal_workspace_bytes(4, 8, 4096, 64, 64, 1) > 256
+    assert L.la_noncausal_workspace_bytes(4, 8, 0, 64, 64, 1) == 0
+    assert L.la_noncausal_workspace_bytes(4, 8, 16, 48, 64, 1) == 0
+    assert L.la_causal_workspace_bytes(1, 1, 10, 48, 64, 1) == 0
+
+
+# Fake, 256-byte aligned "device" addresses: every call below must be rejected
+# by the host-side checks, so nothing is ever dereferenced or launched.
+P = ctypes.c_void_p(1 << 20)
+P2 = ctypes.c_void_p((1 << 20) + (1 << 28))
+P3 = ctypes.c_void_p((1 << 20) + (2 << 28))
+Y = ctypes.c_void_p((1 << 20) + (3 << 28))
+
+
+def _causal(**kw):
+    a = dict(q=P, k=P2, v=P3, y=Y, B=1, H=1, N=8, d=64, dv=64, dt=1, eps=1e-6, S_in=None,
+             z_in=None, S_out=None, z_out=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return la.lib().la_forward_causal(a["q"], a["k"], a["v"], a["y"], a["B"], a["H"], a["N"],
+                                      a["d"], a["dv"], a["dt"], a["eps"], a["S_in"], a["z_in"],
+                                      a["S_out"], a["z_out"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expected", [
+    (dict(q=None), la.LA_ERR_INVALID_ARG),
+    (dict(y=None), la.LA_ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p((1 << 20) + 4)), la.LA_ERR_INVALID_ARG),   # misaligned
+    (dict(d=48), la.LA_ERR_UNSUPPORTED),
+    (dict(dv=256), la.LA_ERR_UNSUPPORTED),
+    (dict(dt=7), la.LA_ERR_UNSUPPORTED),
+    (dict(eps=0.0), la.LA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), la.LA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), la.LA_ERR_INVALID_ARG),
+    (dict(eps=float("inf")), la.LA_ERR_INVALID_ARG),
+    (dict(B=0), la.LA_ERR_INVALID_ARG),
+    (dict(N=-1), la.LA_ERR_INVALID_ARG),
+    (dict(S_in=P), la.LA_ERR_INVALID_ARG),             # S_in without z_in
+    (dict(z_out=P), la.LA_ERR_INVALID_ARG),            # z_out without S_out
+    (dict(y=ctypes.c_void_p((1 << 20) + 64)), la.LA_ERR_INVALID_ARG),  # y overlaps q
+    (dict(B=1 << 14, H=1 << 10, N=1 << 10), la.LA_ERR_INVALID_ARG),    # too large
+])
+def test_causal_rejects_bad_arguments(kw, expected):
+    assert _causal(**kw) == expected
+
+
+def test_noncausal_needs_workspace_and_tokens():
+    L = la.lib()
+    st = L.la_forward_noncausal(P, P2, P3, Y, 1, 1, 8, 64, 64, 1, 1e-6, None, None, None, 0, None)
+    assert st == la.LA_ERR_WORKSPACE
+    st = L.la_forward_noncausal(P, P2, P3, Y, 1, 1, 0, 64, 64, 1, 1e-6, None, None, P, 1 << 20,
+                                None)
+    assert st == la.LA_ERR_INVALID_ARG
+    # misaligned workspace
+    need = L.la_noncausal_workspace_bytes(1, 1, 8, 64, 64, 1)
+    st = L.la_forward_noncausal(P, P2, P3, Y, 1, 1, 8, 64, 64, 1, 1e-6, None, None,
+                                ctypes.c_void_p((3 << 20) + 16), need, None)
+    assert st == la.LA_ERR_WORKSPACE
+
+
+def test_decode_requires_state():
+    L = la.lib()
+    st = L.la_decode_step(P, P2, P3, Y, None, None, 1, 1, 64, 64, 1, 1e-6, None)
+    assert st == la.LA_ERR_INVALID_ARG
+    # y overlapping the state
+    st = L.la_decode_step(P, P2, P3, Y, Y, P, 1, 1, 64, 64, 1, 1e-6, None)
+    assert st == la.LA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 4, 32)
+    with pytest.raises(ValueError):
+        la.forward_causal(q, q, q)

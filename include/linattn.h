@@ -32,7 +32,8 @@
  *             largest early-token outputs by up to 2^-9 of their size, far more
  *             than 2e-2 of the RMS of y for long causal sequences.)
  *  Sizes      B, H >= 1; N >= 0 (N = 0 is a no-op that still writes the
- *             final state when asked); d, dv in {32, 64, 128}.  Other d / dv
+ *             final state when asked; q, k, v, y may then be NULL);
+ *             d, dv in {32, 64, 128}.  Other d / dv
  *             return LA_ERR_UNSUPPORTED.  B*H*N*max(d,dv) must fit in 2^31.
  *  eps        must be finite and > 0, else LA_ERR_INVALID_ARG.
  *  Streams    `stream` is a cudaStream_t (NULL = legacy default stream).  All

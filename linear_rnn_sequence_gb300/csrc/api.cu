@@ -35,9 +35,10 @@ la_status check_common(const void *q, const void *k, const void *v, const float 
     if (!(eps > 0.f) || !std::isfinite(eps)) return LA_ERR_INVALID_ARG;
     const long long elems = (long long)B * H * (N > 0 ? N : 1) * (d > dv ? d : dv);
     if (elems >= (1LL << 31)) return LA_ERR_INVALID_ARG;
+    const size_t es = esize(dt), T = (size_t)B * H * (N > 0 ? N : 0);
+    if (T == 0) return LA_OK;  // no tokens: q, k, v, y are never touched (may be null)
     if (!q || !k || !v || !y) return LA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y)) return LA_ERR_INVALID_ARG;
-    const size_t es = esize(dt), T = (size_t)B * H * (N > 0 ? N : 0);
     const size_t ybytes = T * dv * 4;
     if (overlap(y, ybytes, q, T * d * es) || overlap(y, ybytes, k, T * d * es) ||
         overlap(y, ybytes, v, T * dv * es))

@@ -1,9 +1,686 @@
-// causal_tc.cu -- tensor-core (tcgen05 / TMA / TMEM) chunkwise causal kernel.
-// Not built yet: every shape is served by the CUDA-core kernel for now.
+// causal_tc.cu -- chunkwise causal elu(x)+1 linear attention on the sm_103a
+// tensor cores (tcgen05 MMA, TMEM accumulators, TMA tiles, mbarriers).
+//
+// Method ("Linear Attention/es", "Entrenamiento: forma paralela"): split the
+// sequence into blocks of C = 128 tokens.  For query i of block c
+//   num_i = sum_{j <= i in c} w_ij v_j + phi(q_i)^T S_prev
+//   den_i = sum_{j <= i in c} w_ij     + phi(q_i)^T z_prev,   w_ij = phi(q_i)^T phi(k_j)
+//   y_i   = num_i / max(den_i, eps)
+// then S_prev += sum_{j in c} phi(k_j) v_j^T and z_prev += sum_{j in c} phi(k_j)
+// (the state recursion of "Forma recurrente e inferencia autorregresiva").
+//
+// Precision scheme.  With phi(x) = 1 + psi(x), psi = elu, every phi is close
+// to 1 for inputs of order 1/sqrt(d), so w_ij ~ d with small variations and
+// the output is a near-uniform average; bf16 operands holding phi itself
+// lose those variations.  The kernel therefore feeds only psi (small values)
+// to the tensor cores and carries the constant part exactly in fp32:
+//   w_ij            = d + alpha_i + beta_j + a_i . b_j     (a = bf16 psi(q), b = bf16 psi(k),
+//                                                          alpha_i = sum a_i, beta_j = sum b_j)
+//   S               = 1 u^T + R,  u = sum_j v_j,  R = sum_j b_j v_j^T
+//   z               = n 1 + zeta, n = token count, zeta = sum_j b_j
+//   phi(q_i)^T S    = (d + alpha_i) u + r + a_i R,          r = sum_j beta_j v_j = colsum(R)
+//   phi(q_i)^T z    = (d + alpha_i) n + rho + a_i . zeta,   rho = sum_j beta_j
+// The intra-block weights w_ij (about d) are split into bf16 hi + lo parts
+// for the P.V product, so their rounding error is about 2^-17 of w.
+// All accumulation is fp32 (TMEM).  The result is the exact attention of the
+// features 1 + bf16(psi(x)); the outputs are float32.
+//
+// One CTA owns one head (b, h) and walks its blocks in order.  Warp roles:
+//   warp 0      TMA producer: Q (1 stage), K and V (2 stages) tiles, 128B swizzle
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2..5  row workers, thread = TMEM lane = token row of the block:
+//               phi pass (psi(k) in place in shared memory, psi(q) into TMEM),
+//               weight epilogue (G -> w hi/lo in TMEM), state export
+//               (R -> bf16 operand, zeta, u, r), output epilogue (TMA store).
+// TMEM columns: R [0,dv) | Y [128,128+dv) | G/P [256,384) | psi(q) [384,384+d/2)
+//               | zeta [448,464) | u,r [464,480).
+// Every wait is bounded in time; a wait that runs out records LA_ERR_TIMEOUT
+// in the workspace header and the CTA unwinds (no trap, no hang).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "la_internal.h"
+#include "tc_ptx.cuh"
 
 namespace la {
-bool causal_tc_supported(const FwdArgs &) { return false; }
-size_t causal_tc_workspace(int, int, int, int) { return 0; }
-cudaError_t launch_causal_tc(const FwdArgs &) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;          // tokens per block (MMA M)
+constexpr int kThreads = 192;    // 6 warps
+constexpr int kRowWarp0 = 2;     // first row-worker warp
+constexpr int kWG = 128;         // row-worker threads
+constexpr int kBarWG = 1;        // named barrier id for the row workers
+
+constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColZ = 448, kColUV = 464;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D, int DV>
+struct Layout {
+    static constexpr int kQ = kC * D * 2;           // one Q stage
+    static constexpr int kK = kC * D * 2;
+    static constexpr int kV = kC * DV * 2;
+    static constexpr int kRt = D * DV * 2;          // bf16 R operand
+    static constexpr int kUVB = 16 * kC * 2;        // [16 x C] no-swizzle K-major
+    static constexpr int kYst = 32 * 16 * 4;        // per warp, per buffer
+    static constexpr int oQ = 0;
+    static constexpr int oK = oQ + kQ;              // 2 stages
+    static constexpr int oV = oK + 2 * kK;          // 2 stages
+    static constexpr int oRt = oV + 2 * kV;
+    static constexpr int oUVB = oRt + kRt;          // 2 stages
+    static constexpr int oY = oUVB + 2 * kUVB;      // 4 warps x 2 buffers
+    static constexpr int oSmall = oY + 8 * kYst;
+    static constexpr int kSmall = 4096;
+    static constexpr int bytes = oSmall + kSmall;
+    // request enough that only one CTA fits per SM (TMEM: 512 columns each)
+    static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
+};
+
+// Small shared-memory area (fp32 unless noted).
+struct Small {
+    uint64_t q_full, q_empty, kv_full[2], kv_empty[2];
+    uint64_t phi_done, g_full, h_ready, y_full, st_full, rt_ready;
+    uint32_t tmem_base;
+    int abort_flag;
+    float n_s[2], rho_s[2];        // by block parity: state after block c in [c & 1]
+    float rho_part[4];
+    float beta[kC];                // beta_j of the current block
+    float zeta[2][128];
+    float u[2][128];
+    float r[2][128];
+};
+static_assert(sizeof(Small) <= 4096, "small area");
+
+struct TcParams {
+    int N, BH;
+    float eps;
+    const float *S_in, *z_in;
+    float *S_out, *z_out;
+    unsigned int *err;             // workspace header error word
+    unsigned int *err_where;
+    unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ float psi_f(float x) { return x > 0.f ? x : __expf(x) - 1.f; }
+__device__ __forceinline__ float bf16_round(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Byte offset of element (row, col) in a [rows x 64] bf16 box with 128-byte
+// swizzle, the layout TMA writes (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+    return (uint32_t)row * 128u + ((((uint32_t)col >> 3) ^ ((uint32_t)row & 7u)) << 4) +
+           (((uint32_t)col & 7u) << 1);
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, const Guard &g,
+                                          unsigned int where) {
+    const bool ok = mbar_wait(bar, parity, g, where);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while unwinding after an abort: ignores the abort flag but
+// still gives up after the time limit.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) break;
+}
+
+// Row-worker barrier that also agrees on "someone gave up": returns true if
+// any of the 128 threads passes failed = true.
+__device__ __forceinline__ bool wg_barrier_any(bool failed) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)failed), "n"(kBarWG), "n"(kWG)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------------------ roles
+template <int D, int DV>
+__device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
+                                              const CUtensorMap *qmap, const CUtensorMap *kmap,
+                                              const CUtensorMap *vmap, int head, int nchunks,
+                                              const Guard &g) {
+    using Lay = Layout<D, DV>;
+    constexpr uint32_t qbytes = kC * D * 2, kvbytes = kC * (D + DV) * 2;
+    int last_q = -1, last_kv[2] = {-1, -1};
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = c * kC, s = c & 1;
+        if (c > 0 && !mbar_wait(&S.q_empty, (c - 1) & 1, g, 10)) break;
+        mbar_arrive_expect_tx(&S.q_full, qbytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_3d(sQ + bx * kC * 128, qmap, &S.q_full, bx * 64, t0, head);
+        last_q = c;
+        if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 11)) break;
+        mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_3d(sK + s * Lay::kK + bx * kC * 128, kmap, &S.kv_full[s], bx * 64, t0, head);
+#pragma unroll
+        for (int bx = 0; bx < DV / 64; ++bx)
+            tma_load_3d(sV + s * Lay::kV + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
+        last_kv[s] = c;
+    }
+    if (*g.abort) {  // let the copies already issued land before the CTA exits
+        if (last_q >= 0) drain_wait(&S.q_full, last_q & 1, g.limit_ns);
+        for (int s = 0; s < 2; ++s)
+            if (last_kv[s] >= 0) drain_wait(&S.kv_full[s], (last_kv[s] >> 1) & 1, g.limit_ns);
+    }
+}
+
+template <int D, int DV>
+__device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
+                                         uint8_t *sRt, uint8_t *sUVB, uint64_t *drain,
+                                         int nchunks, const Guard &g) {
+    using Lay = Layout<D, DV>;
+    constexpr uint32_t iG = idesc_bf16(128, kC, 0, 0);   // A = psi(q) in TMEM, B = psi(k) K-major
+    constexpr uint32_t iY = idesc_bf16(128, DV, 0, 1);   // A in TMEM, B MN-major (R~ or V)
+    constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);   // A = psi(k)^T MN-major, B = V MN-major
+    constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);   // A MN-major, B = [1|beta] no swizzle
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 20)) break;
+        if (!mbar_wait(&S.phi_done, c & 1, g, 21)) break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
+        const uint32_t ub = smem_u32(sUVB + s * Lay::kUVB), rb = smem_u32(sRt);
+        // G = psi(Q) psi(K)^T   [C x C], K = d
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t bd =
+                smem_desc(kb + (ks >> 2) * (kC * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128B);
+            mma_ts(tb + kColG, tb + kColAq + ks * 8, bd, iG, ks > 0);
+        }
+        mma_commit(&S.g_full);
+        if (!mbar_wait(&S.rt_ready, c & 1, g, 22)) break;
+        tc_fence_after();
+        // Y = psi(Q) R~_prev   [C x dv], K = d
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t bd = smem_desc(rb + ks * 2048, D * 128, 1024, kSwizzle128B);
+            mma_ts(tb + kColY, tb + kColAq + ks * 8, bd, iY, ks > 0);
+        }
+        // state: R += psi(K)^T V, zeta += psi(K)^T 1, [u r] += V^T [1 beta_hi beta_lo]
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+            const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
+            mma_ss(tb + kColR, ad, vd, iR, 1);
+            mma_ss(tb + kColZ, ad, ud, iZ, 1);
+            mma_ss(tb + kColUV, vd, ud, iZ, 1);
+        }
+        mma_commit(&S.st_full);
+        if (!mbar_wait(&S.h_ready, c & 1, g, 23)) break;
+        tc_fence_after();
+        // Y += P_hi V + P_lo V   (P = masked weights, hi/lo bf16 pairs in TMEM)
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+            const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            mma_ts(tb + kColY, tb + kColG + ks * 16, vd, iY, 1);
+            mma_ts(tb + kColY, tb + kColG + ks * 16 + 8, vd, iY, 1);
+        }
+        mma_commit(&S.y_full);
+        mma_commit(&S.kv_empty[s]);
+    }
+    // every MMA issued so far has completed once `drain` flips
+    mma_commit(drain);
+    drain_wait(drain, 0, g.limit_ns);
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ float warp_sum_f(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D, int DV>
+__device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uint8_t *sK,
+                                         uint8_t *sV, uint8_t *sRt, uint8_t *sUVB, uint8_t *sY,
+                                         const CUtensorMap *ymap, const TcParams &p, int head,
+                                         int nchunks, const Guard &g) {
+    using Lay = Layout<D, DV>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3;                    // TMEM lane quadrant of this warp
+    const int row = wq * 32 + lane;             // token row / state row owned
+    const int wtid = tid - kRowWarp0 * 32;      // 0..127
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const float dd = (float)D;
+    const int N = p.N;
+
+    // constant rows of the [1 | beta_hi | beta_lo] operand: row 0 ones, rows 3..15 zero
+    for (int e = wtid; e < 2 * 16 * kC; e += kWG) {
+        const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
+        *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
+                                           (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
+            __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
+    }
+
+    // ---- initial state, in the split form S = 1 u^T + R, z = n 1 + zeta
+    //      (u = first row of S, n = first entry of z; zero state when absent)
+    {
+        const float *Sin = p.S_in ? p.S_in + (size_t)head * D * DV : nullptr;
+        const float *zin = p.z_in ? p.z_in + (size_t)head * D : nullptr;
+#pragma unroll
+        for (int grp = 0; grp < DV / 16; ++grp) {
+            uint32_t v[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int b = grp * 16 + jj;
+                const float x = (Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f;
+                v[jj] = f2u(x);
+            }
+            tmem_st16(tb + lb + kColR + grp * 16, v);
+            if (row < D) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) pk[m] = pack_bf16x2(u2f(v[2 * m]), u2f(v[2 * m + 1]));
+                const int b0 = grp * 16;
+                uint8_t *box = sRt + (b0 >> 6) * (D * 128);
+                *reinterpret_cast<uint4 *>(box + sw128_off(row, b0 & 63)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(box + sw128_off(row, (b0 & 63) + 8)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        }
+        const float zeta0 = (zin && row < D) ? zin[row] - zin[0] : 0.f;
+        float u0 = 0.f, r0 = 0.f;
+        if (Sin && row < DV) {
+            u0 = Sin[row];
+            for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
+        }
+        const uint32_t zv[4] = {f2u(zeta0), 0u, 0u, 0u};
+        const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
+        tmem_st4(tb + lb + kColZ, zv);
+        tmem_st4(tb + lb + kColUV, uv);
+        S.zeta[1][row] = zeta0;
+        S.u[1][row] = u0;
+        S.r[1][row] = r0;
+        if (wtid == 0) {
+            float rho0 = 0.f;
+            if (zin)
+                for (int a = 1; a < D; ++a) rho0 += zin[a] - zin[0];
+            S.n_s[1] = zin ? zin[0] : 0.f;
+            S.rho_s[1] = rho0;
+        }
+        tmem_wait_st();
+        fence_proxy_async();
+        tc_fence_before();
+        named_bar(kBarWG, kWG);
+        mbar_arrive(&S.rt_ready);
+    }
+
+    bool aborted = false;
+    int last_c = -1;
+    for (int c = 0; c < nchunks && !aborted; ++c) {
+        const int s = c & 1, pb = (c + 1) & 1, cb = c & 1;
+        const int t0 = c * kC, L = min(kC, N - t0);
+        bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 30) &&
+                  wait_warp(&S.q_full, c & 1, g, 31);
+        float alpha = 0.f, den_inter = 0.f;
+        if (ok) {
+            // -- phi pass on K: psi(k) rounded to bf16 in place; beta_j = sum of the rounded row
+            uint8_t *kt = sK + s * Lay::kK;
+            float beta = 0.f;
+#pragma unroll
+            for (int f = 0; f < D / 8; ++f) {
+                uint8_t *pc = kt + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8);
+                uint4 raw = *reinterpret_cast<uint4 *>(pc);
+                uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t pk = pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
+                    beta += bf16_lo_f(pk) + bf16_hi_f(pk);
+                    w[h] = pk;
+                }
+                *reinterpret_cast<uint4 *>(pc) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            S.beta[row] = beta;
+            {
+                const float bh = bf16_round(beta);
+                uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
+            }
+            const float bsum = warp_sum_f(beta);
+            if (lane == 0) S.rho_part[wq] = bsum;
+            // -- phi pass on Q: psi(q) rounded to bf16 -> TMEM (A operand); alpha_i, a_i . zeta_prev
+            const float *zp = S.zeta[pb];
+            float gam = 0.f;
+#pragma unroll
+            for (int grp = 0; grp < D / 32; ++grp) {
+                uint32_t v[16];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const int f = grp * 4 + f4;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t pk =
+                            pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
+                        const float a0 = bf16_lo_f(pk), a1 = bf16_hi_f(pk);
+                        alpha += a0 + a1;
+                        gam = fmaf(a0, zp[f * 8 + 2 * h], gam);
+                        gam = fmaf(a1, zp[f * 8 + 2 * h + 1], gam);
+                        v[f4 * 4 + h] = pk;
+                    }
+                }
+                tmem_st16(tb + lb + kColAq + grp * 16, v);
+            }
+            mbar_arrive(&S.q_empty);
+            den_inter = (dd + alpha) * S.n_s[pb] + S.rho_s[pb] + gam;
+            tmem_wait_st();
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&S.phi_done);
+        }
+        if (wg_barrier_any(!ok)) { aborted = true; break; }  // beta[] visible to all
+
+        // -- weights: w_ij = d + alpha_i + beta_j + G_ij for j <= i, split into bf16 hi + lo
+        ok = wait_warp(&S.g_full, c & 1, g, 32);
+        float den = 0.f;
+        const float base_w = dd + alpha;
+        if (ok) {
+            tc_fence_after();
+            float rowsum = 0.f;
+#pragma unroll 1
+            for (int grp = 0; grp < kC / 16; ++grp) {
+                uint32_t gv[16], out[16];
+                tmem_ld16(tb + lb + kColG + grp * 16, gv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 2) {
+                    const int j = grp * 16 + jj;
+                    const float w0 = (j <= row) ? base_w + S.beta[j] + u2f(gv[jj]) : 0.f;
+                    const float w1 = (j + 1 <= row) ? base_w + S.beta[j + 1] + u2f(gv[jj + 1]) : 0.f;
+                    const uint32_t hi = pack_bf16x2(w0, w1);
+                    const float h0 = bf16_lo_f(hi), h1 = bf16_hi_f(hi);
+                    const uint32_t lo = pack_bf16x2(w0 - h0, w1 - h1);
+                    rowsum += (h0 + bf16_lo_f(lo)) + (h1 + bf16_hi_f(lo));
+                    out[jj >> 1] = hi;
+                    out[8 + (jj >> 1)] = lo;
+                }
+                tmem_st16(tb + lb + kColG + grp * 16, out);
+            }
+            den = den_inter + rowsum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&S.h_ready);
+        }
+
+        // -- state export for the next block: R -> bf16 operand, zeta, u, r, n, rho
+        ok = ok && wait_warp(&S.st_full, c & 1, g, 33);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int grp = 0; grp < DV / 16; ++grp) {
+                uint32_t rv[16];
+                tmem_ld16(tb + lb + kColR + grp * 16, rv);
+                tmem_wait_ld();
+                if (row < D) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) pk[m] = pack_bf16x2(u2f(rv[2 * m]), u2f(rv[2 * m + 1]));
+                    const int b0 = grp * 16;
+                    uint8_t *box = sRt + (b0 >> 6) * (D * 128);
+                    *reinterpret_cast<uint4 *>(box + sw128_off(row, b0 & 63)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(box + sw128_off(row, (b0 & 63) + 8)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+            uint32_t zv[4], uv[4];
+            tmem_ld4(tb + lb + kColZ, zv);
+            tmem_ld4(tb + lb + kColUV, uv);
+            tmem_wait_ld();
+            S.zeta[cb][row] = u2f(zv[0]);
+            S.u[cb][row] = u2f(uv[0]);
+            S.r[cb][row] = u2f(uv[1]) + u2f(uv[2]);
+            if (wtid == 0) {
+                S.n_s[cb] = S.n_s[pb] + (float)L;
+                S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[0] + S.rho_part[1]) +
+                                             (S.rho_part[2] + S.rho_part[3]));
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&S.rt_ready);
+        }
+
+        // -- outputs: y = (Y + (d + alpha_i) u_prev + r_prev) / max(den, eps), TMA-stored
+        ok = ok && wait_warp(&S.y_full, c & 1, g, 34);
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / fmaxf(den, p.eps);
+            const float *up = S.u[pb], *rp = S.r[pb];
+            uint8_t *ybase = sY + (wq * 2) * Lay::kYst;
+#pragma unroll 1
+            for (int grp = 0; grp < DV / 16; ++grp) {
+                uint32_t yv[16];
+                tmem_ld16(tb + lb + kColY + grp * 16, yv);
+                tmem_wait_ld();
+                float o[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int b = grp * 16 + jj;
+                    o[jj] = (u2f(yv[jj]) + fmaf(base_w, up[b], rp[b])) * inv;
+                }
+                uint8_t *yb = ybase + (grp & 1) * Lay::kYst;
+                // the store issued two groups ago (possibly in the previous block)
+                // read this buffer; wait until it has
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                const float4 q0 = make_float4(o[0], o[1], o[2], o[3]);
+                const float4 q1 = make_float4(o[4], o[5], o[6], o[7]);
+                const float4 q2 = make_float4(o[8], o[9], o[10], o[11]);
+                const float4 q3 = make_float4(o[12], o[13], o[14], o[15]);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {  // rotate chunks across lanes: no bank conflicts
+                    const int qq = (q4 + (lane >> 1)) & 3;
+                    const float4 val = qq == 0 ? q0 : qq == 1 ? q1 : qq == 2 ? q2 : q3;
+                    *reinterpret_cast<float4 *>(yb + lane * 64 + qq * 16) = val;
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(ymap, yb, grp * 16, t0 + wq * 32, head);
+                    bulk_commit();
+                }
+            }
+            last_c = c;
+        }
+        if (wg_barrier_any(!ok)) aborted = true;  // small state buffers safe to reuse
+    }
+    if (lane == 0) bulk_wait<0>();
+
+    // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
+    if (!aborted && last_c == nchunks - 1 && p.S_out) {
+        const int lb_ = last_c & 1;
+        tc_fence_after();
+#pragma unroll
+        for (int grp = 0; grp < DV / 16; ++grp) {
+            uint32_t rv[16];
+            tmem_ld16(tb + lb + kColR + grp * 16, rv);
+            tmem_wait_ld();
+            if (row < D) {
+                float *dst = p.S_out + ((size_t)head * D + row) * DV + grp * 16;
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4)
+                    *reinterpret_cast<float4 *>(dst + jj) = make_float4(
+                        u2f(rv[jj]) + S.u[lb_][grp * 16 + jj],
+                        u2f(rv[jj + 1]) + S.u[lb_][grp * 16 + jj + 1],
+                        u2f(rv[jj + 2]) + S.u[lb_][grp * 16 + jj + 2],
+                        u2f(rv[jj + 3]) + S.u[lb_][grp * 16 + jj + 3]);
+            }
+        }
+        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lb_] + S.zeta[lb_][row];
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap ymap,
+                 const TcParams p)
+{
+    using Lay = Layout<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    Small &S = *reinterpret_cast<Small *>(sm + Lay::oSmall);
+    uint8_t *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
+    uint8_t *sRt = sm + Lay::oRt, *sUVB = sm + Lay::oUVB, *sY = sm + Lay::oY;
+    __shared__ uint64_t drain_bar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int head = blockIdx.x;
+    const int nchunks = (p.N + kC - 1) / kC;
+    const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
+
+    if (tid == 0) {
+        S.abort_flag = 0;
+        mbar_init(&S.q_full, 1);
+        mbar_init(&S.q_empty, kWG);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&S.kv_full[s], 1);
+            mbar_init(&S.kv_empty[s], 1);
+        }
+        mbar_init(&S.phi_done, kWG);
+        mbar_init(&S.g_full, 1);
+        mbar_init(&S.h_ready, kWG);
+        mbar_init(&S.y_full, 1);
+        mbar_init(&S.st_full, 1);
+        mbar_init(&S.rt_ready, kWG);
+        mbar_init(&drain_bar, 1);
+        fence_mbar_init();
+        prefetch_tmap(&qmap);
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+        prefetch_tmap(&ymap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, nchunks, g);
+    } else if (warp == 1) {
+        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, &drain_bar, nchunks, g);
+    } else {
+        row_role<D, DV>(S, tb, sQ, sK, sV, sRt, sUVB, sY, &ymap, p, head, nchunks, g);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tb, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 3-D map over [heads][rows][inner] with a box of [1][box_rows][box_inner].
+bool encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz, int inner,
+               int rows, int heads, int box_inner, int box_rows, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * esz, (cuuint64_t)rows * inner * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int DV>
+cudaError_t launch_dv(const FwdArgs &a) {
+    using Lay = Layout<D, DV>;
+    CUtensorMap qm, km, vm, ym;
+    const int BH = a.BH();
+    if (!encode_3d(&qm, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&km, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&vm, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&ym, a.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DV, a.N, BH, 16, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    TcParams p{};
+    p.N = a.N;
+    p.BH = BH;
+    p.eps = a.eps;
+    p.S_in = a.S_in;
+    p.z_in = a.z_in;
+    p.S_out = a.S_out;
+    p.z_out = a.z_out;
+    WsHeader *hdr = static_cast<WsHeader *>(a.ws);
+    p.err = &hdr->error;
+    p.err_where = &hdr->error_where;
+    const long long lim = debug_fault().wait_limit_ns;
+    p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
+    auto kern = causal_tc_kernel<D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay::request);
+    if (e != cudaSuccess) return e;
+    kern<<<BH, kThreads, Lay::request, a.stream>>>(qm, km, vm, ym, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool causal_tc_supported(const FwdArgs &a) {
+    return a.dt == LA_DTYPE_BF16 && (a.d == 64 || a.d == 128) && (a.dv == 64 || a.dv == 128);
+}
+
+size_t causal_tc_workspace(int, int, int, int) { return sizeof(WsHeader); }
+
+cudaError_t launch_causal_tc(const FwdArgs &a) {
+    if (a.d == 64 && a.dv == 64) return launch_dv<64, 64>(a);
+    if (a.d == 64 && a.dv == 128) return launch_dv<64, 128>(a);
+    if (a.d == 128 && a.dv == 64) return launch_dv<128, 64>(a);
+    if (a.d == 128 && a.dv == 128) return launch_dv<128, 128>(a);
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace la

@@ -117,6 +117,10 @@ la_status la_forward_causal(const void *q, const void *k, const void *v, float *
     if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (need > 0) {  // a fresh run-time status for every call that uses the workspace
+        cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s);
+        if (e != cudaSuccess) return LA_ERR_CUDA;
+    }
     if (N == 0) {  // no tokens: the final state is the initial state
         if (S_out) {
             cudaError_t e = cudaSuccess;
@@ -134,10 +138,6 @@ la_status la_forward_causal(const void *q, const void *k, const void *v, float *
     }
     FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out,
               workspace, workspace_bytes, s};
-    if (need > 0) {
-        cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s);
-        if (e != cudaSuccess) return LA_ERR_CUDA;
-    }
     if (causal_tc_supported(a)) return from_cuda(launch_causal_tc(a));
     return from_cuda(launch_causal_simt(a));
 }

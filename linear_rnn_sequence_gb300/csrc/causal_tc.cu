@@ -28,23 +28,41 @@
 // One CTA owns one head (b, h) and walks its blocks in order.  Warp roles:
 //   warp 0      TMA producer: Q (1 stage), K and V (2 stages) tiles, 128B swizzle
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..5  row workers, thread = TMEM lane = token row of the block:
-//               phi pass (psi(k) in place in shared memory, psi(q) into TMEM),
-//               weight epilogue (G -> w hi/lo in TMEM), state export
-//               (R -> bf16 operand, zeta, u, r), output epilogue (TMA store).
+//   warps 2..5  group A (thread = TMEM lane = token row): psi(q) into TMEM,
+//               then the weight epilogue (G -> w hi/lo in TMEM, row sums)
+//   warps 6..9  group B (thread = TMEM lane): psi(k) in place in shared
+//               memory, state export (R -> bf16 operand, zeta, u, r) and the
+//               output epilogue (shared-memory transpose, 16-byte stores)
+// The two groups work on neighbouring blocks at once, so phi, the weight
+// epilogue, the tensor-core MMAs and the output epilogue overlap.
 // TMEM columns: R [0,dv) | Y [128,128+dv) | G/P [256,384) | psi(q) [384,384+d/2)
-//               | zeta [448,464) | u,r [464,480).
+//               | a.zeta [448,464) | zeta [464,480) | u,r [480,496).
 // Every wait is bounded in time; a wait that runs out records LA_ERR_TIMEOUT
 // in the workspace header and the CTA unwinds (no trap, no hang).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
 #include "la_internal.h"
 #include "tc_ptx.cuh"
+
+// Optional per-block timeline of CTA 0 (SM cycle counter) for performance
+// work; compiled in only with -DLA_TRACE, and then read with la_trace_fetch.
+#ifdef LA_TRACE
+__device__ unsigned long long la_trace_buf[256 * 16];
+#define LA_TRACE_POINT(c, ev)                                                   \
+    do {                                                                        \
+        if (blockIdx.x == 0 && (c) < 256) la_trace_buf[(c) * 16 + (ev)] = clock64(); \
+    } while (0)
+#else
+#define LA_TRACE_POINT(c, ev) \
+    do {                      \
+    } while (0)
+#endif
 
 namespace la {
 namespace {
@@ -52,12 +70,14 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 128;          // tokens per block (MMA M)
-constexpr int kThreads = 192;    // 6 warps
-constexpr int kRowWarp0 = 2;     // first row-worker warp
-constexpr int kWG = 128;         // row-worker threads
-constexpr int kBarWG = 1;        // named barrier id for the row workers
+constexpr int kThreads = 320;    // 10 warps
+constexpr int kWarpA = 2;        // first warp of group A
+constexpr int kWarpB = 6;        // first warp of group B
+constexpr int kWG = 128;         // threads per group
+constexpr int kBarA = 1, kBarB = 2;  // named barrier ids
 
-constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColZ = 448, kColUV = 464;
+constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 448,
+                   kColZ = 464, kColUV = 480;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, int DV>
@@ -65,38 +85,50 @@ struct Layout {
     static constexpr int kQ = kC * D * 2;           // one Q stage
     static constexpr int kK = kC * D * 2;
     static constexpr int kV = kC * DV * 2;
-    static constexpr int kRt = D * DV * 2;          // bf16 R operand
-    static constexpr int kUVB = 16 * kC * 2;        // [16 x C] no-swizzle K-major
-    static constexpr int kYst = 32 * 16 * 4;        // per warp, per buffer
+    static constexpr int kRt = D * DV * 2;          // bf16 R operand, 128B-swizzled MN-major
+    static constexpr int kUVB = 16 * kC * 2;        // [1|beta_hi|beta_lo] operand, [16 x C]
+    static constexpr int kZt = 16 * D * 2;          // zeta operand, [16 x d]
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQ;              // 2 stages
     static constexpr int oV = oK + 2 * kK;          // 2 stages
     static constexpr int oRt = oV + 2 * kV;
     static constexpr int oUVB = oRt + kRt;          // 2 stages
-    static constexpr int oY = oUVB + 2 * kUVB;      // 4 warps x 2 buffers
-    static constexpr int oSmall = oY + 8 * kYst;
-    static constexpr int kSmall = 4096;
+    static constexpr int oZt = oUVB + 2 * kUVB;
+    static constexpr int oSmall = oZt + kZt;
+    static constexpr int kSmall = 7 * 1024;
     static constexpr int bytes = oSmall + kSmall;
     // request enough that only one CTA fits per SM (TMEM: 512 columns each)
     static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
 };
 
-// Small shared-memory area (fp32 unless noted).
+// Small shared-memory area.  Per-block values are kept by block parity:
+// [c & 1] holds block c (or, for the state, the state after block c).
 struct Small {
+    alignas(16) float beta[2][kC];     // beta_j = sum of bf16 psi(k_j)
+    alignas(16) float alpha[2][kC];    // alpha_i = sum of bf16 psi(q_i)
+    alignas(16) float rowsum[2][kC];   // sum_{j<=i} w_ij (hi + lo) in the block
+    alignas(16) float u[2][128];
+    alignas(16) float r[2][128];
+    alignas(16) float zeta[128];       // last exported zeta (fp32), for the final state
+    alignas(16) float rho_part[2][4];
+    alignas(16) float e_inv[kC];       // output epilogue: 1 / max(den, eps) per row
+    alignas(16) float e_base[kC];      // output epilogue: d + alpha per row
+    float n_s[2], rho_s[2];
     uint64_t q_full, q_empty, kv_full[2], kv_empty[2];
-    uint64_t phi_done, g_full, h_ready, y_full, st_full, rt_ready;
+    uint64_t phik_done[2];             // by K/V stage: a waiter is never two phases behind
+    uint64_t h_ready[2];               // by block parity: group A may run a block ahead of B
+    uint64_t phiq_done, g_full, aq_free, st_full, rt_ready, y_full, y_empty;
+    uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    float n_s[2], rho_s[2];        // by block parity: state after block c in [c & 1]
-    float rho_part[4];
-    float beta[kC];                // beta_j of the current block
-    float zeta[2][128];
-    float u[2][128];
-    float r[2][128];
 };
-static_assert(sizeof(Small) <= 4096, "small area");
+static_assert(offsetof(Small, beta) % 16 == 0 && offsetof(Small, u) % 16 == 0 &&
+                  offsetof(Small, r) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
+              "vector loads and mbarriers need aligned fields");
+static_assert(sizeof(Small) <= 7 * 1024, "small area");
 
 struct TcParams {
+    float *y;
     int N, BH;
     float eps;
     const float *S_in, *z_in;
@@ -106,7 +138,13 @@ struct TcParams {
     unsigned long long limit_ns;
 };
 
-__device__ __forceinline__ float psi_f(float x) { return x > 0.f ? x : __expf(x) - 1.f; }
+// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
+// lanes with inputs of either sign stay converged: for x > 0 the exponential
+// of 0 is exactly 1 and the second term vanishes.  e^x = 2^(x log2 e) with the
+// flush-to-zero form (x <= 0 here, so a flushed result only means e^x < 2^-126).
+__device__ __forceinline__ float psi_f(float x) {
+    return fmaxf(x, 0.f) + (ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
+}
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }
@@ -116,6 +154,15 @@ __device__ __forceinline__ float bf16_round(float x) {
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
     return (uint32_t)row * 128u + ((((uint32_t)col >> 3) ^ ((uint32_t)row & 7u)) << 4) +
            (((uint32_t)col & 7u) << 1);
+}
+
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ float warp_sum_f(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
 }
 
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
@@ -133,20 +180,21 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint6
         if (globaltimer_ns() - t0 > limit_ns) break;
 }
 
-// Row-worker barrier that also agrees on "someone gave up": returns true if
-// any of the 128 threads passes failed = true.
-__device__ __forceinline__ bool wg_barrier_any(bool failed) {
+// Group barrier that also agrees on "someone gave up": returns true if any of
+// the group's 128 threads passes failed = true.
+template <int BAR>
+__device__ __forceinline__ bool group_any(bool failed) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
         "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)failed), "n"(kBarWG), "n"(kWG)
+        : "r"((uint32_t)failed), "n"(BAR), "n"(kWG)
         : "memory");
     return r != 0;
 }
 
-// ------------------------------------------------------------------ roles
+// ------------------------------------------------------------------ producer
 template <int D, int DV>
 __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
                                               const CUtensorMap *qmap, const CUtensorMap *kmap,
@@ -157,12 +205,6 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
     int last_q = -1, last_kv[2] = {-1, -1};
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kC, s = c & 1;
-        if (c > 0 && !mbar_wait(&S.q_empty, (c - 1) & 1, g, 10)) break;
-        mbar_arrive_expect_tx(&S.q_full, qbytes);
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_3d(sQ + bx * kC * 128, qmap, &S.q_full, bx * 64, t0, head);
-        last_q = c;
         if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 11)) break;
         mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
 #pragma unroll
@@ -172,6 +214,14 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
         for (int bx = 0; bx < DV / 64; ++bx)
             tma_load_3d(sV + s * Lay::kV + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
         last_kv[s] = c;
+        LA_TRACE_POINT(c, 13);
+        if (c > 0 && !mbar_wait(&S.q_empty, (c - 1) & 1, g, 10)) break;
+        mbar_arrive_expect_tx(&S.q_full, qbytes);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_3d(sQ + bx * kC * 128, qmap, &S.q_full, bx * 64, t0, head);
+        last_q = c;
+        LA_TRACE_POINT(c, 14);
     }
     if (*g.abort) {  // let the copies already issued land before the CTA exits
         if (last_q >= 0) drain_wait(&S.q_full, last_q & 1, g.limit_ns);
@@ -180,23 +230,33 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
     }
 }
 
+// ------------------------------------------------------------------ MMA issuer
+// Per block c (one thread issues, in this order):
+//   G  = psi(Q) psi(K)^T                       after psi(q), psi(k) of block c
+//   Y  = psi(Q) R~,  Yz = psi(Q) zeta~         after the previous block's state
+//   R += psi(K)^T V, zeta += psi(K)^T 1,       export and output epilogue
+//   [u r] += V^T [1 beta_hi beta_lo]
+//   Y += P_hi V + P_lo V                       after the weight epilogue
 template <int D, int DV>
 __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
-                                         uint8_t *sRt, uint8_t *sUVB, uint64_t *drain,
-                                         int nchunks, const Guard &g) {
+                                         uint8_t *sRt, uint8_t *sUVB, uint8_t *sZt, int nchunks,
+                                         const Guard &g) {
     using Lay = Layout<D, DV>;
     constexpr uint32_t iG = idesc_bf16(128, kC, 0, 0);   // A = psi(q) in TMEM, B = psi(k) K-major
     constexpr uint32_t iY = idesc_bf16(128, DV, 0, 1);   // A in TMEM, B MN-major (R~ or V)
+    constexpr uint32_t iYz = idesc_bf16(128, 16, 0, 0);  // A in TMEM, B = zeta~ no swizzle
     constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);   // A = psi(k)^T MN-major, B = V MN-major
     constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);   // A MN-major, B = [1|beta] no swizzle
+    const uint32_t rb = smem_u32(sRt), zb = smem_u32(sZt);
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 20)) break;
-        if (!mbar_wait(&S.phi_done, c & 1, g, 21)) break;
+        if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 21)) break;
+        if (!mbar_wait(&S.phiq_done, c & 1, g, 22)) break;
+        LA_TRACE_POINT(c, 10);
         tc_fence_after();
         const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
-        const uint32_t ub = smem_u32(sUVB + s * Lay::kUVB), rb = smem_u32(sRt);
-        // G = psi(Q) psi(K)^T   [C x C], K = d
+        const uint32_t ub = smem_u32(sUVB + s * Lay::kUVB);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t bd =
@@ -204,15 +264,18 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
             mma_ts(tb + kColG, tb + kColAq + ks * 8, bd, iG, ks > 0);
         }
         mma_commit(&S.g_full);
-        if (!mbar_wait(&S.rt_ready, c & 1, g, 22)) break;
+        if (!mbar_wait(&S.rt_ready, c & 1, g, 23)) break;
+        if (!mbar_wait(&S.y_empty, c & 1, g, 24)) break;
+        LA_TRACE_POINT(c, 11);
         tc_fence_after();
-        // Y = psi(Q) R~_prev   [C x dv], K = d
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t bd = smem_desc(rb + ks * 2048, D * 128, 1024, kSwizzle128B);
             mma_ts(tb + kColY, tb + kColAq + ks * 8, bd, iY, ks > 0);
+            const uint64_t zd = smem_desc(zb + ks * 256, 128, D * 16, kSwizzleNone);
+            mma_ts(tb + kColYz, tb + kColAq + ks * 8, zd, iYz, ks > 0);
         }
-        // state: R += psi(K)^T V, zeta += psi(K)^T 1, [u r] += V^T [1 beta_hi beta_lo]
+        mma_commit(&S.aq_free);
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
             const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
@@ -223,9 +286,9 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
             mma_ss(tb + kColUV, vd, ud, iZ, 1);
         }
         mma_commit(&S.st_full);
-        if (!mbar_wait(&S.h_ready, c & 1, g, 23)) break;
+        if (!mbar_wait(&S.h_ready[c & 1], (c >> 1) & 1, g, 25)) break;
+        LA_TRACE_POINT(c, 12);
         tc_fence_after();
-        // Y += P_hi V + P_lo V   (P = masked weights, hi/lo bf16 pairs in TMEM)
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
             const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
@@ -236,42 +299,157 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         mma_commit(&S.kv_empty[s]);
     }
     // every MMA issued so far has completed once `drain` flips
-    mma_commit(drain);
-    drain_wait(drain, 0, g.limit_ns);
+    mma_commit(&S.drain);
+    drain_wait(&S.drain, 0, g.limit_ns);
 }
 
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ float warp_sum_f(float x) {
+// ------------------------------------------------------------------ group A
+// Block c: psi(q) -> TMEM (A operand) and alpha_i; then, once G is ready,
+// w_ij = d + alpha_i + beta_j + G_ij (j <= i, else 0) split into bf16 hi + lo
+// pairs written back over G, and the row sums of hi + lo.
+template <int D, int DV>
+__device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
+                                             int nchunks, const Guard &g) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, row = wq * 32 + lane;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const float dd = (float)D;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cb = c & 1;
+        bool ok = wait_warp(&S.q_full, c & 1, g, 40);
+        if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 0);
+        float alpha = 0.f;
+        if (ok) {
+            tc_fence_after();   // the MMAs that read the previous psi(q) have completed
+            uint4 raw[D / 8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
+            for (int f = 0; f < D / 8; ++f)
+                raw[f] = *reinterpret_cast<const uint4 *>(
+                    sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
+#pragma unroll
+            for (int grp = 0; grp < D / 32; ++grp) {   // 32 features -> 16 TMEM columns
+                uint32_t v[16];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const uint4 r4 = raw[grp * 4 + f4];
+                    const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t pk =
+                            pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
+                        alpha += bf16_lo_f(pk) + bf16_hi_f(pk);
+                        v[f4 * 4 + h] = pk;
+                    }
+                }
+                tmem_st16(tb + lb + kColAq + grp * 16, v);
+            }
+            S.alpha[cb][row] = alpha;
+            mbar_arrive(&S.q_empty);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&S.phiq_done);
+            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 1);
+        }
+        ok = ok && wait_warp(&S.phik_done[c & 1], (c >> 1) & 1, g, 42) &&
+             wait_warp(&S.g_full, c & 1, g, 43);
+        if (ok) {
+            tc_fence_after();
+            const float base_w = dd + alpha;
+            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 2);
+            const float *beta = S.beta[cb];
+            float rowsum = 0.f;
+            // groups entirely above this warp's rows are all zero (causal mask);
+            // the TMEM load of the next group is issued before this group's math
+            const int last_grp = (wq * 32 + 31) >> 4;
+            uint32_t gv[2][16];
+            tmem_ld16(tb + lb + kColG, gv[0]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int grp = 0; grp < kC / 16; ++grp) {
+                uint32_t out[16];
+                if (grp + 1 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 1) * 16, gv[(grp + 1) & 1]);
+                if (grp > last_grp) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) out[m] = 0u;
+                } else {
+                    const uint32_t *gc = gv[grp & 1];
+                    const float4 b0 = *reinterpret_cast<const float4 *>(beta + grp * 16);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 4);
+                    const float4 b2 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 8);
+                    const float4 b3 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 12);
+                    const float bb[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w,
+                                          b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
+                    const int lim = row - grp * 16;  // j - 16 grp <= lim is kept
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 2) {
+                        const float w0 = (jj <= lim) ? base_w + bb[jj] + u2f(gc[jj]) : 0.f;
+                        const float w1 = (jj + 1 <= lim) ? base_w + bb[jj + 1] + u2f(gc[jj + 1]) : 0.f;
+                        const uint32_t hi = pack_bf16x2(w0, w1);
+                        const float h0 = bf16_lo_f(hi), h1 = bf16_hi_f(hi);
+                        const uint32_t lo = pack_bf16x2(w0 - h0, w1 - h1);
+                        rowsum += w0 + w1;   // hi + lo equals w to within 2^-17 w
+                        out[jj >> 1] = hi;
+                        out[8 + (jj >> 1)] = lo;
+                    }
+                }
+                tmem_st16(tb + lb + kColG + grp * 16, out);
+                if (grp + 1 <= last_grp) tmem_wait_ld();
+            }
+            S.rowsum[cb][row] = rowsum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&S.h_ready[cb]);
+            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 3);
+        }
+        if (group_any<kBarA>(!ok)) break;
+    }
 }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// ------------------------------------------------------------------ group B
+template <int D, int DV>
+__device__ __forceinline__ void export_row_bf16(uint8_t *sRt, int row, int grp,
+                                                const uint32_t (&rv)[16]) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) pk[m] = pack_bf16x2(u2f(rv[2 * m]), u2f(rv[2 * m + 1]));
+    const int b0 = grp * 16;
+    uint8_t *box = sRt + (b0 >> 6) * (D * 128);
+    *reinterpret_cast<uint4 *>(box + sw128_off(row, b0 & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4 *>(box + sw128_off(row, (b0 & 63) + 8)) =
+        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+
+// zeta~ operand: [16 x d] K-major, no swizzle; row 0 holds bf16(zeta), rows 1..15 zero.
+__device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
+    return (uint32_t)((n >> 3) * (D * 16) + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
+}
 
 template <int D, int DV>
-__device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uint8_t *sK,
-                                         uint8_t *sV, uint8_t *sRt, uint8_t *sUVB, uint8_t *sY,
-                                         const CUtensorMap *ymap, const TcParams &p, int head,
-                                         int nchunks, const Guard &g) {
+__device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
+                                             uint8_t *sUVB, uint8_t *sZt,
+                                             const TcParams &p,
+                                             int head, int nchunks, const Guard &g) {
     using Lay = Layout<D, DV>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3;                    // TMEM lane quadrant of this warp
-    const int row = wq * 32 + lane;             // token row / state row owned
-    const int wtid = tid - kRowWarp0 * 32;      // 0..127
+    const int wq = warp & 3, row = wq * 32 + lane;
+    const int wtid = tid - kWarpB * 32;   // 0..127
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const float dd = (float)D;
     const int N = p.N;
 
-    // constant rows of the [1 | beta_hi | beta_lo] operand: row 0 ones, rows 3..15 zero
+    // constant operand rows: [1|beta] row 0 = ones, rows 3..15 zero; zeta~ all zero
     for (int e = wtid; e < 2 * 16 * kC; e += kWG) {
         const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
         *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
                                            (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
             __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
     }
+    for (int e = wtid; e < 16 * D; e += kWG)
+        *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(e / D, e % D, D)) = __float2bfloat16_rn(0.f);
 
-    // ---- initial state, in the split form S = 1 u^T + R, z = n 1 + zeta
-    //      (u = first row of S, n = first entry of z; zero state when absent)
+    // ---- initial state in split form S = 1 u^T + R, z = n 1 + zeta (u = first row
+    //      of S, n = first entry of z; zero when absent); buffers [1] = "block -1"
     {
         const float *Sin = p.S_in ? p.S_in + (size_t)head * D * DV : nullptr;
         const float *zin = p.z_in ? p.z_in + (size_t)head * D : nullptr;
@@ -281,21 +459,10 @@ __device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uin
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int b = grp * 16 + jj;
-                const float x = (Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f;
-                v[jj] = f2u(x);
+                v[jj] = f2u((Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f);
             }
             tmem_st16(tb + lb + kColR + grp * 16, v);
-            if (row < D) {
-                uint32_t pk[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) pk[m] = pack_bf16x2(u2f(v[2 * m]), u2f(v[2 * m + 1]));
-                const int b0 = grp * 16;
-                uint8_t *box = sRt + (b0 >> 6) * (D * 128);
-                *reinterpret_cast<uint4 *>(box + sw128_off(row, b0 & 63)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(box + sw128_off(row, (b0 & 63) + 8)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
+            if (row < D) export_row_bf16<D, DV>(sRt, row, grp, v);
         }
         const float zeta0 = (zin && row < D) ? zin[row] - zin[0] : 0.f;
         float u0 = 0.f, r0 = 0.f;
@@ -307,9 +474,11 @@ __device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uin
         const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
         tmem_st4(tb + lb + kColZ, zv);
         tmem_st4(tb + lb + kColUV, uv);
-        S.zeta[1][row] = zeta0;
+        S.zeta[row] = zeta0;
         S.u[1][row] = u0;
         S.r[1][row] = r0;
+        named_bar(kBarB, kWG);  // zero rows of zeta~ written before row 0 below
+        if (row < D) *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
         if (wtid == 0) {
             float rho0 = 0.f;
             if (zin)
@@ -320,197 +489,180 @@ __device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uin
         tmem_wait_st();
         fence_proxy_async();
         tc_fence_before();
-        named_bar(kBarWG, kWG);
+        named_bar(kBarB, kWG);
         mbar_arrive(&S.rt_ready);
+        mbar_arrive(&S.y_empty);
     }
 
-    bool aborted = false;
-    int last_c = -1;
-    for (int c = 0; c < nchunks && !aborted; ++c) {
-        const int s = c & 1, pb = (c + 1) & 1, cb = c & 1;
-        const int t0 = c * kC, L = min(kC, N - t0);
-        bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 30) &&
-                  wait_warp(&S.q_full, c & 1, g, 31);
-        float alpha = 0.f, den_inter = 0.f;
-        if (ok) {
-            // -- phi pass on K: psi(k) rounded to bf16 in place; beta_j = sum of the rounded row
-            uint8_t *kt = sK + s * Lay::kK;
-            float beta = 0.f;
+
+    // psi(k) in place (bf16), beta_j = sum of the rounded row, [1|beta] operand rows
+    auto phi_k = [&](int c) -> bool {
+        const int s = c & 1, cb = c & 1;
+        if (!wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50)) return false;
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 6);
+        uint8_t *kt = sK + s * Lay::kK;
+        float beta = 0.f;
+        // 8 chunks of 8 features per batch: all loads of a batch are issued
+        // before its in-place stores so their latencies overlap
 #pragma unroll
-            for (int f = 0; f < D / 8; ++f) {
-                uint8_t *pc = kt + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8);
-                uint4 raw = *reinterpret_cast<uint4 *>(pc);
-                uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        for (int f0 = 0; f0 < D / 8; f0 += 8) {
+            uint4 raw[8];
+#pragma unroll
+            for (int f = 0; f < 8; ++f)
+                raw[f] = *reinterpret_cast<const uint4 *>(
+                    kt + ((f0 + f) >> 3) * (kC * 128) + sw128_off(row, ((f0 + f) & 7) * 8));
+#pragma unroll
+            for (int f = 0; f < 8; ++f) {
+                uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const uint32_t pk = pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
                     beta += bf16_lo_f(pk) + bf16_hi_f(pk);
                     w[h] = pk;
                 }
-                *reinterpret_cast<uint4 *>(pc) = make_uint4(w[0], w[1], w[2], w[3]);
+                raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            S.beta[row] = beta;
-            {
-                const float bh = bf16_round(beta);
-                uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
-                *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
-                *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
-            }
-            const float bsum = warp_sum_f(beta);
-            if (lane == 0) S.rho_part[wq] = bsum;
-            // -- phi pass on Q: psi(q) rounded to bf16 -> TMEM (A operand); alpha_i, a_i . zeta_prev
-            const float *zp = S.zeta[pb];
-            float gam = 0.f;
 #pragma unroll
-            for (int grp = 0; grp < D / 32; ++grp) {
-                uint32_t v[16];
-#pragma unroll
-                for (int f4 = 0; f4 < 4; ++f4) {
-                    const int f = grp * 4 + f4;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(
-                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const uint32_t pk =
-                            pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
-                        const float a0 = bf16_lo_f(pk), a1 = bf16_hi_f(pk);
-                        alpha += a0 + a1;
-                        gam = fmaf(a0, zp[f * 8 + 2 * h], gam);
-                        gam = fmaf(a1, zp[f * 8 + 2 * h + 1], gam);
-                        v[f4 * 4 + h] = pk;
-                    }
-                }
-                tmem_st16(tb + lb + kColAq + grp * 16, v);
-            }
-            mbar_arrive(&S.q_empty);
-            den_inter = (dd + alpha) * S.n_s[pb] + S.rho_s[pb] + gam;
-            tmem_wait_st();
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(&S.phi_done);
+            for (int f = 0; f < 8; ++f)
+                *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
+                                           sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
         }
-        if (wg_barrier_any(!ok)) { aborted = true; break; }  // beta[] visible to all
+        S.beta[cb][row] = beta;
+        const float bh = bf16_round(beta);
+        uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
+        *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
+        *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
+        const float bsum = warp_sum_f(beta);
+        if (lane == 0) S.rho_part[cb][wq] = bsum;
+        fence_proxy_async();
+        mbar_arrive(&S.phik_done[s]);
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 7);
+        return true;
+    };
 
-        // -- weights: w_ij = d + alpha_i + beta_j + G_ij for j <= i, split into bf16 hi + lo
-        ok = wait_warp(&S.g_full, c & 1, g, 32);
-        float den = 0.f;
-        const float base_w = dd + alpha;
-        if (ok) {
-            tc_fence_after();
-            float rowsum = 0.f;
-#pragma unroll 1
-            for (int grp = 0; grp < kC / 16; ++grp) {
-                uint32_t gv[16], out[16];
-                tmem_ld16(tb + lb + kColG + grp * 16, gv);
-                tmem_wait_ld();
+    // state after block c: R -> bf16 operand, zeta -> zeta~, u, r, n, rho
+    auto export_state = [&](int c) -> bool {
+        const int cb = c & 1, pb = (c + 1) & 1;
+        const int L = min(kC, N - c * kC);
+        if (!wait_warp(&S.st_full, c & 1, g, 51)) return false;
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 4);
+        tc_fence_after();
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    const int j = grp * 16 + jj;
-                    const float w0 = (j <= row) ? base_w + S.beta[j] + u2f(gv[jj]) : 0.f;
-                    const float w1 = (j + 1 <= row) ? base_w + S.beta[j + 1] + u2f(gv[jj + 1]) : 0.f;
-                    const uint32_t hi = pack_bf16x2(w0, w1);
-                    const float h0 = bf16_lo_f(hi), h1 = bf16_hi_f(hi);
-                    const uint32_t lo = pack_bf16x2(w0 - h0, w1 - h1);
-                    rowsum += (h0 + bf16_lo_f(lo)) + (h1 + bf16_hi_f(lo));
-                    out[jj >> 1] = hi;
-                    out[8 + (jj >> 1)] = lo;
-                }
-                tmem_st16(tb + lb + kColG + grp * 16, out);
-            }
-            den = den_inter + rowsum;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&S.h_ready);
-        }
-
-        // -- state export for the next block: R -> bf16 operand, zeta, u, r, n, rho
-        ok = ok && wait_warp(&S.st_full, c & 1, g, 33);
-        if (ok) {
-            tc_fence_after();
-#pragma unroll
-            for (int grp = 0; grp < DV / 16; ++grp) {
-                uint32_t rv[16];
-                tmem_ld16(tb + lb + kColR + grp * 16, rv);
-                tmem_wait_ld();
-                if (row < D) {
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) pk[m] = pack_bf16x2(u2f(rv[2 * m]), u2f(rv[2 * m + 1]));
-                    const int b0 = grp * 16;
-                    uint8_t *box = sRt + (b0 >> 6) * (D * 128);
-                    *reinterpret_cast<uint4 *>(box + sw128_off(row, b0 & 63)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(box + sw128_off(row, (b0 & 63) + 8)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                }
-            }
-            uint32_t zv[4], uv[4];
-            tmem_ld4(tb + lb + kColZ, zv);
-            tmem_ld4(tb + lb + kColUV, uv);
+        for (int grp = 0; grp < DV / 16; grp += 2) {
+            uint32_t rv0[16], rv1[16];
+            tmem_ld16(tb + lb + kColR + grp * 16, rv0);
+            tmem_ld16(tb + lb + kColR + (grp + 1) * 16, rv1);
             tmem_wait_ld();
-            S.zeta[cb][row] = u2f(zv[0]);
-            S.u[cb][row] = u2f(uv[0]);
-            S.r[cb][row] = u2f(uv[1]) + u2f(uv[2]);
-            if (wtid == 0) {
-                S.n_s[cb] = S.n_s[pb] + (float)L;
-                S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[0] + S.rho_part[1]) +
-                                             (S.rho_part[2] + S.rho_part[3]));
+            if (row < D) {
+                export_row_bf16<D, DV>(sRt, row, grp, rv0);
+                export_row_bf16<D, DV>(sRt, row, grp + 1, rv1);
             }
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(&S.rt_ready);
         }
+        uint32_t zv[4], uv[4];
+        tmem_ld4(tb + lb + kColZ, zv);
+        tmem_ld4(tb + lb + kColUV, uv);
+        tmem_wait_ld();
+        if (row < D) {
+            S.zeta[row] = u2f(zv[0]);
+            *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
+                __float2bfloat16_rn(u2f(zv[0]));
+        }
+        S.u[cb][row] = u2f(uv[0]);
+        S.r[cb][row] = u2f(uv[1]) + u2f(uv[2]);
+        if (wtid == 0) {
+            S.n_s[cb] = S.n_s[pb] + (float)L;
+            S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[cb][0] + S.rho_part[cb][1]) +
+                                         (S.rho_part[cb][2] + S.rho_part[cb][3]));
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&S.rt_ready);
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 5);
+        return true;
+    };
 
-        // -- outputs: y = (Y + (d + alpha_i) u_prev + r_prev) / max(den, eps), TMA-stored
-        ok = ok && wait_warp(&S.y_full, c & 1, g, 34);
-        if (ok) {
-            tc_fence_after();
-            const float inv = 1.f / fmaxf(den, p.eps);
-            const float *up = S.u[pb], *rp = S.r[pb];
-            uint8_t *ybase = sY + (wq * 2) * Lay::kYst;
-#pragma unroll 1
-            for (int grp = 0; grp < DV / 16; ++grp) {
-                uint32_t yv[16];
-                tmem_ld16(tb + lb + kColY + grp * 16, yv);
-                tmem_wait_ld();
-                float o[16];
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int b = grp * 16 + jj;
-                    o[jj] = (u2f(yv[jj]) + fmaf(base_w, up[b], rp[b])) * inv;
-                }
-                uint8_t *yb = ybase + (grp & 1) * Lay::kYst;
-                // the store issued two groups ago (possibly in the previous block)
-                // read this buffer; wait until it has
-                if (lane == 0) bulk_wait_read<1>();
-                __syncwarp();
-                const float4 q0 = make_float4(o[0], o[1], o[2], o[3]);
-                const float4 q1 = make_float4(o[4], o[5], o[6], o[7]);
-                const float4 q2 = make_float4(o[8], o[9], o[10], o[11]);
-                const float4 q3 = make_float4(o[12], o[13], o[14], o[15]);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {  // rotate chunks across lanes: no bank conflicts
-                    const int qq = (q4 + (lane >> 1)) & 3;
-                    const float4 val = qq == 0 ? q0 : qq == 1 ? q1 : qq == 2 ? q2 : q3;
-                    *reinterpret_cast<float4 *>(yb + lane * 64 + qq * 16) = val;
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(ymap, yb, grp * 16, t0 + wq * 32, head);
-                    bulk_commit();
-                }
-            }
-            last_c = c;
+    // y = (Y + (d + alpha) u + r) / max((d + alpha) n + rho + a.zeta + rowsum, eps)
+    // Each thread first finishes the denominator of its own row; the values are
+    // then read back through the 16x256b TMEM shape, where 4 neighbouring lanes
+    // hold 8 consecutive columns of one row, so every warp store writes whole
+    // 32-byte sectors (8 rows x 32 bytes).
+    auto epilogue = [&](int c) -> bool {
+        const int cb = c & 1, pb = (c + 1) & 1, t0 = c * kC;
+        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
+            return false;
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 8);
+        tc_fence_after();
+        uint32_t yz[4];
+        tmem_ld4(tb + lb + kColYz, yz);
+        tmem_wait_ld();
+        {
+            const float base_w = dd + S.alpha[cb][row];
+            const float den =
+                fmaf(base_w, S.n_s[pb], S.rho_s[pb]) + u2f(yz[0]) + S.rowsum[cb][row];
+            S.e_inv[row] = 1.f / fmaxf(den, p.eps);
+            S.e_base[row] = base_w;
         }
-        if (wg_barrier_any(!ok)) aborted = true;  // small state buffers safe to reuse
+        __syncwarp();
+        const float *up = S.u[pb], *rp = S.r[pb];
+        float *ychunk = p.y + ((size_t)head * N + t0) * DV;
+        const int tq = lane >> 2, tc = (lane & 3) * 2;
+        constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
+        uint32_t v[2][32];
+        tmem_ld_16x256b_x8(tb + ((uint32_t)(wq * 32) << 16) + kColY, v[0]);
+#pragma unroll
+        for (int part = 0; part < kParts; ++part) {
+            const int half = part & 1, cblk = part >> 1;
+            tmem_wait_ld();
+            if (part + 1 < kParts) {
+                const int h2 = (part + 1) & 1, c2 = (part + 1) >> 1;
+                tmem_ld_16x256b_x8(tb + ((uint32_t)(wq * 32 + 16 * h2) << 16) + kColY + c2 * 64,
+                                   v[(part + 1) & 1]);
+            }
+            const uint32_t *vc = v[part & 1];
+            const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
+            const float invA = S.e_inv[rA], baseA = S.e_base[rA];
+            const float invB = S.e_inv[rB], baseB = S.e_base[rB];
+            const bool okA = t0 + rA < N, okB = t0 + rB < N;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int col = cblk * 64 + 8 * k + tc;
+                const float2 uu = *reinterpret_cast<const float2 *>(up + col);
+                const float2 rr = *reinterpret_cast<const float2 *>(rp + col);
+                const float2 oA = make_float2((u2f(vc[4 * k]) + fmaf(baseA, uu.x, rr.x)) * invA,
+                                              (u2f(vc[4 * k + 1]) + fmaf(baseA, uu.y, rr.y)) * invA);
+                const float2 oB = make_float2((u2f(vc[4 * k + 2]) + fmaf(baseB, uu.x, rr.x)) * invB,
+                                              (u2f(vc[4 * k + 3]) + fmaf(baseB, uu.y, rr.y)) * invB);
+                if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
+                if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&S.y_empty);
+        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 9);
+        return true;
+    };
+
+    // Software pipeline, psi(k) two blocks ahead: iteration c runs the outputs
+    // of block c, psi(k) of block c+2 and the state export after block c+1, so
+    // the tensor core updates the state for block c+1 while psi(k) runs.
+    bool ok0 = phi_k(0);
+    if (ok0 && nchunks > 1) ok0 = phi_k(1);
+    bool aborted = group_any<kBarB>(!ok0);
+    if (!aborted) aborted = group_any<kBarB>(!export_state(0));
+    int last_c = -1;
+    for (int c = 0; c < nchunks && !aborted; ++c) {
+        bool ok = epilogue(c);
+        if (ok && c + 2 < nchunks) ok = phi_k(c + 2);
+        // the export below overwrites the state buffers the outputs above read
+        if (group_any<kBarB>(!ok)) { aborted = true; break; }
+        if (c + 1 < nchunks) ok = export_state(c + 1);
+        if (ok) last_c = c;
+        if (group_any<kBarB>(!ok)) aborted = true;
     }
-    if (lane == 0) bulk_wait<0>();
 
     // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
     if (!aborted && last_c == nchunks - 1 && p.S_out) {
-        const int lb_ = last_c & 1;
+        const int lbuf = last_c & 1;
         tc_fence_after();
 #pragma unroll
         for (int grp = 0; grp < DV / 16; ++grp) {
@@ -522,13 +674,13 @@ __device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uin
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 4)
                     *reinterpret_cast<float4 *>(dst + jj) = make_float4(
-                        u2f(rv[jj]) + S.u[lb_][grp * 16 + jj],
-                        u2f(rv[jj + 1]) + S.u[lb_][grp * 16 + jj + 1],
-                        u2f(rv[jj + 2]) + S.u[lb_][grp * 16 + jj + 2],
-                        u2f(rv[jj + 3]) + S.u[lb_][grp * 16 + jj + 3]);
+                        u2f(rv[jj]) + S.u[lbuf][grp * 16 + jj],
+                        u2f(rv[jj + 1]) + S.u[lbuf][grp * 16 + jj + 1],
+                        u2f(rv[jj + 2]) + S.u[lbuf][grp * 16 + jj + 2],
+                        u2f(rv[jj + 3]) + S.u[lbuf][grp * 16 + jj + 3]);
             }
         }
-        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lb_] + S.zeta[lb_][row];
+        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];
     }
 }
 
@@ -536,7 +688,7 @@ __device__ __forceinline__ void row_role(Small &S, uint32_t tb, uint8_t *sQ, uin
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap ymap,
+                 const __grid_constant__ CUtensorMap vmap,
                  const TcParams p)
 {
     using Lay = Layout<D, DV>;
@@ -545,8 +697,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                                               ~static_cast<uintptr_t>(1023));
     Small &S = *reinterpret_cast<Small *>(sm + Lay::oSmall);
     uint8_t *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
-    uint8_t *sRt = sm + Lay::oRt, *sUVB = sm + Lay::oUVB, *sY = sm + Lay::oY;
-    __shared__ uint64_t drain_bar;
+    uint8_t *sRt = sm + Lay::oRt, *sUVB = sm + Lay::oUVB, *sZt = sm + Lay::oZt;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int head = blockIdx.x;
@@ -561,18 +712,22 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
             mbar_init(&S.kv_full[s], 1);
             mbar_init(&S.kv_empty[s], 1);
         }
-        mbar_init(&S.phi_done, kWG);
+        mbar_init(&S.phiq_done, kWG);
+        mbar_init(&S.phik_done[0], kWG);
+        mbar_init(&S.phik_done[1], kWG);
         mbar_init(&S.g_full, 1);
-        mbar_init(&S.h_ready, kWG);
-        mbar_init(&S.y_full, 1);
+        mbar_init(&S.aq_free, 1);
+        mbar_init(&S.h_ready[0], kWG);
+        mbar_init(&S.h_ready[1], kWG);
         mbar_init(&S.st_full, 1);
         mbar_init(&S.rt_ready, kWG);
-        mbar_init(&drain_bar, 1);
+        mbar_init(&S.y_full, 1);
+        mbar_init(&S.y_empty, kWG);
+        mbar_init(&S.drain, 1);
         fence_mbar_init();
         prefetch_tmap(&qmap);
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
-        prefetch_tmap(&ymap);
     }
     if (warp == 1) {
         tmem_alloc(&S.tmem_base, kTmemCols);
@@ -586,9 +741,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (warp == 0) {
         if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, nchunks, g);
     } else if (warp == 1) {
-        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, &drain_bar, nchunks, g);
+        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, nchunks, g);
+    } else if (warp >= kWarpA && warp < kWarpB) {
+        group_a_role<D, DV>(S, tb, sQ, nchunks, g);
     } else {
-        row_role<D, DV>(S, tb, sQ, sK, sV, sRt, sUVB, sY, &ymap, p, head, nchunks, g);
+        group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, p, head, nchunks, g);
     }
     tc_fence_before();
     __syncthreads();
@@ -635,18 +792,17 @@ bool encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz
 template <int D, int DV>
 cudaError_t launch_dv(const FwdArgs &a) {
     using Lay = Layout<D, DV>;
-    CUtensorMap qm, km, vm, ym;
+    CUtensorMap qm, km, vm;
     const int BH = a.BH();
     if (!encode_3d(&qm, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&km, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&vm, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.N, BH, 64, kC,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&ym, a.y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, DV, a.N, BH, 16, 32,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     TcParams p{};
+    p.y = a.y;
     p.N = a.N;
     p.BH = BH;
     p.eps = a.eps;
@@ -663,7 +819,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::request);
     if (e != cudaSuccess) return e;
-    kern<<<BH, kThreads, Lay::request, a.stream>>>(qm, km, vm, ym, p);
+    kern<<<BH, kThreads, Lay::request, a.stream>>>(qm, km, vm, p);
     return cudaGetLastError();
 }
 
@@ -684,3 +840,10 @@ cudaError_t launch_causal_tc(const FwdArgs &a) {
 }
 
 }  // namespace la
+
+#ifdef LA_TRACE
+extern "C" LA_API void la_trace_fetch(unsigned long long *dst) {
+    cudaDeviceSynchronize();
+    cudaMemcpyFromSymbol(dst, la_trace_buf, sizeof(unsigned long long) * 256 * 16);
+}
+#endif

@@ -131,10 +131,13 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
 
 
 def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_state=False,
-                   out=None, S_out=None, z_out=None, workspace=None, stream=None):
+                   out=None, S_out=None, z_out=None, workspace=None, stream=None,
+                   check_status=False):
     """Causal elu+1 linear attention.  q, k: [B,H,N,d]; v: [B,H,N,dv] (bf16 or fp32).
 
     Returns y [B,H,N,dv] float32 (and the final (S, z) when ``return_state``).
+    With ``check_status`` the call synchronises and raises if a kernel recorded
+    a run-time error (a bounded wait that ran out) in the workspace.
     """
     _check_cuda(q, k, v, S_in, z_in, out, S_out, z_out, workspace)
     B, H, N, d = q.shape
@@ -154,6 +157,10 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
                                  float(eps), _ptr(S_in), _ptr(z_in), _ptr(S_out), _ptr(z_out),
                                  _ptr(workspace), wbytes, _stream_handle(stream, q.device))
     _raise(st, "la_forward_causal")
+    if check_status and workspace is not None:
+        err, where = workspace_header(workspace)
+        if err != LA_OK:
+            raise LinAttnError(err, f"la_forward_causal (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
 
 
@@ -205,6 +212,13 @@ def workspace_status(workspace, stream=None) -> int:
     return int(lib().la_workspace_status(_ptr(workspace),
                                          workspace.numel() * workspace.element_size(),
                                          _stream_handle(stream, workspace.device)))
+
+
+def workspace_header(workspace) -> tuple[int, int]:
+    """(error word, diagnostic word) recorded in a workspace header (synchronises)."""
+    torch.cuda.synchronize(workspace.device)
+    h = workspace[:8].cpu().view(torch.int32)
+    return int(h[0]), int(h[1])
 
 
 def set_scan_fault(skip_publish_segment: int = -1, wait_limit_ns: int = 0) -> None:

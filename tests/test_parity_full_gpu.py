@@ -34,7 +34,7 @@ def test_causal_workload(name, nsample, cuda_device):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
     y, S, z = la.forward_causal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
-                                eps=w.eps, return_state=True)
+                                eps=w.eps, return_state=True, check_status=True)
     torch.cuda.synchronize()
     hs = _heads(w.BH, nsample)
     yo, So, zo = oracle.causal_recurrent(_flat(q)[hs], _flat(k)[hs], _flat(v)[hs], eps=w.eps,
@@ -66,7 +66,7 @@ def test_decode_workload(cuda_device):
     hs = _heads(w.BH, 16)
     idx = torch.tensor(hs, device=cuda_device)
     q, k, v = make_qkv(w, device=cuda_device, gen_device=cuda_device)
-    _, S, z = la.forward_causal(q, k, v, eps=w.eps, return_state=True)
+    _, S, z = la.forward_causal(q, k, v, eps=w.eps, return_state=True, check_status=True)
     qh, kh, vh = (_flat(t).index_select(0, idx).cpu() for t in (q, k, v))
     del q, k, v
     torch.cuda.synchronize()

@@ -39,7 +39,7 @@ def test_causal_matches_oracle(case, cuda_device):
     B, H, N, d, dv, dt, s = case
     q, k, v = random_qkv(B, H, N, d, dv, dtype=dt, scale=s, seed=N)
     y, S, z = la.forward_causal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
-                                return_state=True)
+                                return_state=True, check_status=True)
     torch.cuda.synchronize()
     yo, So, zo = oracle.causal_recurrent(q, k, v, return_state=True)
     tol = tol_for(dt)
@@ -90,7 +90,7 @@ def test_causal_initial_state_and_split(dt, cuda_device):
     B, H, N1, N2, d, dv = 1, 3, 301, 259, 64, 64
     q, k, v = random_qkv(B, H, N1 + N2, d, dv, dtype=dt, scale=0.3, seed=21)
     qd, kd, vd = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device)
-    y_full, S_full, z_full = la.forward_causal(qd, kd, vd, return_state=True)
+    y_full, S_full, z_full = la.forward_causal(qd, kd, vd, return_state=True, check_status=True)
     _, S1, z1 = la.forward_causal(qd[:, :, :N1].contiguous(), kd[:, :, :N1].contiguous(),
                                   vd[:, :, :N1].contiguous(), return_state=True)
     y2, S2, z2 = la.forward_causal(qd[:, :, N1:].contiguous(), kd[:, :, N1:].contiguous(),
@@ -127,7 +127,7 @@ def test_causal_edge_lengths(N, cuda_device):
     z_in = torch.rand(B, H, d, generator=torch.Generator().manual_seed(N + 1)) * 3 + 1
     y, S, z = la.forward_causal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
                                 S_in=S_in.to(cuda_device), z_in=z_in.to(cuda_device),
-                                return_state=True)
+                                return_state=True, check_status=True)
     torch.cuda.synchronize()
     yo, So, zo = oracle.causal_recurrent(q, k, v, S_in=S_in, z_in=z_in, return_state=True)
     assert y.shape == (B, H, N, dv)
@@ -155,7 +155,7 @@ def test_outputs_stay_in_bounds(cuda_device):
     y = ybuf[: B * H * N * dv].view(B, H, N, dv)
     S = Sbuf[: B * H * d * dv].view(B, H, d, dv)
     z = zbuf[: B * H * d].view(B, H, d)
-    la.forward_causal(q, k, v, out=y, S_out=S, z_out=z, return_state=True)
+    la.forward_causal(q, k, v, out=y, S_out=S, z_out=z, return_state=True, check_status=True)
     la.forward_noncausal(q, k, v, out=y, S_out=S, z_out=z, return_state=True)
     torch.cuda.synchronize()
     for buf in (ybuf, Sbuf, zbuf):
@@ -165,8 +165,8 @@ def test_outputs_stay_in_bounds(cuda_device):
 def test_runs_are_bitwise_deterministic(cuda_device):
     q, k, v = (t.to(cuda_device) for t in random_qkv(2, 4, 1500, 128, 128,
                                                      dtype=torch.bfloat16, scale=0.09, seed=9))
-    a = la.forward_causal(q, k, v, return_state=True)
-    b = la.forward_causal(q, k, v, return_state=True)
+    a = la.forward_causal(q, k, v, return_state=True, check_status=True)
+    b = la.forward_causal(q, k, v, return_state=True, check_status=True)
     c = la.forward_noncausal(q, k, v, return_state=True)
     d = la.forward_noncausal(q, k, v, return_state=True)
     torch.cuda.synchronize()

@@ -134,6 +134,31 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v, flo
                          float eps, void *stream);
 
 /*
+ * Non-causal forward that allocates nothing and takes no workspace.  The
+ * pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory themselves, such as an operator or plugin
+ * inside another framework that is handed only its input and output buffers,
+ * or a latency-critical path that must not call cudaMalloc (which can
+ * synchronise the whole device).  It computes exactly what
+ * la_forward_noncausal computes, with the same arguments minus the workspace.
+ *
+ * Scratch: a fixed array of LA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, resident on every GPU that loads the library until the process
+ * exits.  Sizes whose scratch (la_noncausal_workspace_bytes) exceeds it are
+ * rejected with LA_ERR_WORKSPACE before anything is launched.  The first call
+ * on each device looks up the array's device address (a host-side runtime
+ * call); make that first call before any stream capture begins.  All calls
+ * share the array and leave their partial sums in it: calls that can overlap
+ * on the GPU (different streams, different host threads) race and must be
+ * ordered by the caller.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+LA_API la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v,
+                                              float *y, int B, int H, int N, int d, int dv,
+                                              la_dtype dt, float eps, float *S_out, float *z_out,
+                                              void *stream);
+
+/*
  * Synchronise `stream` and report the run-time status recorded in a
  * workspace by the last call that used it: LA_OK, or LA_ERR_TIMEOUT when one
  * of its bounded waits ran out (its outputs are then undefined).  The next

@@ -322,18 +322,20 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         float alpha = 0.f;
         if (ok) {
             tc_fence_after();   // the MMAs that read the previous psi(q) have completed
-            uint4 raw[D / 8];
-#pragma unroll
-            for (int f = 0; f < D / 8; ++f)
-                raw[f] = *reinterpret_cast<const uint4 *>(
-                    sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
-#pragma unroll
+            // a real loop over 32-feature groups keeps the hot code small
+#pragma unroll 1
             for (int grp = 0; grp < D / 32; ++grp) {   // 32 features -> 16 TMEM columns
+                uint4 raw[4];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const int f = grp * 4 + f4;
+                    raw[f4] = *reinterpret_cast<const uint4 *>(
+                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
+                }
                 uint32_t v[16];
 #pragma unroll
                 for (int f4 = 0; f4 < 4; ++f4) {
-                    const uint4 r4 = raw[grp * 4 + f4];
-                    const uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+                    const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const uint32_t pk =
@@ -362,18 +364,13 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             // groups entirely above this warp's rows are all zero (causal mask);
             // the TMEM load of the next group is issued before this group's math
             const int last_grp = (wq * 32 + 31) >> 4;
-            uint32_t gv[2][16];
-            tmem_ld16(tb + lb + kColG, gv[0]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int grp = 0; grp < kC / 16; ++grp) {
+            // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
+            auto weights = [&](int grp, const uint32_t (&gc)[16]) {
                 uint32_t out[16];
-                if (grp + 1 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 1) * 16, gv[(grp + 1) & 1]);
                 if (grp > last_grp) {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) out[m] = 0u;
                 } else {
-                    const uint32_t *gc = gv[grp & 1];
                     const float4 b0 = *reinterpret_cast<const float4 *>(beta + grp * 16);
                     const float4 b1 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 4);
                     const float4 b2 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 8);
@@ -394,7 +391,20 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                     }
                 }
                 tmem_st16(tb + lb + kColG + grp * 16, out);
+            };
+            // two groups per loop trip (ping-pong buffers): the TMEM load of the
+            // next group overlaps this group's math, and the hot code stays small
+            uint32_t gA[16], gB[16];
+            tmem_ld16(tb + lb + kColG, gA);
+            tmem_wait_ld();
+#pragma unroll 1
+            for (int grp = 0; grp < kC / 16; grp += 2) {
+                if (grp + 1 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 1) * 16, gB);
+                weights(grp, gA);
                 if (grp + 1 <= last_grp) tmem_wait_ld();
+                if (grp + 2 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 2) * 16, gA);
+                weights(grp + 1, gB);
+                if (grp + 2 <= last_grp) tmem_wait_ld();
             }
             S.rowsum[cb][row] = rowsum;
             tmem_wait_st();
@@ -504,7 +514,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         float beta = 0.f;
         // 8 chunks of 8 features per batch: all loads of a batch are issued
         // before its in-place stores so their latencies overlap
-#pragma unroll
+#pragma unroll 1
         for (int f0 = 0; f0 < D / 8; f0 += 8) {
             uint4 raw[8];
 #pragma unroll
@@ -607,18 +617,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         float *ychunk = p.y + ((size_t)head * N + t0) * DV;
         const int tq = lane >> 2, tc = (lane & 3) * 2;
         constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
-        uint32_t v[2][32];
-        tmem_ld_16x256b_x8(tb + ((uint32_t)(wq * 32) << 16) + kColY, v[0]);
-#pragma unroll
-        for (int part = 0; part < kParts; ++part) {
+        auto part_addr = [&](int part) {
+            return tb + ((uint32_t)(wq * 32 + 16 * (part & 1)) << 16) + kColY + (part >> 1) * 64;
+        };
+        auto outputs = [&](int part, const uint32_t (&vc)[32]) {
             const int half = part & 1, cblk = part >> 1;
-            tmem_wait_ld();
-            if (part + 1 < kParts) {
-                const int h2 = (part + 1) & 1, c2 = (part + 1) >> 1;
-                tmem_ld_16x256b_x8(tb + ((uint32_t)(wq * 32 + 16 * h2) << 16) + kColY + c2 * 64,
-                                   v[(part + 1) & 1]);
-            }
-            const uint32_t *vc = v[part & 1];
             const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
             const float invA = S.e_inv[rA], baseA = S.e_base[rA];
             const float invB = S.e_inv[rB], baseB = S.e_base[rB];
@@ -635,6 +638,18 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
                 if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
             }
+        };
+        uint32_t vA[32], vB[32];
+        tmem_ld_16x256b_x8(part_addr(0), vA);
+        tmem_wait_ld();
+#pragma unroll 1
+        for (int part = 0; part < kParts; part += 2) {
+            tmem_ld_16x256b_x8(part_addr(part + 1), vB);   // kParts is even
+            outputs(part, vA);
+            tmem_wait_ld();
+            if (part + 2 < kParts) tmem_ld_16x256b_x8(part_addr(part + 2), vA);
+            outputs(part + 1, vB);
+            if (part + 2 < kParts) tmem_wait_ld();
         }
         tc_fence_before();
         mbar_arrive(&S.y_empty);

@@ -85,10 +85,13 @@ LA_API const char *la_version(void);
 
 /*
  * Workspace size in bytes for la_forward_causal with these sizes (0 when the
- * chosen kernels need none).  The workspace holds the per-segment states of
- * the sequence-axis prefix scan ("Entrenamiento: forma paralela": prefix
- * sums over blocks) plus a small header; it must be device memory, 256-byte
- * aligned, and may be reused by later calls on the same stream.
+ * chosen kernels need none).  The workspace holds a small header (run-time
+ * status) and, when the heads alone cannot fill the GPU, the per-segment
+ * states and their prefixes for the sequence-axis split ("Entrenamiento:
+ * forma paralela": cumulative sums by a prefix scan).  The split depends on
+ * the current device's SM count, so query with the device current that will
+ * run the call.  It must be device memory, 256-byte aligned, and may be
+ * reused by later calls on the same stream.
  */
 LA_API size_t la_causal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt);
 

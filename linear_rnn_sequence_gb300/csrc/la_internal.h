@@ -60,6 +60,7 @@ cudaError_t launch_noncausal_simt(const FwdArgs &a);
 // tcgen05 / TMA path (bf16 inputs, d and dv in {64, 128}).
 bool causal_tc_supported(const FwdArgs &a);
 size_t causal_tc_workspace(int BH, int N, int d, int dv);
+int causal_tc_launches(int BH, int N);   // kernels one causal call launches
 cudaError_t launch_causal_tc(const FwdArgs &a);
 
 }  // namespace la

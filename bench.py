@@ -299,10 +299,15 @@ def path_dtype(w):
 
 
 def launches_per_call(mode, w):
-    """Kernels of ours that one call launches (the launch list under ncu agrees)."""
+    """Kernels of ours that one call launches (the launch list under ncu agrees).
+
+    A causal call launches one kernel, or three (segment states, their prefix
+    scan, the chunk kernel) when the workspace holds segment states, i.e. when
+    it is larger than its 256-byte header.
+    """
     from linear_rnn_sequence_gb300 import linattn as la
     if mode == "causal":
-        return 1
+        return 3 if la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 256 else 1
     if mode == "noncausal":
         return 2
     return 1

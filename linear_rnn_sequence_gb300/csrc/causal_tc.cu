@@ -727,6 +727,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int nloc = min(p.N - tok0, p.seg_chunks * kC);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
+    if (tid == 0) LA_TRACE_POINT(0, 15);
 
     if (tid == 0) {
         S.abort_flag = 0;
@@ -991,8 +992,11 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 }
 
 // Exclusive prefix over the segments of each head, in a fixed order:
-// P_0 = S_in (or 0), P_s = P_{s-1} + S_{s-1}; the same for z.
-__global__ void __launch_bounds__(256)
+// P_0 = S_in (or 0), P_s = P_{s-1} + S_{s-1}; the same for z.  One thread per
+// state element (grid: heads x element blocks); the segment loop issues its
+// loads ahead of the running sum.
+constexpr int kScanThreads = 128;
+__global__ void __launch_bounds__(kScanThreads)
 scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_seg,
                    float *__restrict__ S_pre, float *__restrict__ z_pre,
                    const float *__restrict__ S_in, const float *__restrict__ z_in, int nseg,
@@ -1000,20 +1004,29 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
 {
     const int head = blockIdx.x;
     const int nS = D * DV;
-    for (int e = threadIdx.x; e < nS + D; e += blockDim.x) {
-        const bool isS = e < nS;
-        const int o = isS ? e : e - nS;
-        const float *src = isS ? S_seg : z_seg;
-        float *dst = isS ? S_pre : z_pre;
-        const int stride = isS ? nS : D;
-        float acc = 0.f;
-        if (isS && S_in) acc = S_in[(size_t)head * nS + o];
-        if (!isS && z_in) acc = z_in[(size_t)head * D + o];
-        for (int sg = 0; sg < nseg; ++sg) {
-            const size_t idx = ((size_t)head * nseg + sg) * stride + o;
-            dst[idx] = acc;
-            acc += src[idx];
-        }
+    const int e = blockIdx.y * kScanThreads + threadIdx.x;
+    if (e >= nS + D) return;
+    const bool isS = e < nS;
+    const int o = isS ? e : e - nS;
+    const float *src = isS ? S_seg : z_seg;
+    float *dst = isS ? S_pre : z_pre;
+    const size_t stride = isS ? (size_t)nS : (size_t)D;
+    float acc = 0.f;
+    if (isS && S_in) acc = S_in[(size_t)head * nS + o];
+    if (!isS && z_in) acc = z_in[(size_t)head * D + o];
+    const size_t base = (size_t)head * nseg * stride + o;
+    int sg = 0;
+    for (; sg + 4 <= nseg; sg += 4) {
+        const float s0 = src[base + (sg + 0) * stride], s1 = src[base + (sg + 1) * stride];
+        const float s2 = src[base + (sg + 2) * stride], s3 = src[base + (sg + 3) * stride];
+        dst[base + (sg + 0) * stride] = acc; acc += s0;
+        dst[base + (sg + 1) * stride] = acc; acc += s1;
+        dst[base + (sg + 2) * stride] = acc; acc += s2;
+        dst[base + (sg + 3) * stride] = acc; acc += s3;
+    }
+    for (; sg < nseg; ++sg) {
+        dst[base + sg * stride] = acc;
+        acc += src[base + sg * stride];
     }
 }
 
@@ -1123,8 +1136,9 @@ cudaError_t launch_dv(const FwdArgs &a) {
         if (e != cudaSuccess) return e;
         skern<<<items, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg, z_seg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        scan_states_kernel<<<BH, 256, 0, a.stream>>>(S_seg, z_seg, S_pre, z_pre, a.S_in, a.z_in,
-                                                     p.nseg, D, DV);
+        const dim3 sgrid(BH, (D * DV + D + kScanThreads - 1) / kScanThreads);
+        scan_states_kernel<<<sgrid, kScanThreads, 0, a.stream>>>(S_seg, z_seg, S_pre, z_pre,
+                                                                a.S_in, a.z_in, p.nseg, D, DV);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         p.S_in = S_pre;
         p.z_in = z_pre;

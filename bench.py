@@ -119,7 +119,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.idx, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -164,17 +164,24 @@ def flush_l2(buf):
     buf.zero_()
 
 
-def time_steps(fn, steps, warmup, world, flush=None):
+def time_steps(fn, steps, warmup, world, flush=None, min_warm_s=0.0):
     """Run `warmup` untimed steps, then exactly `steps` timed steps.
 
+    Warm-up continues (untimed) until at least `min_warm_s` seconds have
+    passed, so that clock samples taken alongside see the GPU under load.
     Returns (total_ms (max over ranks), per-step kernel ms list from events on
     the launching stream).  If `flush` is given it runs between timed steps,
     outside the per-step event pairs.
     """
     stream = torch.cuda.current_stream()
+    t_warm = time.perf_counter()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    while time.perf_counter() - t_warm < min_warm_s:
+        for _ in range(8):
+            fn()
+        torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     barrier(world)
@@ -252,8 +259,10 @@ def run_ours(args, world, rank, local):
     def step():
         la.forward_causal(q, k, v, eps=w.eps, out=y, workspace=ws)
 
+    # clocks: sampled every 50 ms from the start of the (load-keeping) warm-up
+    # through the timed steps
     with ClockSampler(local) as clk:
-        total_ms, per = time_steps(step, args.steps, args.warmup, world)
+        total_ms, per = time_steps(step, args.steps, args.warmup, world, min_warm_s=0.6)
     clocks = clk.summary()
     T = w.B * w.H * w.N
     tokens = w.B * w.N
@@ -455,6 +464,52 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_case(args):
+    """A few launches of one kernel on one workload, for ncu captures.
+
+    --profile-case causal|long|noncausal|decode picks the workload
+    (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 / B256 H32 d128
+    decode); --batch overrides B for a smaller capture.
+    """
+    from linear_rnn_sequence_gb300 import linattn as la
+    names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
+             "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128"}
+    w = WORKLOADS[names[args.profile_case]]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if w.mode == "decode":
+        g = torch.Generator(device=dev).manual_seed(w.seed + 1)
+        sc = torch.tensor(w.step_scale, device=dev)
+        S = torch.randn(w.B, w.H, w.d, w.dv, generator=g, device=dev)
+        z = torch.rand(w.B, w.H, w.d, generator=g, device=dev) * 1000 + 1
+        q, k = ((torch.randn(w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype) for _ in range(2))
+        v = (torch.randn(w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
+        y = torch.empty(w.B, w.H, w.dv, device=dev)
+        fn = lambda: la.decode_step(q, k, v, S, z, eps=w.eps, out=y)
+    else:
+        q, k, v = make_qkv(w, device=dev, gen_device=dev)
+        y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+        if w.mode == "noncausal":
+            ws = la.alloc_workspace(la.noncausal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv), dev)
+            fn = lambda: la.forward_noncausal(q, k, v, eps=w.eps, out=y, workspace=ws)
+        else:
+            ws = la.alloc_workspace(la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+            fn = lambda: la.forward_causal(q, k, v, eps=w.eps, out=y, workspace=ws)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "B": w.B, "H": w.H, "N": w.N,
+                      "d": w.d, "dv": w.dv, "ms_per_call": e0.elapsed_time(e1) / 3}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,8 +519,13 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode"])
+    ap.add_argument("--batch", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))

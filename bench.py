@@ -318,7 +318,10 @@ def launches_per_call(mode, w):
     if mode == "causal":
         return 3 if la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 256 else 1
     if mode == "noncausal":
-        return 2
+        # tensor-core path (bf16, d and dv in {64, 128}): segment states, their
+        # per-head sum, the query kernel; otherwise two CUDA-core kernels
+        tc = w.dtype == torch.bfloat16 and w.d in (64, 128) and w.dv in (64, 128)
+        return 3 if tc else 2
     return 1
 
 

@@ -96,8 +96,10 @@ size_t la_causal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt
 }
 
 size_t la_noncausal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
-    (void)dt;
     if (B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    FwdArgs a{};
+    a.B = B; a.H = H; a.N = N; a.d = d; a.dv = dv; a.dt = dt;
+    if (noncausal_tc_supported(a)) return noncausal_tc_workspace(B * H, N, d, dv);
     return noncausal_simt_workspace(B * H, N, d, dv);
 }
 
@@ -155,8 +157,12 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, floa
         return LA_ERR_INVALID_ARG;
     const size_t need = la_noncausal_workspace_bytes(B, H, N, d, dv, dt);
     if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // a fresh run-time status for every call
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
     FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, nullptr, nullptr, S_out, z_out,
-              workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+              workspace, workspace_bytes, s};
+    if (noncausal_tc_supported(a)) return from_cuda(launch_noncausal_tc(a));
     return from_cuda(launch_noncausal_simt(a));
 }
 

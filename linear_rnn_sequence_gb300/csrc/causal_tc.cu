@@ -48,7 +48,8 @@
 #include <mutex>
 
 #include "la_internal.h"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
+#include "tc_state.cuh"
 
 // Optional per-block timeline of CTA 0 (SM cycle counter) for performance
 // work; compiled in only with -DLA_TRACE, and then read with la_trace_fetch.
@@ -69,12 +70,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 128;          // tokens per block (MMA M)
 constexpr int kThreads = 320;    // 10 warps
 constexpr int kWarpA = 2;        // first warp of group A
 constexpr int kWarpB = 6;        // first warp of group B
-constexpr int kWG = 128;         // threads per group
-constexpr int kBarA = 1, kBarB = 2;  // named barrier ids
 
 constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 448,
                    kColZ = 464, kColUV = 480;
@@ -126,75 +124,6 @@ static_assert(offsetof(Small, beta) % 16 == 0 && offsetof(Small, u) % 16 == 0 &&
                   offsetof(Small, r) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
               "vector loads and mbarriers need aligned fields");
 static_assert(sizeof(Small) <= 7 * 1024, "small area");
-
-struct TcParams {
-    float *y;
-    int N, BH;
-    int nseg;                      // segments per head (work items = BH * nseg)
-    int seg_chunks;                // blocks per segment (the last one may be shorter)
-    float eps;
-    const float *S_in, *z_in;
-    float *S_out, *z_out;
-    unsigned int *err;             // workspace header error word
-    unsigned int *err_where;
-    unsigned long long limit_ns;
-};
-
-// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
-// lanes with inputs of either sign stay converged: for x > 0 the exponential
-// of 0 is exactly 1 and the second term vanishes.  e^x = 2^(x log2 e) with the
-// flush-to-zero form (x <= 0 here, so a flushed result only means e^x < 2^-126).
-__device__ __forceinline__ float psi_f(float x) {
-    return fmaxf(x, 0.f) + (ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
-}
-__device__ __forceinline__ float bf16_round(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
-}
-
-// Byte offset of element (row, col) in a [rows x 64] bf16 box with 128-byte
-// swizzle, the layout TMA writes (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
-    return (uint32_t)row * 128u + ((((uint32_t)col >> 3) ^ ((uint32_t)row & 7u)) << 4) +
-           (((uint32_t)col & 7u) << 1);
-}
-
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
-__device__ __forceinline__ float warp_sum_f(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, const Guard &g,
-                                          unsigned int where) {
-    const bool ok = mbar_wait(bar, parity, g, where);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used only while unwinding after an abort: ignores the abort flag but
-// still gives up after the time limit.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > limit_ns) break;
-}
-
-// Group barrier that also agrees on "someone gave up": returns true if any of
-// the group's 128 threads passes failed = true.
-template <int BAR>
-__device__ __forceinline__ bool group_any(bool failed) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)failed), "n"(BAR), "n"(kWG)
-        : "memory");
-    return r != 0;
-}
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -781,216 +710,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     }
 }
 
-// ------------------------------------------------------------------ segment states
-// For long sequences with few heads the sequence axis is split into segments
-// ("Linear Attention/es", "Entrenamiento: forma paralela": the cumulative sums
-// can be formed with a prefix scan).  Three launches, with no waits between
-// CTAs:
-//   1. causal_state_kernel: per (head, segment), the segment's own state
-//      S_s = sum phi(k_j) v_j^T, z_s = sum phi(k_j) from K and V (tensor cores);
-//   2. scan_states_kernel: per head, exclusive prefixes P_s = S_in + sum_{s'<s} S_s';
-//   3. causal_tc_kernel: every (head, segment) runs from its prefix.
-// The state pass reuses the split form of the main kernel: R = psi(K)^T V,
-// zeta = psi(K)^T 1 and u = V^T 1 accumulate in TMEM, and the plain state is
-// S = 1 u^T + R, z = n 1 + zeta.
-constexpr int kStateThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 psi(k) / export
-constexpr uint32_t kStColR = 0, kStColZ = 128, kStColU = 144, kStTmemCols = 256;
-
-template <int D, int DV>
-struct StateLayout {
-    static constexpr int kK = kC * D * 2;
-    static constexpr int kV = kC * DV * 2;
-    static constexpr int kOnes = 16 * kC * 2;      // [16 x C] operand, row 0 = ones
-    static constexpr int oK = 0;                   // 2 stages
-    static constexpr int oV = oK + 2 * kK;         // 2 stages
-    static constexpr int oOnes = oV + 2 * kV;
-    static constexpr int oPad = oOnes + kOnes;     // 16 KB the padded M = 128 operands may touch
-    static constexpr int oSmall = oPad + 16384;
-    static constexpr int bytes = oSmall + 2048;
-    static constexpr int request = bytes + 1024;
-};
-
-struct StateSmall {
-    alignas(16) float u[128];
-    uint64_t kv_full[2], kv_empty[2], phik_done[2], init_done, st_done;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-template <int D, int DV>
-__global__ void __launch_bounds__(kStateThreads)
-causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                    const TcParams p, float *__restrict__ S_seg, float *__restrict__ z_seg)
-{
-    using Lay = StateLayout<D, DV>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
-    StateSmall &S = *reinterpret_cast<StateSmall *>(sm + Lay::oSmall);
-    uint8_t *sK = sm + Lay::oK, *sV = sm + Lay::oV, *sOnes = sm + Lay::oOnes;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int item = blockIdx.x;
-    const int head = item / p.nseg, seg = item - head * p.nseg;
-    const int tok0 = seg * p.seg_chunks * kC;
-    const int nloc = min(p.N - tok0, p.seg_chunks * kC);
-    const int nchunks = (nloc + kC - 1) / kC;
-    const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
-
-    if (tid == 0) {
-        S.abort_flag = 0;
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&S.kv_full[s], 1);
-            mbar_init(&S.kv_empty[s], 1);
-            mbar_init(&S.phik_done[s], kWG);
-        }
-        mbar_init(&S.init_done, kWG);
-        mbar_init(&S.st_done, 1);
-        fence_mbar_init();
-        prefetch_tmap(&kmap);
-        prefetch_tmap(&vmap);
-    }
-    if (warp == 1) {
-        tmem_alloc(&S.tmem_base, kStTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tb = S.tmem_base;
-
-    if (warp == 0) {
-        if (lane == 0) {   // TMA: K and V blocks of this segment
-            constexpr uint32_t kvbytes = kC * (D + DV) * 2;
-            int last_kv[2] = {-1, -1};
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1, t0 = tok0 + c * kC;
-                if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 60)) break;
-                mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
-                for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load_3d(sK + s * Lay::kK + bx * kC * 128, &kmap, &S.kv_full[s], bx * 64, t0, head);
-                for (int bx = 0; bx < DV / 64; ++bx)
-                    tma_load_3d(sV + s * Lay::kV + bx * kC * 128, &vmap, &S.kv_full[s], bx * 64, t0, head);
-                last_kv[s] = c;
-            }
-            if (*g.abort)
-                for (int s = 0; s < 2; ++s)
-                    if (last_kv[s] >= 0) drain_wait(&S.kv_full[s], (last_kv[s] >> 1) & 1, g.limit_ns);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {   // MMA: R += psi(K)^T V, zeta += psi(K)^T 1, u += V^T 1
-            constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);
-            constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);
-            const uint32_t ob = smem_u32(sOnes);
-            bool ok = mbar_wait(&S.init_done, 0, g, 61);
-            for (int c = 0; ok && c < nchunks; ++c) {
-                const int s = c & 1;
-                if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 62)) break;
-                if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 63)) break;
-                tc_fence_after();
-                const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
-#pragma unroll
-                for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
-                    const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
-                    const uint64_t od = smem_desc(ob + ks * 256, 128, 2048, kSwizzleNone);
-                    mma_ss(tb + kStColR, ad, vd, iR, 1);
-                    mma_ss(tb + kStColZ, ad, od, iZ, 1);
-                    mma_ss(tb + kStColU, vd, od, iZ, 1);
-                }
-                mma_commit(&S.kv_empty[s]);
-            }
-            mma_commit(&S.st_done);
-            drain_wait(&S.st_done, 0, g.limit_ns);
-        }
-    } else {
-        const int wq = warp & 3, row = wq * 32 + lane, wtid = tid - 64;
-        const uint32_t lb = (uint32_t)(wq * 32) << 16;
-        // ones operand (row 0 = 1, rows 1..15 = 0) and a zeroed pad region
-        for (int e = wtid; e < 16 * kC; e += kWG) {
-            const int n = e / kC, k = e % kC;
-            *reinterpret_cast<__nv_bfloat16 *>(sOnes + (n >> 3) * 2048 + (k >> 3) * 128 +
-                                               (n & 7) * 16 + (k & 7) * 2) =
-                __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
-        }
-        for (int e = wtid; e < 16384 / 16; e += kWG)
-            reinterpret_cast<uint4 *>(sm + Lay::oPad)[e] = make_uint4(0u, 0u, 0u, 0u);
-        {   // zero accumulators
-            uint32_t zero[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) zero[m] = 0u;
-#pragma unroll
-            for (int grp = 0; grp < DV / 16; ++grp) tmem_st16(tb + lb + kStColR + grp * 16, zero);
-            tmem_st16(tb + lb + kStColZ, zero);
-            tmem_st16(tb + lb + kStColU, zero);
-            tmem_wait_st();
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(&S.init_done);
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1;
-            ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 64);
-            if (!ok) break;
-            uint8_t *kt = sK + s * Lay::kK;
-#pragma unroll 1
-            for (int f0 = 0; f0 < D / 8; f0 += 8) {
-                uint4 raw[8];
-#pragma unroll
-                for (int f = 0; f < 8; ++f)
-                    raw[f] = *reinterpret_cast<const uint4 *>(
-                        kt + ((f0 + f) >> 3) * (kC * 128) + sw128_off(row, ((f0 + f) & 7) * 8));
-#pragma unroll
-                for (int f = 0; f < 8; ++f) {
-                    uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        w[h] = pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
-                    raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-#pragma unroll
-                for (int f = 0; f < 8; ++f)
-                    *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
-                                               sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
-            }
-            fence_proxy_async();
-            mbar_arrive(&S.phik_done[s]);
-        }
-        ok = ok && wait_warp(&S.st_done, 0, g, 65);
-        if (ok) {   // plain state of the segment: S = 1 u^T + R, z = n 1 + zeta
-            tc_fence_after();
-            uint32_t zv[4], uv[4];
-            tmem_ld4(tb + lb + kStColZ, zv);
-            tmem_ld4(tb + lb + kStColU, uv);
-            tmem_wait_ld();
-            S.u[row] = u2f(uv[0]);
-            named_bar(kBarA, kWG);
-            float *dst = S_seg + (size_t)item * D * DV;
-#pragma unroll 1
-            for (int grp = 0; grp < DV / 16; ++grp) {
-                uint32_t rv[16];
-                tmem_ld16(tb + lb + kStColR + grp * 16, rv);
-                tmem_wait_ld();
-                if (row < D)
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4)
-                        *reinterpret_cast<float4 *>(dst + (size_t)row * DV + grp * 16 + jj) =
-                            make_float4(u2f(rv[jj]) + S.u[grp * 16 + jj],
-                                        u2f(rv[jj + 1]) + S.u[grp * 16 + jj + 1],
-                                        u2f(rv[jj + 2]) + S.u[grp * 16 + jj + 2],
-                                        u2f(rv[jj + 3]) + S.u[grp * 16 + jj + 3]);
-            }
-            if (row < D) z_seg[(size_t)item * D + row] = (float)nloc + u2f(zv[0]);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tb, kStTmemCols);
-    }
-}
-
+// ------------------------------------------------------------------ segment prefix scan
 // Exclusive prefix over the segments of each head, in a fixed order:
 // P_0 = S_in (or 0), P_s = P_{s-1} + S_{s-1}; the same for z.  One thread per
 // state element (grid: heads x element blocks); the segment loop issues its
@@ -1031,47 +751,6 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// 3-D map over [heads][rows][inner] with a box of [1][box_rows][box_inner].
-bool encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz, int inner,
-               int rows, int heads, int box_inner, int box_rows, CUtensorMapSwizzle sw) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)heads};
-    const cuuint64_t strides[2] = {(cuuint64_t)inner * esz, (cuuint64_t)rows * inner * esz};
-    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 152;
-    return n;
-}
-
 // Split the sequence only when the heads alone leave SMs idle: then aim for
 // about four waves of (head, segment) items, at least one block per segment.
 void choose_segments(int BH, int N, int &nseg, int &seg_chunks) {

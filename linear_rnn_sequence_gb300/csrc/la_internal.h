@@ -62,5 +62,8 @@ bool causal_tc_supported(const FwdArgs &a);
 size_t causal_tc_workspace(int BH, int N, int d, int dv);
 int causal_tc_launches(int BH, int N);   // kernels one causal call launches
 cudaError_t launch_causal_tc(const FwdArgs &a);
+bool noncausal_tc_supported(const FwdArgs &a);
+size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
+cudaError_t launch_noncausal_tc(const FwdArgs &a);
 
 }  // namespace la

@@ -1,0 +1,138 @@
+// tc_common.cuh -- helpers shared by the tensor-core kernels (causal and
+// non-causal): the psi feature function, swizzled shared-memory addressing,
+// warp-uniform bounded waits, group barriers, TMA tensor-map encoding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <mutex>
+
+#include "la_internal.h"
+#include "tc_ptx.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;          // tokens per block (MMA M)
+constexpr int kWG = 128;         // threads per row-worker group
+constexpr int kBarA = 1, kBarB = 2;  // named barrier ids of the two row-worker groups
+
+struct TcParams {
+    float *y;
+    int N, BH;
+    int nseg;                      // segments per head (work items = BH * nseg)
+    int seg_chunks;                // blocks per segment (the last one may be shorter)
+    float eps;
+    const float *S_in, *z_in;
+    float *S_out, *z_out;
+    unsigned int *err;             // workspace header error word
+    unsigned int *err_where;
+    unsigned long long limit_ns;
+};
+
+// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
+// lanes with inputs of either sign stay converged: for x > 0 the exponential
+// of 0 is exactly 1 and the second term vanishes.  e^x = 2^(x log2 e) with the
+// flush-to-zero form (x <= 0 here, so a flushed result only means e^x < 2^-126).
+__device__ __forceinline__ float psi_f(float x) {
+    return fmaxf(x, 0.f) + (ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
+}
+__device__ __forceinline__ float bf16_round(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Byte offset of element (row, col) in a [rows x 64] bf16 box with 128-byte
+// swizzle, the layout TMA writes (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+    return (uint32_t)row * 128u + ((((uint32_t)col >> 3) ^ ((uint32_t)row & 7u)) << 4) +
+           (((uint32_t)col & 7u) << 1);
+}
+
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ float warp_sum_f(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, const Guard &g,
+                                          unsigned int where) {
+    const bool ok = mbar_wait(bar, parity, g, where);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while unwinding after an abort: ignores the abort flag but
+// still gives up after the time limit.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) break;
+}
+
+// Group barrier that also agrees on "someone gave up": returns true if any of
+// the group's 128 threads passes failed = true.
+template <int BAR>
+__device__ __forceinline__ bool group_any(bool failed) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)failed), "n"(BAR), "n"(kWG)
+        : "memory");
+    return r != 0;
+}
+
+
+// ------------------------------------------------------------------ host helpers
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 3-D map over [heads][rows][inner] with a box of [1][box_rows][box_inner].
+bool encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz, int inner,
+               int rows, int heads, int box_inner, int box_rows, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * esz, (cuuint64_t)rows * inner * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 152;
+    return n;
+}
+
+}  // namespace
+}  // namespace la

@@ -165,8 +165,11 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
 
 
 def forward_noncausal(q, k, v, eps: float = 1e-6, return_state=False, out=None, S_out=None,
-                      z_out=None, workspace=None, stream=None):
-    """Non-causal elu+1 linear attention.  Returns y [B,H,N,dv] float32 (+ S, z)."""
+                      z_out=None, workspace=None, stream=None, check_status=False):
+    """Non-causal elu+1 linear attention.  Returns y [B,H,N,dv] float32 (+ S, z).
+
+    ``check_status`` as for :func:`forward_causal`.
+    """
     _check_cuda(q, k, v, out, S_out, z_out, workspace)
     B, H, N, d = q.shape
     dv = v.shape[-1]
@@ -185,6 +188,10 @@ def forward_noncausal(q, k, v, eps: float = 1e-6, return_state=False, out=None, 
                                     float(eps), _ptr(S_out), _ptr(z_out), _ptr(workspace), wbytes,
                                     _stream_handle(stream, q.device))
     _raise(st, "la_forward_noncausal")
+    if check_status and workspace is not None:
+        err, where = workspace_header(workspace)
+        if err != LA_OK:
+            raise LinAttnError(err, f"la_forward_noncausal (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
 
 

@@ -53,7 +53,7 @@ def test_noncausal_matches_oracle(case, cuda_device):
     B, H, N, d, dv, dt, s = case
     q, k, v = random_qkv(B, H, N, d, dv, dtype=dt, scale=s, seed=N + 1)
     y, S, z = la.forward_noncausal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
-                                   return_state=True)
+                                   return_state=True, check_status=True)
     torch.cuda.synchronize()
     yo, So, zo = oracle.noncausal(q, k, v, return_state=True)
     tol = tol_for(dt)
@@ -167,8 +167,8 @@ def test_runs_are_bitwise_deterministic(cuda_device):
                                                      dtype=torch.bfloat16, scale=0.09, seed=9))
     a = la.forward_causal(q, k, v, return_state=True, check_status=True)
     b = la.forward_causal(q, k, v, return_state=True, check_status=True)
-    c = la.forward_noncausal(q, k, v, return_state=True)
-    d = la.forward_noncausal(q, k, v, return_state=True)
+    c = la.forward_noncausal(q, k, v, return_state=True, check_status=True)
+    d = la.forward_noncausal(q, k, v, return_state=True, check_status=True)
     torch.cuda.synchronize()
     for x, y in zip(a + c, b + d):
         assert torch.equal(x, y)
@@ -190,3 +190,21 @@ def test_workspace_too_small_is_rejected(cuda_device):
     with pytest.raises(la.LinAttnError) as ei:
         la.forward_noncausal(q, k, v, workspace=ws)
     assert ei.value.status == la.LA_ERR_WORKSPACE
+
+
+# The tensor-core non-causal path (bf16, d and dv in {64, 128}): every shape,
+# ragged tails, one-block and many-segment splits (few heads, long sequences).
+@pytest.mark.parametrize("B,H,N,d,dv", [
+    (1, 1, 1, 64, 64), (1, 2, 2, 128, 128), (1, 2, 127, 64, 128), (1, 2, 128, 128, 64),
+    (1, 2, 129, 64, 64), (2, 3, 1000, 64, 128), (1, 3, 2049, 128, 64),
+    (1, 1, 20000, 64, 64), (1, 2, 9001, 128, 128),
+])
+def test_noncausal_tc_shapes(B, H, N, d, dv, cuda_device):
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=d ** -0.5, seed=N + d)
+    y, S, z = la.forward_noncausal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                   return_state=True, check_status=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.noncausal(q, k, v, return_state=True)
+    e = (rel_max_err(y, yo), rel_max_err(S, So), rel_max_err(z, zo))
+    print(f"noncausal tc B{B}H{H}N{N}d{d}dv{dv}: y {e[0]:.2e} S {e[1]:.2e} z {e[2]:.2e}")
+    assert max(e) <= TOL_BF16

@@ -326,11 +326,24 @@ def launches_per_call(mode, w):
 
 
 def load_traffic(name):
-    """DRAM bytes per launch from a committed ncu summary, if one matches the current kernel."""
+    """DRAM bytes per launch of the dominant kernel, from a committed ncu summary.
+
+    The entry lists the sources the kernel was built from and their sha256 at
+    capture time; once any of them has changed the figure no longer describes
+    the kernel that runs, and null is returned.
+    """
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            return json.load(f).get(name)
+            e = json.load(f)["workloads"].get(name)
+        if not e:
+            return None
+        h = hashlib.sha256()
+        for src in e["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return int(e["bytes"]) if h.hexdigest() == e["sha256"] else None
     except Exception:
         return None
 

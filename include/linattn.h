@@ -170,14 +170,20 @@ LA_API la_status la_forward_noncausal_noalloc(const void *q, const void *k, cons
 LA_API la_status la_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Test hook (host side only, process-wide, not thread-safe): when
- * skip_publish_segment >= 0, the causal scan's CTA for that segment index
- * never publishes its state, so its successor's bounded wait runs out;
- * wait_limit_ns bounds every inter-CTA wait (<= 0 restores the default of
- * about one second).  Pass (-1, 0) to turn the hook off.  Nothing faults,
- * traps or hangs: the waiter records LA_ERR_TIMEOUT and returns.
+ * Test hook for the failure path (host side only, process-wide, not
+ * thread-safe; no counterpart on the pages).  wait_limit_ns bounds every
+ * wait of the tensor-core kernels (<= 0 restores the default of about one
+ * second).  When drop_load_item >= 0, the tensor-core launch's work item
+ * with that index (the CTA index: a (head, segment) item of
+ * la_forward_causal, or a (head, query range) item of la_forward_noncausal)
+ * announces its first tile copy on its mbarrier but never issues it, so every
+ * wait on that tile runs out.  Nothing faults, traps or hangs: the waiter
+ * records LA_ERR_TIMEOUT in the workspace header, the CTA unwinds (letting
+ * the copies it did issue land and freeing its TMEM) and the call's outputs
+ * are undefined; la_workspace_status then reports LA_ERR_TIMEOUT.  Pass
+ * (-1, 0) to turn the hook off.
  */
-LA_API void la_debug_set_scan_fault(int skip_publish_segment, long long wait_limit_ns);
+LA_API void la_debug_set_fault(int drop_load_item, long long wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -190,8 +190,8 @@ la_status la_workspace_status(const void *workspace, size_t workspace_bytes, voi
     return h.error == 0 ? LA_OK : static_cast<la_status>(h.error);
 }
 
-void la_debug_set_scan_fault(int skip_publish_segment, long long wait_limit_ns) {
-    debug_fault().skip_publish_segment = skip_publish_segment;
+void la_debug_set_fault(int drop_load_item, long long wait_limit_ns) {
+    debug_fault().drop_load_item = drop_load_item;
     debug_fault().wait_limit_ns = wait_limit_ns;
 }
 

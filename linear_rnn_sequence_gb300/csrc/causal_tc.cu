@@ -130,21 +130,26 @@ template <int D, int DV>
 __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
                                               const CUtensorMap *qmap, const CUtensorMap *kmap,
                                               const CUtensorMap *vmap, int head, int tok0,
-                                              int nchunks, const Guard &g) {
+                                              int nchunks, bool drop_first, const Guard &g) {
     using Lay = Layout<D, DV>;
     constexpr uint32_t qbytes = kC * D * 2, kvbytes = kC * (D + DV) * 2;
     int last_q = -1, last_kv[2] = {-1, -1};
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = tok0 + c * kC, s = c & 1;
+        // block 0's copies read only q, k, v; every later wait may depend on
+        // the initial state, which the previous kernel (if any) writes
+        if (c == 1) griddep_wait();
         if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 11)) break;
         mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
+        if (!(drop_first && c == 0)) {   // test hook: a copy that never arrives
 #pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_3d(sK + s * Lay::kK + bx * kC * 128, kmap, &S.kv_full[s], bx * 64, t0, head);
+            for (int bx = 0; bx < D / 64; ++bx)
+                tma_load_3d(sK + s * Lay::kK + bx * kC * 128, kmap, &S.kv_full[s], bx * 64, t0, head);
 #pragma unroll
-        for (int bx = 0; bx < DV / 64; ++bx)
-            tma_load_3d(sV + s * Lay::kV + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
-        last_kv[s] = c;
+            for (int bx = 0; bx < DV / 64; ++bx)
+                tma_load_3d(sV + s * Lay::kV + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
+            last_kv[s] = c;
+        }
         LA_TRACE_POINT(c, 13);
         if (c > 0 && !mbar_wait(&S.q_empty, (c - 1) & 1, g, 10)) break;
         mbar_arrive_expect_tx(&S.q_full, qbytes);
@@ -692,8 +697,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     tc_fence_after();
     const uint32_t tb = S.tmem_base;
 
+    // With the sequence split, this kernel may start while the prefix scan
+    // still runs (programmatic dependent launch): every thread but the
+    // producer waits for it here, before its first bounded wait or read of
+    // the initial state; the producer waits after issuing block 0's copies.
+    if (warp != 0) griddep_wait();
     if (warp == 0) {
-        if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, tok0, nchunks, g);
+        if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, tok0, nchunks,
+                                           item == p.drop_item, g);
     } else if (warp == 1) {
         if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, nchunks, g);
     } else if (warp >= kWarpA && warp < kWarpB) {
@@ -722,6 +733,8 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
                    const float *__restrict__ S_in, const float *__restrict__ z_in, int nseg,
                    int D, int DV)
 {
+    griddep_launch_dependents();
+    griddep_wait();   // S_seg, z_seg come from the state pass
     const int head = blockIdx.x;
     const int nS = D * DV;
     const int e = blockIdx.y * kScanThreads + threadIdx.x;
@@ -799,6 +812,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.err_where = &hdr->error_where;
     const long long lim = debug_fault().wait_limit_ns;
     p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
+    p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
     if (p.nseg > 1) {
         // segment states, then their exclusive prefixes, which become the
@@ -816,9 +830,10 @@ cudaError_t launch_dv(const FwdArgs &a) {
         skern<<<items, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg, z_seg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const dim3 sgrid(BH, (D * DV + D + kScanThreads - 1) / kScanThreads);
-        scan_states_kernel<<<sgrid, kScanThreads, 0, a.stream>>>(S_seg, z_seg, S_pre, z_pre,
-                                                                a.S_in, a.z_in, p.nseg, D, DV);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_overlapped(scan_states_kernel, sgrid, dim3(kScanThreads), 0, a.stream,
+                              (const float *)S_seg, (const float *)z_seg, S_pre, z_pre, a.S_in,
+                              a.z_in, p.nseg, D, DV);
+        if (e != cudaSuccess) return e;
         p.S_in = S_pre;
         p.z_in = z_pre;
     }
@@ -826,6 +841,9 @@ cudaError_t launch_dv(const FwdArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::request);
     if (e != cudaSuccess) return e;
+    if (p.nseg > 1)
+        return launch_overlapped(kern, dim3(items), dim3(kThreads), Lay::request, a.stream, qm, km,
+                                 vm, p);
     kern<<<items, kThreads, Lay::request, a.stream>>>(qm, km, vm, p);
     return cudaGetLastError();
 }

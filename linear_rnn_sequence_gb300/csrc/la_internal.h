@@ -39,15 +39,15 @@ struct DecodeArgs {
 struct WsHeader {
     unsigned int error;         // 0 = ok, else an la_status value (LA_ERR_TIMEOUT)
     unsigned int error_where;   // diagnostic: which segment gave up
-    unsigned int ticket;        // dynamic segment ticket counter
+    unsigned int reserved;
     unsigned int pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 
-// Process-wide test hook state (see la_debug_set_scan_fault).
+// Process-wide test hook state (see la_debug_set_fault).
 struct DebugFault {
-    int skip_publish_segment = -1;
-    long long wait_limit_ns = 0;
+    int drop_load_item = -1;      // work item whose first tile copy is never issued
+    long long wait_limit_ns = 0;  // <= 0: default limit of every bounded wait
 };
 DebugFault &debug_fault();
 

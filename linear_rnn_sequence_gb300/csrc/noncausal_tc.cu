@@ -86,6 +86,8 @@ noncausal_prepare_kernel(const float *__restrict__ S_seg, const float *__restric
 {
     using Img = OpImage<D, DV>;
     constexpr int kSBlocks = D * DV / (4 * kPrepThreads);
+    griddep_launch_dependents();
+    griddep_wait();   // S_seg, z_seg come from the state pass
     const int head = blockIdx.x, tid = threadIdx.x;
     uint8_t *img = img_all + (size_t)head * Img::stride;
     if ((int)blockIdx.y < kSBlocks) {
@@ -154,6 +156,7 @@ struct QParams {
     unsigned int *err;
     unsigned int *err_where;
     unsigned long long limit_ns;
+    int drop_item;                 // test hook: this item's first Q copy is never issued (-1: off)
 };
 
 struct QSmall {
@@ -179,7 +182,8 @@ struct QLayout {
     // TMEM: accumulators Y_0, Y_1 [0, 2 dv), denominators [2 dv, 2 dv + 32)
     static constexpr uint32_t colDen = 2 * DV;
     static constexpr uint32_t tmem_cols = (2 * DV + 32 <= 256) ? 256 : 512;
-    static constexpr int min_blocks = (tmem_cols <= 256) ? 2 : 1;
+    // two CTAs per SM when both TMEM and shared memory allow it
+    static constexpr int min_blocks = (tmem_cols <= 256 && request <= 113 * 1024) ? 2 : 1;
     static_assert(oOp % 1024 == 0, "swizzled operands need 1024-byte alignment");
 };
 
@@ -228,25 +232,40 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
     const uint32_t tb = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {   // operand image once, then the Q tiles of this range
-            mbar_arrive_expect_tx(&S.op_full, Img::bytes);
-            bulk_load(sOp, p.img + (size_t)head * Img::stride, Img::bytes, &S.op_full);
-            int last[kQStages];
-            for (int s = 0; s < kQStages; ++s) last[s] = -1;
-            for (int c = 0; c < nchunks; ++c) {
+        if (lane == 0) {   // Q tiles of this range and, once it exists, the operand image
+            // The first kQStages tiles read only q, so they are issued before
+            // waiting for the kernels that write the image (this kernel may
+            // start while they run: programmatic dependent launch).
+            const int npre = min(nchunks, kQStages);
+            const bool drop = item == p.drop_item;   // test hook: block 0 never arrives
+            int c_last = -1;                          // last block whose copy was issued
+            auto load_q = [&](int c) {
                 const int s = c % kQStages;
-                if (c >= kQStages && !mbar_wait(&S.q_empty[s], ((c / kQStages) - 1) & 1, g, 70))
-                    break;
                 mbar_arrive_expect_tx(&S.q_full[s], kC * D * 2);
+                if (c == 0 && drop) return;
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load_3d(sQ + s * Lay::kQ + bx * kC * 128, &qmap, &S.q_full[s], bx * 64,
                                 tok0 + c * kC, head);
-                last[s] = c;
+                c_last = c;
+            };
+            for (int c = 0; c < npre; ++c) load_q(c);
+            griddep_wait();
+            mbar_arrive_expect_tx(&S.op_full, Img::bytes);
+            bulk_load(sOp, p.img + (size_t)head * Img::stride, Img::bytes, &S.op_full);
+            for (int c = npre; c < nchunks; ++c) {
+                if (!mbar_wait(&S.q_empty[c % kQStages], ((c / kQStages) - 1) & 1, g, 70)) break;
+                load_q(c);
             }
             if (*g.abort) {   // no copy may still be landing when the CTA exits
                 drain_wait(&S.op_full, 0, g.limit_ns);
-                for (int s = 0; s < kQStages; ++s)
-                    if (last[s] >= 0) drain_wait(&S.q_full[s], (last[s] / kQStages) & 1, g.limit_ns);
+                // copies were issued for every block up to c_last (block 0
+                // excepted when dropped); the newest one on each stage:
+                for (int s = 0; s < kQStages; ++s) {
+                    if (c_last < 0) break;
+                    const int c = c_last - ((c_last - s) % kQStages + kQStages) % kQStages;
+                    if (c < 0 || (c == 0 && drop)) continue;
+                    drain_wait(&S.q_full[s], (c / kQStages) & 1, g.limit_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -255,6 +274,7 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
             constexpr uint32_t iZ = idesc_bf16(128, 16, 0, 0);   // A K-major, B K-major
             const uint32_t hb = smem_u32(sOp + Img::kHi), lb2 = smem_u32(sOp + Img::kLo);
             const uint32_t zb = smem_u32(sOp + Img::kZt);
+            griddep_wait();   // bounded waits below start once the image exists
             bool ok = mbar_wait(&S.op_full, 0, g, 71);
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int s = c % kQStages, b = c & 1;
@@ -285,6 +305,8 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
         const int row = (warp & 3) * 32 + lane;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kQStages;
+            // tiles from kQStages on wait for the MMA, hence for the image
+            if (c == kQStages) griddep_wait();
             const bool ok = wait_warp(&S.q_full[s], (c / kQStages) & 1, g, 74);
             if (ok) {
                 uint8_t *qt = sQ + s * Lay::kQ;
@@ -316,6 +338,7 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
     } else {
         // group B: column sums of S once, then the normaliser epilogue per block
         const int wq = warp & 3, row = wq * 32 + lane, wtid = tid - kQWarpB * 32;
+        griddep_wait();
         bool ok = wait_warp(&S.op_full, 0, g, 75);
         ok = !group_any<kBarB>(!ok);   // all four warps agree before the named barriers below
         if (ok) {
@@ -337,7 +360,7 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
         }
         const float zsum = *reinterpret_cast<const float *>(sOp + Img::kZsum);
         const int tq = lane >> 2, tcol = (lane & 3) * 2;
-        constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
+        constexpr int kParts = 2 * (DV / 32);   // (16-lane half, 32-column block) pairs
         for (int c = 0; ok && c < nchunks; ++c) {
             const int b = c & 1;
             ok = wait_warp(&S.acc_full[b], (c >> 1) & 1, g, 76);
@@ -353,18 +376,18 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
                 float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
                 auto part_addr = [&](int part) {
                     return tb + ((uint32_t)(wq * 32 + 16 * (part & 1)) << 16) + (uint32_t)(b * DV) +
-                           (part >> 1) * 64;
+                           (part >> 1) * 32;
                 };
                 // 16x256b shape: 4 neighbouring lanes hold 8 consecutive columns of
                 // one row, so each warp store covers whole 32-byte sectors
-                auto outputs = [&](int part, const uint32_t (&vc)[32]) {
+                auto outputs = [&](int part, const uint32_t (&vc)[16]) {
                     const int half = part & 1, cblk = part >> 1;
                     const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
                     const float invA = S.e_inv[rA], invB = S.e_inv[rB];
                     const bool okA = t0 + rA < nloc, okB = t0 + rB < nloc;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int col = cblk * 64 + 8 * k + tcol;
+                    for (int k = 0; k < 4; ++k) {
+                        const int col = cblk * 32 + 8 * k + tcol;
                         const float2 cs = *reinterpret_cast<const float2 *>(S.colsum + col);
                         const float2 oA = make_float2((u2f(vc[4 * k]) + cs.x) * invA,
                                                       (u2f(vc[4 * k + 1]) + cs.y) * invA);
@@ -374,15 +397,15 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
                         if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
                     }
                 };
-                uint32_t vA[32], vB[32];
-                tmem_ld_16x256b_x8(part_addr(0), vA);
+                uint32_t vA[16], vB[16];
+                tmem_ld_16x256b_x4(part_addr(0), vA);
                 tmem_wait_ld();
 #pragma unroll 1
                 for (int part = 0; part < kParts; part += 2) {
-                    tmem_ld_16x256b_x8(part_addr(part + 1), vB);   // kParts is even
+                    tmem_ld_16x256b_x4(part_addr(part + 1), vB);   // kParts is even
                     outputs(part, vA);
                     tmem_wait_ld();
-                    if (part + 2 < kParts) tmem_ld_16x256b_x8(part_addr(part + 2), vA);
+                    if (part + 2 < kParts) tmem_ld_16x256b_x4(part_addr(part + 2), vA);
                     outputs(part + 1, vB);
                     if (part + 2 < kParts) tmem_wait_ld();
                 }
@@ -452,6 +475,7 @@ cudaError_t launch_nc(const FwdArgs &a) {
     sp.err = &hdr->error;
     sp.err_where = &hdr->error_where;
     sp.limit_ns = limit_ns;
+    sp.drop_item = -1;
     char *ws = static_cast<char *>(a.ws);
     float *S_seg = reinterpret_cast<float *>(ws + sizeof(WsHeader));
     float *z_seg = S_seg + (size_t)BH * sp.nseg * D * DV;
@@ -464,10 +488,13 @@ cudaError_t launch_nc(const FwdArgs &a) {
     skern<<<BH * sp.nseg, kStateThreads, SL::request, a.stream>>>(km, vm, sp, S_seg, z_seg);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+    // the prepare and query kernels may start while their predecessor runs;
+    // each waits for it (griddep_wait) before touching what it writes
     const dim3 pgrid(BH, D * DV / (4 * kPrepThreads) + 1);
-    noncausal_prepare_kernel<D, DV><<<pgrid, kPrepThreads, 0, a.stream>>>(S_seg, z_seg, sp.nseg, img,
-                                                                          a.S_out, a.z_out);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_overlapped(noncausal_prepare_kernel<D, DV>, pgrid, dim3(kPrepThreads), 0, a.stream,
+                          (const float *)S_seg, (const float *)z_seg, sp.nseg, img, a.S_out,
+                          a.z_out);
+    if (e != cudaSuccess) return e;
 
     QParams qp{};
     qp.y = a.y;
@@ -478,12 +505,13 @@ cudaError_t launch_nc(const FwdArgs &a) {
     qp.err = &hdr->error;
     qp.err_where = &hdr->error_where;
     qp.limit_ns = limit_ns;
+    qp.drop_item = debug_fault().drop_load_item;
     auto qkern = noncausal_query_kernel<D, DV>;
     if ((e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   QL::request)) != cudaSuccess)
         return e;
-    qkern<<<BH * qp.nq, kQThreads, QL::request, a.stream>>>(qm, qp);
-    return cudaGetLastError();
+    return launch_overlapped(qkern, dim3(BH * qp.nq), dim3(kQThreads), QL::request, a.stream, qm,
+                             qp);
 }
 
 }  // namespace

@@ -9,6 +9,7 @@
 
 #include <cstddef>
 #include <mutex>
+#include <utility>
 
 #include "la_internal.h"
 #include "tc_ptx.cuh"
@@ -33,6 +34,7 @@ struct TcParams {
     unsigned int *err;             // workspace header error word
     unsigned int *err_where;
     unsigned long long limit_ns;
+    int drop_item;                 // test hook: this item's first K/V copy is never issued (-1: off)
 };
 
 // psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
@@ -124,6 +126,25 @@ bool encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esz
     return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch `kern` with programmatic stream serialization: it may start while
+// the previous kernel in the stream is still running, and must call
+// griddep_wait before it reads anything that kernel writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 int num_sms() {

@@ -63,6 +63,8 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const int nloc = min(p.N - tok0, p.seg_chunks * kC);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
+    // reads only K and V: the consumer of S_seg waits for this whole grid
+    griddep_launch_dependents();
 
     if (tid == 0) {
         S.abort_flag = 0;

@@ -67,8 +67,8 @@ def lib():
             L.la_decode_step.restype = i
             L.la_workspace_status.argtypes = [vp, sz, vp]
             L.la_workspace_status.restype = i
-            L.la_debug_set_scan_fault.argtypes = [i, ctypes.c_longlong]
-            L.la_debug_set_scan_fault.restype = None
+            L.la_debug_set_fault.argtypes = [i, ctypes.c_longlong]
+            L.la_debug_set_fault.restype = None
             _lib = L
     return _lib
 
@@ -228,6 +228,6 @@ def workspace_header(workspace) -> tuple[int, int]:
     return int(h[0]), int(h[1])
 
 
-def set_scan_fault(skip_publish_segment: int = -1, wait_limit_ns: int = 0) -> None:
-    """Test hook: see la_debug_set_scan_fault in include/linattn.h."""
-    lib().la_debug_set_scan_fault(int(skip_publish_segment), int(wait_limit_ns))
+def set_fault(drop_load_item: int = -1, wait_limit_ns: int = 0) -> None:
+    """Test hook: see la_debug_set_fault in include/linattn.h."""
+    lib().la_debug_set_fault(int(drop_load_item), int(wait_limit_ns))

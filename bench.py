@@ -89,12 +89,22 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's figure, on every rank (NCCL on the GPUs, gloo on CPU)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank.
+
+    Every rank runs the same per-GPU workload (weak scaling, replicas), so the
+    job processes world * units_per_rank units per step."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
 
 
 # ----------------------------------------------------------------------------
@@ -267,7 +277,7 @@ def run_ours(args, world, rank, local):
     T = w.B * w.H * w.N
     tokens = w.B * w.N
     ms_per_step = total_ms / args.steps
-    value = world * tokens / (ms_per_step * 1e-3)
+    value = whole_job_rate(tokens, world, ms_per_step)
     launch_ms = sum(per) / len(per)
     bytes_launch = T * alg_bytes_per_token_head(w)
     flops_launch = T * alg_flops_per_token_head(w.d, w.dv)

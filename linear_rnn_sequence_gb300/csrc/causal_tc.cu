@@ -74,9 +74,28 @@ constexpr int kThreads = 320;    // 10 warps
 constexpr int kWarpA = 2;        // first warp of group A
 constexpr int kWarpB = 6;        // first warp of group B
 
-constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 448,
-                   kColZ = 464, kColUV = 480;
+constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 464,
+                   kColZ = 480, kColUV = 496;
 constexpr uint32_t kTmemCols = 512;
+
+// Augmentation step.  One extra K = 16 slice on the psi(q) operand carries
+// per-row constants, so the MMAs add the fp32 parts of the split form:
+//   A' row i  = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0...]      (TMEM, after psi(q))
+//   B' key j  = [beta_hi, beta_lo, 1, 1, 1, 0...]        -> G  = d + alpha_i + beta_j + a_i.b_j
+//   B'' col c = [r_hi, r_lo, u_hi, u_hi, u_hi, u_lo, u_lo, 0...]
+//                                                        -> Y  = (d + alpha_i) u + r + a_i R
+//   Bz  col 0 = [rho_hi, rho_lo, n_hi, n_hi, n_hi, n_lo, n_lo, 0...]
+//                                                        -> Yz = (d + alpha_i) n + rho + a_i.zeta
+// (x_hi = bf16(x), x_lo = bf16(x - x_hi): the pairs carry x to about 2^-17
+// of its value; the dropped alpha_lo * u_lo term is smaller still).  Each
+// B tile is [rows x 16] bf16, K-major without swizzle.
+constexpr uint32_t kAugCols = 8;   // TMEM columns of the A' slice (16 bf16)
+static_assert(kColAq + 64 + kAugCols <= kColYz, "psi(q) and its augmentation fit below Yz");
+
+// Byte offset of (row n, k) in a [rows x 16] K-major no-swizzle bf16 tile.
+__device__ __forceinline__ uint32_t k16_off(int n, int k) {
+    return (uint32_t)((n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
+}
 
 template <int D, int DV>
 struct Layout {
@@ -86,14 +105,20 @@ struct Layout {
     static constexpr int kRt = D * DV * 2;          // bf16 R operand, 128B-swizzled MN-major
     static constexpr int kUVB = 16 * kC * 2;        // [1|beta_hi|beta_lo] operand, [16 x C]
     static constexpr int kZt = 16 * D * 2;          // zeta operand, [16 x d]
+    static constexpr int kGB = kC * 16 * 2;         // B' (G augmentation), [C x 16]
+    static constexpr int kYB = DV * 16 * 2;         // B'' (Y augmentation), [dv x 16]
+    static constexpr int kZB = 16 * 16 * 2;         // Bz (Yz augmentation), [16 x 16]
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQ;              // 2 stages
     static constexpr int oV = oK + 2 * kK;          // 2 stages
     static constexpr int oRt = oV + 2 * kV;
     static constexpr int oUVB = oRt + kRt;          // 2 stages
     static constexpr int oZt = oUVB + 2 * kUVB;
-    static constexpr int oSmall = oZt + kZt;
-    static constexpr int kSmall = 7 * 1024;
+    static constexpr int oGB = oZt + kZt;           // 2 stages
+    static constexpr int oYB = oGB + 2 * kGB;
+    static constexpr int oZB = oYB + kYB;
+    static constexpr int oSmall = oZB + kZB;
+    static constexpr int kSmall = 4 * 1024;
     static constexpr int bytes = oSmall + kSmall;
     // request enough that only one CTA fits per SM (TMEM: 512 columns each)
     static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
@@ -102,15 +127,10 @@ struct Layout {
 // Small shared-memory area.  Per-block values are kept by block parity:
 // [c & 1] holds block c (or, for the state, the state after block c).
 struct Small {
-    alignas(16) float beta[2][kC];     // beta_j = sum of bf16 psi(k_j)
-    alignas(16) float alpha[2][kC];    // alpha_i = sum of bf16 psi(q_i)
-    alignas(16) float rowsum[2][kC];   // sum_{j<=i} w_ij (hi + lo) in the block
     alignas(16) float u[2][128];
-    alignas(16) float r[2][128];
     alignas(16) float zeta[128];       // last exported zeta (fp32), for the final state
     alignas(16) float rho_part[2][4];
     alignas(16) float e_inv[kC];       // output epilogue: 1 / max(den, eps) per row
-    alignas(16) float e_base[kC];      // output epilogue: d + alpha per row
     float n_s[2], rho_s[2];
     uint64_t q_full, q_empty, kv_full[2], kv_empty[2];
     uint64_t phik_done[2];             // by K/V stage: a waiter is never two phases behind
@@ -120,10 +140,9 @@ struct Small {
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(offsetof(Small, beta) % 16 == 0 && offsetof(Small, u) % 16 == 0 &&
-                  offsetof(Small, r) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
+static_assert(offsetof(Small, u) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
               "vector loads and mbarriers need aligned fields");
-static_assert(sizeof(Small) <= 7 * 1024, "small area");
+static_assert(sizeof(Small) <= 4 * 1024, "small area");
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -168,22 +187,28 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
 
 // ------------------------------------------------------------------ MMA issuer
 // Per block c (one thread issues, in this order):
-//   G  = psi(Q) psi(K)^T                       after psi(q), psi(k) of block c
-//   Y  = psi(Q) R~,  Yz = psi(Q) zeta~         after the previous block's state
-//   R += psi(K)^T V, zeta += psi(K)^T 1,       export and output epilogue
+//   G  = psi(Q) psi(K)^T + A' B'^T = w         after psi(q), psi(k) of block c
+//   Y  = psi(Q) R~ + A' B''^T,                 after the previous block's state
+//   Yz = psi(Q) zeta~ + A' Bz^T                export and output epilogue
+//   R += psi(K)^T V, zeta += psi(K)^T 1,
 //   [u r] += V^T [1 beta_hi beta_lo]
-//   Y += P_hi V + P_lo V                       after the weight epilogue
+//   Y += P_hi V + P_lo V, Yz += (P_hi + P_lo) 1   after the weight epilogue
 template <int D, int DV>
 __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
-                                         uint8_t *sRt, uint8_t *sUVB, uint8_t *sZt, int nchunks,
+                                         uint8_t *sRt, uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
+                                         uint8_t *sYB, uint8_t *sZB, int nchunks,
                                          const Guard &g) {
     using Lay = Layout<D, DV>;
     constexpr uint32_t iG = idesc_bf16(128, kC, 0, 0);   // A = psi(q) in TMEM, B = psi(k) K-major
     constexpr uint32_t iY = idesc_bf16(128, DV, 0, 1);   // A in TMEM, B MN-major (R~ or V)
+    constexpr uint32_t iYk = idesc_bf16(128, DV, 0, 0);  // A in TMEM, B'' K-major
     constexpr uint32_t iYz = idesc_bf16(128, 16, 0, 0);  // A in TMEM, B = zeta~ no swizzle
     constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);   // A = psi(k)^T MN-major, B = V MN-major
     constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);   // A MN-major, B = [1|beta] no swizzle
+    constexpr uint32_t aAug = kColAq + D / 2;            // A' columns
     const uint32_t rb = smem_u32(sRt), zb = smem_u32(sZt);
+    const uint64_t yaug = smem_desc(smem_u32(sYB), 128, 256, kSwizzleNone);
+    const uint64_t zaug = smem_desc(smem_u32(sZB), 128, 256, kSwizzleNone);
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 20)) break;
@@ -199,6 +224,9 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
                 smem_desc(kb + (ks >> 2) * (kC * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128B);
             mma_ts(tb + kColG, tb + kColAq + ks * 8, bd, iG, ks > 0);
         }
+        // + d + alpha_i + beta_j: G is the full weight w_ij
+        mma_ts(tb + kColG, tb + aAug, smem_desc(smem_u32(sGB + s * Lay::kGB), 128, 256, kSwizzleNone),
+               iG, 1);
         mma_commit(&S.g_full);
         if (!mbar_wait(&S.rt_ready, c & 1, g, 23)) break;
         if (!mbar_wait(&S.y_empty, c & 1, g, 24)) break;
@@ -211,6 +239,9 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
             const uint64_t zd = smem_desc(zb + ks * 256, 128, D * 16, kSwizzleNone);
             mma_ts(tb + kColYz, tb + kColAq + ks * 8, zd, iYz, ks > 0);
         }
+        // + (d + alpha_i) u + r and + (d + alpha_i) n + rho
+        mma_ts(tb + kColY, tb + aAug, yaug, iYk, 1);
+        mma_ts(tb + kColYz, tb + aAug, zaug, iYz, 1);
         mma_commit(&S.aq_free);
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
@@ -228,8 +259,12 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
             const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
             mma_ts(tb + kColY, tb + kColG + ks * 16, vd, iY, 1);
             mma_ts(tb + kColY, tb + kColG + ks * 16 + 8, vd, iY, 1);
+            // row sums of the weights (hi + lo) into Yz column 0 (ones row of [1|beta])
+            mma_ts(tb + kColYz, tb + kColG + ks * 16, ud, iYz, 1);
+            mma_ts(tb + kColYz, tb + kColG + ks * 16 + 8, ud, iYz, 1);
         }
         mma_commit(&S.y_full);
         mma_commit(&S.kv_empty[s]);
@@ -240,9 +275,10 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
 }
 
 // ------------------------------------------------------------------ group A
-// Block c: psi(q) -> TMEM (A operand) and alpha_i; then, once G is ready,
-// w_ij = d + alpha_i + beta_j + G_ij (j <= i, else 0) split into bf16 hi + lo
-// pairs written back over G, and the row sums of hi + lo.
+// Block c: psi(q) -> TMEM (A operand) and its augmentation slice A' (which
+// carries alpha_i = sum of the rounded psi(q_i) and d); then, once G = w is
+// ready, w_ij (j <= i, else 0) split into bf16 hi + lo pairs written back
+// over G (the row sums come from the tensor core).
 template <int D, int DV>
 __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
                                              int nchunks, const Guard &g) {
@@ -282,7 +318,14 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                 }
                 tmem_st16(tb + lb + kColAq + grp * 16, v);
             }
-            S.alpha[cb][row] = alpha;
+            {   // A' = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0, ...]
+                const float ah = bf16_round(alpha);
+                const uint32_t aug0[4] = {pack_bf16x2(1.f, 1.f), pack_bf16x2(ah, alpha - ah),
+                                          pack_bf16x2(dd, ah), pack_bf16x2(dd, 0.f)};
+                const uint32_t aug1[4] = {0u, 0u, 0u, 0u};
+                tmem_st4(tb + lb + kColAq + D / 2, aug0);
+                tmem_st4(tb + lb + kColAq + D / 2 + 4, aug1);
+            }
             mbar_arrive(&S.q_empty);
             tmem_wait_st();
             tc_fence_before();
@@ -293,35 +336,26 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
              wait_warp(&S.g_full, c & 1, g, 43);
         if (ok) {
             tc_fence_after();
-            const float base_w = dd + alpha;
             if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 2);
-            const float *beta = S.beta[cb];
-            float rowsum = 0.f;
             // groups entirely above this warp's rows are all zero (causal mask);
             // the TMEM load of the next group is issued before this group's math
             const int last_grp = (wq * 32 + 31) >> 4;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
+            // (hi + lo equals w to within about 2^-17 w)
             auto weights = [&](int grp, const uint32_t (&gc)[16]) {
                 uint32_t out[16];
                 if (grp > last_grp) {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) out[m] = 0u;
                 } else {
-                    const float4 b0 = *reinterpret_cast<const float4 *>(beta + grp * 16);
-                    const float4 b1 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 4);
-                    const float4 b2 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 8);
-                    const float4 b3 = *reinterpret_cast<const float4 *>(beta + grp * 16 + 12);
-                    const float bb[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w,
-                                          b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
-                    const int lim = row - grp * 16;  // j - 16 grp <= lim is kept
+                    // j - 16 grp <= lim is kept; whole groups below the warp's rows keep all
+                    const int lim = (wq * 32 >= grp * 16 + 15) ? 15 : row - grp * 16;
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 2) {
-                        const float w0 = (jj <= lim) ? base_w + bb[jj] + u2f(gc[jj]) : 0.f;
-                        const float w1 = (jj + 1 <= lim) ? base_w + bb[jj + 1] + u2f(gc[jj + 1]) : 0.f;
+                        const float w0 = (jj <= lim) ? u2f(gc[jj]) : 0.f;
+                        const float w1 = (jj + 1 <= lim) ? u2f(gc[jj + 1]) : 0.f;
                         const uint32_t hi = pack_bf16x2(w0, w1);
-                        const float h0 = bf16_lo_f(hi), h1 = bf16_hi_f(hi);
-                        const uint32_t lo = pack_bf16x2(w0 - h0, w1 - h1);
-                        rowsum += w0 + w1;   // hi + lo equals w to within 2^-17 w
+                        const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
                         out[jj >> 1] = hi;
                         out[8 + (jj >> 1)] = lo;
                     }
@@ -342,7 +376,6 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                 weights(grp + 1, gB);
                 if (grp + 2 <= last_grp) tmem_wait_ld();
             }
-            S.rowsum[cb][row] = rowsum;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&S.h_ready[cb]);
@@ -373,7 +406,8 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
 
 template <int D, int DV>
 __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
-                                             uint8_t *sUVB, uint8_t *sZt,
+                                             uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
+                                             uint8_t *sYB, uint8_t *sZB,
                                              const TcParams &p, int head, int item,
                                              int tok0, int nloc, bool last_seg, int nchunks,
                                              const Guard &g) {
@@ -382,7 +416,6 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     const int wq = warp & 3, row = wq * 32 + lane;
     const int wtid = tid - kWarpB * 32;   // 0..127
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
-    const float dd = (float)D;
     const int N = nloc;   // tokens of this work item (segment)
 
     // constant operand rows: [1|beta] row 0 = ones, rows 3..15 zero; zeta~ all zero
@@ -394,6 +427,20 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     }
     for (int e = wtid; e < 16 * D; e += kWG)
         *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(e / D, e % D, D)) = __float2bfloat16_rn(0.f);
+    // B' rows: slots 8..15 are zero for good (slots 0..7 are written per block)
+    for (int s = 0; s < 2; ++s)
+        *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    // B'' row of column c, Bz row 0: [x_hi, x_lo, y_hi, y_hi, y_hi, y_lo, y_lo, 0 | 0...]
+    // for (x, y) = (r_c, u_c) and (rho, n)
+    auto aug_row = [](uint8_t *tile, int n, float x, float y) {
+        const float xh = bf16_round(x), yh = bf16_round(y);
+        const float yl = y - yh;
+        *reinterpret_cast<uint4 *>(tile + k16_off(n, 0)) =
+            make_uint4(pack_bf16x2(xh, x - xh), pack_bf16x2(yh, yh), pack_bf16x2(yh, yl),
+                       pack_bf16x2(yl, 0.f));
+        *reinterpret_cast<uint4 *>(tile + k16_off(n, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    };
+    if (wtid > 0 && wtid < 16) aug_row(sZB, wtid, 0.f, 0.f);   // rows 1..15 of Bz stay zero
 
     // ---- initial state in split form S = 1 u^T + R, z = n 1 + zeta (u = first row
     //      of S, n = first entry of z; zero when absent); buffers [1] = "block -1"
@@ -425,7 +472,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         tmem_st4(tb + lb + kColUV, uv);
         S.zeta[row] = zeta0;
         S.u[1][row] = u0;
-        S.r[1][row] = r0;
+        if (row < DV) aug_row(sYB, row, r0, u0);
         named_bar(kBarB, kWG);  // zero rows of zeta~ written before row 0 below
         if (row < D) *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
         if (wtid == 0) {
@@ -434,6 +481,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 for (int a = 1; a < D; ++a) rho0 += zin[a] - zin[0];
             S.n_s[1] = zin ? zin[0] : 0.f;
             S.rho_s[1] = rho0;
+            aug_row(sZB, 0, rho0, S.n_s[1]);
         }
         tmem_wait_st();
         fence_proxy_async();
@@ -476,11 +524,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
                                            sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
         }
-        S.beta[cb][row] = beta;
         const float bh = bf16_round(beta);
         uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
         *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
         *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
+        // B' row of key j: [beta_hi, beta_lo, 1, 1, 1, 0, 0, 0]
+        *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) =
+            make_uint4(pack_bf16x2(bh, beta - bh), pack_bf16x2(1.f, 1.f), pack_bf16x2(1.f, 0.f), 0u);
         const float bsum = warp_sum_f(beta);
         if (lane == 0) S.rho_part[cb][wq] = bsum;
         fence_proxy_async();
@@ -517,11 +567,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 __float2bfloat16_rn(u2f(zv[0]));
         }
         S.u[cb][row] = u2f(uv[0]);
-        S.r[cb][row] = u2f(uv[1]) + u2f(uv[2]);
+        if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u2f(uv[0]));
         if (wtid == 0) {
             S.n_s[cb] = S.n_s[pb] + (float)L;
             S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[cb][0] + S.rho_part[cb][1]) +
                                          (S.rho_part[cb][2] + S.rho_part[cb][3]));
+            aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -530,29 +581,23 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         return true;
     };
 
-    // y = (Y + (d + alpha) u + r) / max((d + alpha) n + rho + a.zeta + rowsum, eps)
-    // Each thread first finishes the denominator of its own row; the values are
-    // then read back through the 16x256b TMEM shape, where 4 neighbouring lanes
-    // hold 8 consecutive columns of one row, so every warp store writes whole
-    // 32-byte sectors (8 rows x 32 bytes).
+    // y = Y / max(Yz, eps): the tensor core has already summed every part of
+    // the numerator ((d + alpha) u + r + a R + P V) and of the denominator
+    // ((d + alpha) n + rho + a.zeta + sum_j P_ij).  Each thread takes 1/den of
+    // its own row; the values are then read back through the 16x256b TMEM
+    // shape, where 4 neighbouring lanes hold 8 consecutive columns of one row,
+    // so every warp store writes whole 32-byte sectors (8 rows x 32 bytes).
     auto epilogue = [&](int c) -> bool {
-        const int cb = c & 1, pb = (c + 1) & 1, t0 = c * kC;
-        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
-            return false;
+        const int t0 = c * kC;
+        // Y and Yz are complete once y_full flips (the P.V MMAs waited for group A)
+        if (!wait_warp(&S.y_full, c & 1, g, 53)) return false;
         if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 8);
         tc_fence_after();
         uint32_t yz[4];
         tmem_ld4(tb + lb + kColYz, yz);
         tmem_wait_ld();
-        {
-            const float base_w = dd + S.alpha[cb][row];
-            const float den =
-                fmaf(base_w, S.n_s[pb], S.rho_s[pb]) + u2f(yz[0]) + S.rowsum[cb][row];
-            S.e_inv[row] = 1.f / fmaxf(den, p.eps);
-            S.e_base[row] = base_w;
-        }
+        S.e_inv[row] = 1.f / fmaxf(u2f(yz[0]), p.eps);
         __syncwarp();
-        const float *up = S.u[pb], *rp = S.r[pb];
         float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
         const int tq = lane >> 2, tc = (lane & 3) * 2;
         constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
@@ -562,18 +607,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         auto outputs = [&](int part, const uint32_t (&vc)[32]) {
             const int half = part & 1, cblk = part >> 1;
             const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
-            const float invA = S.e_inv[rA], baseA = S.e_base[rA];
-            const float invB = S.e_inv[rB], baseB = S.e_base[rB];
+            const float invA = S.e_inv[rA], invB = S.e_inv[rB];
             const bool okA = t0 + rA < N, okB = t0 + rB < N;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int col = cblk * 64 + 8 * k + tc;
-                const float2 uu = *reinterpret_cast<const float2 *>(up + col);
-                const float2 rr = *reinterpret_cast<const float2 *>(rp + col);
-                const float2 oA = make_float2((u2f(vc[4 * k]) + fmaf(baseA, uu.x, rr.x)) * invA,
-                                              (u2f(vc[4 * k + 1]) + fmaf(baseA, uu.y, rr.y)) * invA);
-                const float2 oB = make_float2((u2f(vc[4 * k + 2]) + fmaf(baseB, uu.x, rr.x)) * invB,
-                                              (u2f(vc[4 * k + 3]) + fmaf(baseB, uu.y, rr.y)) * invB);
+                const float2 oA = make_float2(u2f(vc[4 * k]) * invA, u2f(vc[4 * k + 1]) * invA);
+                const float2 oB = make_float2(u2f(vc[4 * k + 2]) * invB, u2f(vc[4 * k + 3]) * invB);
                 if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
                 if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
             }
@@ -652,6 +692,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     Small &S = *reinterpret_cast<Small *>(sm + Lay::oSmall);
     uint8_t *sQ = sm + Lay::oQ, *sK = sm + Lay::oK, *sV = sm + Lay::oV;
     uint8_t *sRt = sm + Lay::oRt, *sUVB = sm + Lay::oUVB, *sZt = sm + Lay::oZt;
+    uint8_t *sGB = sm + Lay::oGB, *sYB = sm + Lay::oYB, *sZB = sm + Lay::oZB;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // work item = (head, segment of seg_chunks blocks)
@@ -706,11 +747,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
         if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, tok0, nchunks,
                                            item == p.drop_item, g);
     } else if (warp == 1) {
-        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, nchunks, g);
+        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
     } else if (warp >= kWarpA && warp < kWarpB) {
         group_a_role<D, DV>(S, tb, sQ, nchunks, g);
     } else {
-        group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, p, head, item, tok0, nloc,
+        group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0, nloc,
                             seg == p.nseg - 1, nchunks, g);
     }
     tc_fence_before();

@@ -54,10 +54,10 @@
 // Optional per-block timeline of CTA 0 (SM cycle counter) for performance
 // work; compiled in only with -DLA_TRACE, and then read with la_trace_fetch.
 #ifdef LA_TRACE
-__device__ unsigned long long la_trace_buf[256 * 16];
+__device__ unsigned long long la_trace_buf[256 * 32];
 #define LA_TRACE_POINT(c, ev)                                                   \
     do {                                                                        \
-        if (blockIdx.x == 0 && (c) < 256) la_trace_buf[(c) * 16 + (ev)] = clock64(); \
+        if (blockIdx.x == 0 && (c) < 256) la_trace_buf[(c) * 32 + (ev)] = clock64(); \
     } while (0)
 #else
 #define LA_TRACE_POINT(c, ev) \
@@ -70,9 +70,15 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;    // 10 warps
-constexpr int kWarpA = 2;        // first warp of group A
-constexpr int kWarpB = 6;        // first warp of group B
+constexpr int kThreads = 576;    // 18 warps
+constexpr int kWarpA1 = 2;       // first warp of group A1 (psi(q)); warps 0, 1: producer, MMA
+constexpr int kWarpA2 = 6;       // first warp of group A2 (weight epilogue)
+constexpr int kWarpB1 = 10;      // first warp of group B1 (psi(k), state export)
+constexpr int kWarpB2 = 14;      // first warp of group B2 (output epilogue)
+constexpr int kBarA2 = 3, kBarB2 = 4;   // named barriers of A2, B2 (A1 uses kBarA, B1 kBarB)
+static_assert(kWarpA2 - kWarpA1 == 4 && kWarpB1 - kWarpA2 == 4 && kWarpB2 - kWarpB1 == 4 &&
+                  kThreads == (kWarpB2 + 4) * 32,
+              "four warps per row-worker group, one per TMEM lane quarter");
 
 constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 464,
                    kColZ = 480, kColUV = 496;
@@ -127,6 +133,7 @@ struct Layout {
 // Small shared-memory area.  Per-block values are kept by block parity:
 // [c & 1] holds block c (or, for the state, the state after block c).
 struct Small {
+    alignas(16) float rowsum[2][kC];   // sum_{j<=i} w_ij (hi + lo) of block c, by parity
     alignas(16) float u[2][128];
     alignas(16) float zeta[128];       // last exported zeta (fp32), for the final state
     alignas(16) float rho_part[2][4];
@@ -188,11 +195,13 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
 // ------------------------------------------------------------------ MMA issuer
 // Per block c (one thread issues, in this order):
 //   G  = psi(Q) psi(K)^T + A' B'^T = w         after psi(q), psi(k) of block c
-//   Y  = psi(Q) R~ + A' B''^T,                 after the previous block's state
-//   Yz = psi(Q) zeta~ + A' Bz^T                export and output epilogue
-//   R += psi(K)^T V, zeta += psi(K)^T 1,
+//   R += psi(K)^T V, zeta += psi(K)^T 1,       after the previous state's export
 //   [u r] += V^T [1 beta_hi beta_lo]
-//   Y += P_hi V + P_lo V, Yz += (P_hi + P_lo) 1   after the weight epilogue
+//   Y  = psi(Q) R~ + A' B''^T,                 after the previous output epilogue
+//   Yz = psi(Q) zeta~ + A' Bz^T
+//   Y += P_hi V + P_lo V                       after the weight epilogue
+// The export of the state after block c waits for both st_full and aq_free:
+// the second says Y and Yz no longer read the operands it overwrites.
 template <int D, int DV>
 __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
                                          uint8_t *sRt, uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
@@ -228,7 +237,22 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         mma_ts(tb + kColG, tb + aAug, smem_desc(smem_u32(sGB + s * Lay::kGB), 128, 256, kSwizzleNone),
                iG, 1);
         mma_commit(&S.g_full);
+        // state update first: it only has to wait for the export of the
+        // previous state (out of TMEM), and fills the tensor pipe while the
+        // output epilogue of the previous block still reads Y
         if (!mbar_wait(&S.rt_ready, c & 1, g, 23)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+            const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
+            const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
+            mma_ss(tb + kColR, ad, vd, iR, 1);
+            mma_ss(tb + kColZ, ad, ud, iZ, 1);
+            mma_ss(tb + kColUV, vd, ud, iZ, 1);
+        }
+        mma_commit(&S.st_full);
+        LA_TRACE_POINT(c, 24);
         if (!mbar_wait(&S.y_empty, c & 1, g, 24)) break;
         LA_TRACE_POINT(c, 11);
         tc_fence_after();
@@ -242,29 +266,17 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         // + (d + alpha_i) u + r and + (d + alpha_i) n + rho
         mma_ts(tb + kColY, tb + aAug, yaug, iYk, 1);
         mma_ts(tb + kColYz, tb + aAug, zaug, iYz, 1);
+        // psi(q) and the exported state operands (R~, zeta~, B'', Bz) are free
         mma_commit(&S.aq_free);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-            const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
-            const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
-            const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
-            mma_ss(tb + kColR, ad, vd, iR, 1);
-            mma_ss(tb + kColZ, ad, ud, iZ, 1);
-            mma_ss(tb + kColUV, vd, ud, iZ, 1);
-        }
-        mma_commit(&S.st_full);
+        LA_TRACE_POINT(c, 25);
         if (!mbar_wait(&S.h_ready[c & 1], (c >> 1) & 1, g, 25)) break;
         LA_TRACE_POINT(c, 12);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
             const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
-            const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
             mma_ts(tb + kColY, tb + kColG + ks * 16, vd, iY, 1);
             mma_ts(tb + kColY, tb + kColG + ks * 16 + 8, vd, iY, 1);
-            // row sums of the weights (hi + lo) into Yz column 0 (ones row of [1|beta])
-            mma_ts(tb + kColYz, tb + kColG + ks * 16, ud, iYz, 1);
-            mma_ts(tb + kColYz, tb + kColG + ks * 16 + 8, ud, iYz, 1);
         }
         mma_commit(&S.y_full);
         mma_commit(&S.kv_empty[s]);
@@ -274,20 +286,17 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
     drain_wait(&S.drain, 0, g.limit_ns);
 }
 
-// ------------------------------------------------------------------ group A
+// ------------------------------------------------------------------ group A1
 // Block c: psi(q) -> TMEM (A operand) and its augmentation slice A' (which
-// carries alpha_i = sum of the rounded psi(q_i) and d); then, once G = w is
-// ready, w_ij (j <= i, else 0) split into bf16 hi + lo pairs written back
-// over G (the row sums come from the tensor core).
+// carries alpha_i = sum of the rounded psi(q_i) and d).
 template <int D, int DV>
-__device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
-                                             int nchunks, const Guard &g) {
+__device__ __forceinline__ void psiq_role(Small &S, uint32_t tb, const uint8_t *sQ,
+                                          int nchunks, const Guard &g) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const float dd = (float)D;
     for (int c = 0; c < nchunks; ++c) {
-        const int cb = c & 1;
         bool ok = wait_warp(&S.q_full, c & 1, g, 40);
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 0);
@@ -330,10 +339,24 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&S.phiq_done);
+            if (lane == 0) LA_TRACE_POINT(c, 16 + wq);
             if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 1);
         }
-        ok = ok && wait_warp(&S.phik_done[c & 1], (c >> 1) & 1, g, 42) &&
-             wait_warp(&S.g_full, c & 1, g, 43);
+        if (group_any<kBarA>(!ok)) break;
+    }
+}
+
+// ------------------------------------------------------------------ group A2
+// Block c, once G = w is ready: w_ij (j <= i, else 0) split into bf16 hi + lo
+// pairs written back over G (the row sums come from the tensor core).
+template <int D, int DV>
+__device__ __forceinline__ void weights_role(Small &S, uint32_t tb, int nchunks, const Guard &g) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, row = wq * 32 + lane;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cb = c & 1;
+        const bool ok = wait_warp(&S.g_full, c & 1, g, 43);
         if (ok) {
             tc_fence_after();
             if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 2);
@@ -342,6 +365,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             const int last_grp = (wq * 32 + 31) >> 4;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
             // (hi + lo equals w to within about 2^-17 w)
+            float rowsum = 0.f;
             auto weights = [&](int grp, const uint32_t (&gc)[16]) {
                 uint32_t out[16];
                 if (grp > last_grp) {
@@ -356,6 +380,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                         const float w1 = (jj + 1 <= lim) ? u2f(gc[jj + 1]) : 0.f;
                         const uint32_t hi = pack_bf16x2(w0, w1);
                         const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
+                        rowsum += w0 + w1;   // hi + lo equals w to within 2^-17 w
                         out[jj >> 1] = hi;
                         out[8 + (jj >> 1)] = lo;
                     }
@@ -376,12 +401,14 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                 weights(grp + 1, gB);
                 if (grp + 2 <= last_grp) tmem_wait_ld();
             }
+            S.rowsum[cb][row] = rowsum;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&S.h_ready[cb]);
+            if (lane == 0) LA_TRACE_POINT(c, 20 + wq);
             if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 3);
         }
-        if (group_any<kBarA>(!ok)) break;
+        if (group_any<kBarA2>(!ok)) break;
     }
 }
 
@@ -414,7 +441,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     using Lay = Layout<D, DV>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
-    const int wtid = tid - kWarpB * 32;   // 0..127
+    const int wtid = tid - kWarpB1 * 32;   // 0..127
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const int N = nloc;   // tokens of this work item (segment)
 
@@ -488,7 +515,6 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         tc_fence_before();
         named_bar(kBarB, kWG);
         mbar_arrive(&S.rt_ready);
-        mbar_arrive(&S.y_empty);
     }
 
 
@@ -535,6 +561,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         if (lane == 0) S.rho_part[cb][wq] = bsum;
         fence_proxy_async();
         mbar_arrive(&S.phik_done[s]);
+        if (lane == 0) LA_TRACE_POINT(c, 26 + wq);
         if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 7);
         return true;
     };
@@ -543,7 +570,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     auto export_state = [&](int c) -> bool {
         const int cb = c & 1, pb = (c + 1) & 1;
         const int L = min(kC, N - c * kC);
-        if (!wait_warp(&S.st_full, c & 1, g, 51)) return false;
+        if (!wait_warp(&S.st_full, c & 1, g, 51) || !wait_warp(&S.aq_free, c & 1, g, 54))
+            return false;
         if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 4);
         tc_fence_after();
 #pragma unroll
@@ -581,22 +609,70 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         return true;
     };
 
-    // y = Y / max(Yz, eps): the tensor core has already summed every part of
-    // the numerator ((d + alpha) u + r + a R + P V) and of the denominator
-    // ((d + alpha) n + rho + a.zeta + sum_j P_ij).  Each thread takes 1/den of
+    // Software pipeline, psi(k) two blocks ahead: iteration c runs psi(k) of
+    // block c+2 and the state export after block c+1, so the tensor core
+    // updates the state for block c+1 while psi(k) runs.
+    bool ok0 = phi_k(0);
+    if (ok0 && nchunks > 1) ok0 = phi_k(1);
+    bool aborted = group_any<kBarB>(!ok0);
+    if (!aborted) aborted = group_any<kBarB>(!export_state(0));
+    for (int c = 0; c + 1 < nchunks && !aborted; ++c) {
+        bool ok = true;
+        if (c + 2 < nchunks) ok = phi_k(c + 2);
+        if (ok) ok = export_state(c + 1);
+        if (group_any<kBarB>(!ok)) aborted = true;
+    }
+
+    // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
+    if (!aborted && p.S_out && last_seg) {
+        const int lbuf = (nchunks - 1) & 1;
+        tc_fence_after();
+#pragma unroll
+        for (int grp = 0; grp < DV / 16; ++grp) {
+            uint32_t rv[16];
+            tmem_ld16(tb + lb + kColR + grp * 16, rv);
+            tmem_wait_ld();
+            if (row < D) {
+                float *dst = p.S_out + ((size_t)head * D + row) * DV + grp * 16;
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 4)
+                    *reinterpret_cast<float4 *>(dst + jj) = make_float4(
+                        u2f(rv[jj]) + S.u[lbuf][grp * 16 + jj],
+                        u2f(rv[jj + 1]) + S.u[lbuf][grp * 16 + jj + 1],
+                        u2f(rv[jj + 2]) + S.u[lbuf][grp * 16 + jj + 2],
+                        u2f(rv[jj + 3]) + S.u[lbuf][grp * 16 + jj + 3]);
+            }
+        }
+        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];
+    }
+}
+
+// ------------------------------------------------------------------ group B2
+template <int D, int DV>
+__device__ __forceinline__ void output_role(Small &S, uint32_t tb, const TcParams &p, int head,
+                                            int tok0, int nloc, int nchunks, const Guard &g) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, row = wq * 32 + lane;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const int N = nloc;   // tokens of this work item (segment)
+    mbar_arrive(&S.y_empty);   // Y is free for block 0
+
+    // y = Y / max(Yz + rowsum, eps): the tensor core has already summed every
+    // part of the numerator ((d + alpha) u + r + a R + P V) and the inter-block
+    // denominator ((d + alpha) n + rho + a.zeta).  Each thread takes 1/den of
     // its own row; the values are then read back through the 16x256b TMEM
     // shape, where 4 neighbouring lanes hold 8 consecutive columns of one row,
     // so every warp store writes whole 32-byte sectors (8 rows x 32 bytes).
     auto epilogue = [&](int c) -> bool {
-        const int t0 = c * kC;
-        // Y and Yz are complete once y_full flips (the P.V MMAs waited for group A)
-        if (!wait_warp(&S.y_full, c & 1, g, 53)) return false;
+        const int t0 = c * kC, cb = c & 1;
+        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
+            return false;
         if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 8);
         tc_fence_after();
         uint32_t yz[4];
         tmem_ld4(tb + lb + kColYz, yz);
         tmem_wait_ld();
-        S.e_inv[row] = 1.f / fmaxf(u2f(yz[0]), p.eps);
+        S.e_inv[row] = 1.f / fmaxf(u2f(yz[0]) + S.rowsum[cb][row], p.eps);
         __syncwarp();
         float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
         const int tq = lane >> 2, tc = (lane & 3) * 2;
@@ -636,46 +712,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         return true;
     };
 
-    // Software pipeline, psi(k) two blocks ahead: iteration c runs the outputs
-    // of block c, psi(k) of block c+2 and the state export after block c+1, so
-    // the tensor core updates the state for block c+1 while psi(k) runs.
-    bool ok0 = phi_k(0);
-    if (ok0 && nchunks > 1) ok0 = phi_k(1);
-    bool aborted = group_any<kBarB>(!ok0);
-    if (!aborted) aborted = group_any<kBarB>(!export_state(0));
-    int last_c = -1;
-    for (int c = 0; c < nchunks && !aborted; ++c) {
-        bool ok = epilogue(c);
-        if (ok && c + 2 < nchunks) ok = phi_k(c + 2);
-        // the export below overwrites the state buffers the outputs above read
-        if (group_any<kBarB>(!ok)) { aborted = true; break; }
-        if (c + 1 < nchunks) ok = export_state(c + 1);
-        if (ok) last_c = c;
-        if (group_any<kBarB>(!ok)) aborted = true;
-    }
-
-    // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
-    if (!aborted && last_c == nchunks - 1 && p.S_out && last_seg) {
-        const int lbuf = last_c & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int grp = 0; grp < DV / 16; ++grp) {
-            uint32_t rv[16];
-            tmem_ld16(tb + lb + kColR + grp * 16, rv);
-            tmem_wait_ld();
-            if (row < D) {
-                float *dst = p.S_out + ((size_t)head * D + row) * DV + grp * 16;
-#pragma unroll
-                for (int jj = 0; jj < 16; jj += 4)
-                    *reinterpret_cast<float4 *>(dst + jj) = make_float4(
-                        u2f(rv[jj]) + S.u[lbuf][grp * 16 + jj],
-                        u2f(rv[jj + 1]) + S.u[lbuf][grp * 16 + jj + 1],
-                        u2f(rv[jj + 2]) + S.u[lbuf][grp * 16 + jj + 2],
-                        u2f(rv[jj + 3]) + S.u[lbuf][grp * 16 + jj + 3]);
-            }
-        }
-        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];
-    }
+    for (int c = 0; c < nchunks; ++c)
+        if (group_any<kBarB2>(!epilogue(c))) break;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -748,8 +786,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                                            item == p.drop_item, g);
     } else if (warp == 1) {
         if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
-    } else if (warp >= kWarpA && warp < kWarpB) {
-        group_a_role<D, DV>(S, tb, sQ, nchunks, g);
+    } else if (warp < kWarpA2) {
+        psiq_role<D, DV>(S, tb, sQ, nchunks, g);
+    } else if (warp < kWarpB1) {
+        weights_role<D, DV>(S, tb, nchunks, g);
+    } else if (warp >= kWarpB2) {
+        output_role<D, DV>(S, tb, p, head, tok0, nloc, nchunks, g);
     } else {
         group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0, nloc,
                             seg == p.nseg - 1, nchunks, g);
@@ -916,6 +958,6 @@ cudaError_t launch_causal_tc(const FwdArgs &a) {
 #ifdef LA_TRACE
 extern "C" LA_API void la_trace_fetch(unsigned long long *dst) {
     cudaDeviceSynchronize();
-    cudaMemcpyFromSymbol(dst, la_trace_buf, sizeof(unsigned long long) * 256 * 16);
+    cudaMemcpyFromSymbol(dst, la_trace_buf, sizeof(unsigned long long) * 256 * 32);
 }
 #endif

@@ -70,15 +70,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 576;    // 18 warps
-constexpr int kWarpA1 = 2;       // first warp of group A1 (psi(q)); warps 0, 1: producer, MMA
-constexpr int kWarpA2 = 6;       // first warp of group A2 (weight epilogue)
-constexpr int kWarpB1 = 10;      // first warp of group B1 (psi(k), state export)
-constexpr int kWarpB2 = 14;      // first warp of group B2 (output epilogue)
-constexpr int kBarA2 = 3, kBarB2 = 4;   // named barriers of A2, B2 (A1 uses kBarA, B1 kBarB)
-static_assert(kWarpA2 - kWarpA1 == 4 && kWarpB1 - kWarpA2 == 4 && kWarpB2 - kWarpB1 == 4 &&
-                  kThreads == (kWarpB2 + 4) * 32,
-              "four warps per row-worker group, one per TMEM lane quarter");
+constexpr int kThreads = 576;    // 18 warps: producer, MMA, group A (8), group B (8)
+constexpr int kWarpA = 2;        // first warp of group A
+constexpr int kWarpB = 10;       // first warp of group B
+static_assert(kThreads == (kWarpB + 8) * 32 && kWarpB - kWarpA == 8,
+              "eight warps per row-worker group, two per TMEM lane quarter");
 
 constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 464,
                    kColZ = 480, kColUV = 496;
@@ -124,7 +120,7 @@ struct Layout {
     static constexpr int oYB = oGB + 2 * kGB;
     static constexpr int oZB = oYB + kYB;
     static constexpr int oSmall = oZB + kZB;
-    static constexpr int kSmall = 4 * 1024;
+    static constexpr int kSmall = 6 * 1024;
     static constexpr int bytes = oSmall + kSmall;
     // request enough that only one CTA fits per SM (TMEM: 512 columns each)
     static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
@@ -133,11 +129,13 @@ struct Layout {
 // Small shared-memory area.  Per-block values are kept by block parity:
 // [c & 1] holds block c (or, for the state, the state after block c).
 struct Small {
-    alignas(16) float rowsum[2][kC];   // sum_{j<=i} w_ij (hi + lo) of block c, by parity
+    alignas(16) float rowsum[2][2][kC];   // [block parity][half] partial sums_{j<=i} w_ij
     alignas(16) float u[2][128];
     alignas(16) float zeta[128];       // last exported zeta (fp32), for the final state
     alignas(16) float rho_part[2][4];
-    alignas(16) float e_inv[kC];       // output epilogue: 1 / max(den, eps) per row
+    alignas(16) float e_inv[2][kC];    // output epilogue: 1 / max(den, eps) per row, per half
+    alignas(16) float alpha_part[kC];  // psi(q) row sums of the second half
+    alignas(16) float beta_part[kC];   // psi(k) row sums of the second half
     float n_s[2], rho_s[2];
     uint64_t q_full, q_empty, kv_full[2], kv_empty[2];
     uint64_t phik_done[2];             // by K/V stage: a waiter is never two phases behind
@@ -149,7 +147,7 @@ struct Small {
 };
 static_assert(offsetof(Small, u) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
               "vector loads and mbarriers need aligned fields");
-static_assert(sizeof(Small) <= 4 * 1024, "small area");
+static_assert(sizeof(Small) <= 6 * 1024, "small area");
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -286,133 +284,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
     drain_wait(&S.drain, 0, g.limit_ns);
 }
 
-// ------------------------------------------------------------------ group A1
-// Block c: psi(q) -> TMEM (A operand) and its augmentation slice A' (which
-// carries alpha_i = sum of the rounded psi(q_i) and d).
-template <int D, int DV>
-__device__ __forceinline__ void psiq_role(Small &S, uint32_t tb, const uint8_t *sQ,
-                                          int nchunks, const Guard &g) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, row = wq * 32 + lane;
-    const uint32_t lb = (uint32_t)(wq * 32) << 16;
-    const float dd = (float)D;
-    for (int c = 0; c < nchunks; ++c) {
-        bool ok = wait_warp(&S.q_full, c & 1, g, 40);
-        if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 0);
-        float alpha = 0.f;
-        if (ok) {
-            tc_fence_after();   // the MMAs that read the previous psi(q) have completed
-            // a real loop over 32-feature groups keeps the hot code small
-#pragma unroll 1
-            for (int grp = 0; grp < D / 32; ++grp) {   // 32 features -> 16 TMEM columns
-                uint4 raw[4];
-#pragma unroll
-                for (int f4 = 0; f4 < 4; ++f4) {
-                    const int f = grp * 4 + f4;
-                    raw[f4] = *reinterpret_cast<const uint4 *>(
-                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
-                }
-                uint32_t v[16];
-#pragma unroll
-                for (int f4 = 0; f4 < 4; ++f4) {
-                    const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const uint32_t pk =
-                            pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
-                        alpha += bf16_lo_f(pk) + bf16_hi_f(pk);
-                        v[f4 * 4 + h] = pk;
-                    }
-                }
-                tmem_st16(tb + lb + kColAq + grp * 16, v);
-            }
-            {   // A' = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0, ...]
-                const float ah = bf16_round(alpha);
-                const uint32_t aug0[4] = {pack_bf16x2(1.f, 1.f), pack_bf16x2(ah, alpha - ah),
-                                          pack_bf16x2(dd, ah), pack_bf16x2(dd, 0.f)};
-                const uint32_t aug1[4] = {0u, 0u, 0u, 0u};
-                tmem_st4(tb + lb + kColAq + D / 2, aug0);
-                tmem_st4(tb + lb + kColAq + D / 2 + 4, aug1);
-            }
-            mbar_arrive(&S.q_empty);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&S.phiq_done);
-            if (lane == 0) LA_TRACE_POINT(c, 16 + wq);
-            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 1);
-        }
-        if (group_any<kBarA>(!ok)) break;
-    }
-}
-
-// ------------------------------------------------------------------ group A2
-// Block c, once G = w is ready: w_ij (j <= i, else 0) split into bf16 hi + lo
-// pairs written back over G (the row sums come from the tensor core).
-template <int D, int DV>
-__device__ __forceinline__ void weights_role(Small &S, uint32_t tb, int nchunks, const Guard &g) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, row = wq * 32 + lane;
-    const uint32_t lb = (uint32_t)(wq * 32) << 16;
-    for (int c = 0; c < nchunks; ++c) {
-        const int cb = c & 1;
-        const bool ok = wait_warp(&S.g_full, c & 1, g, 43);
-        if (ok) {
-            tc_fence_after();
-            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 2);
-            // groups entirely above this warp's rows are all zero (causal mask);
-            // the TMEM load of the next group is issued before this group's math
-            const int last_grp = (wq * 32 + 31) >> 4;
-            // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
-            // (hi + lo equals w to within about 2^-17 w)
-            float rowsum = 0.f;
-            auto weights = [&](int grp, const uint32_t (&gc)[16]) {
-                uint32_t out[16];
-                if (grp > last_grp) {
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) out[m] = 0u;
-                } else {
-                    // j - 16 grp <= lim is kept; whole groups below the warp's rows keep all
-                    const int lim = (wq * 32 >= grp * 16 + 15) ? 15 : row - grp * 16;
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 2) {
-                        const float w0 = (jj <= lim) ? u2f(gc[jj]) : 0.f;
-                        const float w1 = (jj + 1 <= lim) ? u2f(gc[jj + 1]) : 0.f;
-                        const uint32_t hi = pack_bf16x2(w0, w1);
-                        const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
-                        rowsum += w0 + w1;   // hi + lo equals w to within 2^-17 w
-                        out[jj >> 1] = hi;
-                        out[8 + (jj >> 1)] = lo;
-                    }
-                }
-                tmem_st16(tb + lb + kColG + grp * 16, out);
-            };
-            // two groups per loop trip (ping-pong buffers): the TMEM load of the
-            // next group overlaps this group's math, and the hot code stays small
-            uint32_t gA[16], gB[16];
-            tmem_ld16(tb + lb + kColG, gA);
-            tmem_wait_ld();
-#pragma unroll 1
-            for (int grp = 0; grp < kC / 16; grp += 2) {
-                if (grp + 1 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 1) * 16, gB);
-                weights(grp, gA);
-                if (grp + 1 <= last_grp) tmem_wait_ld();
-                if (grp + 2 <= last_grp) tmem_ld16(tb + lb + kColG + (grp + 2) * 16, gA);
-                weights(grp + 1, gB);
-                if (grp + 2 <= last_grp) tmem_wait_ld();
-            }
-            S.rowsum[cb][row] = rowsum;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&S.h_ready[cb]);
-            if (lane == 0) LA_TRACE_POINT(c, 20 + wq);
-            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 3);
-        }
-        if (group_any<kBarA2>(!ok)) break;
-    }
-}
-
-// ------------------------------------------------------------------ group B
+// ------------------------------------------------------------------ state operands
 template <int D, int DV>
 __device__ __forceinline__ void export_row_bf16(uint8_t *sRt, int row, int grp,
                                                 const uint32_t (&rv)[16]) {
@@ -431,6 +303,139 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
     return (uint32_t)((n >> 3) * (D * 16) + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
 }
 
+// ------------------------------------------------------------------ group A
+// Eight warps, two per TMEM lane quarter; the two threads of a token row
+// (halves h = 0, 1) share its work.  Block c: psi(q) of half the features
+// each -> TMEM (A operand); h = 0 then adds the augmentation slice A' (with
+// alpha_i = sum of the rounded psi(q_i) over both halves, and d).  Once
+// G = w is ready, every other 16-column group each: w_ij (j <= i, else 0)
+// split into bf16 hi + lo pairs written back over G, and the partial row sums.
+template <int D, int DV>
+__device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
+                                             int nchunks, const Guard &g) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, row = wq * 32 + lane;
+    const int h = (warp - kWarpA) >> 2;
+    const uint32_t lb = (uint32_t)(wq * 32) << 16;
+    const float dd = (float)D;
+    // groups entirely above this warp's rows are all zero (causal mask)
+    const int last_grp = (wq * 32 + 31) >> 4;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cb = c & 1;
+        bool ok = wait_warp(&S.q_full, c & 1, g, 40);
+        if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
+        float alpha = 0.f;
+        if (ok) {
+            tc_fence_after();   // the MMAs that read the previous psi(q) have completed
+            // a real loop over 32-feature groups keeps the hot code small
+#pragma unroll 1
+            for (int gq = 0; gq < D / 64; ++gq) {
+                const int grp = h * (D / 64) + gq;   // 32 features -> 16 TMEM columns
+                uint4 raw[4];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const int f = grp * 4 + f4;
+                    raw[f4] = *reinterpret_cast<const uint4 *>(
+                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
+                }
+                uint32_t v[16];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
+#pragma unroll
+                    for (int hw = 0; hw < 4; ++hw) {
+                        const uint32_t pk =
+                            pack_bf16x2(psi_f(bf16_lo_f(w[hw])), psi_f(bf16_hi_f(w[hw])));
+                        alpha += bf16_lo_f(pk) + bf16_hi_f(pk);
+                        v[f4 * 4 + hw] = pk;
+                    }
+                }
+                tmem_st16(tb + lb + kColAq + grp * 16, v);
+            }
+            mbar_arrive(&S.q_empty);
+            if (h == 1) S.alpha_part[row] = alpha;
+            tmem_wait_st();
+            tc_fence_before();
+        }
+        // both halves of psi(q) are in TMEM, and alpha_part is written, past here
+        if (group_any<kBarA, 2 * kWG>(!ok)) break;
+        if (h == 0) {   // A' = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0, ...]
+            alpha += S.alpha_part[row];
+            const float ah = bf16_round(alpha);
+            const uint32_t aug0[4] = {pack_bf16x2(1.f, 1.f), pack_bf16x2(ah, alpha - ah),
+                                      pack_bf16x2(dd, ah), pack_bf16x2(dd, 0.f)};
+            const uint32_t aug1[4] = {0u, 0u, 0u, 0u};
+            tmem_st4(tb + lb + kColAq + D / 2, aug0);
+            tmem_st4(tb + lb + kColAq + D / 2 + 4, aug1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&S.phiq_done);
+            if (lane == 0) LA_TRACE_POINT(c, 16 + wq);
+            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 1);
+        }
+        ok = wait_warp(&S.g_full, c & 1, g, 43);
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 2);
+            // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
+            // (hi + lo equals w to within about 2^-17 w)
+            float rowsum = 0.f;
+            auto weights = [&](int grp, const uint32_t (&gc)[16]) {
+                uint32_t out[16];
+                if (grp > last_grp) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) out[m] = 0u;
+                } else {
+                    // j - 16 grp <= lim is kept; whole groups below the warp's rows keep all
+                    const int lim = (wq * 32 >= grp * 16 + 15) ? 15 : row - grp * 16;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 2) {
+                        const float w0 = (jj <= lim) ? u2f(gc[jj]) : 0.f;
+                        const float w1 = (jj + 1 <= lim) ? u2f(gc[jj + 1]) : 0.f;
+                        const uint32_t hi = pack_bf16x2(w0, w1);
+                        const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
+                        rowsum += w0 + w1;
+                        out[jj >> 1] = hi;
+                        out[8 + (jj >> 1)] = lo;
+                    }
+                }
+                tmem_st16(tb + lb + kColG + grp * 16, out);
+            };
+            // this half's groups h, h + 2, h + 4, h + 6, two per loop trip
+            // (ping-pong buffers: the TMEM load of the next group overlaps
+            // this group's math, and the hot code stays small)
+            uint32_t gA[16], gB[16];
+            if (h <= last_grp) {
+                tmem_ld16(tb + lb + kColG + h * 16, gA);
+                tmem_wait_ld();
+            }
+#pragma unroll 1
+            for (int t = 0; t < kC / 64; ++t) {
+                const int g0 = h + 4 * t, g1 = g0 + 2, g2 = g0 + 4;
+                const bool more = t + 1 < kC / 64;
+                if (g1 <= last_grp) tmem_ld16(tb + lb + kColG + g1 * 16, gB);
+                weights(g0, gA);
+                if (g1 <= last_grp) tmem_wait_ld();
+                if (more && g2 <= last_grp) tmem_ld16(tb + lb + kColG + g2 * 16, gA);
+                weights(g1, gB);
+                if (more && g2 <= last_grp) tmem_wait_ld();
+            }
+            S.rowsum[cb][h][row] = rowsum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&S.h_ready[cb]);
+            if (lane == 0 && h == 1) LA_TRACE_POINT(c, 20 + wq);
+            if (lane == 0 && wq == 3 && h == 1) LA_TRACE_POINT(c, 3);
+        }
+        if (group_any<kBarA, 2 * kWG>(!ok)) break;
+    }
+}
+
+// ------------------------------------------------------------------ group B
+// Eight warps, two per TMEM lane quarter, the two threads of a row (halves
+// h = 0, 1) sharing its work: psi(k) in place over half of the features,
+// the state export of half of R's columns, half of the output columns.
 template <int D, int DV>
 __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
                                              uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
@@ -441,22 +446,23 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     using Lay = Layout<D, DV>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
-    const int wtid = tid - kWarpB1 * 32;   // 0..127
+    const int h = (warp - kWarpB) >> 2;
+    const int wtid = tid - kWarpB * 32;   // 0..255
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const int N = nloc;   // tokens of this work item (segment)
+    constexpr int kRGroups = DV / 32;     // 16-column groups of R (and Y) per half
 
     // constant operand rows: [1|beta] row 0 = ones, rows 3..15 zero; zeta~ all zero
-    for (int e = wtid; e < 2 * 16 * kC; e += kWG) {
+    for (int e = wtid; e < 2 * 16 * kC; e += 2 * kWG) {
         const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
         *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
                                            (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
             __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
     }
-    for (int e = wtid; e < 16 * D; e += kWG)
+    for (int e = wtid; e < 16 * D; e += 2 * kWG)
         *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(e / D, e % D, D)) = __float2bfloat16_rn(0.f);
     // B' rows: slots 8..15 are zero for good (slots 0..7 are written per block)
-    for (int s = 0; s < 2; ++s)
-        *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(sGB + h * Lay::kGB + k16_off(row, 8)) = make_uint4(0u, 0u, 0u, 0u);
     // B'' row of column c, Bz row 0: [x_hi, x_lo, y_hi, y_hi, y_hi, y_lo, y_lo, 0 | 0...]
     // for (x, y) = (r_c, u_c) and (rho, n)
     auto aug_row = [](uint8_t *tile, int n, float x, float y) {
@@ -468,6 +474,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         *reinterpret_cast<uint4 *>(tile + k16_off(n, 8)) = make_uint4(0u, 0u, 0u, 0u);
     };
     if (wtid > 0 && wtid < 16) aug_row(sZB, wtid, 0.f, 0.f);   // rows 1..15 of Bz stay zero
+    mbar_arrive(&S.y_empty);   // Y is free for block 0
 
     // ---- initial state in split form S = 1 u^T + R, z = n 1 + zeta (u = first row
     //      of S, n = first entry of z; zero when absent); buffers [1] = "block -1"
@@ -477,7 +484,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const float *Sin = p.S_in ? p.S_in + (size_t)item * D * DV : nullptr;
         const float *zin = p.z_in ? p.z_in + (size_t)item * D : nullptr;
 #pragma unroll
-        for (int grp = 0; grp < DV / 16; ++grp) {
+        for (int gq = 0; gq < kRGroups; ++gq) {
+            const int grp = h * kRGroups + gq;
             uint32_t v[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
@@ -487,21 +495,25 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             tmem_st16(tb + lb + kColR + grp * 16, v);
             if (row < D) export_row_bf16<D, DV>(sRt, row, grp, v);
         }
-        const float zeta0 = (zin && row < D) ? zin[row] - zin[0] : 0.f;
-        float u0 = 0.f, r0 = 0.f;
-        if (Sin && row < DV) {
-            u0 = Sin[row];
-            for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
+        float zeta0 = 0.f;
+        if (h == 0) {
+            zeta0 = (zin && row < D) ? zin[row] - zin[0] : 0.f;
+            float u0 = 0.f, r0 = 0.f;
+            if (Sin && row < DV) {
+                u0 = Sin[row];
+                for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
+            }
+            const uint32_t zv[4] = {f2u(zeta0), 0u, 0u, 0u};
+            const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
+            tmem_st4(tb + lb + kColZ, zv);
+            tmem_st4(tb + lb + kColUV, uv);
+            S.zeta[row] = zeta0;
+            S.u[1][row] = u0;
+            if (row < DV) aug_row(sYB, row, r0, u0);
         }
-        const uint32_t zv[4] = {f2u(zeta0), 0u, 0u, 0u};
-        const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
-        tmem_st4(tb + lb + kColZ, zv);
-        tmem_st4(tb + lb + kColUV, uv);
-        S.zeta[row] = zeta0;
-        S.u[1][row] = u0;
-        if (row < DV) aug_row(sYB, row, r0, u0);
-        named_bar(kBarB, kWG);  // zero rows of zeta~ written before row 0 below
-        if (row < D) *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
+        named_bar(kBarB, 2 * kWG);  // zero rows of zeta~ written before row 0 below
+        if (h == 0 && row < D)
+            *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
         if (wtid == 0) {
             float rho0 = 0.f;
             if (zin)
@@ -513,69 +525,83 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         tmem_wait_st();
         fence_proxy_async();
         tc_fence_before();
-        named_bar(kBarB, kWG);
-        mbar_arrive(&S.rt_ready);
+        mbar_arrive(&S.rt_ready);   // every thread, after its own writes
     }
 
-
-    // psi(k) in place (bf16), beta_j = sum of the rounded row, [1|beta] operand rows
+    // psi(k) in place (bf16) over this half's features; beta_j = sum of the
+    // rounded row over both halves; h = 0 writes the [1|beta] and B' rows.
+    // Returns false when the group gave up (agreed at the group barrier).
     auto phi_k = [&](int c) -> bool {
         const int s = c & 1, cb = c & 1;
-        if (!wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50)) return false;
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 6);
+        const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
         float beta = 0.f;
-        // 8 chunks of 8 features per batch: all loads of a batch are issued
-        // before its in-place stores so their latencies overlap
+        if (ok) {
+            constexpr int kChunks = D / 16;                       // 8-feature chunks per half
+            constexpr int kBatch = kChunks < 8 ? kChunks : 8;
+            // all loads of a batch are issued before its in-place stores so
+            // their latencies overlap
 #pragma unroll 1
-        for (int f0 = 0; f0 < D / 8; f0 += 8) {
-            uint4 raw[8];
+            for (int b0 = 0; b0 < kChunks; b0 += kBatch) {
+                const int f0 = h * kChunks + b0;
+                uint4 raw[kBatch];
 #pragma unroll
-            for (int f = 0; f < 8; ++f)
-                raw[f] = *reinterpret_cast<const uint4 *>(
-                    kt + ((f0 + f) >> 3) * (kC * 128) + sw128_off(row, ((f0 + f) & 7) * 8));
+                for (int f = 0; f < kBatch; ++f)
+                    raw[f] = *reinterpret_cast<const uint4 *>(
+                        kt + ((f0 + f) >> 3) * (kC * 128) + sw128_off(row, ((f0 + f) & 7) * 8));
 #pragma unroll
-            for (int f = 0; f < 8; ++f) {
-                uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
+                for (int f = 0; f < kBatch; ++f) {
+                    uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t pk = pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
-                    beta += bf16_lo_f(pk) + bf16_hi_f(pk);
-                    w[h] = pk;
+                    for (int hw = 0; hw < 4; ++hw) {
+                        const uint32_t pk =
+                            pack_bf16x2(psi_f(bf16_lo_f(w[hw])), psi_f(bf16_hi_f(w[hw])));
+                        beta += bf16_lo_f(pk) + bf16_hi_f(pk);
+                        w[hw] = pk;
+                    }
+                    raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
 #pragma unroll
-            for (int f = 0; f < 8; ++f)
-                *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
-                                           sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
+                for (int f = 0; f < kBatch; ++f)
+                    *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
+                                               sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
+            }
+            if (h == 1) S.beta_part[row] = beta;
+            fence_proxy_async();
         }
-        const float bh = bf16_round(beta);
-        uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
-        *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
-        *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
-        // B' row of key j: [beta_hi, beta_lo, 1, 1, 1, 0, 0, 0]
-        *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) =
-            make_uint4(pack_bf16x2(bh, beta - bh), pack_bf16x2(1.f, 1.f), pack_bf16x2(1.f, 0.f), 0u);
-        const float bsum = warp_sum_f(beta);
-        if (lane == 0) S.rho_part[cb][wq] = bsum;
-        fence_proxy_async();
-        mbar_arrive(&S.phik_done[s]);
-        if (lane == 0) LA_TRACE_POINT(c, 26 + wq);
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 7);
+        if (group_any<kBarB, 2 * kWG>(!ok)) return false;
+        if (h == 0) {
+            beta += S.beta_part[row];
+            const float bh = bf16_round(beta);
+            uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
+            *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
+            // B' row of key j: [beta_hi, beta_lo, 1, 1, 1, 0, 0, 0]
+            *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) = make_uint4(
+                pack_bf16x2(bh, beta - bh), pack_bf16x2(1.f, 1.f), pack_bf16x2(1.f, 0.f), 0u);
+            const float bsum = warp_sum_f(beta);
+            if (lane == 0) S.rho_part[cb][wq] = bsum;
+            fence_proxy_async();
+            mbar_arrive(&S.phik_done[s]);
+            if (lane == 0) LA_TRACE_POINT(c, 26 + wq);
+            if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 7);
+        }
         return true;
     };
 
-    // state after block c: R -> bf16 operand, zeta -> zeta~, u, r, n, rho
+    // state after block c: R -> bf16 operand (this half's columns); h = 0:
+    // zeta -> zeta~, u, r, n, rho and the augmentation rows
     auto export_state = [&](int c) -> bool {
         const int cb = c & 1, pb = (c + 1) & 1;
         const int L = min(kC, N - c * kC);
         if (!wait_warp(&S.st_full, c & 1, g, 51) || !wait_warp(&S.aq_free, c & 1, g, 54))
             return false;
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 4);
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 4);
         tc_fence_after();
 #pragma unroll
-        for (int grp = 0; grp < DV / 16; grp += 2) {
+        for (int gq = 0; gq < kRGroups; gq += 2) {
+            const int grp = h * kRGroups + gq;
             uint32_t rv0[16], rv1[16];
             tmem_ld16(tb + lb + kColR + grp * 16, rv0);
             tmem_ld16(tb + lb + kColR + (grp + 1) * 16, rv1);
@@ -585,42 +611,96 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 export_row_bf16<D, DV>(sRt, row, grp + 1, rv1);
             }
         }
-        uint32_t zv[4], uv[4];
-        tmem_ld4(tb + lb + kColZ, zv);
-        tmem_ld4(tb + lb + kColUV, uv);
-        tmem_wait_ld();
-        if (row < D) {
-            S.zeta[row] = u2f(zv[0]);
-            *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
-                __float2bfloat16_rn(u2f(zv[0]));
-        }
-        S.u[cb][row] = u2f(uv[0]);
-        if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u2f(uv[0]));
-        if (wtid == 0) {
-            S.n_s[cb] = S.n_s[pb] + (float)L;
-            S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[cb][0] + S.rho_part[cb][1]) +
-                                         (S.rho_part[cb][2] + S.rho_part[cb][3]));
-            aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
+        if (h == 0) {
+            uint32_t zv[4], uv[4];
+            tmem_ld4(tb + lb + kColZ, zv);
+            tmem_ld4(tb + lb + kColUV, uv);
+            tmem_wait_ld();
+            if (row < D) {
+                S.zeta[row] = u2f(zv[0]);
+                *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
+                    __float2bfloat16_rn(u2f(zv[0]));
+            }
+            S.u[cb][row] = u2f(uv[0]);
+            if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u2f(uv[0]));
+            if (wtid == 0) {
+                S.n_s[cb] = S.n_s[pb] + (float)L;
+                S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[cb][0] + S.rho_part[cb][1]) +
+                                             (S.rho_part[cb][2] + S.rho_part[cb][3]));
+                aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
+            }
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&S.rt_ready);
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 5);
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 5);
         return true;
     };
 
-    // Software pipeline, psi(k) two blocks ahead: iteration c runs psi(k) of
-    // block c+2 and the state export after block c+1, so the tensor core
-    // updates the state for block c+1 while psi(k) runs.
-    bool ok0 = phi_k(0);
-    if (ok0 && nchunks > 1) ok0 = phi_k(1);
-    bool aborted = group_any<kBarB>(!ok0);
-    if (!aborted) aborted = group_any<kBarB>(!export_state(0));
-    for (int c = 0; c + 1 < nchunks && !aborted; ++c) {
-        bool ok = true;
-        if (c + 2 < nchunks) ok = phi_k(c + 2);
-        if (ok) ok = export_state(c + 1);
-        if (group_any<kBarB>(!ok)) aborted = true;
+    // y = Y / max(Yz + rowsum, eps): the tensor core has already summed every
+    // part of the numerator ((d + alpha) u + r + a R + P V) and the inter-block
+    // denominator ((d + alpha) n + rho + a.zeta).  Each thread takes 1/den of
+    // its own row; the values are then read back through the 16x256b TMEM
+    // shape, where 4 neighbouring lanes hold 8 consecutive columns of one row,
+    // so every warp store writes whole 32-byte sectors (8 rows x 32 bytes).
+    // Half h takes the 16-lane half h of its quarter (parts h, h + 2, ...).
+    auto epilogue = [&](int c) -> bool {
+        const int t0 = c * kC, cb = c & 1;
+        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
+            return false;
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 8);
+        tc_fence_after();
+        uint32_t yz[4];
+        tmem_ld4(tb + lb + kColYz, yz);
+        tmem_wait_ld();
+        S.e_inv[h][row] =
+            1.f / fmaxf(u2f(yz[0]) + (S.rowsum[cb][0][row] + S.rowsum[cb][1][row]), p.eps);
+        __syncwarp();
+        float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
+        const int tq = lane >> 2, tc = (lane & 3) * 2;
+        constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
+        auto part_addr = [&](int part) {
+            return tb + ((uint32_t)(wq * 32 + 16 * (part & 1)) << 16) + kColY + (part >> 1) * 64;
+        };
+        const float *einv = S.e_inv[h];
+        auto outputs = [&](int part, const uint32_t (&vc)[32]) {
+            const int half = part & 1, cblk = part >> 1;
+            const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
+            const float invA = einv[rA], invB = einv[rB];
+            const bool okA = t0 + rA < N, okB = t0 + rB < N;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int col = cblk * 64 + 8 * k + tc;
+                const float2 oA = make_float2(u2f(vc[4 * k]) * invA, u2f(vc[4 * k + 1]) * invA);
+                const float2 oB = make_float2(u2f(vc[4 * k + 2]) * invB, u2f(vc[4 * k + 3]) * invB);
+                if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
+                if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
+            }
+        };
+        uint32_t vA[32];
+#pragma unroll 1
+        for (int part = h; part < kParts; part += 2) {
+            tmem_ld_16x256b_x8(part_addr(part), vA);
+            tmem_wait_ld();
+            outputs(part, vA);
+        }
+        tc_fence_before();
+        mbar_arrive(&S.y_empty);
+        if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 9);
+        return true;
+    };
+
+    // Software pipeline, psi(k) two blocks ahead: iteration c runs the outputs
+    // of block c, psi(k) of block c+2 and the state export after block c+1.
+    bool aborted = !phi_k(0);
+    if (!aborted && nchunks > 1) aborted = !phi_k(1);
+    if (!aborted) aborted = group_any<kBarB, 2 * kWG>(!export_state(0));
+    for (int c = 0; c < nchunks && !aborted; ++c) {
+        bool ok = epilogue(c);
+        if (group_any<kBarB, 2 * kWG>(!ok)) { aborted = true; break; }
+        if (c + 2 < nchunks && !phi_k(c + 2)) { aborted = true; break; }
+        if (c + 1 < nchunks) ok = export_state(c + 1);
+        if (group_any<kBarB, 2 * kWG>(!ok)) aborted = true;
     }
 
     // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
@@ -628,7 +708,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const int lbuf = (nchunks - 1) & 1;
         tc_fence_after();
 #pragma unroll
-        for (int grp = 0; grp < DV / 16; ++grp) {
+        for (int gq = 0; gq < kRGroups; ++gq) {
+            const int grp = h * kRGroups + gq;
             uint32_t rv[16];
             tmem_ld16(tb + lb + kColR + grp * 16, rv);
             tmem_wait_ld();
@@ -643,77 +724,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                         u2f(rv[jj + 3]) + S.u[lbuf][grp * 16 + jj + 3]);
             }
         }
-        if (row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];
+        if (h == 0 && row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];
     }
-}
-
-// ------------------------------------------------------------------ group B2
-template <int D, int DV>
-__device__ __forceinline__ void output_role(Small &S, uint32_t tb, const TcParams &p, int head,
-                                            int tok0, int nloc, int nchunks, const Guard &g) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, row = wq * 32 + lane;
-    const uint32_t lb = (uint32_t)(wq * 32) << 16;
-    const int N = nloc;   // tokens of this work item (segment)
-    mbar_arrive(&S.y_empty);   // Y is free for block 0
-
-    // y = Y / max(Yz + rowsum, eps): the tensor core has already summed every
-    // part of the numerator ((d + alpha) u + r + a R + P V) and the inter-block
-    // denominator ((d + alpha) n + rho + a.zeta).  Each thread takes 1/den of
-    // its own row; the values are then read back through the 16x256b TMEM
-    // shape, where 4 neighbouring lanes hold 8 consecutive columns of one row,
-    // so every warp store writes whole 32-byte sectors (8 rows x 32 bytes).
-    auto epilogue = [&](int c) -> bool {
-        const int t0 = c * kC, cb = c & 1;
-        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
-            return false;
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 8);
-        tc_fence_after();
-        uint32_t yz[4];
-        tmem_ld4(tb + lb + kColYz, yz);
-        tmem_wait_ld();
-        S.e_inv[row] = 1.f / fmaxf(u2f(yz[0]) + S.rowsum[cb][row], p.eps);
-        __syncwarp();
-        float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
-        const int tq = lane >> 2, tc = (lane & 3) * 2;
-        constexpr int kParts = 2 * (DV / 64);   // (16-lane half, 64-column block) pairs
-        auto part_addr = [&](int part) {
-            return tb + ((uint32_t)(wq * 32 + 16 * (part & 1)) << 16) + kColY + (part >> 1) * 64;
-        };
-        auto outputs = [&](int part, const uint32_t (&vc)[32]) {
-            const int half = part & 1, cblk = part >> 1;
-            const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
-            const float invA = S.e_inv[rA], invB = S.e_inv[rB];
-            const bool okA = t0 + rA < N, okB = t0 + rB < N;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int col = cblk * 64 + 8 * k + tc;
-                const float2 oA = make_float2(u2f(vc[4 * k]) * invA, u2f(vc[4 * k + 1]) * invA);
-                const float2 oB = make_float2(u2f(vc[4 * k + 2]) * invB, u2f(vc[4 * k + 3]) * invB);
-                if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
-                if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
-            }
-        };
-        uint32_t vA[32], vB[32];
-        tmem_ld_16x256b_x8(part_addr(0), vA);
-        tmem_wait_ld();
-#pragma unroll 1
-        for (int part = 0; part < kParts; part += 2) {
-            tmem_ld_16x256b_x8(part_addr(part + 1), vB);   // kParts is even
-            outputs(part, vA);
-            tmem_wait_ld();
-            if (part + 2 < kParts) tmem_ld_16x256b_x8(part_addr(part + 2), vA);
-            outputs(part + 1, vB);
-            if (part + 2 < kParts) tmem_wait_ld();
-        }
-        tc_fence_before();
-        mbar_arrive(&S.y_empty);
-        if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 9);
-        return true;
-    };
-
-    for (int c = 0; c < nchunks; ++c)
-        if (group_any<kBarB2>(!epilogue(c))) break;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -745,22 +757,22 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     if (tid == 0) {
         S.abort_flag = 0;
         mbar_init(&S.q_full, 1);
-        mbar_init(&S.q_empty, kWG);
+        mbar_init(&S.q_empty, 2 * kWG);        // every group-A thread
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.kv_full[s], 1);
             mbar_init(&S.kv_empty[s], 1);
         }
-        mbar_init(&S.phiq_done, kWG);
-        mbar_init(&S.phik_done[0], kWG);
+        mbar_init(&S.phiq_done, kWG);          // group-A first halves
+        mbar_init(&S.phik_done[0], kWG);       // group-B first halves
         mbar_init(&S.phik_done[1], kWG);
         mbar_init(&S.g_full, 1);
         mbar_init(&S.aq_free, 1);
-        mbar_init(&S.h_ready[0], kWG);
-        mbar_init(&S.h_ready[1], kWG);
+        mbar_init(&S.h_ready[0], 2 * kWG);     // every group-A thread
+        mbar_init(&S.h_ready[1], 2 * kWG);
         mbar_init(&S.st_full, 1);
-        mbar_init(&S.rt_ready, kWG);
+        mbar_init(&S.rt_ready, 2 * kWG);       // every group-B thread
         mbar_init(&S.y_full, 1);
-        mbar_init(&S.y_empty, kWG);
+        mbar_init(&S.y_empty, 2 * kWG);        // every group-B thread
         mbar_init(&S.drain, 1);
         fence_mbar_init();
         prefetch_tmap(&qmap);
@@ -786,12 +798,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
                                            item == p.drop_item, g);
     } else if (warp == 1) {
         if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
-    } else if (warp < kWarpA2) {
-        psiq_role<D, DV>(S, tb, sQ, nchunks, g);
-    } else if (warp < kWarpB1) {
-        weights_role<D, DV>(S, tb, nchunks, g);
-    } else if (warp >= kWarpB2) {
-        output_role<D, DV>(S, tb, p, head, tok0, nloc, nchunks, g);
+    } else if (warp < kWarpB) {
+        group_a_role<D, DV>(S, tb, sQ, nchunks, g);
     } else {
         group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0, nloc,
                             seg == p.nseg - 1, nchunks, g);

@@ -80,15 +80,15 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint6
 }
 
 // Group barrier that also agrees on "someone gave up": returns true if any of
-// the group's 128 threads passes failed = true.
-template <int BAR>
+// the group's COUNT threads passes failed = true.
+template <int BAR, int COUNT = kWG>
 __device__ __forceinline__ bool group_any(bool failed) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
         "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)failed), "n"(BAR), "n"(kWG)
+        : "r"((uint32_t)failed), "n"(BAR), "n"(COUNT)
         : "memory");
     return r != 0;
 }

@@ -501,6 +501,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             float u0 = 0.f, r0 = 0.f;
             if (Sin && row < DV) {
                 u0 = Sin[row];
+                // independent loads, issued 16 at a time ahead of the sums
+#pragma unroll 16
                 for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
             }
             const uint32_t zv[4] = {f2u(zeta0), 0u, 0u, 0u};
@@ -516,8 +518,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
         if (wtid == 0) {
             float rho0 = 0.f;
-            if (zin)
-                for (int a = 1; a < D; ++a) rho0 += zin[a] - zin[0];
+            if (zin) {
+                const float z0 = zin[0];
+#pragma unroll 16
+                for (int a = 1; a < D; ++a) rho0 += zin[a] - z0;
+            }
             S.n_s[1] = zin ? zin[0] : 0.f;
             S.rho_s[1] = rho0;
             aug_row(sZB, 0, rho0, S.n_s[1]);

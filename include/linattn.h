@@ -116,6 +116,36 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Device staging memory, in bytes, that la_forward_causal_host needs for
+ * these sizes (0 for N == 0 or unsupported sizes).  Like the workspace size,
+ * it depends on the current device's SM count.
+ */
+LA_API size_t la_causal_host_buffer_bytes(int B, int H, int N, int d, int dv, la_dtype dt);
+
+/*
+ * la_forward_causal on HOST buffers (no counterpart on the pages: it is the
+ * path for callers whose q, k, v and y live in host memory).  q, k, v, y (and
+ * the optional S_out, z_out, both or neither) are host pointers with the same
+ * layouts as in la_forward_causal; the initial state is zero.  The call
+ * copies the inputs to the device, runs the forward and copies y (and the
+ * final state) back, pipelined over groups of heads: the upload of one group,
+ * the kernels of the previous one and the download of the one before run at
+ * once, on two streams the call creates and destroys plus `stream`, which the
+ * work is ordered after.  It returns when the results are in host memory.
+ * Page-locked host memory gives asynchronous full-speed copies; pageable
+ * memory works but its copies are staged by the driver and do not overlap.
+ * dev_buf is caller-owned device memory of at least
+ * la_causal_host_buffer_bytes(...) bytes, 256-byte aligned; its contents are
+ * scratch.  Errors: as la_forward_causal (checked per group), LA_ERR_WORKSPACE
+ * for a missing, short or misaligned dev_buf, LA_ERR_TIMEOUT when a bounded
+ * wait of any group ran out (the outputs are then undefined).
+ */
+LA_API la_status la_forward_causal_host(const void *q, const void *k, const void *v, float *y,
+                                        int B, int H, int N, int d, int dv, la_dtype dt,
+                                        float eps, float *S_out, float *z_out, void *dev_buf,
+                                        size_t dev_buf_bytes, void *stream);
+
+/*
  * Non-causal forward ("Linear Attention/es", "Reformulación con núcleos"):
  *   S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j) over all N tokens, then
  *   y_i = phi(q_i)^T S / max(phi(q_i)^T z, eps) for every i.

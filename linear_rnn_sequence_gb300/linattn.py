@@ -65,6 +65,11 @@ def lib():
             L.la_forward_noncausal.restype = i
             L.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
             L.la_decode_step.restype = i
+            L.la_causal_host_buffer_bytes.argtypes = [i, i, i, i, i, i]
+            L.la_causal_host_buffer_bytes.restype = sz
+            L.la_forward_causal_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
+                                                 sz, vp]
+            L.la_forward_causal_host.restype = i
             L.la_workspace_status.argtypes = [vp, sz, vp]
             L.la_workspace_status.restype = i
             L.la_debug_set_fault.argtypes = [i, ctypes.c_longlong]
@@ -161,6 +166,43 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
         err, where = workspace_header(workspace)
         if err != LA_OK:
             raise LinAttnError(err, f"la_forward_causal (run time, wait site {where})")
+    return (y, S_out, z_out) if return_state else y
+
+
+def causal_host_buffer_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(lib().la_causal_host_buffer_bytes(B, H, N, d, dv, code))
+
+
+def forward_causal_host(q, k, v, eps: float = 1e-6, return_state=False, out=None, S_out=None,
+                        z_out=None, dev_buf=None, device=None, stream=None):
+    """Causal forward on host (CPU) tensors through la_forward_causal_host.
+
+    q, k: [B,H,N,d]; v: [B,H,N,dv] CPU tensors (bf16 or fp32; page-locked
+    memory makes the copies overlap).  Returns y [B,H,N,dv] float32 on the CPU
+    (and the final (S, z) when ``return_state``).  ``dev_buf`` is the device
+    staging memory (allocated on ``device`` when not given).
+    """
+    for t in (q, k, v, out, S_out, z_out):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("forward_causal_host takes contiguous CPU tensors")
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32)
+        z_out = torch.empty((B, H, d), dtype=torch.float32)
+    if dev_buf is None:
+        dev_buf = alloc_workspace(int(lib().la_causal_host_buffer_bytes(B, H, N, d, dv, dt)), dev)
+    nbytes = 0 if dev_buf is None else dev_buf.numel() * dev_buf.element_size()
+    st = lib().la_forward_causal_host(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                      float(eps), _ptr(S_out), _ptr(z_out), _ptr(dev_buf), nbytes,
+                                      _stream_handle(stream, dev))
+    _raise(st, "la_forward_causal_host")
     return (y, S_out, z_out) if return_state else y
 
 

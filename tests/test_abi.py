@@ -126,6 +126,25 @@ def test_decode_requires_state():
     assert st == la.LA_ERR_INVALID_ARG
 
 
+def test_host_entry_point_rejects_bad_arguments():
+    L = la.lib()
+    h = ctypes.c_void_p(1 << 20)
+    # null inputs, mismatched state pointers, bad eps, unsupported sizes: no copy is issued
+    assert L.la_forward_causal_host(None, h, h, h, 1, 1, 8, 64, 64, 1, 1e-6, None, None, P, 1 << 30,
+                                    None) == la.LA_ERR_INVALID_ARG
+    assert L.la_forward_causal_host(h, h, h, Y, 1, 1, 8, 64, 64, 1, 1e-6, h, None, P, 1 << 30,
+                                    None) == la.LA_ERR_INVALID_ARG
+    assert L.la_forward_causal_host(h, h, h, Y, 1, 1, 8, 64, 64, 1, 0.0, None, None, P, 1 << 30,
+                                    None) == la.LA_ERR_INVALID_ARG
+    assert L.la_forward_causal_host(h, h, h, Y, 1, 1, 8, 48, 64, 1, 1e-6, None, None, P, 1 << 30,
+                                    None) == la.LA_ERR_UNSUPPORTED
+    # y overlapping q in host memory
+    assert L.la_forward_causal_host(h, P2, P3, ctypes.c_void_p((1 << 20) + 64), 1, 1, 8, 64, 64, 1,
+                                    1e-6, None, None, P, 1 << 30, None) == la.LA_ERR_INVALID_ARG
+    assert L.la_causal_host_buffer_bytes(1, 1, 0, 64, 64, 1) == 0
+    assert L.la_causal_host_buffer_bytes(2, 8, 1000, 64, 64, 1) > 0
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     q = torch.zeros(1, 1, 4, 32)

@@ -208,3 +208,32 @@ def test_noncausal_tc_shapes(B, H, N, d, dv, cuda_device):
     e = (rel_max_err(y, yo), rel_max_err(S, So), rel_max_err(z, zo))
     print(f"noncausal tc B{B}H{H}N{N}d{d}dv{dv}: y {e[0]:.2e} S {e[1]:.2e} z {e[2]:.2e}")
     assert max(e) <= TOL_BF16
+
+
+@pytest.mark.parametrize("B,H,N,d,dv,dt,pinned", [
+    (2, 8, 700, 128, 128, torch.bfloat16, True),     # 16 heads in 8 groups
+    (1, 3, 257, 64, 64, torch.bfloat16, False),      # pageable memory, fewer heads than groups
+    (1, 5, 300, 64, 32, torch.float32, True),        # CUDA-core path
+])
+def test_causal_host_buffers_match_oracle(B, H, N, d, dv, dt, pinned, cuda_device):
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=dt, scale=d ** -0.5, seed=N + H)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    y, S, z = la.forward_causal_host(q, k, v, return_state=True, device=cuda_device)
+    assert not y.is_cuda and y.shape == (B, H, N, dv)
+    yo, So, zo = oracle.causal_recurrent(q, k, v, return_state=True)
+    tol = tol_for(dt)
+    assert rel_max_err(y, yo) <= tol
+    assert rel_max_err(S, So) <= tol and rel_max_err(z, zo) <= tol
+    # same numbers as the device-pointer entry point, up to summation order
+    yd = la.forward_causal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device)).cpu()
+    assert rel_max_err(y, yd.double().numpy()) <= tol
+
+
+def test_causal_host_buffer_too_small_is_rejected(cuda_device):
+    q, k, v = random_qkv(1, 2, 256, 64, 64, dtype=torch.bfloat16)
+    need = la.causal_host_buffer_bytes(1, 2, 256, 64, 64)
+    buf = torch.empty(need - 256, dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(la.LinAttnError) as ei:
+        la.forward_causal_host(q, k, v, dev_buf=buf, device=cuda_device)
+    assert ei.value.status == la.LA_ERR_WORKSPACE

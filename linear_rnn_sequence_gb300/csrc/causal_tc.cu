@@ -20,23 +20,29 @@
 //   z               = n 1 + zeta, n = token count, zeta = sum_j b_j
 //   phi(q_i)^T S    = (d + alpha_i) u + r + a_i R,          r = sum_j beta_j v_j = colsum(R)
 //   phi(q_i)^T z    = (d + alpha_i) n + rho + a_i . zeta,   rho = sum_j beta_j
-// The intra-block weights w_ij (about d) are split into bf16 hi + lo parts
-// for the P.V product, so their rounding error is about 2^-17 of w.
-// All accumulation is fp32 (TMEM).  The result is the exact attention of the
-// features 1 + bf16(psi(x)); the outputs are float32.
+// The constant parts enter the MMAs through one extra K = 16 slice of the
+// psi(q) operand (carrying 1, alpha and d as bf16 hi/lo pairs) against small
+// tiles holding beta, u, r, n and rho, so the tensor core returns the full
+// weight w, numerator and inter-block denominator.  The intra-block weights
+// w_ij (about d) are split into bf16 hi + lo parts for the P.V product, so
+// their rounding error is about 2^-17 of w.  All accumulation is fp32 (TMEM).
+// The result is the exact attention of the features 1 + bf16(psi(x)); the
+// outputs are float32.
 //
-// One CTA owns one head (b, h) and walks its blocks in order.  Warp roles:
-//   warp 0      TMA producer: Q (1 stage), K and V (2 stages) tiles, 128B swizzle
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..5  group A (thread = TMEM lane = token row): psi(q) into TMEM,
-//               then the weight epilogue (G -> w hi/lo in TMEM, row sums)
-//   warps 6..9  group B (thread = TMEM lane): psi(k) in place in shared
-//               memory, state export (R -> bf16 operand, zeta, u, r) and the
-//               output epilogue (shared-memory transpose, 16-byte stores)
-// The two groups work on neighbouring blocks at once, so phi, the weight
-// epilogue, the tensor-core MMAs and the output epilogue overlap.
-// TMEM columns: R [0,dv) | Y [128,128+dv) | G/P [256,384) | psi(q) [384,384+d/2)
-//               | a.zeta [448,464) | zeta [464,480) | u,r [480,496).
+// One CTA owns one (head, segment) work item and walks its blocks in order.
+// Warp roles (18 warps):
+//   warp 0       TMA producer: Q (1 stage), K and V (2 stages) tiles, 128B swizzle
+//   warp 1       TMEM allocator and single-thread MMA issuer
+//   warps 2..9   group A, two warps per TMEM lane quarter (the pair splits a
+//                token row): psi(q) into TMEM, then the weight epilogue
+//                (G -> w hi/lo in TMEM, row sums)
+//   warps 10..17 group B, likewise: psi(k) in place in shared memory, the
+//                state export (R -> bf16 operand, zeta, u, r, n, rho) and the
+//                output epilogue (16x256b TMEM loads, 32-byte-sector stores)
+// The two groups work on neighbouring blocks at once, so the psi passes, the
+// weight epilogue, the tensor-core MMAs and the output epilogue overlap.
+// TMEM columns: R [0,dv) | Y [128,128+dv) | G/P [256,384) | psi(q) and its
+// augmentation [384,384+d/2+8) | a.zeta [464,480) | zeta [480,496) | u,r [496,512).
 // Every wait is bounded in time; a wait that runs out records LA_ERR_TIMEOUT
 // in the workspace header and the CTA unwinds (no trap, no hang).
 #include <cuda.h>

@@ -4,7 +4,7 @@
 // The B*H heads are cut into groups.  Group i goes through three streams:
 // its q, k, v copies on an upload stream, its forward on the caller's stream,
 // and its y (and final state) copies on a download stream, ordered by events.
-// Two device staging sets alternate between the groups, so the upload of
+// Three device staging sets rotate between the groups, so the upload of
 // group i+1, the forward of group i and the download of group i-1 can run at
 // once, and uploads and downloads use both directions of the host link.
 // Every group is an ordinary la_forward_causal call on device pointers: heads
@@ -19,8 +19,8 @@
 namespace la {
 namespace {
 
-constexpr int kHostGroups = 8;    // head groups per call (fewer when there are fewer heads)
-constexpr int kHostSets = 2;      // device staging sets
+constexpr int kHostGroups = 16;   // head groups per call (fewer when there are fewer heads)
+constexpr int kHostSets = 3;      // device staging sets
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 

@@ -38,11 +38,14 @@ struct TcParams {
 };
 
 // psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
-// lanes with inputs of either sign stay converged: for x > 0 the exponential
-// of 0 is exactly 1 and the second term vanishes.  e^x = 2^(x log2 e) with the
-// flush-to-zero form (x <= 0 here, so a flushed result only means e^x < 2^-126).
+// lanes with inputs of either sign stay converged: e^min(x,0) - 1 is 0 for
+// x > 0, and for x <= 0 it is at least x (e^x >= 1 + x), so the maximum with
+// x picks the right branch.  e^x = 2^(x log2 e) with the flush-to-zero form
+// (x <= 0 here, so a flushed result only means e^x < 2^-126).  Where e^x - 1
+// and x are within the exponential's rounding of each other (|x| < ~1e-3)
+// either one is psi(x) to well below the bf16 rounding the result gets.
 __device__ __forceinline__ float psi_f(float x) {
-    return fmaxf(x, 0.f) + (ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
+    return fmaxf(x, ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
 }
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));

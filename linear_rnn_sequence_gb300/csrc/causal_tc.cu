@@ -332,6 +332,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
         float alpha = 0.f;
+        uint64_t alpha2 = f2pack(0.f, 0.f);
         if (ok) {
             tc_fence_after();   // the MMAs that read the previous psi(q) have completed
             // a real loop over 32-feature groups keeps the hot code small
@@ -351,15 +352,15 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                     const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk =
-                            pack_bf16x2(psi_f(bf16_lo_f(w[hw])), psi_f(bf16_hi_f(w[hw])));
-                        alpha += bf16_lo_f(pk) + bf16_hi_f(pk);
+                        const uint32_t pk = psi_bf16x2(w[hw]);
+                        alpha2 = acc_bf16x2(alpha2, pk);
                         v[f4 * 4 + hw] = pk;
                     }
                 }
                 tmem_st16(tb + lb + kColAq + grp * 16, v);
             }
             mbar_arrive(&S.q_empty);
+            alpha = f2sum(alpha2);
             if (h == 1) S.alpha_part[row] = alpha;
             tmem_wait_st();
             tc_fence_before();
@@ -548,6 +549,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
         float beta = 0.f;
+        uint64_t beta2 = f2pack(0.f, 0.f);
         if (ok) {
             constexpr int kChunks = D / 16;                       // 8-feature chunks per half
             constexpr int kBatch = kChunks < 8 ? kChunks : 8;
@@ -566,9 +568,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk =
-                            pack_bf16x2(psi_f(bf16_lo_f(w[hw])), psi_f(bf16_hi_f(w[hw])));
-                        beta += bf16_lo_f(pk) + bf16_hi_f(pk);
+                        const uint32_t pk = psi_bf16x2(w[hw]);
+                        beta2 = acc_bf16x2(beta2, pk);
                         w[hw] = pk;
                     }
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -578,6 +579,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
                                                sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
             }
+            beta = f2sum(beta2);
             if (h == 1) S.beta_part[row] = beta;
             fence_proxy_async();
         }

@@ -47,6 +47,50 @@ struct TcParams {
 __device__ __forceinline__ float psi_f(float x) {
     return fmaxf(x, ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
 }
+// Packed fp32 pairs (two floats in one 64-bit register; the f32x2 arithmetic
+// of sm_100 and later does both lanes in one instruction).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// psi of both bf16 halves of w, rounded back to bf16x2 (psi_f on each half,
+// with the multiply and the -1 done on the pair).
+__device__ __forceinline__ uint32_t psi_bf16x2(uint32_t w) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1;
+    f2unpack(f2mul(f2pack(fminf(x0, 0.f), fminf(x1, 0.f)),
+                   f2pack(1.4426950408889634f, 1.4426950408889634f)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), f2pack(-1.f, -1.f)), e0, e1);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(fmaxf(x1, e1)), "f"(fmaxf(x0, e0)));
+    return r;
+}
+
+// acc (two fp32 lanes) += the two bf16 halves of p.
+__device__ __forceinline__ uint64_t acc_bf16x2(uint64_t acc, uint32_t p) {
+    return f2add(acc, f2pack(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)));
+}
+__device__ __forceinline__ float f2sum(uint64_t v) {
+    float a, b;
+    f2unpack(v, a, b);
+    return a + b;
+}
+
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }

@@ -174,8 +174,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 for (int f = 0; f < 8; ++f) {
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        w[h] = pack_bf16x2(psi_f(bf16_lo_f(w[h])), psi_f(bf16_hi_f(w[h])));
+                    for (int h = 0; h < 4; ++h) w[h] = psi_bf16x2(w[h]);
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
 #pragma unroll

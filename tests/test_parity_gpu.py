@@ -237,3 +237,29 @@ def test_causal_host_buffer_too_small_is_rejected(cuda_device):
     with pytest.raises(la.LinAttnError) as ei:
         la.forward_causal_host(q, k, v, dev_buf=buf, device=cuda_device)
     assert ei.value.status == la.LA_ERR_WORKSPACE
+
+
+# The tensor-core causal path for every (d, dv) pair, ragged tails, one-block
+# sequences and the sequence split (few heads, long sequences), with and
+# without an initial state.
+@pytest.mark.parametrize("B,H,N,d,dv,with_state", [
+    (1, 1, 1, 64, 64, False), (1, 2, 127, 64, 128, True), (1, 2, 129, 128, 64, False),
+    (2, 3, 1000, 64, 128, False), (1, 3, 2049, 128, 64, True), (1, 1, 20000, 64, 64, True),
+    (1, 2, 9001, 128, 128, False), (96, 1, 300, 64, 128, False),
+])
+def test_causal_tc_shapes(B, H, N, d, dv, with_state, cuda_device):
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=d ** -0.5, seed=N + dv)
+    S_in = z_in = None
+    if with_state:
+        g = torch.Generator().manual_seed(N)
+        S_in = torch.randn(B, H, d, dv, generator=g) * 0.5
+        z_in = torch.rand(B, H, d, generator=g) * 5 + 1
+    y, S, z = la.forward_causal(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                S_in=None if S_in is None else S_in.to(cuda_device),
+                                z_in=None if z_in is None else z_in.to(cuda_device),
+                                return_state=True, check_status=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.causal_recurrent(q, k, v, S_in=S_in, z_in=z_in, return_state=True)
+    e = (rel_max_err(y, yo), rel_max_err(S, So), rel_max_err(z, zo))
+    print(f"causal tc B{B}H{H}N{N}d{d}dv{dv} state={with_state}: y {e[0]:.2e} S {e[1]:.2e} z {e[2]:.2e}")
+    assert max(e) <= TOL_BF16

@@ -37,16 +37,6 @@ struct TcParams {
     int drop_item;                 // test hook: this item's first K/V copy is never issued (-1: off)
 };
 
-// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0), written without a branch so
-// lanes with inputs of either sign stay converged: e^min(x,0) - 1 is 0 for
-// x > 0, and for x <= 0 it is at least x (e^x >= 1 + x), so the maximum with
-// x picks the right branch.  e^x = 2^(x log2 e) with the flush-to-zero form
-// (x <= 0 here, so a flushed result only means e^x < 2^-126).  Where e^x - 1
-// and x are within the exponential's rounding of each other (|x| < ~1e-3)
-// either one is psi(x) to well below the bf16 rounding the result gets.
-__device__ __forceinline__ float psi_f(float x) {
-    return fmaxf(x, ex2_ftz(fminf(x, 0.f) * 1.4426950408889634f) - 1.f);
-}
 // Packed fp32 pairs (two floats in one 64-bit register; the f32x2 arithmetic
 // of sm_100 and later does both lanes in one instruction).
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
@@ -68,8 +58,15 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
     return r;
 }
 
-// psi of both bf16 halves of w, rounded back to bf16x2 (psi_f on each half,
-// with the multiply and the -1 done on the pair).
+// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0) of both bf16 halves of w,
+// rounded back to bf16x2.  Written without a branch so lanes with inputs of
+// either sign stay converged: e^min(x,0) - 1 is 0 for x > 0, and for x <= 0
+// it is at least x (e^x >= 1 + x), so the maximum with x picks the right
+// branch.  e^x = 2^(x log2 e) with the flush-to-zero form (x <= 0 here, so a
+// flushed result only means e^x < 2^-126).  Where e^x - 1 and x are within
+// the exponential's rounding of each other (|x| < ~1e-3) either one is psi(x)
+// to well below the bf16 rounding the result gets.  The multiply and the -1
+// run on the packed pair.
 __device__ __forceinline__ uint32_t psi_bf16x2(uint32_t w) {
     const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
     float t0, t1, e0, e1;

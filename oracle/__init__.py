@@ -19,6 +19,10 @@ C loops in ``linattn_oracle.c``:
 * ``causal_chunked(q, k, v, C)``   -- blockwise form ("Linear Attention/es",
   "Entrenamiento: forma paralela").
 * ``decode_step(q, k, v, S, z)``   -- one recurrent step on a stored state.
+* ``causal_backward(q, k, v, dy)`` -- gradients of sum_t dy_t . y_t of the
+  causal form with respect to q, k, v (and the initial state), by the chain
+  rule through the recurrence ("Linear Attention/es", "Entrenamiento: forma
+  paralela" motivates it; the recurrence is "Forma recurrente ...").
 
 Shapes: q, k ``[..., N, d]``; v ``[..., N, dv]``; leading dims are flattened
 into independent heads.  States: S ``[..., d, dv]``, z ``[..., d]``.
@@ -70,6 +74,8 @@ def _bind(lib):
     lib.oracle_causal_chunked.restype = i
     lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, i, i, i, dbl, i]
     lib.oracle_decode_step.restype = i
+    lib.oracle_causal_backward.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, P, P, P, P, i]
+    lib.oracle_causal_backward.restype = i
     return lib
 
 
@@ -192,3 +198,27 @@ def decode_step(q, k, v, S, z, eps: float = 1e-6, nthreads: int | None = None):
     if rc:
         raise RuntimeError("oracle_decode_step failed")
     return y, S, z
+
+
+def causal_backward(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
+                    return_state_grad: bool = False, nthreads: int | None = None):
+    """Gradients of L = sum_t dy_t . y_t, y the causal output of (q, k, v).
+
+    Returns (dq, dk, dv), plus (dS_in, dz_in) when ``return_state_grad``.
+    """
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    dy = _f64(dy)
+    if dy.shape != v.shape:
+        raise ValueError(f"dy{dy.shape} must match v{v.shape}")
+    gq, gk, gv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+    S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
+    z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
+    gS = np.empty(lead + (d, dv)) if return_state_grad else None
+    gz = np.empty(lead + (d,)) if return_state_grad else None
+    rc = _load().oracle_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq), _ptr(gk),
+                                        _ptr(gv), BH, N, d, dv, float(eps), _ptr(S_in),
+                                        _ptr(z_in), _ptr(gS), _ptr(gz),
+                                        nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_causal_backward failed")
+    return (gq, gk, gv, gS, gz) if return_state_grad else (gq, gk, gv)

@@ -240,17 +240,19 @@ static int run_jobs(job_t base, int nthreads)
     if (nthreads > base.BH) nthreads = base.BH > 0 ? base.BH : 1;
     job_t *jobs = malloc(sizeof(job_t) * nthreads);
     pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
-    int started = 0;
     for (int t = 0; t < nthreads; ++t) {
         jobs[t] = base;
         jobs[t].h_begin = (int)((long)base.BH * t / nthreads);
         jobs[t].h_end = (int)((long)base.BH * (t + 1) / nthreads);
     }
+    char *joined = calloc((size_t)nthreads, 1);
     for (int t = 1; t < nthreads; ++t)
-        if (pthread_create(&th[t], NULL, worker, &jobs[t]) == 0) ++started;
+        if (pthread_create(&th[t], NULL, worker, &jobs[t]) == 0) joined[t] = 1;
         else worker(&jobs[t]); /* fall back to running it on this thread */
     worker(&jobs[0]);
-    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    for (int t = 1; t < nthreads; ++t)
+        if (joined[t]) pthread_join(th[t], NULL);
+    free(joined);
     free(jobs); free(th);
     return 0;
 }
@@ -314,4 +316,147 @@ int oracle_decode_step(const double *q, const double *k, const double *v, double
     J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S; J.z_in = z;
     J.S_out = S; J.z_out = z; J.BH = BH; J.N = 1; J.d = d; J.dv = dv; J.eps = eps;
     return run_jobs(J, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gradients of the causal form.                                            */
+/* ------------------------------------------------------------------------ */
+/* [P1] "Entrenamiento: forma paralela" names training through the causal
+ * recurrence as the reason for the parallel form; training needs the
+ * gradients of a scalar loss L with respect to q, k, v.  Given dy_t = dL/dy_t
+ * they follow from the recurrence of "Forma recurrente e inferencia
+ * autorregresiva" by the chain rule, taken in the recurrence's own order
+ * (forward in t, then backward in t):
+ *
+ *   with D_t = max(den_t, eps), den_t = phi(q_t)^T z_t, y_t = S_t^T phi(q_t) / D_t:
+ *     g_t   = dy_t / D_t                         dL/d(num_t)
+ *     e_t   = -(dy_t . y_t) / D_t  if den_t >= eps, else 0   dL/d(den_t)
+ *     dL/dphi(q_t) = S_t g_t + z_t e_t
+ *   the state gradients run backwards from t = N:
+ *     Sh_t = sum_{s >= t} phi(q_s) g_s^T,   zh_t = sum_{s >= t} phi(q_s) e_s
+ *     dL/dphi(k_t) = Sh_t v_t + zh_t,   dL/dv_t = Sh_t^T phi(k_t)
+ *   and dL/dS_in = Sh_1, dL/dz_in = zh_1.
+ * phi'(x) = 1 (x > 0), e^x (x <= 0), the derivative of the piecewise form of
+ * [P2] "La función ELU + 1"; both branches give 1 at x = 0.
+ * The clamp passes the gradient when den_t >= eps (it is inactive there) and
+ * blocks it below eps, as clamp_min does in the pages' examples.           */
+static double dphi(double x) { return x > 0.0 ? 1.0 : exp(x); }
+
+typedef struct {
+    const double *q, *k, *v, *dy;
+    double *dq, *dk, *dvv;
+    const double *S_in, *z_in;
+    double *dS_in, *dz_in;
+    int BH, N, d, dv;
+    double eps;
+    int h_begin, h_end;
+} bjob_t;
+
+static void head_backward(const bjob_t *J, int h)
+{
+    const int N = J->N, d = J->d, dv = J->dv;
+    const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
+    const double *v = J->v + (long)h * N * dv, *dy = J->dy + (long)h * N * dv;
+    double *dq = J->dq + (long)h * N * d, *dk = J->dk + (long)h * N * d;
+    double *dvv = J->dvv + (long)h * N * dv;
+    double *S = calloc((size_t)d * dv, sizeof(double));
+    double *z = calloc((size_t)d, sizeof(double));
+    double *fk = malloc(sizeof(double) * d), *fq = malloc(sizeof(double) * d);
+    double *y = malloc(sizeof(double) * dv);
+    double *g = malloc(sizeof(double) * ((size_t)N * dv + 1));  /* g_t for every t */
+    double *e = malloc(sizeof(double) * ((size_t)N + 1));       /* e_t for every t */
+    if (J->S_in) memcpy(S, J->S_in + (long)h * d * dv, sizeof(double) * d * dv);
+    if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
+    /* forward in t: the state after token t, then dL/dphi(q_t) */
+    for (int t = 0; t < N; ++t) {
+        for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) {
+            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];
+            z[a] += fk[a];
+        }
+        for (int a = 0; a < d; ++a) fq[a] = phi(q[(long)t * d + a]);
+        double den = 0.0;
+        for (int a = 0; a < d; ++a) den += fq[a] * z[a];
+        const double D = clamp_den(den, J->eps);
+        double dyy = 0.0;
+        for (int b = 0; b < dv; ++b) {
+            double num = 0.0;
+            for (int a = 0; a < d; ++a) num += fq[a] * S[(long)a * dv + b];
+            y[b] = num / D;
+            dyy += dy[(long)t * dv + b] * y[b];
+        }
+        for (int b = 0; b < dv; ++b) g[(long)t * dv + b] = dy[(long)t * dv + b] / D;
+        e[t] = den >= J->eps ? -dyy / D : 0.0;
+        for (int a = 0; a < d; ++a) {
+            double s = z[a] * e[t];
+            for (int b = 0; b < dv; ++b) s += S[(long)a * dv + b] * g[(long)t * dv + b];
+            dq[(long)t * d + a] = s * dphi(q[(long)t * d + a]);
+        }
+    }
+    /* backward in t: Sh, zh include token t itself (y_s reads S_s for s >= t) */
+    memset(S, 0, sizeof(double) * d * dv);
+    memset(z, 0, sizeof(double) * d);
+    for (int t = N - 1; t >= 0; --t) {
+        for (int a = 0; a < d; ++a) fq[a] = phi(q[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) {
+            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a] * g[(long)t * dv + b];
+            z[a] += fq[a] * e[t];
+        }
+        for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) {
+            double s = z[a];
+            for (int b = 0; b < dv; ++b) s += S[(long)a * dv + b] * v[(long)t * dv + b];
+            dk[(long)t * d + a] = s * dphi(k[(long)t * d + a]);
+        }
+        for (int b = 0; b < dv; ++b) {
+            double s = 0.0;
+            for (int a = 0; a < d; ++a) s += S[(long)a * dv + b] * fk[a];
+            dvv[(long)t * dv + b] = s;
+        }
+    }
+    if (J->dS_in) memcpy(J->dS_in + (long)h * d * dv, S, sizeof(double) * d * dv);
+    if (J->dz_in) memcpy(J->dz_in + (long)h * d, z, sizeof(double) * d);
+    free(S); free(z); free(fk); free(fq); free(y); free(g); free(e);
+}
+
+static void *bworker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    for (int h = J->h_begin; h < J->h_end; ++h) head_backward(J, h);
+    return NULL;
+}
+
+/* Gradients of sum_t dy_t . y_t for the causal recurrent form.  q, k, dq, dk:
+ * [BH][N][d]; v, dy, dvv: [BH][N][dv].  S_in/z_in may be NULL (zero state);
+ * dS_in [BH][d][dv] and dz_in [BH][d] may be NULL.  Returns 0 on success.   */
+int oracle_causal_backward(const double *q, const double *k, const double *v,
+                           const double *dy, double *dq, double *dk, double *dvv,
+                           int BH, int N, int d, int dv, double eps,
+                           const double *S_in, const double *z_in,
+                           double *dS_in, double *dz_in, int nthreads)
+{
+    if (BH < 0 || N < 0 || d <= 0 || dv <= 0) return 1;
+    bjob_t base = {0};
+    base.q = q; base.k = k; base.v = v; base.dy = dy; base.dq = dq; base.dk = dk;
+    base.dvv = dvv; base.S_in = S_in; base.z_in = z_in; base.dS_in = dS_in;
+    base.dz_in = dz_in; base.BH = BH; base.N = N; base.d = d; base.dv = dv; base.eps = eps;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > BH) nthreads = BH > 0 ? BH : 1;
+    bjob_t *jobs = malloc(sizeof(bjob_t) * nthreads);
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].h_begin = (int)((long)BH * t / nthreads);
+        jobs[t].h_end = (int)((long)BH * (t + 1) / nthreads);
+    }
+    char *joined = calloc((size_t)nthreads, 1);
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, bworker, &jobs[t]) == 0) joined[t] = 1;
+        else bworker(&jobs[t]); /* fall back to running it on this thread */
+    bworker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (joined[t]) pthread_join(th[t], NULL);
+    free(joined);
+    free(jobs); free(th);
+    return 0;
 }

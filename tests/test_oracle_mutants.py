@@ -3,7 +3,8 @@
 Each mutant is a textual edit of a copy of ``oracle/linattn_oracle.c``,
 compiled to a temporary library and swapped in for the real one.  The pins
 run here are the hand-derived golden cases, the numpy brute force and the
-chunked-vs-recurrent agreement from ``test_oracle.py``.
+chunked-vs-recurrent agreement from ``test_oracle.py``, and, for the
+gradients, central differences of the forward (``backward_pins.py``).
 """
 import ctypes
 import json
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 
 import oracle
+from tests import backward_pins
 
 HERE = os.path.dirname(__file__)
 SRC = os.path.join(os.path.dirname(HERE), "oracle", "linattn_oracle.c")
@@ -30,6 +32,15 @@ MUTANTS = {
     "quadratic_exclusive": ("const int jmax = J->causal ? i : N - 1;", "const int jmax = J->causal ? i - 1 : N - 1;"),
     "noncausal_transposed_state": ("for (int a = 0; a < d; ++a) num += f[a] * S[(long)a * dv + b];",
                                    "for (int a = 0; a < d; ++a) num += f[a] * S[(long)b * dv + a];"),
+    # gradients of the causal form
+    "bwd_den_term_dropped": ("e[t] = den >= J->eps ? -dyy / D : 0.0;", "e[t] = 0.0;"),
+    "bwd_clamp_passes_gradient": ("e[t] = den >= J->eps ? -dyy / D : 0.0;", "e[t] = -dyy / D;"),
+    "bwd_dphi_is_one": ("return x > 0.0 ? 1.0 : exp(x);", "return x > 0.0 ? 1.0 : 1.0;"),
+    "bwd_g_not_divided": ("g[(long)t * dv + b] = dy[(long)t * dv + b] / D;",
+                          "g[(long)t * dv + b] = dy[(long)t * dv + b];"),
+    "bwd_zh_dropped_from_dk": ("double s = z[a];", "double s = 0.0;"),
+    "bwd_dv_uses_phi_q": ("s += S[(long)a * dv + b] * fk[a];", "s += S[(long)a * dv + b] * fq[a];"),
+    "bwd_state_grad_not_reset": ("memset(S, 0, sizeof(double) * d * dv);", ";"),
 }
 
 
@@ -75,6 +86,10 @@ def _pins_pass() -> bool:
         return False
     if not np.allclose(oracle.causal_chunked(q, k, v, 7), oracle.causal_recurrent(q, k, v),
                        rtol=1e-11):
+        return False
+    # gradients: central differences of the forward, with an initial state
+    # and a clamp that is active for some tokens only
+    if not (backward_pins.fd_pin_passes(seed=3) and backward_pins.fd_pin_passes(seed=4)):
         return False
     return True
 

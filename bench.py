@@ -3,8 +3,8 @@
 Headline step: one causal chunkwise forward (la_forward_causal) over the
 B=8, H=16, N=8192, d=dv=128 bf16 workload (tokens = B*N positions, all heads).
 Each extra mode (non-causal B4 H8 N4096 d64, long causal B1 H32 N131072 d64,
-recurrent decode B256 H32 d128) is timed the same way and reported under
-"modes" with its own roofline.
+recurrent decode B256 H32 d128, gradients of the causal form at B8 H16 N8192
+d128) is timed the same way and reported under "modes" with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -28,7 +28,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from linear_rnn_sequence_gb300.workloads import WORKLOADS, Workload, make_qkv  # noqa: E402
+from linear_rnn_sequence_gb300.workloads import (WORKLOADS, Workload, make_backward_inputs,  # noqa: E402
+                                                 make_qkv)
 
 METRIC = "causal linear-attn tokens/s & TFLOP/s on 1 GB300, % roofline; decode tokens/s"
 HEADLINE = "causal_bf16_b8h16n8192d128"
@@ -50,6 +51,21 @@ def alg_flops_per_token_head(d, dv):
 
 def alg_bytes_per_token_head(w: Workload):
     return (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4  # q, k, v read; y (fp32) written
+
+
+def bwd_flops_per_token_head(d, dv):
+    # forward direction: S update 2*d*dv, S g 2*d*dv; reverse: Sh update
+    # 2*d*dv, Sh v 2*d*dv, Sh^T phi(k) 2*d*dv; plus den, e, z e, zh terms
+    return 10 * d * dv + 8 * d + 4 * dv
+
+
+def bwd_bytes_per_token_head(w: Workload):
+    # q, k, v read; dy (fp32) read; dq, dk, dv (fp32) written
+    return (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4 + (2 * w.d + w.dv) * 4
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def decode_bytes_per_head_step(w: Workload):
@@ -454,6 +470,32 @@ def run_modes(args, world, dev, peaks, peak_kind):
                                           heads * alg_flops_per_token_head(w.d, w.dv),
                                           sum(per) / len(per), peaks, peak_kind,
                                           load_traffic(w.name))}
+    del qs, ks, vs, S, z
+    torch.cuda.empty_cache()
+
+    # gradients of the causal form (CUDA cores, fp32): inputs larger than L2
+    w = WORKLOADS["causal_backward_bf16_b8h16n8192d128"]
+    q, k, v, dy = make_backward_inputs(w, device=dev, gen_device=dev)
+    outs = (torch.empty(w.B, w.H, w.N, w.d, device=dev), torch.empty(w.B, w.H, w.N, w.d, device=dev),
+            torch.empty(w.B, w.H, w.N, w.dv, device=dev))
+    ws = la.alloc_workspace(la.causal_backward_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype),
+                            dev)
+    total, per = time_steps(lambda: la.backward_causal(q, k, v, dy, eps=w.eps, out=outs,
+                                                       workspace=ws),
+                            max(3, min(args.steps, 10)), args.warmup, world)
+    T = w.BH * w.N
+    ms = sum(per) / len(per)
+    alg_flops, alg_bytes = T * bwd_flops_per_token_head(w.d, w.dv), T * bwd_bytes_per_token_head(w)
+    tflops = alg_flops / (ms * 1e-3) / 1e12
+    modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+                     "l2": "inputs larger than L2",
+                     "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
+                                  "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
+                                  "traffic": None,
+                                  "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
+                                  "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
+    del q, k, v, dy, outs, ws
+    torch.cuda.empty_cache()
     return modes
 
 
@@ -490,13 +532,15 @@ def run_reference(args, world, rank):
 def profile_case(args):
     """A few launches of one kernel on one workload, for ncu captures.
 
-    --profile-case causal|long|noncausal|decode picks the workload
+    --profile-case causal|long|noncausal|decode|backward picks the workload
     (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 / B256 H32 d128
-    decode); --batch overrides B for a smaller capture.
+    decode / gradients at B8 H16 N8192 d128); --batch overrides B for a
+    smaller capture.
     """
     from linear_rnn_sequence_gb300 import linattn as la
     names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
-             "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128"}
+             "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128",
+             "backward": "causal_backward_bf16_b8h16n8192d128"}
     w = WORKLOADS[names[args.profile_case]]
     if args.batch:
         w = w.with_(B=args.batch)
@@ -511,6 +555,14 @@ def profile_case(args):
         v = (torch.randn(w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
         y = torch.empty(w.B, w.H, w.dv, device=dev)
         fn = lambda: la.decode_step(q, k, v, S, z, eps=w.eps, out=y)
+    elif w.mode == "backward":
+        q, k, v, dy = make_backward_inputs(w, device=dev, gen_device=dev)
+        outs = (torch.empty(w.B, w.H, w.N, w.d, device=dev),
+                torch.empty(w.B, w.H, w.N, w.d, device=dev),
+                torch.empty(w.B, w.H, w.N, w.dv, device=dev))
+        ws = la.alloc_workspace(
+            la.causal_backward_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+        fn = lambda: la.backward_causal(q, k, v, dy, eps=w.eps, out=outs, workspace=ws)
     else:
         q, k, v = make_qkv(w, device=dev, gen_device=dev)
         y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
@@ -542,7 +594,7 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode"])
+    ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward"])
     ap.add_argument("--batch", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -124,6 +124,46 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Workspace size in bytes for la_backward_causal (0 for N == 0 or
+ * unsupported sizes).  It holds the run-time status header, per-segment
+ * forward and reverse state sums for the sequence-axis split, and two floats
+ * per token (1 / max(den_t, eps) and dL/d den_t).  It depends on the current
+ * device's SM count; it must be device memory, 256-byte aligned, and may be
+ * reused by later calls on the same stream.
+ */
+LA_API size_t la_causal_backward_workspace_bytes(int B, int H, int N, int d, int dv,
+                                                 la_dtype dt);
+
+/*
+ * Gradients of the causal forward (training through the recurrence:
+ * "Linear Attention/es", "Entrenamiento: forma paralela").  Given
+ * dy = dL/dy (float32, [B][H][N][dv]) for the output y of la_forward_causal
+ * on the same q, k, v, eps and initial state, writes
+ *   grad_q = dL/dq, grad_k = dL/dk   float32 [B][H][N][d]
+ *   grad_v = dL/dv                   float32 [B][H][N][dv]
+ * and, when grad_S_in / grad_z_in are non-NULL (both or neither), the
+ * gradients with respect to the initial state, float32 [B][H][d][dv] and
+ * [B][H][d] (also when S_in / z_in are NULL: the initial state is then the
+ * zero state).  By the chain rule through the recurrence, with
+ * D_t = max(den_t, eps) and g_t = dy_t / D_t:
+ *   e_t            = -(dy_t . y_t) / D_t  when den_t >= eps, else 0
+ *   dL/dphi(q_t)   = S_t g_t + z_t e_t
+ *   dL/dphi(k_t)   = sum_{s>=t} phi(q_s) (g_s . v_t + e_s)
+ *   dL/dv_t        = sum_{s>=t} g_s (phi(q_s) . phi(k_t))
+ * and dL/dx = dL/dphi(x) * phi'(x), phi'(x) = 1 (x > 0), e^x (x <= 0).
+ * y is not an input: the kernels recompute what they need.  Everything runs
+ * in float32 on the CUDA cores.  All tensor pointers are device pointers,
+ * 16-byte aligned; no output may overlap an input, the workspace or another
+ * output.  Errors as la_forward_causal.
+ */
+LA_API la_status la_backward_causal(const void *q, const void *k, const void *v,
+                                    const float *dy, float *grad_q, float *grad_k,
+                                    float *grad_v, int B, int H, int N, int d, int dv,
+                                    la_dtype dt, float eps, const float *S_in,
+                                    const float *z_in, float *grad_S_in, float *grad_z_in,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Device staging memory, in bytes, that la_forward_causal_host needs for
  * these sizes (0 for N == 0 or unsupported sizes).  Like the workspace size,
  * it depends on the current device's SM count.

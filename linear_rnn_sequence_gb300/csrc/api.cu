@@ -180,6 +180,58 @@ la_status la_decode_step(const void *q, const void *k, const void *v, float *y, 
     return from_cuda(launch_decode_simt(a));
 }
 
+size_t la_causal_backward_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
+    if (B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return 0;
+    if ((long long)B * H * N * (d > dv ? d : dv) >= (1LL << 31)) return 0;
+    return causal_backward_workspace(B * H, N, d, dv);
+}
+
+la_status la_backward_causal(const void *q, const void *k, const void *v, const float *dy,
+                             float *grad_q, float *grad_k, float *grad_v, int B, int H, int N,
+                             int d, int dv, la_dtype dt, float eps, const float *S_in,
+                             const float *z_in, float *grad_S_in, float *grad_z_in,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    la_status st = check_common(q, k, v, grad_v, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
+    if ((st = check_state(grad_S_in, grad_z_in, false)) != LA_OK) return st;
+    const size_t BH = (size_t)B * H, T = BH * N, es = esize(dt);
+    const size_t sb = BH * d * dv * 4, zb = BH * d * 4;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0) {
+        if (!dy || !grad_q || !grad_k) return LA_ERR_INVALID_ARG;
+        if (!aligned16(dy) || !aligned16(grad_q) || !aligned16(grad_k)) return LA_ERR_INVALID_ARG;
+    }
+    const size_t need = la_causal_backward_workspace_bytes(B, H, N, d, dv, dt);
+    // no output may overlap an input, the workspace or another output
+    const struct { const void *p; size_t n; } outs[] = {
+        {grad_q, T * d * 4}, {grad_k, T * d * 4}, {grad_v, T * dv * 4},
+        {grad_S_in, grad_S_in ? sb : 0}, {grad_z_in, grad_z_in ? zb : 0}};
+    const struct { const void *p; size_t n; } ins[] = {
+        {q, T * d * es}, {k, T * d * es}, {v, T * dv * es}, {dy, T * dv * 4},
+        {S_in, S_in ? sb : 0}, {z_in, z_in ? zb : 0}, {workspace, need}};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const auto &in : ins)
+            if (overlap(outs[i].p, outs[i].n, in.p, in.n)) return LA_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return LA_ERR_INVALID_ARG;
+    }
+    if (T == 0) {   // no tokens: the initial state gets no gradient
+        if (grad_S_in) {
+            cudaError_t e = cudaMemsetAsync(grad_S_in, 0, sb, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(grad_z_in, 0, zb, s);
+            return from_cuda(e);
+        }
+        return LA_OK;
+    }
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
+    BwdArgs a{q, k, v, dy, grad_q, grad_k, grad_v, B, H, N, d, dv, dt, eps, S_in, z_in,
+              grad_S_in, grad_z_in, workspace, workspace_bytes, s};
+    return from_cuda(launch_causal_backward(a));
+}
+
 la_status la_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
     if (!workspace || workspace_bytes < sizeof(WsHeader)) return LA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

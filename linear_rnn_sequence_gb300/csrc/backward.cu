@@ -1,0 +1,710 @@
+// backward.cu -- gradients of the causal form on CUDA cores, fp32.
+//
+// Training through the causal recurrence ("Linear Attention/es",
+// "Entrenamiento: forma paralela") needs dL/dq, dL/dk, dL/dv for an upstream
+// gradient dy = dL/dy.  By the chain rule through the recurrence of
+// "Forma recurrente e inferencia autorregresiva", with
+//   z_t = z_in + sum_{j<=t} phi(k_j),  S_t = S_in + sum_{j<=t} phi(k_j) v_j^T,
+//   den_t = phi(q_t)^T z_t,  D_t = max(den_t, eps),  y_t = S_t^T phi(q_t) / D_t:
+//   g_t = dy_t / D_t,  h_t = S_t g_t
+//   e_t = -(phi(q_t) . h_t) / D_t  if den_t >= eps, else 0      (dL/d den_t)
+//   dL/dphi(q_t) = h_t + z_t e_t
+//   Sh_t = sum_{s>=t} phi(q_s) g_s^T,  zh_t = sum_{s>=t} phi(q_s) e_s
+//   dL/dphi(k_t) = Sh_t v_t + zh_t,    dL/dv_t = Sh_t^T phi(k_t)
+//   dL/dS_in = Sh_1,  dL/dz_in = zh_1
+// and dL/dx = dL/dphi(x) * phi'(x), phi'(x) = 1 (x > 0), e^x (x <= 0), which
+// is min(phi(x), 1).
+//
+// Precision.  y_t is a weighted mean of the v_j, so in dL/dphi(q_t) the two
+// terms h_t and z_t e_t agree to leading order and their difference is about
+// ten times smaller than either; the rounding of S_t, summed over thousands
+// of tokens, would be amplified by that factor.  phi = 1 + psi (psi = elu) is
+// therefore carried split, as S_t = 1 u_t^T + R_t and z_t = n_t 1 + zeta_t
+// with u_t = sum v_j, n_t the token count, R_t = sum psi(k_j) v_j^T and
+// zeta_t = sum psi(k_j) (an initial state is split the same way, u_in and
+// n_in being its row means).  With hR = R_t g_t, and den_t = n_t sum(phi(q_t))
+// + phi(q_t).zeta_t, the leading terms cancel algebraically:
+//   dL/dphi(q_t) = c_t 1 + hR + zeta_t e_t,
+//   c_t = ((u_t.g_t)(phi(q_t).zeta_t) - n_t (phi(q_t).hR)) / D_t,
+//   e_t = -(sum(phi(q_t)) (u_t.g_t) + phi(q_t).hR) / D_t
+// (when the clamp is active e_t = 0 and c_t = u_t.g_t).  Everything is fp32 FMA.
+//
+// Work split: the sequence of each head is cut into P segments of whole
+// 32-token chunks.  Up to six launches:
+//   0. seed        split S_in, z_in into (R, zeta, u, n)         (S_in only)
+//   1. kv_states   per (head, segment < P-1): its (R, zeta, u, n) sums (P > 1)
+//   2. scan        exclusive prefix over segments, from the seed
+//   3. dq          per (head, segment), tokens in order from the prefix:
+//                  dq; per token 1/D_t and e_t into the workspace; the
+//                  segment's own sums of phi(q) g^T and phi(q) e
+//   4. scan        exclusive suffix over segments of those sums
+//   5. dkdv        per (head, segment), tokens in reverse from the suffix:
+//                  dk, dv; segment 0 ends with dL/dS_in, dL/dz_in
+// Inside a CTA the state lives in registers: thread (a, part) owns row a and
+// every kRT-th 4-column group of it, so a row reduction is a few lane
+// shuffles.  The reverse pass keeps a second, column-owned copy of Sh for the
+// reductions over rows that dv needs.  While a chunk is processed the next
+// one is already in flight from global memory into registers.
+#include <algorithm>
+
+#include "la_device.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kBC = 32;   // tokens per staged chunk
+
+// psi(x) = elu(x) = phi(x) - 1.
+__device__ __forceinline__ float psi_f(float x) { return x > 0.f ? x : __expf(x) - 1.f; }
+
+template <int D, int DV>
+struct Cfg {
+    static constexpr int kNT = D * DV >= 2048 ? 512 : 256;   // threads per CTA
+    // per (head, segment): R or Sh [D][DV], zeta or zh [D], u [DV], n, padding
+    static constexpr int kE = D * DV + D + DV + 4;
+    static constexpr int kOffZ = D * DV, kOffU = D * DV + D, kOffN = D * DV + D + DV;
+};
+
+// Row-owned tiling of a ROWS x COLS matrix over NT threads: thread tid owns
+// row tid / kRT and the 4-column groups g with g % kRT == tid % kRT.
+template <int NT, int ROWS, int COLS>
+struct Tile {
+    static constexpr int kRT = NT / ROWS;
+    static constexpr int kG = COLS / 4 / kRT;
+    static_assert(kRT >= 2 && kRT <= 16 && (kRT & (kRT - 1)) == 0 && kG >= 1 &&
+                  kG * 4 * kRT == COLS, "tile");
+    __device__ static int col(int i, int part) { return 4 * (i * kRT + part); }
+};
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+    static constexpr int n = 4;
+    __device__ static void unpack(uint4 u, float *o) {
+        o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+        o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void unpack(uint4 u, float *o) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = __uint_as_float(w[i] << 16);
+            o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// One chunk (kBC rows of width W) of a row-major global array, held in
+// registers between its load and its store into shared memory as fp32.
+template <int W, typename T, int NT>
+struct ChunkLoad {
+    static constexpr int n = Vec<T>::n;
+    static constexpr int kVecs = kBC * W / n;
+    static constexpr int kPer = (kVecs + NT - 1) / NT;
+    uint4 r[kPer];
+    // rows [0, L) of the chunk starting at src; the rest read as zero
+    __device__ __forceinline__ void load(const T *src, int L) {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = (threadIdx.x + i * NT) * n;
+            r[i] = (e < kBC * W && e / W < L) ? __ldg(reinterpret_cast<const uint4 *>(src + e))
+                                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    // dst[kBC][W] = op(x) on rows [0, L), 0 on the others
+    template <typename Op>
+    __device__ __forceinline__ void store(float *dst, int L, Op op) const {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = (threadIdx.x + i * NT) * n;
+            if (e >= kBC * W) continue;
+            float x[n];
+            Vec<T>::unpack(r[i], x);
+            const bool valid = e / W < L;
+#pragma unroll
+            for (int j = 0; j < n; ++j) x[j] = valid ? op(x[j]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < n; j += 4) st4(dst + e + j, make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]));
+        }
+    }
+};
+
+struct Ident { __device__ float operator()(float x) const { return x; } };
+struct Phi { __device__ float operator()(float x) const { return phi_f(x); } };
+struct Psi { __device__ float operator()(float x) const { return psi_f(x); } };
+
+struct Seg {
+    int h, p, t0, t1;
+};
+__device__ __forceinline__ Seg segment(int P, int seg_chunks, int N) {
+    Seg s;
+    s.h = blockIdx.x / P;
+    s.p = blockIdx.x % P;
+    s.t0 = s.p * seg_chunks * kBC;
+    s.t1 = min(N, s.t0 + seg_chunks * kBC);
+    return s;
+}
+
+template <int G>
+__device__ __forceinline__ float lane_group_sum(float x) {
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// ---- 0. split an initial state into (R, zeta, u, n) -------------------------
+template <int D, int DV>
+__global__ void bwd_seed_kernel(const float *__restrict__ S_in, const float *__restrict__ z_in,
+                                float *__restrict__ seed)
+{
+    using C = Cfg<D, DV>;
+    __shared__ float su[DV];
+    __shared__ float sn;
+    const int h = blockIdx.x;
+    const float *S = S_in + (size_t)h * D * DV, *z = z_in + (size_t)h * D;
+    float *o = seed + (size_t)h * C::kE;
+    for (int b = threadIdx.x; b < DV; b += blockDim.x) {
+        float s = 0.f;
+        for (int a = 0; a < D; ++a) s += S[a * DV + b];
+        su[b] = s / D;
+        o[C::kOffU + b] = su[b];
+    }
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int a = 0; a < D; ++a) s += z[a];
+        sn = s / D;
+        o[C::kOffN] = sn;
+        o[C::kOffN + 1] = o[C::kOffN + 2] = o[C::kOffN + 3] = 0.f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < D * DV; e += blockDim.x) o[e] = S[e] - su[e % DV];
+    for (int a = threadIdx.x; a < D; a += blockDim.x) o[C::kOffZ + a] = z[a] - sn;
+}
+
+// ---- 1. per-segment sums (R, zeta, u, n) ------------------------------------
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(Cfg<D, DV>::kNT)
+bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, int P,
+                     int seg_chunks, float *__restrict__ states)
+{
+    using C = Cfg<D, DV>;
+    constexpr int NT = C::kNT;
+    using RT = Tile<NT, D, DV>;
+    extern __shared__ float4 smem4[];
+    float *sPk = reinterpret_cast<float *>(smem4);   // [kBC][D] psi(k)
+    float *sV = sPk + kBC * D;                        // [kBC][DV]
+    const Seg sg = segment(P, seg_chunks, N);
+    if (sg.p == P - 1) return;   // no later segment reads the last one's sums
+    const int tid = threadIdx.x, a = tid / RT::kRT, part = tid % RT::kRT;
+    float R[4 * RT::kG];
+#pragma unroll
+    for (int i = 0; i < 4 * RT::kG; ++i) R[i] = 0.f;
+    float zeta = 0.f, u = 0.f;
+    ChunkLoad<D, T, NT> lk;
+    ChunkLoad<DV, T, NT> lv;
+    lk.load(k + ((size_t)sg.h * N + sg.t0) * D, min(kBC, sg.t1 - sg.t0));
+    lv.load(v + ((size_t)sg.h * N + sg.t0) * DV, min(kBC, sg.t1 - sg.t0));
+    for (int c0 = sg.t0; c0 < sg.t1; c0 += kBC) {
+        const int L = min(kBC, sg.t1 - c0);
+        __syncthreads();
+        lk.store(sPk, L, Psi());
+        lv.store(sV, L, Ident());
+        __syncthreads();
+        if (c0 + kBC < sg.t1) {
+            const size_t nrow = (size_t)sg.h * N + c0 + kBC;
+            const int nL = min(kBC, sg.t1 - c0 - kBC);
+            lk.load(k + nrow * D, nL);
+            lv.load(v + nrow * DV, nL);
+        }
+        if (tid < DV)
+            for (int t = 0; t < L; ++t) u += sV[t * DV + tid];
+        for (int t = 0; t < L; ++t) {
+            const float pk = sPk[t * D + a];
+            zeta += pk;
+#pragma unroll
+            for (int i = 0; i < RT::kG; ++i) {
+                const float4 x = ld4(sV + t * DV + RT::col(i, part));
+                R[4 * i] = fmaf(pk, x.x, R[4 * i]);
+                R[4 * i + 1] = fmaf(pk, x.y, R[4 * i + 1]);
+                R[4 * i + 2] = fmaf(pk, x.z, R[4 * i + 2]);
+                R[4 * i + 3] = fmaf(pk, x.w, R[4 * i + 3]);
+            }
+        }
+    }
+    float *out = states + ((size_t)sg.h * P + sg.p) * C::kE;
+#pragma unroll
+    for (int i = 0; i < RT::kG; ++i)
+        st4(out + a * DV + RT::col(i, part), make_float4(R[4 * i], R[4 * i + 1], R[4 * i + 2], R[4 * i + 3]));
+    if (part == 0) out[C::kOffZ + a] = zeta;
+    if (tid < DV) out[C::kOffU + tid] = u;
+    if (tid < 4) out[C::kOffN + tid] = tid == 0 ? (float)(sg.t1 - sg.t0) : 0.f;
+}
+
+// ---- 2./4. exclusive scan over segments, one thread per state element -----
+// Forward (reverse == 0): entry p becomes seed + sum_{p' < p} entry p' (the
+// last segment's entry is never read).  Reverse: sum_{p' > p} entry p'.
+__global__ void bwd_scan_kernel(float *__restrict__ states, int P, int E, int blocks_per_head,
+                                const float *__restrict__ seed, int reverse)
+{
+    const int h = blockIdx.x / blocks_per_head;
+    const int e = (blockIdx.x % blocks_per_head) * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    float *col = states + (size_t)h * P * E + e;
+    float run = 0.f;
+    if (!reverse) {
+        if (seed) run = seed[(size_t)h * E + e];
+        for (int p = 0; p < P; ++p) {
+            const float x = p < P - 1 ? col[(size_t)p * E] : 0.f;
+            col[(size_t)p * E] = run;
+            run += x;
+        }
+    } else {
+        for (int p = P - 1; p >= 0; --p) {
+            const float x = col[(size_t)p * E];
+            col[(size_t)p * E] = run;
+            run += x;
+        }
+    }
+}
+
+// ---- 3. dq, 1/D_t, e_t, and the segment's sums of phi(q) g^T, phi(q) e ----
+template <int D, int DV>
+struct DqSmem {
+    static constexpr size_t floats = 4 * (size_t)kBC * D + 3 * (size_t)kBC * DV + D + DV + 8 * kBC;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
+bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+              const float *__restrict__ dy, float *__restrict__ dq, int N, int P, int seg_chunks,
+              float eps, const float *__restrict__ prefix, float *__restrict__ rev_local,
+              float *__restrict__ dinv_out, float *__restrict__ e_out)
+{
+    using C = Cfg<D, DV>;
+    constexpr int NT = C::kNT, NW = NT / 32;
+    using RT = Tile<NT, D, DV>;
+    static_assert(NT >= D + DV, "one thread per feature and per value column");
+    extern __shared__ float4 smem4[];
+    float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D] phi(q)
+    float *sPk = sFq + kBC * D;                     // [kBC][D] psi(k)
+    float *sZt = sPk + kBC * D;                     // [kBC][D] zeta_t
+    float *sH = sZt + kBC * D;                      // [kBC][D] hR_t = R_t g_t
+    float *sV = sH + kBC * D;                       // [kBC][DV]
+    float *sG = sV + kBC * DV;                      // [kBC][DV] dy_t, then g_t
+    float *sUt = sG + kBC * DV;                     // [kBC][DV] u_t
+    float *sZrun = sUt + kBC * DV;                  // [D]  zeta before the chunk
+    float *sUrun = sZrun + D;                       // [DV] u before the chunk
+    float *sDinv = sUrun + DV;                      // [kBC] 1 / D_t
+    float *sAct = sDinv + kBC;                      // [kBC] 1 where den_t >= eps
+    float *sSq = sAct + kBC;                        // [kBC] sum of phi(q_t)
+    float *sFz = sSq + kBC;                         // [kBC] phi(q_t) . zeta_t
+    float *sUg = sFz + kBC;                         // [kBC] u_t . g_t
+    float *sNt = sUg + kBC;                         // [kBC] n_t
+    float *sE = sNt + kBC;                          // [kBC] e_t
+    float *sC = sE + kBC;                           // [kBC] c_t
+    const Seg sg = segment(P, seg_chunks, N);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int a = tid / RT::kRT, part = tid % RT::kRT;
+
+    float R[4 * RT::kG], Sh[4 * RT::kG];
+    const float *pre = prefix + ((size_t)sg.h * P + sg.p) * C::kE;
+#pragma unroll
+    for (int i = 0; i < RT::kG; ++i) {
+        const float4 x = ld4(pre + a * DV + RT::col(i, part));
+        R[4 * i] = x.x; R[4 * i + 1] = x.y; R[4 * i + 2] = x.z; R[4 * i + 3] = x.w;
+        Sh[4 * i] = Sh[4 * i + 1] = Sh[4 * i + 2] = Sh[4 * i + 3] = 0.f;
+    }
+    if (tid < D) sZrun[tid] = pre[C::kOffZ + tid];
+    else if (tid < D + DV) sUrun[tid - D] = pre[C::kOffU + tid - D];
+    float n_run = pre[C::kOffN];
+    float zh = 0.f;
+
+    ChunkLoad<D, T, NT> lq, lk;
+    ChunkLoad<DV, T, NT> lv;
+    ChunkLoad<DV, float, NT> ldy;
+    {
+        const size_t row0 = (size_t)sg.h * N + sg.t0;
+        const int L = min(kBC, sg.t1 - sg.t0);
+        lq.load(q + row0 * D, L); lk.load(k + row0 * D, L);
+        lv.load(v + row0 * DV, L); ldy.load(dy + row0 * DV, L);
+    }
+    for (int c0 = sg.t0; c0 < sg.t1; c0 += kBC) {
+        const int L = min(kBC, sg.t1 - c0);
+        const size_t row0 = (size_t)sg.h * N + c0;
+        __syncthreads();   // the previous chunk is consumed
+        lq.store(sFq, L, Phi());
+        lk.store(sPk, L, Psi());
+        lv.store(sV, L, Ident());
+        ldy.store(sG, L, Ident());
+        __syncthreads();
+        if (c0 + kBC < sg.t1) {   // the next chunk flies in while this one is processed
+            const size_t nrow = row0 + kBC;
+            const int nL = min(kBC, sg.t1 - c0 - kBC);
+            lq.load(q + nrow * D, nL); lk.load(k + nrow * D, nL);
+            lv.load(v + nrow * DV, nL); ldy.load(dy + nrow * DV, nL);
+        }
+        // zeta_t and u_t for every token of the chunk (both include token t)
+        if (tid < D) {
+            float run = sZrun[tid];
+            for (int t = 0; t < kBC; ++t) {
+                run += sPk[t * D + tid];
+                sZt[t * D + tid] = run;
+            }
+            sZrun[tid] = run;
+        } else if (tid < D + DV) {
+            const int b = tid - D;
+            float run = sUrun[b];
+            for (int t = 0; t < kBC; ++t) {
+                run += sV[t * DV + b];
+                sUt[t * DV + b] = run;
+            }
+            sUrun[b] = run;
+        }
+        __syncthreads();
+        // per token: den_t = n_t sum(phi(q_t)) + phi(q_t).zeta_t, u_t.dy_t; one warp per token
+        for (int t = warp; t < kBC; t += NW) {
+            float sq = 0.f, fz = 0.f, ug = 0.f;
+            for (int x = lane; x < D; x += 32) {
+                const float f = sFq[t * D + x];
+                sq += f;
+                fz = fmaf(f, sZt[t * D + x], fz);
+            }
+            for (int b = lane; b < DV; b += 32) ug = fmaf(sUt[t * DV + b], sG[t * DV + b], ug);
+            sq = warp_sum(sq);
+            fz = warp_sum(fz);
+            ug = warp_sum(ug);
+            if (lane == 0) {
+                const float nt = n_run + (float)min(t + 1, L);
+                const float den = fmaf(nt, sq, fz);
+                const float dinv = 1.f / fmaxf(den, eps);
+                sDinv[t] = dinv;
+                sAct[t] = t < L && den >= eps ? 1.f : 0.f;
+                sSq[t] = sq;
+                sFz[t] = fz;
+                sUg[t] = ug * dinv;
+                sNt[t] = nt;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < kBC * DV; e += NT) sG[e] *= sDinv[e / DV];
+        __syncthreads();
+        // the recurrence: R_t = R_{t-1} + psi(k_t) v_t^T, hR_t = R_t g_t;
+        // and the segment's sum of phi(q_t) g_t^T
+        for (int t = 0; t < L; ++t) {
+            const float pk = sPk[t * D + a], fq = sFq[t * D + a];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < RT::kG; ++i) {
+                const float4 x = ld4(sV + t * DV + RT::col(i, part));
+                const float4 g = ld4(sG + t * DV + RT::col(i, part));
+                R[4 * i] = fmaf(pk, x.x, R[4 * i]);
+                R[4 * i + 1] = fmaf(pk, x.y, R[4 * i + 1]);
+                R[4 * i + 2] = fmaf(pk, x.z, R[4 * i + 2]);
+                R[4 * i + 3] = fmaf(pk, x.w, R[4 * i + 3]);
+                acc[0] = fmaf(R[4 * i], g.x, acc[0]);
+                acc[1] = fmaf(R[4 * i + 1], g.y, acc[1]);
+                acc[2] = fmaf(R[4 * i + 2], g.z, acc[2]);
+                acc[3] = fmaf(R[4 * i + 3], g.w, acc[3]);
+                Sh[4 * i] = fmaf(fq, g.x, Sh[4 * i]);
+                Sh[4 * i + 1] = fmaf(fq, g.y, Sh[4 * i + 1]);
+                Sh[4 * i + 2] = fmaf(fq, g.z, Sh[4 * i + 2]);
+                Sh[4 * i + 3] = fmaf(fq, g.w, Sh[4 * i + 3]);
+            }
+            const float hsum = lane_group_sum<RT::kRT>((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            if (part == 0) sH[t * D + a] = hsum;
+        }
+        __syncthreads();
+        // e_t and c_t (see the header: the leading terms cancel algebraically)
+        for (int t = warp; t < kBC; t += NW) {
+            float fh = 0.f;
+            for (int x = lane; x < D; x += 32) fh = fmaf(sFq[t * D + x], sH[t * D + x], fh);
+            fh = warp_sum(fh);
+            if (lane == 0) {
+                float e = 0.f, c = t < L ? sUg[t] : 0.f;
+                if (sAct[t] != 0.f) {
+                    e = -fmaf(sSq[t], sUg[t], fh) * sDinv[t];
+                    c = fmaf(sUg[t], sFz[t], -sNt[t] * fh) * sDinv[t];
+                }
+                sE[t] = e;
+                sC[t] = c;
+            }
+        }
+        __syncthreads();
+        // dq_t = (c_t + hR_t + zeta_t e_t) * phi'(q_t)
+        for (int e = tid; e < L * D; e += NT) {
+            const int t = e / D;
+            dq[row0 * D + e] = (sC[t] + fmaf(sZt[e], sE[t], sH[e])) * fminf(sFq[e], 1.f);
+        }
+        if (tid < L) {
+            dinv_out[row0 + tid] = sDinv[tid];
+            e_out[row0 + tid] = sE[tid];
+        }
+        if (part == 0)
+            for (int t = 0; t < L; ++t) zh = fmaf(sFq[t * D + a], sE[t], zh);
+        n_run += (float)L;
+    }
+    float *out = rev_local + ((size_t)sg.h * P + sg.p) * C::kE;
+#pragma unroll
+    for (int i = 0; i < RT::kG; ++i)
+        st4(out + a * DV + RT::col(i, part), make_float4(Sh[4 * i], Sh[4 * i + 1], Sh[4 * i + 2], Sh[4 * i + 3]));
+    if (part == 0) out[C::kOffZ + a] = zh;
+    for (int e = tid; e < DV + 4; e += NT) out[C::kOffU + e] = 0.f;   // unused slots
+}
+
+// ---- 5. dk, dv (and dL/dS_in, dL/dz_in from segment 0) --------------------
+template <int D, int DV>
+struct DkdvSmem {
+    static constexpr size_t floats = 3 * (size_t)kBC * D + 3 * (size_t)kBC * DV + 2 * kBC;
+    static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
+bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                const float *__restrict__ dy, float *__restrict__ dk, float *__restrict__ dvg,
+                int N, int P, int seg_chunks, const float *__restrict__ suffix,
+                const float *__restrict__ dinv, const float *__restrict__ e_in,
+                float *__restrict__ grad_S, float *__restrict__ grad_z)
+{
+    using C = Cfg<D, DV>;
+    constexpr int NT = C::kNT;
+    using RT = Tile<NT, D, DV>;    // copy 1: thread owns row a of Sh
+    using CT = Tile<NT, DV, D>;    // copy 2: thread owns column b of Sh
+    extern __shared__ float4 smem4[];
+    float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D]
+    float *sFk = sFq + kBC * D;                     // [kBC][D]
+    float *sDK = sFk + kBC * D;                     // [kBC][D]
+    float *sV = sDK + kBC * D;                      // [kBC][DV]
+    float *sG = sV + kBC * DV;                      // [kBC][DV] dy_t, then g_t
+    float *sDV = sG + kBC * DV;                     // [kBC][DV]
+    float *sE = sDV + kBC * DV;                     // [kBC]
+    float *sDinv = sE + kBC;                        // [kBC]
+    const Seg sg = segment(P, seg_chunks, N);
+    const int tid = threadIdx.x;
+    const int a = tid / RT::kRT, part = tid % RT::kRT;
+    const int b = tid / CT::kRT, part2 = tid % CT::kRT;
+
+    float S1[4 * RT::kG], S2[4 * CT::kG];
+    const float *suf = suffix + ((size_t)sg.h * P + sg.p) * C::kE;
+#pragma unroll
+    for (int i = 0; i < RT::kG; ++i) {
+        const float4 x = ld4(suf + a * DV + RT::col(i, part));
+        S1[4 * i] = x.x; S1[4 * i + 1] = x.y; S1[4 * i + 2] = x.z; S1[4 * i + 3] = x.w;
+    }
+#pragma unroll
+    for (int i = 0; i < CT::kG; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) S2[4 * i + r] = suf[(CT::col(i, part2) + r) * DV + b];
+    float zh = suf[C::kOffZ + a];
+
+    ChunkLoad<D, T, NT> lq, lk;
+    ChunkLoad<DV, T, NT> lv;
+    ChunkLoad<DV, float, NT> ldy;
+    float pdinv = 0.f, pe = 0.f;
+    const int nch = (sg.t1 - sg.t0 + kBC - 1) / kBC;
+    auto issue = [&](int c) {
+        const int c0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - c0);
+        const size_t row0 = (size_t)sg.h * N + c0;
+        lq.load(q + row0 * D, L); lk.load(k + row0 * D, L);
+        lv.load(v + row0 * DV, L); ldy.load(dy + row0 * DV, L);
+        pdinv = tid < L ? __ldg(dinv + row0 + tid) : 0.f;
+        pe = tid < L ? __ldg(e_in + row0 + tid) : 0.f;
+    };
+    issue(nch - 1);
+    for (int c = nch - 1; c >= 0; --c) {
+        const int c0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - c0);
+        const size_t row0 = (size_t)sg.h * N + c0;
+        __syncthreads();   // the previous chunk's outputs are written
+        lq.store(sFq, L, Phi());
+        lk.store(sFk, L, Phi());
+        lv.store(sV, L, Ident());
+        ldy.store(sG, L, Ident());
+        if (tid < kBC) {
+            sE[tid] = pe;
+            sDinv[tid] = pdinv;
+        }
+        __syncthreads();
+        if (c > 0) issue(c - 1);
+        for (int e = tid; e < kBC * DV; e += NT) sG[e] *= sDinv[e / DV];
+        __syncthreads();
+        for (int t = L - 1; t >= 0; --t) {
+            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T, zh_t = zh_{t+1} + phi(q_t) e_t
+            const float fq = sFq[t * D + a];
+            zh = fmaf(fq, sE[t], zh);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < RT::kG; ++i) {
+                const float4 g = ld4(sG + t * DV + RT::col(i, part));
+                const float4 x = ld4(sV + t * DV + RT::col(i, part));
+                S1[4 * i] = fmaf(fq, g.x, S1[4 * i]);
+                S1[4 * i + 1] = fmaf(fq, g.y, S1[4 * i + 1]);
+                S1[4 * i + 2] = fmaf(fq, g.z, S1[4 * i + 2]);
+                S1[4 * i + 3] = fmaf(fq, g.w, S1[4 * i + 3]);
+                acc[0] = fmaf(S1[4 * i], x.x, acc[0]);
+                acc[1] = fmaf(S1[4 * i + 1], x.y, acc[1]);
+                acc[2] = fmaf(S1[4 * i + 2], x.z, acc[2]);
+                acc[3] = fmaf(S1[4 * i + 3], x.w, acc[3]);
+            }
+            const float dfk = lane_group_sum<RT::kRT>((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            if (part == 0) sDK[t * D + a] = (dfk + zh) * fminf(sFk[t * D + a], 1.f);
+            // the same update on the column-owned copy, then dv_t = Sh_t^T phi(k_t)
+            const float gb = sG[t * DV + b];
+            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < CT::kG; ++i) {
+                const float4 fq4 = ld4(sFq + t * D + CT::col(i, part2));
+                const float4 fk4 = ld4(sFk + t * D + CT::col(i, part2));
+                S2[4 * i] = fmaf(fq4.x, gb, S2[4 * i]);
+                S2[4 * i + 1] = fmaf(fq4.y, gb, S2[4 * i + 1]);
+                S2[4 * i + 2] = fmaf(fq4.z, gb, S2[4 * i + 2]);
+                S2[4 * i + 3] = fmaf(fq4.w, gb, S2[4 * i + 3]);
+                acc2[0] = fmaf(S2[4 * i], fk4.x, acc2[0]);
+                acc2[1] = fmaf(S2[4 * i + 1], fk4.y, acc2[1]);
+                acc2[2] = fmaf(S2[4 * i + 2], fk4.z, acc2[2]);
+                acc2[3] = fmaf(S2[4 * i + 3], fk4.w, acc2[3]);
+            }
+            const float dvb = lane_group_sum<CT::kRT>((acc2[0] + acc2[1]) + (acc2[2] + acc2[3]));
+            if (part2 == 0) sDV[t * DV + b] = dvb;
+        }
+        __syncthreads();
+        for (int e = tid * 4; e < L * D; e += NT * 4) st4(dk + row0 * D + e, ld4(sDK + e));
+        for (int e = tid * 4; e < L * DV; e += NT * 4) st4(dvg + row0 * DV + e, ld4(sDV + e));
+    }
+    if (sg.p == 0 && grad_S) {
+        float *gS = grad_S + (size_t)sg.h * D * DV;
+#pragma unroll
+        for (int i = 0; i < RT::kG; ++i)
+            st4(gS + a * DV + RT::col(i, part), make_float4(S1[4 * i], S1[4 * i + 1], S1[4 * i + 2], S1[4 * i + 3]));
+        if (part == 0) grad_z[(size_t)sg.h * D + a] = zh;
+    }
+}
+
+// ---- host side --------------------------------------------------------------
+struct BwdPlan {
+    int P = 1, seg_chunks = 1, E = 0;
+    size_t seed_off = 0, fwd_off = 0, rev_off = 0, dinv_off = 0, e_off = 0, total = 0;
+};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 148;
+    return n;
+}
+
+// Segments per head: minimise (waves of one CTA per SM) x (chunks per
+// segment + about two chunks of fixed cost for the state traffic).
+BwdPlan make_plan(int BH, int N, int d, int dv) {
+    BwdPlan pl;
+    const int nchunks = std::max(1, (N + kBC - 1) / kBC);
+    const long slots = sm_count();
+    long best = -1;
+    for (int P = 1; P <= std::min(nchunks, 64); ++P) {
+        const int sc = (nchunks + P - 1) / P;
+        if ((nchunks + sc - 1) / sc != P) continue;   // no empty segments
+        const long waves = ((long)BH * P + slots - 1) / slots;
+        const long cost = waves * (sc + (P > 1 ? 2 : 0));
+        if (best < 0 || cost < best) { best = cost; pl.P = P; pl.seg_chunks = sc; }
+    }
+    pl.E = d * dv + d + dv + 4;
+    const size_t st = up256((size_t)BH * pl.P * pl.E * sizeof(float));
+    pl.seed_off = sizeof(WsHeader);
+    pl.fwd_off = pl.seed_off + up256((size_t)BH * pl.E * sizeof(float));
+    pl.rev_off = pl.fwd_off + st;
+    pl.dinv_off = pl.rev_off + st;
+    pl.e_off = pl.dinv_off + up256((size_t)BH * N * sizeof(float));
+    pl.total = pl.e_off + up256((size_t)BH * N * sizeof(float));
+    return pl;
+}
+
+template <int D, int DV, typename T>
+cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
+    using C = Cfg<D, DV>;
+    const int BH = a.B * a.H;
+    char *ws = static_cast<char *>(a.ws);
+    float *seed = reinterpret_cast<float *>(ws + pl.seed_off);
+    float *fwd = reinterpret_cast<float *>(ws + pl.fwd_off);
+    float *rev = reinterpret_cast<float *>(ws + pl.rev_off);
+    float *dinv = reinterpret_cast<float *>(ws + pl.dinv_off);
+    float *ev = reinterpret_cast<float *>(ws + pl.e_off);
+    const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k),
+            *v = static_cast<const T *>(a.v);
+    const int grid = BH * pl.P, bph = (pl.E + 255) / 256;
+    constexpr size_t kv_smem = sizeof(float) * kBC * (D + DV);
+    constexpr size_t dq_smem = DqSmem<D, DV>::bytes, dkdv_smem = DkdvSmem<D, DV>::bytes;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, DV, T>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv_smem)) != cudaSuccess)
+        return e;
+    if (a.S_in) {
+        bwd_seed_kernel<D, DV><<<BH, 128, 0, a.stream>>>(a.S_in, a.z_in, seed);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (pl.P > 1) {
+        bwd_kv_states_kernel<D, DV, T><<<grid, C::kNT, kv_smem, a.stream>>>(k, v, a.N, pl.P,
+                                                                           pl.seg_chunks, fwd);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(fwd, pl.P, pl.E, bph, a.S_in ? seed : nullptr, 0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_dq_kernel<D, DV, T><<<grid, C::kNT, dq_smem, a.stream>>>(q, k, v, a.dy, a.dq, a.N, pl.P,
+                                                                pl.seg_chunks, a.eps, fwd, rev,
+                                                                dinv, ev);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(rev, pl.P, pl.E, bph, nullptr, 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_dkdv_kernel<D, DV, T><<<grid, C::kNT, dkdv_smem, a.stream>>>(q, k, v, a.dy, a.dk, a.dv_grad,
+                                                                    a.N, pl.P, pl.seg_chunks, rev,
+                                                                    dinv, ev, a.grad_S_in,
+                                                                    a.grad_z_in);
+    return cudaGetLastError();
+}
+
+template <int D, int DV>
+cudaError_t launch_dims(const BwdArgs &a, const BwdPlan &pl) {
+    return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16>(a, pl)
+                                 : launch_typed<D, DV, float>(a, pl);
+}
+
+template <int D>
+cudaError_t launch_dv(const BwdArgs &a, const BwdPlan &pl) {
+    switch (a.dv) {
+    case 32: return launch_dims<D, 32>(a, pl);
+    case 64: return launch_dims<D, 64>(a, pl);
+    default: return launch_dims<D, 128>(a, pl);
+    }
+}
+
+}  // namespace
+
+size_t causal_backward_workspace(int BH, int N, int d, int dv) {
+    return make_plan(BH, N, d, dv).total;
+}
+
+int causal_backward_launches(int BH, int N, int d, int dv, bool with_state) {
+    return 4 + (make_plan(BH, N, d, dv).P > 1 ? 1 : 0) + (with_state ? 1 : 0);
+}
+
+cudaError_t launch_causal_backward(const BwdArgs &a) {
+    const BwdPlan pl = make_plan(a.B * a.H, a.N, a.d, a.dv);
+    if (a.ws_bytes < pl.total) return cudaErrorInvalidValue;
+    switch (a.d) {
+    case 32: return launch_dv<32>(a, pl);
+    case 64: return launch_dv<64>(a, pl);
+    default: return launch_dv<128>(a, pl);
+    }
+}
+
+}  // namespace la

@@ -35,6 +35,21 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+// Gradients of the causal form; pointers are device pointers.
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *dy;
+    float *dq, *dk, *dv_grad;
+    int B, H, N, d, dv;
+    la_dtype dt;
+    float eps;
+    const float *S_in, *z_in;      // nullable (zero initial state)
+    float *grad_S_in, *grad_z_in;  // nullable
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
 // Workspace header written at the start of every workspace (256 bytes).
 struct WsHeader {
     unsigned int error;         // 0 = ok, else an la_status value (LA_ERR_TIMEOUT)
@@ -65,5 +80,10 @@ cudaError_t launch_causal_tc(const FwdArgs &a);
 bool noncausal_tc_supported(const FwdArgs &a);
 size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
 cudaError_t launch_noncausal_tc(const FwdArgs &a);
+
+// gradients of the causal form (CUDA cores, fp32)
+size_t causal_backward_workspace(int BH, int N, int d, int dv);
+int causal_backward_launches(int BH, int N, int d, int dv, bool with_state);
+cudaError_t launch_causal_backward(const BwdArgs &a);
 
 }  // namespace la

@@ -70,6 +70,11 @@ def lib():
             L.la_forward_causal_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
                                                  sz, vp]
             L.la_forward_causal_host.restype = i
+            L.la_causal_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            L.la_causal_backward_workspace_bytes.restype = sz
+            L.la_backward_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                             vp, vp, vp, vp, vp, sz, vp]
+            L.la_backward_causal.restype = i
             L.la_workspace_status.argtypes = [vp, sz, vp]
             L.la_workspace_status.restype = i
             L.la_debug_set_fault.argtypes = [i, ctypes.c_longlong]
@@ -167,6 +172,49 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
         if err != LA_OK:
             raise LinAttnError(err, f"la_forward_causal (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
+
+
+def causal_backward_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(lib().la_causal_backward_workspace_bytes(B, H, N, d, dv, code))
+
+
+def backward_causal(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
+                    return_state_grad=False, out=None, workspace=None, stream=None):
+    """Gradients of the causal forward for the upstream gradient ``dy``.
+
+    q, k: [B,H,N,d]; v: [B,H,N,dv] (bf16 or fp32); dy: [B,H,N,dv] float32.
+    Returns (dq, dk, dv) float32, plus (dS_in, dz_in) when ``return_state_grad``.
+    ``out`` may be a preallocated (dq, dk, dv) triple.
+    """
+    _check_cuda(q, k, v, dy, S_in, z_in, workspace)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    if dy.shape != v.shape or dy.dtype != torch.float32:
+        raise ValueError("dy must be float32 with the shape of v")
+    if out is None:
+        out = (torch.empty((B, H, N, d), dtype=torch.float32, device=q.device),
+               torch.empty((B, H, N, d), dtype=torch.float32, device=q.device),
+               torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device))
+    gq, gk, gv = out
+    _check_cuda(gq, gk, gv)
+    gS = gz = None
+    if return_state_grad:
+        gS = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        gz = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = int(lib().la_causal_backward_workspace_bytes(B, H, N, d, dv, dt))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().la_backward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq), _ptr(gk),
+                                  _ptr(gv), B, H, N, d, dv, dt, float(eps), _ptr(S_in),
+                                  _ptr(z_in), _ptr(gS), _ptr(gz), _ptr(workspace), wbytes,
+                                  _stream_handle(stream, q.device))
+    _raise(st, "la_backward_causal")
+    return (gq, gk, gv, gS, gz) if return_state_grad else (gq, gk, gv)
 
 
 def causal_host_buffer_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:

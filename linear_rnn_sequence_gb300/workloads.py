@@ -10,7 +10,9 @@ in that order as iid N(0, 1) float32 tensors of the full ``[B, H, N, d]`` /
 workload's input dtype (bf16 by round-to-nearest-even).  The decode workload
 draws its prefill (unscaled) from a generator seeded ``seed`` and its per-step
 q, k, v (scaled by 1/sqrt(d)) from a second generator seeded ``seed + 1``,
-step after step, q then k then v.
+step after step, q then k then v.  The backward workload draws q, k, v as the
+causal one does and then, from the same generator, the upstream gradient dy
+as iid N(0, 1) float32 of shape ``[B, H, N, dv]`` (unscaled).
 """
 from __future__ import annotations
 
@@ -23,7 +25,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    mode: str            # "causal" | "noncausal" | "decode"
+    mode: str            # "causal" | "noncausal" | "decode" | "backward"
     B: int
     H: int
     N: int               # sequence length (decode: prefill length)
@@ -57,6 +59,10 @@ WORKLOADS = {
     # long-context causal.
     "causal_bf16_b1h32n131072d64": Workload("causal_bf16_b1h32n131072d64", "causal", 1, 32,
                                             131072, 64, 64, torch.bfloat16, 1.0 / math.sqrt(64)),
+    # gradients of the causal form at the training shape.
+    "causal_backward_bf16_b8h16n8192d128": Workload("causal_backward_bf16_b8h16n8192d128",
+                                                    "backward", 8, 16, 8192, 128, 128,
+                                                    torch.bfloat16, 1.0 / math.sqrt(128)),
     # recurrent decode from a 1024-token prefill.
     "decode_bf16_b256h32d128": Workload("decode_bf16_b256h32d128", "decode", 256, 32, 1024, 128,
                                         128, torch.bfloat16, 1.0, steps=4096,
@@ -86,6 +92,17 @@ def make_qkv(w: Workload, device="cpu", gen_device="cpu"):
     return q, k, v
 
 
+def make_backward_inputs(w: Workload, device="cpu", gen_device="cpu"):
+    """Draw (q, k, v, dy): q, k, v as ``make_qkv``, then dy from the same generator."""
+    g = torch.Generator(device=gen_device)
+    g.manual_seed(w.seed)
+    q = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    k = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    v = _draw(g, (w.B, w.H, w.N, w.dv), w.scale, w.dtype, device)
+    dy = _draw(g, (w.B, w.H, w.N, w.dv), 1.0, torch.float32, device)
+    return q, k, v, dy
+
+
 def decode_step_generator(w: Workload, gen_device="cpu") -> torch.Generator:
     g = torch.Generator(device=gen_device)
     g.manual_seed(w.seed + 1)
@@ -105,3 +122,9 @@ def random_qkv(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="c
     """Ad-hoc seeded draw with the same recipe (for edge-case tests)."""
     w = Workload("adhoc", "causal", B, H, N, d, dv, dtype, scale, seed)
     return make_qkv(w, device=device)
+
+
+def random_qkv_dy(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="cpu"):
+    """Ad-hoc seeded (q, k, v, dy) draw with the backward recipe."""
+    w = Workload("adhoc", "backward", B, H, N, d, dv, dtype, scale, seed)
+    return make_backward_inputs(w, device=device)

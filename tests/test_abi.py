@@ -150,3 +150,34 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 4, 32)
     with pytest.raises(ValueError):
         la.forward_causal(q, q, q)
+
+
+def test_backward_rejects_bad_arguments():
+    L = la.lib()
+    need = L.la_causal_backward_workspace_bytes(1, 1, 8, 64, 64, 1)
+    assert need > 256
+    assert L.la_causal_backward_workspace_bytes(1, 1, 0, 64, 64, 1) == 0
+    assert L.la_causal_backward_workspace_bytes(1, 1, 8, 48, 64, 1) == 0
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(12)]   # far apart, 16-byte aligned
+    q, k, v, dy, gq, gk, gv, S, z, gS, gz, ws = p
+
+    def call(**kw):
+        a = dict(q=q, k=k, v=v, dy=dy, gq=gq, gk=gk, gv=gv, B=1, H=1, N=8, d=64, dv=64, dt=1,
+                 eps=1e-6, S=None, z=None, gS=None, gz=None, ws=ws, wsb=need)
+        a.update(kw)
+        return L.la_backward_causal(a["q"], a["k"], a["v"], a["dy"], a["gq"], a["gk"], a["gv"],
+                                    a["B"], a["H"], a["N"], a["d"], a["dv"], a["dt"], a["eps"],
+                                    a["S"], a["z"], a["gS"], a["gz"], a["ws"], a["wsb"], None)
+
+    assert call(dy=None) == la.LA_ERR_INVALID_ARG
+    assert call(eps=0.0) == la.LA_ERR_INVALID_ARG
+    assert call(d=48) == la.LA_ERR_UNSUPPORTED
+    assert call(dt=7) == la.LA_ERR_UNSUPPORTED
+    assert call(gq=ctypes.c_void_p(q.value + 256)) == la.LA_ERR_INVALID_ARG    # dq over q
+    assert call(gk=ctypes.c_void_p(ws.value + 512)) == la.LA_ERR_INVALID_ARG   # dk over the workspace
+    assert call(gv=ctypes.c_void_p(gq.value + 16)) == la.LA_ERR_INVALID_ARG    # two outputs overlap
+    assert call(gS=gS) == la.LA_ERR_INVALID_ARG                                # dS without dz
+    assert call(S=S) == la.LA_ERR_INVALID_ARG                                  # S_in without z_in
+    assert call(gq=ctypes.c_void_p(gq.value + 4)) == la.LA_ERR_INVALID_ARG     # misaligned
+    assert call(wsb=need - 1) == la.LA_ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p(ws.value + 16)) == la.LA_ERR_WORKSPACE      # not 256-aligned

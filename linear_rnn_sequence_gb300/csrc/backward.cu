@@ -40,11 +40,15 @@
 //   4. scan        exclusive suffix over segments of those sums
 //   5. dkdv        per (head, segment), tokens in reverse from the suffix:
 //                  dk, dv; segment 0 ends with dL/dS_in, dL/dz_in
-// Inside a CTA the state lives in registers: thread (a, part) owns row a and
-// every kRT-th 4-column group of it, so a row reduction is a few lane
-// shuffles.  The reverse pass keeps a second, column-owned copy of Sh for the
-// reductions over rows that dv needs.  While a chunk is processed the next
-// one is already in flight from global memory into registers.
+// Inside a CTA the state lives in registers, tiled so that every reduction a
+// token needs stays inside one warp: for a reduction over value columns, warp
+// w owns a band of rows and lane l a few columns of each (the row's operands
+// are then warp-uniform broadcasts from shared memory); the reverse pass keeps
+// a second copy of Sh tiled the other way round for the reductions over rows
+// that dv needs.  A warp reduces its lanes' partial sums with a
+// reduce-scatter, so each lane ends with one finished row.  While a chunk is
+// processed the next one is already in flight from global memory into
+// registers.
 #include <algorithm>
 
 #include "la_device.cuh"
@@ -66,19 +70,69 @@ struct Cfg {
     static constexpr int kOffZ = D * DV, kOffU = D * DV + D, kOffN = D * DV + D + DV;
 };
 
-// Row-owned tiling of a ROWS x COLS matrix over NT threads: thread tid owns
-// row tid / kRT and the 4-column groups g with g % kRT == tid % kRT.
+// Tiling of a ROWS x COLS matrix over NT threads: warp w owns rows
+// [w RPW, (w+1) RPW) and lane l owns columns [l CPL, (l+1) CPL) of each.
 template <int NT, int ROWS, int COLS>
-struct Tile {
-    static constexpr int kRT = NT / ROWS;
-    static constexpr int kG = COLS / 4 / kRT;
-    static_assert(kRT >= 2 && kRT <= 16 && (kRT & (kRT - 1)) == 0 && kG >= 1 &&
-                  kG * 4 * kRT == COLS, "tile");
-    __device__ static int col(int i, int part) { return 4 * (i * kRT + part); }
+struct WarpRows {
+    static constexpr int NW = NT / 32;
+    static constexpr int RPW = ROWS / NW, CPL = COLS / 32;
+    static_assert(RPW >= 2 && RPW <= 8 && (RPW & (RPW - 1)) == 0 && RPW * NW == ROWS &&
+                  CPL >= 1 && CPL <= 4 && CPL * 32 == COLS, "tile");
+    // the row whose finished sum lane `lane` holds after reduce_scatter<RPW>
+    __device__ static int row_of(int lane) {
+        int r = 0;
+#pragma unroll
+        for (int m = RPW, o = 16; m > 1; m >>= 1, o >>= 1)
+            if (lane & o) r += m >> 1;
+        return r;
+    }
+    // lanes that write the finished rows (one per row)
+    __device__ static bool writer(int lane) { return (lane & (32 / RPW - 1)) == 0; }
 };
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+
+// n consecutive floats (n in {1, 2, 4, 8}, p aligned to min(n, 4) floats)
+template <int n>
+__device__ __forceinline__ void ldn(const float *p, float (&o)[n]) {
+    if constexpr (n >= 4) {
+#pragma unroll
+        for (int i = 0; i < n; i += 4) {
+            const float4 x = ld4(p + i);
+            o[i] = x.x; o[i + 1] = x.y; o[i + 2] = x.z; o[i + 3] = x.w;
+        }
+    } else if constexpr (n == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        o[0] = x.x; o[1] = x.y;
+    } else {
+        o[0] = *p;
+    }
+}
+
+// Sum M per-lane values over the 32 lanes of a warp.  Each halving step
+// trades half of the values with the partner lane, so the warp spends
+// M - 1 + log2(32 / M) shuffles; lane l returns the total of value
+// WarpRows::row_of(l).
+template <int M>
+__device__ __forceinline__ float reduce_scatter(const float (&x)[M], int lane) {
+    float cur[M];
+#pragma unroll
+    for (int j = 0; j < M; ++j) cur[j] = x[j];
+#pragma unroll
+    for (int m = M, o = 16; m > 1; m >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < m / 2; ++j) {
+            const float send = up ? cur[j] : cur[j + m / 2];
+            const float keep = up ? cur[j + m / 2] : cur[j];
+            cur[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (int o = 16 / M; o > 0; o >>= 1) cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], o);
+    return cur[0];
+}
 
 template <typename T> struct Vec;
 template <> struct Vec<float> {
@@ -151,13 +205,6 @@ __device__ __forceinline__ Seg segment(int P, int seg_chunks, int N) {
     return s;
 }
 
-template <int G>
-__device__ __forceinline__ float lane_group_sum(float x) {
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
 // ---- 0. split an initial state into (R, zeta, u, n) -------------------------
 template <int D, int DV>
 __global__ void bwd_seed_kernel(const float *__restrict__ S_in, const float *__restrict__ z_in,
@@ -189,60 +236,63 @@ __global__ void bwd_seed_kernel(const float *__restrict__ S_in, const float *__r
 
 // ---- 1. per-segment sums (R, zeta, u, n) ------------------------------------
 template <int D, int DV, typename T>
-__global__ void __launch_bounds__(Cfg<D, DV>::kNT)
+__global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
 bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, int P,
                      int seg_chunks, float *__restrict__ states)
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT;
-    using RT = Tile<NT, D, DV>;
+    using RT = WarpRows<NT, D, DV>;
     extern __shared__ float4 smem4[];
     float *sPk = reinterpret_cast<float *>(smem4);   // [kBC][D] psi(k)
     float *sV = sPk + kBC * D;                        // [kBC][DV]
     const Seg sg = segment(P, seg_chunks, N);
     if (sg.p == P - 1) return;   // no later segment reads the last one's sums
-    const int tid = threadIdx.x, a = tid / RT::kRT, part = tid % RT::kRT;
-    float R[4 * RT::kG];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
+    float R[RT::RPW][RT::CPL];
 #pragma unroll
-    for (int i = 0; i < 4 * RT::kG; ++i) R[i] = 0.f;
+    for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+        for (int c = 0; c < RT::CPL; ++c) R[r][c] = 0.f;
     float zeta = 0.f, u = 0.f;
     ChunkLoad<D, T, NT> lk;
     ChunkLoad<DV, T, NT> lv;
     lk.load(k + ((size_t)sg.h * N + sg.t0) * D, min(kBC, sg.t1 - sg.t0));
     lv.load(v + ((size_t)sg.h * N + sg.t0) * DV, min(kBC, sg.t1 - sg.t0));
-    for (int c0 = sg.t0; c0 < sg.t1; c0 += kBC) {
-        const int L = min(kBC, sg.t1 - c0);
+    for (int t0 = sg.t0; t0 < sg.t1; t0 += kBC) {
+        const int L = min(kBC, sg.t1 - t0);
         __syncthreads();
         lk.store(sPk, L, Psi());
         lv.store(sV, L, Ident());
         __syncthreads();
-        if (c0 + kBC < sg.t1) {
-            const size_t nrow = (size_t)sg.h * N + c0 + kBC;
-            const int nL = min(kBC, sg.t1 - c0 - kBC);
+        if (t0 + kBC < sg.t1) {
+            const size_t nrow = (size_t)sg.h * N + t0 + kBC;
+            const int nL = min(kBC, sg.t1 - t0 - kBC);
             lk.load(k + nrow * D, nL);
             lv.load(v + nrow * DV, nL);
         }
-        if (tid < DV)
-            for (int t = 0; t < L; ++t) u += sV[t * DV + tid];
+        if (tid < D)
+            for (int t = 0; t < L; ++t) zeta += sPk[t * D + tid];
+        else if (tid < D + DV)
+            for (int t = 0; t < L; ++t) u += sV[t * DV + tid - D];
         for (int t = 0; t < L; ++t) {
-            const float pk = sPk[t * D + a];
-            zeta += pk;
+            float pk[RT::RPW], x[RT::CPL];
+            ldn(sPk + t * D + r0, pk);
+            ldn(sV + t * DV + c0, x);
 #pragma unroll
-            for (int i = 0; i < RT::kG; ++i) {
-                const float4 x = ld4(sV + t * DV + RT::col(i, part));
-                R[4 * i] = fmaf(pk, x.x, R[4 * i]);
-                R[4 * i + 1] = fmaf(pk, x.y, R[4 * i + 1]);
-                R[4 * i + 2] = fmaf(pk, x.z, R[4 * i + 2]);
-                R[4 * i + 3] = fmaf(pk, x.w, R[4 * i + 3]);
-            }
+            for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+                for (int c = 0; c < RT::CPL; ++c) R[r][c] = fmaf(pk[r], x[c], R[r][c]);
         }
     }
     float *out = states + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int i = 0; i < RT::kG; ++i)
-        st4(out + a * DV + RT::col(i, part), make_float4(R[4 * i], R[4 * i + 1], R[4 * i + 2], R[4 * i + 3]));
-    if (part == 0) out[C::kOffZ + a] = zeta;
-    if (tid < DV) out[C::kOffU + tid] = u;
+    for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+        for (int c = 0; c < RT::CPL; ++c) out[(r0 + r) * DV + c0 + c] = R[r][c];
+    if (tid < D) out[C::kOffZ + tid] = zeta;
+    else if (tid < D + DV) out[C::kOffU + tid - D] = u;
     if (tid < 4) out[C::kOffN + tid] = tid == 0 ? (float)(sg.t1 - sg.t0) : 0.f;
 }
 
@@ -280,7 +330,10 @@ struct DqSmem {
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-template <int D, int DV, typename T>
+// SEG: the sequence is split (P > 1), so the segment's sums of phi(q) g^T
+// and phi(q) e are needed by the reverse scan; with one segment the reverse
+// pass starts from zero and they are skipped.
+template <int D, int DV, typename T, bool SEG>
 __global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
 bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ dy, float *__restrict__ dq, int N, int P, int seg_chunks,
@@ -289,7 +342,7 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT, NW = NT / 32;
-    using RT = Tile<NT, D, DV>;
+    using RT = WarpRows<NT, D, DV>;
     static_assert(NT >= D + DV, "one thread per feature and per value column");
     extern __shared__ float4 smem4[];
     float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D] phi(q)
@@ -311,15 +364,17 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float *sC = sE + kBC;                           // [kBC] c_t
     const Seg sg = segment(P, seg_chunks, N);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int a = tid / RT::kRT, part = tid % RT::kRT;
+    const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
+    const int my_row = r0 + RT::row_of(lane);
+    const bool writer = RT::writer(lane);
 
-    float R[4 * RT::kG], Sh[4 * RT::kG];
+    float R[RT::RPW][RT::CPL], Sh[RT::RPW][RT::CPL];
     const float *pre = prefix + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int i = 0; i < RT::kG; ++i) {
-        const float4 x = ld4(pre + a * DV + RT::col(i, part));
-        R[4 * i] = x.x; R[4 * i + 1] = x.y; R[4 * i + 2] = x.z; R[4 * i + 3] = x.w;
-        Sh[4 * i] = Sh[4 * i + 1] = Sh[4 * i + 2] = Sh[4 * i + 3] = 0.f;
+    for (int r = 0; r < RT::RPW; ++r) {
+        ldn(pre + (r0 + r) * DV + c0, R[r]);
+#pragma unroll
+        for (int c = 0; c < RT::CPL; ++c) Sh[r][c] = 0.f;
     }
     if (tid < D) sZrun[tid] = pre[C::kOffZ + tid];
     else if (tid < D + DV) sUrun[tid - D] = pre[C::kOffU + tid - D];
@@ -335,18 +390,18 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         lq.load(q + row0 * D, L); lk.load(k + row0 * D, L);
         lv.load(v + row0 * DV, L); ldy.load(dy + row0 * DV, L);
     }
-    for (int c0 = sg.t0; c0 < sg.t1; c0 += kBC) {
-        const int L = min(kBC, sg.t1 - c0);
-        const size_t row0 = (size_t)sg.h * N + c0;
+    for (int t0 = sg.t0; t0 < sg.t1; t0 += kBC) {
+        const int L = min(kBC, sg.t1 - t0);
+        const size_t row0 = (size_t)sg.h * N + t0;
         __syncthreads();   // the previous chunk is consumed
         lq.store(sFq, L, Phi());
         lk.store(sPk, L, Psi());
         lv.store(sV, L, Ident());
         ldy.store(sG, L, Ident());
         __syncthreads();
-        if (c0 + kBC < sg.t1) {   // the next chunk flies in while this one is processed
+        if (t0 + kBC < sg.t1) {   // the next chunk flies in while this one is processed
             const size_t nrow = row0 + kBC;
-            const int nL = min(kBC, sg.t1 - c0 - kBC);
+            const int nL = min(kBC, sg.t1 - t0 - kBC);
             lq.load(q + nrow * D, nL); lk.load(k + nrow * D, nL);
             lv.load(v + nrow * DV, nL); ldy.load(dy + nrow * DV, nL);
         }
@@ -398,27 +453,23 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         // the recurrence: R_t = R_{t-1} + psi(k_t) v_t^T, hR_t = R_t g_t;
         // and the segment's sum of phi(q_t) g_t^T
         for (int t = 0; t < L; ++t) {
-            const float pk = sPk[t * D + a], fq = sFq[t * D + a];
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float pk[RT::RPW], fq[RT::RPW], x[RT::CPL], g[RT::CPL], acc[RT::RPW];
+            ldn(sPk + t * D + r0, pk);      // warp-uniform
+            ldn(sFq + t * D + r0, fq);      // warp-uniform
+            ldn(sV + t * DV + c0, x);
+            ldn(sG + t * DV + c0, g);
 #pragma unroll
-            for (int i = 0; i < RT::kG; ++i) {
-                const float4 x = ld4(sV + t * DV + RT::col(i, part));
-                const float4 g = ld4(sG + t * DV + RT::col(i, part));
-                R[4 * i] = fmaf(pk, x.x, R[4 * i]);
-                R[4 * i + 1] = fmaf(pk, x.y, R[4 * i + 1]);
-                R[4 * i + 2] = fmaf(pk, x.z, R[4 * i + 2]);
-                R[4 * i + 3] = fmaf(pk, x.w, R[4 * i + 3]);
-                acc[0] = fmaf(R[4 * i], g.x, acc[0]);
-                acc[1] = fmaf(R[4 * i + 1], g.y, acc[1]);
-                acc[2] = fmaf(R[4 * i + 2], g.z, acc[2]);
-                acc[3] = fmaf(R[4 * i + 3], g.w, acc[3]);
-                Sh[4 * i] = fmaf(fq, g.x, Sh[4 * i]);
-                Sh[4 * i + 1] = fmaf(fq, g.y, Sh[4 * i + 1]);
-                Sh[4 * i + 2] = fmaf(fq, g.z, Sh[4 * i + 2]);
-                Sh[4 * i + 3] = fmaf(fq, g.w, Sh[4 * i + 3]);
+            for (int r = 0; r < RT::RPW; ++r) {
+                acc[r] = 0.f;
+#pragma unroll
+                for (int c = 0; c < RT::CPL; ++c) {
+                    R[r][c] = fmaf(pk[r], x[c], R[r][c]);
+                    acc[r] = fmaf(R[r][c], g[c], acc[r]);
+                    if constexpr (SEG) Sh[r][c] = fmaf(fq[r], g[c], Sh[r][c]);
+                }
             }
-            const float hsum = lane_group_sum<RT::kRT>((acc[0] + acc[1]) + (acc[2] + acc[3]));
-            if (part == 0) sH[t * D + a] = hsum;
+            const float hsum = reduce_scatter<RT::RPW>(acc, lane);
+            if (writer) sH[t * D + my_row] = hsum;
         }
         __syncthreads();
         // e_t and c_t (see the header: the leading terms cancel algebraically)
@@ -446,16 +497,19 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             dinv_out[row0 + tid] = sDinv[tid];
             e_out[row0 + tid] = sE[tid];
         }
-        if (part == 0)
-            for (int t = 0; t < L; ++t) zh = fmaf(sFq[t * D + a], sE[t], zh);
+        if (SEG && tid < D)
+            for (int t = 0; t < L; ++t) zh = fmaf(sFq[t * D + tid], sE[t], zh);
         n_run += (float)L;
     }
-    float *out = rev_local + ((size_t)sg.h * P + sg.p) * C::kE;
+    if constexpr (SEG) {
+        float *out = rev_local + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int i = 0; i < RT::kG; ++i)
-        st4(out + a * DV + RT::col(i, part), make_float4(Sh[4 * i], Sh[4 * i + 1], Sh[4 * i + 2], Sh[4 * i + 3]));
-    if (part == 0) out[C::kOffZ + a] = zh;
-    for (int e = tid; e < DV + 4; e += NT) out[C::kOffU + e] = 0.f;   // unused slots
+        for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+            for (int c = 0; c < RT::CPL; ++c) out[(r0 + r) * DV + c0 + c] = Sh[r][c];
+        if (tid < D) out[C::kOffZ + tid] = zh;
+        for (int e = tid; e < DV + 4; e += NT) out[C::kOffU + e] = 0.f;   // unused slots
+    }
 }
 
 // ---- 5. dk, dv (and dL/dS_in, dL/dz_in from segment 0) --------------------
@@ -475,34 +529,33 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT;
-    using RT = Tile<NT, D, DV>;    // copy 1: thread owns row a of Sh
-    using CT = Tile<NT, DV, D>;    // copy 2: thread owns column b of Sh
+    using RT = WarpRows<NT, D, DV>;   // copy 1 of Sh: rows per warp, for Sh v
+    using CT = WarpRows<NT, DV, D>;   // copy 2, transposed: columns per warp, for Sh^T phi(k)
     extern __shared__ float4 smem4[];
     float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D]
     float *sFk = sFq + kBC * D;                     // [kBC][D]
-    float *sDK = sFk + kBC * D;                     // [kBC][D]
+    float *sDK = sFk + kBC * D;                     // [kBC][D] zh_t, then dk_t
     float *sV = sDK + kBC * D;                      // [kBC][DV]
     float *sG = sV + kBC * DV;                      // [kBC][DV] dy_t, then g_t
     float *sDV = sG + kBC * DV;                     // [kBC][DV]
     float *sE = sDV + kBC * DV;                     // [kBC]
     float *sDinv = sE + kBC;                        // [kBC]
     const Seg sg = segment(P, seg_chunks, N);
-    const int tid = threadIdx.x;
-    const int a = tid / RT::kRT, part = tid % RT::kRT;
-    const int b = tid / CT::kRT, part2 = tid % CT::kRT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;       // copy 1
+    const int b0 = warp * CT::RPW, a0 = lane * CT::CPL;       // copy 2
+    const int my_row = r0 + RT::row_of(lane), my_col = b0 + CT::row_of(lane);
+    const bool wr1 = RT::writer(lane), wr2 = CT::writer(lane);
 
-    float S1[4 * RT::kG], S2[4 * CT::kG];
+    float S1[RT::RPW][RT::CPL], S2[CT::RPW][CT::CPL];
     const float *suf = suffix + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int i = 0; i < RT::kG; ++i) {
-        const float4 x = ld4(suf + a * DV + RT::col(i, part));
-        S1[4 * i] = x.x; S1[4 * i + 1] = x.y; S1[4 * i + 2] = x.z; S1[4 * i + 3] = x.w;
-    }
+    for (int r = 0; r < RT::RPW; ++r) ldn(suf + (r0 + r) * DV + c0, S1[r]);
 #pragma unroll
-    for (int i = 0; i < CT::kG; ++i)
+    for (int i = 0; i < CT::RPW; ++i)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) S2[4 * i + r] = suf[(CT::col(i, part2) + r) * DV + b];
-    float zh = suf[C::kOffZ + a];
+        for (int j = 0; j < CT::CPL; ++j) S2[i][j] = suf[(a0 + j) * DV + b0 + i];
+    float zh = tid < D ? suf[C::kOffZ + tid] : 0.f;   // thread a < D carries zh[a]
 
     ChunkLoad<D, T, NT> lq, lk;
     ChunkLoad<DV, T, NT> lv;
@@ -510,8 +563,8 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     float pdinv = 0.f, pe = 0.f;
     const int nch = (sg.t1 - sg.t0 + kBC - 1) / kBC;
     auto issue = [&](int c) {
-        const int c0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - c0);
-        const size_t row0 = (size_t)sg.h * N + c0;
+        const int t0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - t0);
+        const size_t row0 = (size_t)sg.h * N + t0;
         lq.load(q + row0 * D, L); lk.load(k + row0 * D, L);
         lv.load(v + row0 * DV, L); ldy.load(dy + row0 * DV, L);
         pdinv = tid < L ? __ldg(dinv + row0 + tid) : 0.f;
@@ -519,8 +572,8 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     };
     issue(nch - 1);
     for (int c = nch - 1; c >= 0; --c) {
-        const int c0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - c0);
-        const size_t row0 = (size_t)sg.h * N + c0;
+        const int t0 = sg.t0 + c * kBC, L = min(kBC, sg.t1 - t0);
+        const size_t row0 = (size_t)sg.h * N + t0;
         __syncthreads();   // the previous chunk's outputs are written
         lq.store(sFq, L, Phi());
         lk.store(sFk, L, Phi());
@@ -533,45 +586,46 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
         __syncthreads();
         if (c > 0) issue(c - 1);
         for (int e = tid; e < kBC * DV; e += NT) sG[e] *= sDinv[e / DV];
+        // zh_t = zh_{t+1} + phi(q_t) e_t for every token of the chunk, last first
+        if (tid < D)
+            for (int t = L - 1; t >= 0; --t) {
+                zh = fmaf(sFq[t * D + tid], sE[t], zh);
+                sDK[t * D + tid] = zh;
+            }
         __syncthreads();
         for (int t = L - 1; t >= 0; --t) {
-            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T, zh_t = zh_{t+1} + phi(q_t) e_t
-            const float fq = sFq[t * D + a];
-            zh = fmaf(fq, sE[t], zh);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T on both copies
+            float fq[RT::RPW], g[RT::CPL], x[RT::CPL], acc[RT::RPW];
+            ldn(sFq + t * D + r0, fq);       // warp-uniform
+            ldn(sG + t * DV + c0, g);
+            ldn(sV + t * DV + c0, x);
 #pragma unroll
-            for (int i = 0; i < RT::kG; ++i) {
-                const float4 g = ld4(sG + t * DV + RT::col(i, part));
-                const float4 x = ld4(sV + t * DV + RT::col(i, part));
-                S1[4 * i] = fmaf(fq, g.x, S1[4 * i]);
-                S1[4 * i + 1] = fmaf(fq, g.y, S1[4 * i + 1]);
-                S1[4 * i + 2] = fmaf(fq, g.z, S1[4 * i + 2]);
-                S1[4 * i + 3] = fmaf(fq, g.w, S1[4 * i + 3]);
-                acc[0] = fmaf(S1[4 * i], x.x, acc[0]);
-                acc[1] = fmaf(S1[4 * i + 1], x.y, acc[1]);
-                acc[2] = fmaf(S1[4 * i + 2], x.z, acc[2]);
-                acc[3] = fmaf(S1[4 * i + 3], x.w, acc[3]);
-            }
-            const float dfk = lane_group_sum<RT::kRT>((acc[0] + acc[1]) + (acc[2] + acc[3]));
-            if (part == 0) sDK[t * D + a] = (dfk + zh) * fminf(sFk[t * D + a], 1.f);
-            // the same update on the column-owned copy, then dv_t = Sh_t^T phi(k_t)
-            const float gb = sG[t * DV + b];
-            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int r = 0; r < RT::RPW; ++r) {
+                acc[r] = 0.f;
 #pragma unroll
-            for (int i = 0; i < CT::kG; ++i) {
-                const float4 fq4 = ld4(sFq + t * D + CT::col(i, part2));
-                const float4 fk4 = ld4(sFk + t * D + CT::col(i, part2));
-                S2[4 * i] = fmaf(fq4.x, gb, S2[4 * i]);
-                S2[4 * i + 1] = fmaf(fq4.y, gb, S2[4 * i + 1]);
-                S2[4 * i + 2] = fmaf(fq4.z, gb, S2[4 * i + 2]);
-                S2[4 * i + 3] = fmaf(fq4.w, gb, S2[4 * i + 3]);
-                acc2[0] = fmaf(S2[4 * i], fk4.x, acc2[0]);
-                acc2[1] = fmaf(S2[4 * i + 1], fk4.y, acc2[1]);
-                acc2[2] = fmaf(S2[4 * i + 2], fk4.z, acc2[2]);
-                acc2[3] = fmaf(S2[4 * i + 3], fk4.w, acc2[3]);
+                for (int cc = 0; cc < RT::CPL; ++cc) {
+                    S1[r][cc] = fmaf(fq[r], g[cc], S1[r][cc]);
+                    acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
+                }
             }
-            const float dvb = lane_group_sum<CT::kRT>((acc2[0] + acc2[1]) + (acc2[2] + acc2[3]));
-            if (part2 == 0) sDV[t * DV + b] = dvb;
+            const float dfk = reduce_scatter<RT::RPW>(acc, lane);
+            if (wr1)   // dk_t = (Sh_t v_t + zh_t) * phi'(k_t)
+                sDK[t * D + my_row] = (dfk + sDK[t * D + my_row]) * fminf(sFk[t * D + my_row], 1.f);
+            float gb[CT::RPW], fq2[CT::CPL], fk2[CT::CPL], acc2[CT::RPW];
+            ldn(sG + t * DV + b0, gb);       // warp-uniform
+            ldn(sFq + t * D + a0, fq2);
+            ldn(sFk + t * D + a0, fk2);
+#pragma unroll
+            for (int i = 0; i < CT::RPW; ++i) {
+                acc2[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < CT::CPL; ++j) {
+                    S2[i][j] = fmaf(fq2[j], gb[i], S2[i][j]);
+                    acc2[i] = fmaf(S2[i][j], fk2[j], acc2[i]);
+                }
+            }
+            const float dvb = reduce_scatter<CT::RPW>(acc2, lane);   // dv_t = Sh_t^T phi(k_t)
+            if (wr2) sDV[t * DV + my_col] = dvb;
         }
         __syncthreads();
         for (int e = tid * 4; e < L * D; e += NT * 4) st4(dk + row0 * D + e, ld4(sDK + e));
@@ -580,9 +634,10 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     if (sg.p == 0 && grad_S) {
         float *gS = grad_S + (size_t)sg.h * D * DV;
 #pragma unroll
-        for (int i = 0; i < RT::kG; ++i)
-            st4(gS + a * DV + RT::col(i, part), make_float4(S1[4 * i], S1[4 * i + 1], S1[4 * i + 2], S1[4 * i + 3]));
-        if (part == 0) grad_z[(size_t)sg.h * D + a] = zh;
+        for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+            for (int cc = 0; cc < RT::CPL; ++cc) gS[(r0 + r) * DV + c0 + cc] = S1[r][cc];
+        if (tid < D) grad_z[(size_t)sg.h * D + tid] = zh;
     }
 }
 
@@ -603,7 +658,9 @@ int sm_count() {
 }
 
 // Segments per head: minimise (waves of one CTA per SM) x (chunks per
-// segment + about two chunks of fixed cost for the state traffic).
+// segment), where a split sequence costs about 1.4 times as much per chunk
+// (the segment sums of the kv pass and of the dq pass: 7 instead of 5 FMAs
+// per state element and token) plus two chunks of fixed cost for the scans.
 BwdPlan make_plan(int BH, int N, int d, int dv) {
     BwdPlan pl;
     const int nchunks = std::max(1, (N + kBC - 1) / kBC);
@@ -613,7 +670,7 @@ BwdPlan make_plan(int BH, int N, int d, int dv) {
         const int sc = (nchunks + P - 1) / P;
         if ((nchunks + sc - 1) / sc != P) continue;   // no empty segments
         const long waves = ((long)BH * P + slots - 1) / slots;
-        const long cost = waves * (sc + (P > 1 ? 2 : 0));
+        const long cost = waves * (P > 1 ? 7L * sc + 10 : 5L * sc);
         if (best < 0 || cost < best) { best = cost; pl.P = P; pl.seg_chunks = sc; }
     }
     pl.E = d * dv + d + dv + 4;
@@ -643,7 +700,9 @@ cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
     constexpr size_t kv_smem = sizeof(float) * kBC * (D + DV);
     constexpr size_t dq_smem = DqSmem<D, DV>::bytes, dkdv_smem = DkdvSmem<D, DV>::bytes;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T>,
+    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, DV, T>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv_smem)) != cudaSuccess)
@@ -659,11 +718,18 @@ cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
     }
     bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(fwd, pl.P, pl.E, bph, a.S_in ? seed : nullptr, 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_dq_kernel<D, DV, T><<<grid, C::kNT, dq_smem, a.stream>>>(q, k, v, a.dy, a.dq, a.N, pl.P,
-                                                                pl.seg_chunks, a.eps, fwd, rev,
-                                                                dinv, ev);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(rev, pl.P, pl.E, bph, nullptr, 1);
+    if (pl.P > 1) {
+        bwd_dq_kernel<D, DV, T, true><<<grid, C::kNT, dq_smem, a.stream>>>(
+            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(rev, pl.P, pl.E, bph, nullptr, 1);
+    } else {   // one segment: the reverse pass starts from the zero state
+        bwd_dq_kernel<D, DV, T, false><<<grid, C::kNT, dq_smem, a.stream>>>(
+            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(rev, 0, (size_t)BH * pl.E * sizeof(float), a.stream)) != cudaSuccess)
+            return e;
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dkdv_kernel<D, DV, T><<<grid, C::kNT, dkdv_smem, a.stream>>>(q, k, v, a.dy, a.dk, a.dv_grad,
                                                                     a.N, pl.P, pl.seg_chunks, rev,

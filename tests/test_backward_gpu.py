@@ -108,3 +108,16 @@ def test_backward_workload_sampled_heads(name, heads, cuda_device):
     for h in heads:
         want = oracle.causal_backward(flat(q)[h], flat(k)[h], flat(v)[h], flat(dy)[h])
         _check([flat(dq)[h], flat(dk)[h], flat(dvv)[h]], want)
+
+
+def test_backward_long_sequence_sampled_heads(cuda_device):
+    """B1 H32 N131072 d64: the sequence is split into segments joined by the
+    prefix and suffix scans; whole heads are checked against the oracle."""
+    w = WORKLOADS["causal_bf16_b1h32n131072d64"]
+    q, k, v, dy = make_backward_inputs(w.with_(mode="backward"))
+    dq, dk, dvv = la.backward_causal(*(t.to(cuda_device) for t in (q, k, v, dy)))
+    torch.cuda.synchronize()
+    flat = lambda t: t.reshape(w.BH, w.N, t.shape[-1])
+    for h in (0, 31):
+        want = oracle.causal_backward(flat(q)[h], flat(k)[h], flat(v)[h], flat(dy)[h])
+        _check([flat(dq)[h], flat(dk)[h], flat(dvv)[h]], want)

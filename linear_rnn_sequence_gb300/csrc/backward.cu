@@ -40,14 +40,13 @@
 //   4. scan        exclusive suffix over segments of those sums
 //   5. dkdv        per (head, segment), tokens in reverse from the suffix:
 //                  dk, dv; segment 0 ends with dL/dS_in, dL/dz_in
-// Inside a CTA the state lives in registers, tiled so that every reduction a
-// token needs stays inside one warp: for a reduction over value columns, warp
-// w owns a band of rows and lane l a few columns of each (the row's operands
-// are then warp-uniform broadcasts from shared memory); the reverse pass keeps
-// a second copy of Sh tiled the other way round for the reductions over rows
-// that dv needs.  A warp reduces its lanes' partial sums with a
-// reduce-scatter, so each lane ends with one finished row.  While a chunk is
-// processed the next one is already in flight from global memory into
+// Inside a CTA the state lives in registers: warp w owns a band of rows and
+// lane l a few columns of each, so the row's operands are warp-uniform
+// broadcasts from shared memory and a reduction over value columns stays in
+// the warp (a reduce-scatter: each lane ends with one finished row).  dv needs
+// reductions over rows; the reverse pass writes per-warp partial sums to
+// shared memory and adds them across the warps every 8 tokens.  While a chunk
+// is processed the next one is already in flight from global memory into
 // registers.
 #include <algorithm>
 
@@ -107,6 +106,18 @@ __device__ __forceinline__ void ldn(const float *p, float (&o)[n]) {
         o[0] = x.x; o[1] = x.y;
     } else {
         o[0] = *p;
+    }
+}
+
+template <int n>
+__device__ __forceinline__ void stn(float *p, const float (&x)[n]) {
+    if constexpr (n >= 4) {
+#pragma unroll
+        for (int i = 0; i < n; i += 4) st4(p + i, make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]));
+    } else if constexpr (n == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
+    } else {
+        *p = x[0];
     }
 }
 
@@ -515,7 +526,9 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 // ---- 5. dk, dv (and dL/dS_in, dL/dz_in from segment 0) --------------------
 template <int D, int DV>
 struct DkdvSmem {
-    static constexpr size_t floats = 3 * (size_t)kBC * D + 3 * (size_t)kBC * DV + 2 * kBC;
+    static constexpr int kGrp = 8;   // tokens whose dv partial sums are reduced together
+    static constexpr size_t floats = 3 * (size_t)kBC * D + 3 * (size_t)kBC * DV + 2 * kBC +
+                                     (size_t)kGrp * (Cfg<D, DV>::kNT / 32) * DV;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -529,8 +542,8 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT;
-    using RT = WarpRows<NT, D, DV>;   // copy 1 of Sh: rows per warp, for Sh v
-    using CT = WarpRows<NT, DV, D>;   // copy 2, transposed: columns per warp, for Sh^T phi(k)
+    constexpr int NW = NT / 32, kGrp = DkdvSmem<D, DV>::kGrp;
+    using RT = WarpRows<NT, D, DV>;   // Sh: a band of rows per warp, a few columns per lane
     extern __shared__ float4 smem4[];
     float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D]
     float *sFk = sFq + kBC * D;                     // [kBC][D]
@@ -540,21 +553,17 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     float *sDV = sG + kBC * DV;                     // [kBC][DV]
     float *sE = sDV + kBC * DV;                     // [kBC]
     float *sDinv = sE + kBC;                        // [kBC]
+    float *sPart = sDinv + kBC;                     // [kGrp][NW][DV] per-warp partial dv
     const Seg sg = segment(P, seg_chunks, N);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;       // copy 1
-    const int b0 = warp * CT::RPW, a0 = lane * CT::CPL;       // copy 2
-    const int my_row = r0 + RT::row_of(lane), my_col = b0 + CT::row_of(lane);
-    const bool wr1 = RT::writer(lane), wr2 = CT::writer(lane);
+    const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
+    const int my_row = r0 + RT::row_of(lane);
+    const bool wr1 = RT::writer(lane);
 
-    float S1[RT::RPW][RT::CPL], S2[CT::RPW][CT::CPL];
+    float S1[RT::RPW][RT::CPL];
     const float *suf = suffix + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
     for (int r = 0; r < RT::RPW; ++r) ldn(suf + (r0 + r) * DV + c0, S1[r]);
-#pragma unroll
-    for (int i = 0; i < CT::RPW; ++i)
-#pragma unroll
-        for (int j = 0; j < CT::CPL; ++j) S2[i][j] = suf[(a0 + j) * DV + b0 + i];
     float zh = tid < D ? suf[C::kOffZ + tid] : 0.f;   // thread a < D carries zh[a]
 
     ChunkLoad<D, T, NT> lq, lk;
@@ -593,12 +602,18 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 sDK[t * D + tid] = zh;
             }
         __syncthreads();
+        int slot = 0;
         for (int t = L - 1; t >= 0; --t) {
-            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T on both copies
-            float fq[RT::RPW], g[RT::CPL], x[RT::CPL], acc[RT::RPW];
+            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T; dk_t from Sh_t v_t (a reduction over
+            // columns, inside the warp); dv_t = Sh_t^T phi(k_t) from per-warp partial
+            // sums over the warp's rows, added across warps every kGrp tokens
+            float fq[RT::RPW], fk[RT::RPW], g[RT::CPL], x[RT::CPL], acc[RT::RPW], pv[RT::CPL];
             ldn(sFq + t * D + r0, fq);       // warp-uniform
+            ldn(sFk + t * D + r0, fk);       // warp-uniform
             ldn(sG + t * DV + c0, g);
             ldn(sV + t * DV + c0, x);
+#pragma unroll
+            for (int cc = 0; cc < RT::CPL; ++cc) pv[cc] = 0.f;
 #pragma unroll
             for (int r = 0; r < RT::RPW; ++r) {
                 acc[r] = 0.f;
@@ -606,26 +621,26 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 for (int cc = 0; cc < RT::CPL; ++cc) {
                     S1[r][cc] = fmaf(fq[r], g[cc], S1[r][cc]);
                     acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
+                    pv[cc] = fmaf(S1[r][cc], fk[r], pv[cc]);
                 }
             }
             const float dfk = reduce_scatter<RT::RPW>(acc, lane);
             if (wr1)   // dk_t = (Sh_t v_t + zh_t) * phi'(k_t)
                 sDK[t * D + my_row] = (dfk + sDK[t * D + my_row]) * fminf(sFk[t * D + my_row], 1.f);
-            float gb[CT::RPW], fq2[CT::CPL], fk2[CT::CPL], acc2[CT::RPW];
-            ldn(sG + t * DV + b0, gb);       // warp-uniform
-            ldn(sFq + t * D + a0, fq2);
-            ldn(sFk + t * D + a0, fk2);
+            stn(sPart + (slot * NW + warp) * DV + c0, pv);
+            if (++slot == kGrp || t == 0) {   // uniform across the CTA
+                __syncthreads();
+                // slot s holds token t + slot - 1 - s
+                for (int e = tid; e < slot * DV; e += NT) {
+                    const int s = e / DV, b = e % DV;
+                    float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < CT::RPW; ++i) {
-                acc2[i] = 0.f;
-#pragma unroll
-                for (int j = 0; j < CT::CPL; ++j) {
-                    S2[i][j] = fmaf(fq2[j], gb[i], S2[i][j]);
-                    acc2[i] = fmaf(S2[i][j], fk2[j], acc2[i]);
+                    for (int w = 0; w < NW; ++w) sum += sPart[(s * NW + w) * DV + b];
+                    sDV[(t + slot - 1 - s) * DV + b] = sum;
                 }
+                __syncthreads();
+                slot = 0;
             }
-            const float dvb = reduce_scatter<CT::RPW>(acc2, lane);   // dv_t = Sh_t^T phi(k_t)
-            if (wr2) sDV[t * DV + my_col] = dvb;
         }
         __syncthreads();
         for (int e = tid * 4; e < L * D; e += NT * 4) st4(dk + row0 * D + e, ld4(sDK + e));

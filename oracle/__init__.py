@@ -19,6 +19,9 @@ C loops in ``linattn_oracle.c``:
 * ``causal_chunked(q, k, v, C)``   -- blockwise form ("Linear Attention/es",
   "Entrenamiento: forma paralela").
 * ``decode_step(q, k, v, S, z)``   -- one recurrent step on a stored state.
+* ``causal_recurrent_decay(q, k, v, gamma)`` -- the recurrent form with a
+  per-head decay, S_t = gamma S_{t-1} + phi(k_t) v_t^T and likewise z_t
+  ("Linear Attention/es", "Variantes y extensiones", RetNet).
 * ``causal_backward(q, k, v, dy)`` -- gradients of sum_t dy_t . y_t of the
   causal form with respect to q, k, v (and the initial state), by the chain
   rule through the recurrence ("Linear Attention/es", "Entrenamiento: forma
@@ -74,6 +77,8 @@ def _bind(lib):
     lib.oracle_causal_chunked.restype = i
     lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, i, i, i, dbl, i]
     lib.oracle_decode_step.restype = i
+    lib.oracle_causal_recurrent_decay.argtypes = [P, P, P, P, i, i, i, i, dbl, P, P, P, P, P, i]
+    lib.oracle_causal_recurrent_decay.restype = i
     lib.oracle_causal_backward.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, P, P, P, P, i]
     lib.oracle_causal_backward.restype = i
     return lib
@@ -222,3 +227,29 @@ def causal_backward(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
     if rc:
         raise RuntimeError("oracle_causal_backward failed")
     return (gq, gk, gv, gS, gz) if return_state_grad else (gq, gk, gv)
+
+
+def causal_recurrent_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=None,
+                           return_state: bool = False, nthreads: int | None = None):
+    """Recurrent form with decay.  ``gamma`` has one value per head: shape [H]
+    for q of shape [B, H, N, d] (broadcast over B), or one value per head of
+    the flattened leading shape."""
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    g = _f64(gamma).reshape(-1)
+    if g.size != BH:
+        if len(lead) >= 1 and g.size == lead[-1]:
+            g = np.broadcast_to(g, lead).reshape(-1)
+        else:
+            raise ValueError(f"gamma has {g.size} values for {BH} heads")
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    y = np.empty(lead + (N, dv))
+    S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
+    z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
+    S = np.empty(lead + (d, dv)) if return_state else None
+    z = np.empty(lead + (d,)) if return_state else None
+    rc = _load().oracle_causal_recurrent_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                               float(eps), _ptr(g), _ptr(S_in), _ptr(z_in),
+                                               _ptr(S), _ptr(z), nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_causal_recurrent_decay failed")
+    return (y, S, z) if return_state else y

@@ -63,12 +63,17 @@ typedef struct {
     double *S_out, *z_out;     /* nullable */
     int BH, N, d, dv, causal, chunk;
     double eps;
+    const double *gamma;       /* nullable: per-head decay (recurrent form only) */
     int h_begin, h_end;
 } job_t;
 
 /* [P1] "Forma recurrente ..." / [P2] "La formulación recurrente paso a paso":
  * for t = 1..N: S += phi(k_t) v_t^T, z += phi(k_t) (update first), then
- * y_t = phi(q_t)^T S / max(phi(q_t)^T z, eps).                            */
+ * y_t = phi(q_t)^T S / max(phi(q_t)^T z, eps).
+ * With a decay ([P1] "Variantes y extensiones", RetNet: S_t = gamma S_{t-1}
+ * + phi(k_t) v_t^T, one gamma per head for the multi-scale retention the
+ * section mentions) the state is first multiplied by gamma; z is decayed
+ * the same way so that y_t stays a normalised average.                    */
 static void head_recurrent(const job_t *J, int h)
 {
     const int N = J->N, d = J->d, dv = J->dv;
@@ -82,6 +87,13 @@ static void head_recurrent(const job_t *J, int h)
     if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
     for (int t = 0; t < N; ++t) {
         for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        if (J->gamma) {
+            const double g = J->gamma[h];
+            for (int a = 0; a < d; ++a) {
+                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;
+                z[a] *= g;
+            }
+        }
         for (int a = 0; a < d; ++a) {
             for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];
             z[a] += fk[a];
@@ -267,6 +279,20 @@ int oracle_causal_recurrent(const double *q, const double *k, const double *v, d
     job_t J = {0};
     J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S_in; J.z_in = z_in;
     J.S_out = S_out; J.z_out = z_out; J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    return run_jobs(J, nthreads);
+}
+
+/* Causal recurrent form with a per-head decay gamma[BH] (0 < gamma <= 1). */
+int oracle_causal_recurrent_decay(const double *q, const double *k, const double *v, double *y,
+                                  int BH, int N, int d, int dv, double eps, const double *gamma,
+                                  const double *S_in, const double *z_in,
+                                  double *S_out, double *z_out, int nthreads)
+{
+    if (!gamma) return 1;
+    job_t J = {0};
+    J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S_in; J.z_in = z_in;
+    J.S_out = S_out; J.z_out = z_out; J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    J.gamma = gamma;
     return run_jobs(J, nthreads);
 }
 

@@ -41,6 +41,10 @@ MUTANTS = {
     "bwd_zh_dropped_from_dk": ("double s = z[a];", "double s = 0.0;"),
     "bwd_dv_uses_phi_q": ("s += S[(long)a * dv + b] * fk[a];", "s += S[(long)a * dv + b] * fq[a];"),
     "bwd_state_grad_not_reset": ("memset(S, 0, sizeof(double) * d * dv);", ";"),
+    # decay
+    "decay_skips_z": ("                z[a] *= g;\n", ""),
+    "decay_squared_on_S": ("for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;",
+                           "for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g * g;"),
 }
 
 
@@ -91,6 +95,12 @@ def _pins_pass() -> bool:
     # and a clamp that is active for some tokens only
     if not (backward_pins.fd_pin_passes(seed=3) and backward_pins.fd_pin_passes(seed=4)):
         return False
+    # decay: the pairwise form with gamma^(t-j) weights
+    from tests.test_oracle_decay import brute_decay
+    for gam in (0.5, 0.9):
+        if not np.allclose(oracle.causal_recurrent_decay(q, k, v, [gam]),
+                           brute_decay(q, k, v, gam), rtol=1e-11):
+            return False
     return True
 
 

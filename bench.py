@@ -4,7 +4,9 @@ Headline step: one causal chunkwise forward (la_forward_causal) over the
 B=8, H=16, N=8192, d=dv=128 bf16 workload (tokens = B*N positions, all heads).
 Each extra mode (non-causal B4 H8 N4096 d64, long causal B1 H32 N131072 d64,
 recurrent decode B256 H32 d128, gradients of the causal form at B8 H16 N8192
-d128) is timed the same way and reported under "modes" with its own roofline.
+d128, and the per-head decay variants: causal B8 H16 N8192 d128 and decode
+B256 H32 d128) is timed the same way and reported under "modes" with its own
+roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -28,8 +30,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from linear_rnn_sequence_gb300.workloads import (WORKLOADS, Workload, make_backward_inputs,  # noqa: E402
-                                                 make_qkv)
+from linear_rnn_sequence_gb300.workloads import (WORKLOADS, Workload, head_decays,  # noqa: E402
+                                                 make_backward_inputs, make_qkv)
 
 METRIC = "causal linear-attn tokens/s & TFLOP/s on 1 GB300, % roofline; decode tokens/s"
 HEADLINE = "causal_bf16_b8h16n8192d128"
@@ -66,6 +68,12 @@ def bwd_bytes_per_token_head(w: Workload):
 
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
 ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def decay_flops_per_token_head(d, dv):
+    # the recurrent definition: decay of S (d*dv) and z (d), update 2*d*dv + d,
+    # query 2*d*dv + 2d + dv
+    return 5 * d * dv + 4 * d + dv
 
 
 def decode_bytes_per_head_step(w: Workload):
@@ -496,6 +504,56 @@ def run_modes(args, world, dev, peaks, peak_kind):
                                   "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
     del q, k, v, dy, outs, ws
     torch.cuda.empty_cache()
+
+    # causal with a per-head decay (CUDA cores, fp32)
+    w = WORKLOADS["causal_decay_bf16_b8h16n8192d128"]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    gam = head_decays(w.H).to(dev)
+    y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    total, per = time_steps(lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y),
+                            max(3, min(args.steps, 10)), args.warmup, world)
+    T = w.BH * w.N
+    ms = sum(per) / len(per)
+    tflops = T * decay_flops_per_token_head(w.d, w.dv) / (ms * 1e-3) / 1e12
+    modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+                     "l2": "inputs larger than L2",
+                     "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
+                                  "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
+                                  "traffic": None,
+                                  "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
+                                  "hbm_roof_fraction": T * alg_bytes_per_token_head(w)
+                                  / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
+    del q, k, v, y
+    torch.cuda.empty_cache()
+
+    # decode with a per-head decay: state from a decayed 1024-token prefill
+    w = WORKLOADS["decode_decay_bf16_b256h32d128"]
+    gam = head_decays(w.H).to(dev)
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    _, S, z = la.forward_causal_decay(q, k, v, gam, return_state=True)
+    del q, k, v
+    torch.cuda.empty_cache()
+    g = torch.Generator(device=dev).manual_seed(w.seed + 1)
+    sc = torch.tensor(w.step_scale, device=dev)
+    qs = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    ks = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    vs = (torch.randn(nsteps, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
+    it[0] = 0
+
+    def ddstep():
+        i = it[0] % nsteps
+        it[0] += 1
+        la.decode_step_decay(qs[i], ks[i], vs[i], S, z, gam, eps=w.eps, out=yd)
+
+    total, per = time_steps(ddstep, nsteps, args.warmup, world)
+    ms = total / nsteps
+    modes[w.name] = {"tokens_per_s": world * w.B / (ms * 1e-3), "ms_per_step": ms,
+                     "steps_timed": nsteps, "l2": "state (512 MB) larger than L2",
+                     "roofline": roofline(w.BH * decode_bytes_per_head_step(w),
+                                          w.BH * decay_flops_per_token_head(w.d, w.dv),
+                                          sum(per) / len(per), peaks, peak_kind, None)}
+    del qs, ks, vs, S, z
+    torch.cuda.empty_cache()
     return modes
 
 
@@ -532,21 +590,23 @@ def run_reference(args, world, rank):
 def profile_case(args):
     """A few launches of one kernel on one workload, for ncu captures.
 
-    --profile-case causal|long|noncausal|decode|backward picks the workload
+    --profile-case causal|long|noncausal|decode|backward|causal_decay|decode_decay picks the workload
     (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 / B256 H32 d128
-    decode / gradients at B8 H16 N8192 d128); --batch overrides B for a
-    smaller capture.
+    decode / gradients at B8 H16 N8192 d128 / the decay variants of the causal
+    and decode workloads); --batch overrides B for a smaller capture.
     """
     from linear_rnn_sequence_gb300 import linattn as la
     names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
              "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128",
-             "backward": "causal_backward_bf16_b8h16n8192d128"}
+             "backward": "causal_backward_bf16_b8h16n8192d128",
+             "causal_decay": "causal_decay_bf16_b8h16n8192d128",
+             "decode_decay": "decode_decay_bf16_b256h32d128"}
     w = WORKLOADS[names[args.profile_case]]
     if args.batch:
         w = w.with_(B=args.batch)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if w.mode == "decode":
+    if w.mode in ("decode", "decode_decay"):
         g = torch.Generator(device=dev).manual_seed(w.seed + 1)
         sc = torch.tensor(w.step_scale, device=dev)
         S = torch.randn(w.B, w.H, w.d, w.dv, generator=g, device=dev)
@@ -554,7 +614,16 @@ def profile_case(args):
         q, k = ((torch.randn(w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype) for _ in range(2))
         v = (torch.randn(w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
         y = torch.empty(w.B, w.H, w.dv, device=dev)
-        fn = lambda: la.decode_step(q, k, v, S, z, eps=w.eps, out=y)
+        if w.mode == "decode":
+            fn = lambda: la.decode_step(q, k, v, S, z, eps=w.eps, out=y)
+        else:
+            gam = head_decays(w.H).to(dev)
+            fn = lambda: la.decode_step_decay(q, k, v, S, z, gam, eps=w.eps, out=y)
+    elif w.mode == "causal_decay":
+        q, k, v = make_qkv(w, device=dev, gen_device=dev)
+        y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+        gam = head_decays(w.H).to(dev)
+        fn = lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y)
     elif w.mode == "backward":
         q, k, v, dy = make_backward_inputs(w, device=dev, gen_device=dev)
         outs = (torch.empty(w.B, w.H, w.N, w.d, device=dev),
@@ -594,7 +663,8 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward"])
+    ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward",
+                                               "causal_decay", "decode_decay"])
     ap.add_argument("--batch", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

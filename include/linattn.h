@@ -124,6 +124,37 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Causal forward with a per-head decay ("Linear Attention/es", "Variantes y
+ * extensiones", RetNet: the unbounded cumulative sum is replaced by
+ *   S_t = gamma_h S_{t-1} + phi(k_t) v_t^T,  z_t = gamma_h z_{t-1} + phi(k_t),
+ *   y_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps),
+ * one gamma per head for the multi-scale retention the section mentions; z
+ * is decayed like S so that y stays a normalised average).  gamma is a DEVICE
+ * array of H floats in [0, 1], shared by the B batch rows; its values are
+ * not checked (a value outside [0, 1] gives a meaningless result, not an
+ * error).  Arguments, layouts and the initial / final state as in
+ * la_forward_causal; no workspace is needed.  Computed blockwise in fp32 on
+ * the CUDA cores (the blocks' pairs weighted by gamma^(i-j), the carried
+ * state by gamma^(i+1)), for both input dtypes.  NULL gamma:
+ * LA_ERR_INVALID_ARG.
+ */
+LA_API la_status la_forward_causal_decay(const void *q, const void *k, const void *v, float *y,
+                                         int B, int H, int N, int d, int dv, la_dtype dt,
+                                         float eps, const float *gamma, const float *S_in,
+                                         const float *z_in, float *S_out, float *z_out,
+                                         void *stream);
+
+/*
+ * One decode step with a per-head decay, in place on (S, z):
+ *   S <- gamma_h S + phi(k) v^T,  z <- gamma_h z + phi(k),
+ *   y = phi(q)^T S / max(phi(q)^T z, eps).
+ * gamma as in la_forward_causal_decay; the rest as in la_decode_step.
+ */
+LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *v, float *y,
+                                      float *S, float *z, int B, int H, int d, int dv,
+                                      la_dtype dt, float eps, const float *gamma, void *stream);
+
+/*
  * Workspace size in bytes for la_backward_causal (0 for N == 0 or
  * unsupported sizes).  It holds the run-time status header, per-segment
  * forward and reverse state sums for the sequence-axis split, and two floats

@@ -180,6 +180,59 @@ la_status la_decode_step(const void *q, const void *k, const void *v, float *y, 
     return from_cuda(launch_decode_simt(a));
 }
 
+la_status la_forward_causal_decay(const void *q, const void *k, const void *v, float *y, int B,
+                                  int H, int N, int d, int dv, la_dtype dt, float eps,
+                                  const float *gamma, const float *S_in, const float *z_in,
+                                  float *S_out, float *z_out, void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
+    if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
+    const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
+    if (overlap(y, T * dv * 4, S_in, sb) || overlap(y, T * dv * 4, z_in, zb) ||
+        overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb) ||
+        overlap(y, T * dv * 4, gamma, (size_t)H * 4))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {  // no tokens: the final state is the initial state
+        if (S_out) {
+            cudaError_t e = cudaSuccess;
+            if (!S_in) e = cudaMemsetAsync(S_out, 0, sb, s);
+            else if (S_in != S_out)
+                e = cudaMemcpyAsync(S_out, S_in, sb, cudaMemcpyDeviceToDevice, s);
+            if (e == cudaSuccess) {
+                if (!z_in) e = cudaMemsetAsync(z_out, 0, zb, s);
+                else if (z_in != z_out)
+                    e = cudaMemcpyAsync(z_out, z_in, zb, cudaMemcpyDeviceToDevice, s);
+            }
+            return from_cuda(e);
+        }
+        return LA_OK;
+    }
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out, nullptr, 0, s};
+    a.gamma = gamma;
+    return from_cuda(launch_causal_simt(a));
+}
+
+la_status la_decode_step_decay(const void *q, const void *k, const void *v, float *y, float *S,
+                               float *z, int B, int H, int d, int dv, la_dtype dt, float eps,
+                               const float *gamma, void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, 1, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S, z, true)) != LA_OK) return st;
+    const size_t yb = (size_t)B * H * dv * 4, sb = (size_t)B * H * d * dv * 4,
+                 zb = (size_t)B * H * d * 4;
+    if (overlap(y, yb, S, sb) || overlap(y, yb, z, zb) || overlap(S, sb, z, zb) ||
+        overlap(gamma, (size_t)H * 4, S, sb) || overlap(gamma, (size_t)H * 4, z, zb) ||
+        overlap(gamma, (size_t)H * 4, y, yb))
+        return LA_ERR_INVALID_ARG;
+    DecodeArgs a{q, k, v, y, S, z, B, H, d, dv, dt, eps, static_cast<cudaStream_t>(stream)};
+    a.gamma = gamma;
+    return from_cuda(launch_decode_simt(a));
+}
+
 size_t la_causal_backward_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
     if (B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
     if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return 0;

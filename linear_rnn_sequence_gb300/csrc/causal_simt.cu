@@ -11,6 +11,12 @@
 // y are independent; the denominator is recomputed by each column block).
 // The state S[:, cols] (d x 32) and z live in shared memory for the whole
 // sequence; only q, k, v are read and y written.
+//
+// With a per-head decay gamma (RetNet in "Variantes y extensiones":
+// S_t = gamma S_{t-1} + phi(k_t) v_t^T, z alike) token i of a block sees the
+// pairs j <= i weighted by gamma^(i-j) and the state of the previous blocks
+// by gamma^(i+1); after a block of L tokens the state becomes
+// gamma^L S_prev + sum_j gamma^(L-1-j) phi(k_j) v_j^T.
 #include "la_device.cuh"
 #include "la_internal.h"
 
@@ -25,15 +31,16 @@ template <int D>
 struct SimtSmem {
     static constexpr int QS = D + 1;  // padded row stride for phi(Q), phi(K)
     static constexpr size_t bytes =
-        sizeof(float) * (2 * kC * QS + kC * kCols + D * kCols + D + kC * (kC + 1) + 2 * kC);
+        sizeof(float) * (2 * kC * QS + kC * kCols + D * kCols + D + kC * (kC + 1) + 2 * kC + kC + 1);
 };
 
-template <int D, typename T>
+template <int D, typename T, bool DECAY>
 __global__ void __launch_bounds__(kThreads)
 causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    float *__restrict__ y, int N, int DV, float eps,
                    const float *__restrict__ S_in, const float *__restrict__ z_in,
-                   float *__restrict__ S_out, float *__restrict__ z_out)
+                   float *__restrict__ S_out, float *__restrict__ z_out,
+                   const float *__restrict__ gamma, int H)
 {
     constexpr int QS = SimtSmem<D>::QS;
     extern __shared__ float sm[];
@@ -45,6 +52,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     float *Ps = zs + D;                   // [kC][kC+1] masked w_ij
     float *dinter = Ps + kC * (kC + 1);   // [kC] phi(q_i)^T z_prev
     float *dens = dinter + kC;            // [kC] clamped denominators
+    float *pw = dens + kC;                // [kC+1] gamma^m
 
     const int head = blockIdx.x;
     const int col0 = blockIdx.y * kCols;
@@ -59,6 +67,14 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         Ss[i] = S_in ? S_in[((long)head * D + a) * DV + col0 + c] : 0.f;
     }
     for (int a = tid; a < D; a += kThreads) zs[a] = z_in ? z_in[(long)head * D + a] : 0.f;
+    if (DECAY && tid == 0) {
+        const float g = gamma[head % H];
+        float p = 1.f;
+        for (int m = 0; m <= kC; ++m) {
+            pw[m] = p;
+            p *= g;
+        }
+    }
 
     for (int t0 = 0; t0 < N; t0 += kC) {
         const int L = min(kC, N - t0);
@@ -89,12 +105,14 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                 for (int r = 0; r < 4; ++r) acc[r] = fmaf(Qs[(i0 + r) * QS + a], kv, acc[r]);
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) Ps[(i0 + r) * (kC + 1) + j] = (j <= i0 + r) ? acc[r] : 0.f;
+            for (int r = 0; r < 4; ++r)
+                Ps[(i0 + r) * (kC + 1) + j] =
+                    (j <= i0 + r) ? (DECAY ? acc[r] * pw[i0 + r - j] : acc[r]) : 0.f;
         }
         if (tid < kC) {
             float s = 0.f;
             for (int a = 0; a < D; ++a) s = fmaf(Qs[tid * QS + a], zs[a], s);
-            dinter[tid] = s;
+            dinter[tid] = DECAY ? s * pw[tid + 1] : s;
         }
         __syncthreads();
         if (tid < kC) {
@@ -113,6 +131,9 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 #pragma unroll
                 for (int r = 0; r < 4; ++r) acc[r] = fmaf(Qs[(i0 + r) * QS + a], s, acc[r]);
             }
+            if (DECAY)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] *= pw[i0 + r + 1];
             for (int j = 0; j < kC; ++j) {
                 const float vj = Vs[j * kCols + c];
 #pragma unroll
@@ -125,16 +146,30 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         __syncthreads();
 
         // state update: S[a][c] += sum_j phi(k_j)[a] v_j[c];  z += sum_j phi(k_j)
-        for (int e = tid; e < D * kCols; e += kThreads) {
-            const int a = e / kCols, c = e % kCols;
-            float s = Ss[e];
-            for (int j = 0; j < kC; ++j) s = fmaf(Ks[j * QS + a], Vs[j * kCols + c], s);
-            Ss[e] = s;
-        }
-        for (int a = tid; a < D; a += kThreads) {
-            float s = zs[a];
-            for (int j = 0; j < kC; ++j) s += Ks[j * QS + a];
-            zs[a] = s;
+        if (DECAY) {   // gamma^L S_prev + sum_{j<L} gamma^(L-1-j) phi(k_j) v_j^T
+            for (int e = tid; e < D * kCols; e += kThreads) {
+                const int a = e / kCols, c = e % kCols;
+                float s = Ss[e] * pw[L];
+                for (int j = 0; j < L; ++j) s = fmaf(Ks[j * QS + a] * pw[L - 1 - j], Vs[j * kCols + c], s);
+                Ss[e] = s;
+            }
+            for (int a = tid; a < D; a += kThreads) {
+                float s = zs[a] * pw[L];
+                for (int j = 0; j < L; ++j) s = fmaf(Ks[j * QS + a], pw[L - 1 - j], s);
+                zs[a] = s;
+            }
+        } else {
+            for (int e = tid; e < D * kCols; e += kThreads) {
+                const int a = e / kCols, c = e % kCols;
+                float s = Ss[e];
+                for (int j = 0; j < kC; ++j) s = fmaf(Ks[j * QS + a], Vs[j * kCols + c], s);
+                Ss[e] = s;
+            }
+            for (int a = tid; a < D; a += kThreads) {
+                float s = zs[a];
+                for (int j = 0; j < kC; ++j) s += Ks[j * QS + a];
+                zs[a] = s;
+            }
         }
     }
     __syncthreads();
@@ -147,23 +182,25 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         for (int a = tid; a < D; a += kThreads) z_out[(long)head * D + a] = zs[a];
 }
 
-template <int D, typename T>
+template <int D, typename T, bool DECAY>
 cudaError_t launch_t(const FwdArgs &a) {
     const size_t smem = SimtSmem<D>::bytes;
-    auto kern = causal_simt_kernel<D, T>;
+    auto kern = causal_simt_kernel<D, T, DECAY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.BH(), a.dv / kCols);
     kern<<<grid, kThreads, smem, a.stream>>>((const T *)a.q, (const T *)a.k, (const T *)a.v,
                                              a.y, a.N, a.dv, a.eps, a.S_in, a.z_in, a.S_out,
-                                             a.z_out);
+                                             a.z_out, a.gamma, a.H);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const FwdArgs &a) {
-    return a.dt == LA_DTYPE_BF16 ? launch_t<D, __nv_bfloat16>(a) : launch_t<D, float>(a);
+    if (a.gamma)
+        return a.dt == LA_DTYPE_BF16 ? launch_t<D, __nv_bfloat16, true>(a) : launch_t<D, float, true>(a);
+    return a.dt == LA_DTYPE_BF16 ? launch_t<D, __nv_bfloat16, false>(a) : launch_t<D, float, false>(a);
 }
 
 }  // namespace

@@ -3,6 +3,8 @@
 // "Linear Attention/es", "Forma recurrente e inferencia autorregresiva":
 //   S <- S + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T S / max(phi(q)^T z, eps)
 // (update first, then read, as in "La formulación recurrente paso a paso").
+// With a per-head decay gamma (RetNet in "Variantes y extensiones":
+// S <- gamma S + phi(k) v^T, and z alike) the stored state is scaled first.
 //
 // The step is bound by HBM: per head it reads and writes d*dv*4 bytes of S
 // and does 2*d*dv FMAs.  One CTA of 8 warps owns one head.  Warp w owns the
@@ -47,10 +49,11 @@ template <> struct FVec<4> {
 
 constexpr int kDecodeWarps = 8;
 
-template <int D, int DV, typename T>
+template <int D, int DV, typename T, bool DECAY>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                   float *__restrict__ y, float *__restrict__ S, float *__restrict__ z, float eps)
+                   float *__restrict__ y, float *__restrict__ S, float *__restrict__ z, float eps,
+                   const float *__restrict__ gamma, int H)
 {
     constexpr int NW = kDecodeWarps;
     constexpr int RPW = D / NW;   // rows of S per warp
@@ -64,6 +67,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long qk_off = (long)head * D, v_off = (long)head * DV;
     float *Sh = S + (long)head * D * DV;
+    const float g = DECAY ? gamma[head % H] : 1.f;
 
     // Issue the state loads first: they are the whole cost of the step.
     FVec<VEC> s[RPW];
@@ -77,7 +81,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         const float fk = phi_f(to_f(k[qk_off + i]));
         fq_s[i] = fq;
         fk_s[i] = fk;
-        const float zn = z[qk_off + i] + fk;
+        const float zn = DECAY ? fmaf(g, z[qk_off + i], fk) : z[qk_off + i] + fk;
         z[qk_off + i] = zn;
         dp = fmaf(fq, zn, dp);
     }
@@ -95,7 +99,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         const float fk = fk_s[a], fq = fq_s[a];
 #pragma unroll
         for (int c = 0; c < VEC; ++c) {
-            const float sn = fmaf(fk, vv[c], s[r].x[c]);
+            const float sn = fmaf(fk, vv[c], DECAY ? g * s[r].x[c] : s[r].x[c]);
             s[r].x[c] = sn;
             acc[c] = fmaf(fq, sn, acc[c]);
         }
@@ -113,17 +117,19 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     }
 }
 
+template <int D, int DV, typename T, bool DECAY>
+cudaError_t launch_typed(const DecodeArgs &a) {
+    decode_step_kernel<D, DV, T, DECAY><<<a.B * a.H, kDecodeWarps * 32, 0, a.stream>>>(
+        (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.S, a.z, a.eps, a.gamma, a.H);
+    return cudaGetLastError();
+}
+
 template <int D, int DV>
 cudaError_t launch_dv(const DecodeArgs &a) {
-    const int grid = a.B * a.H;
     if (a.dt == LA_DTYPE_BF16)
-        decode_step_kernel<D, DV, __nv_bfloat16><<<grid, kDecodeWarps * 32, 0, a.stream>>>(
-            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v,
-            a.y, a.S, a.z, a.eps);
-    else
-        decode_step_kernel<D, DV, float><<<grid, kDecodeWarps * 32, 0, a.stream>>>(
-            (const float *)a.q, (const float *)a.k, (const float *)a.v, a.y, a.S, a.z, a.eps);
-    return cudaGetLastError();
+        return a.gamma ? launch_typed<D, DV, __nv_bfloat16, true>(a)
+                       : launch_typed<D, DV, __nv_bfloat16, false>(a);
+    return a.gamma ? launch_typed<D, DV, float, true>(a) : launch_typed<D, DV, float, false>(a);
 }
 
 template <int D>

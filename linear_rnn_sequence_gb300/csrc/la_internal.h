@@ -23,6 +23,7 @@ struct FwdArgs {
     void *ws;                   // workspace (may be null when none is needed)
     size_t ws_bytes;
     cudaStream_t stream;
+    const float *gamma = nullptr;   // per-head decay [H] (device), null: none
     int BH() const { return B * H; }
 };
 
@@ -33,6 +34,7 @@ struct DecodeArgs {
     la_dtype dt;
     float eps;
     cudaStream_t stream;
+    const float *gamma = nullptr;   // per-head decay [H] (device), null: none
 };
 
 // Gradients of the causal form; pointers are device pointers.

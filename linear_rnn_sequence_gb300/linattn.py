@@ -70,6 +70,11 @@ def lib():
             L.la_forward_causal_host.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
                                                  sz, vp]
             L.la_forward_causal_host.restype = i
+            L.la_forward_causal_decay.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
+                                                  vp, vp, vp]
+            L.la_forward_causal_decay.restype = i
+            L.la_decode_step_decay.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+            L.la_decode_step_decay.restype = i
             L.la_causal_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
             L.la_causal_backward_workspace_bytes.restype = sz
             L.la_backward_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
@@ -172,6 +177,47 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
         if err != LA_OK:
             raise LinAttnError(err, f"la_forward_causal (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
+
+
+def forward_causal_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=None,
+                         return_state=False, out=None, S_out=None, z_out=None, stream=None):
+    """Causal attention with a per-head decay ``gamma`` (float32 CUDA tensor [H]).
+
+    q, k: [B,H,N,d]; v: [B,H,N,dv].  Returns y [B,H,N,dv] float32 (and the
+    final (S, z) when ``return_state``).
+    """
+    _check_cuda(q, k, v, gamma, S_in, z_in, out, S_out, z_out)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    if gamma.shape != (H,) or gamma.dtype != torch.float32:
+        raise ValueError("gamma must be a float32 tensor of shape [H]")
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    st = lib().la_forward_causal_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                       float(eps), _ptr(gamma), _ptr(S_in), _ptr(z_in),
+                                       _ptr(S_out), _ptr(z_out), _stream_handle(stream, q.device))
+    _raise(st, "la_forward_causal_decay")
+    return (y, S_out, z_out) if return_state else y
+
+
+def decode_step_decay(q, k, v, S, z, gamma, eps: float = 1e-6, out=None, stream=None):
+    """One decode step with decay; S and z are updated in place.  Returns y."""
+    _check_cuda(q, k, v, S, z, gamma, out)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if gamma.shape != (H,) or gamma.dtype != torch.float32:
+        raise ValueError("gamma must be a float32 tensor of shape [H]")
+    y = out if out is not None else torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    st = lib().la_decode_step_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), B, H,
+                                    d, dv, _dtype_code(q), float(eps), _ptr(gamma),
+                                    _stream_handle(stream, q.device))
+    _raise(st, "la_decode_step_decay")
+    return y
 
 
 def causal_backward_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int:

@@ -12,7 +12,10 @@ draws its prefill (unscaled) from a generator seeded ``seed`` and its per-step
 q, k, v (scaled by 1/sqrt(d)) from a second generator seeded ``seed + 1``,
 step after step, q then k then v.  The backward workload draws q, k, v as the
 causal one does and then, from the same generator, the upstream gradient dy
-as iid N(0, 1) float32 of shape ``[B, H, N, dv]`` (unscaled).
+as iid N(0, 1) float32 of shape ``[B, H, N, dv]`` (unscaled).  The decay
+workloads draw as their plain counterparts and use one fixed decay per head,
+gamma_h = 1 - 2^(-5 - 8 h / H): from 1 - 1/32 (a memory of about 32 tokens)
+to about 1 - 2^-13, a spread of time scales across the heads.
 """
 from __future__ import annotations
 
@@ -25,7 +28,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    mode: str            # "causal" | "noncausal" | "decode" | "backward"
+    mode: str            # "causal" | "noncausal" | "decode" | "backward" | "causal_decay" | "decode_decay"
     B: int
     H: int
     N: int               # sequence length (decode: prefill length)
@@ -63,6 +66,14 @@ WORKLOADS = {
     "causal_backward_bf16_b8h16n8192d128": Workload("causal_backward_bf16_b8h16n8192d128",
                                                     "backward", 8, 16, 8192, 128, 128,
                                                     torch.bfloat16, 1.0 / math.sqrt(128)),
+    # causal with a per-head decay, training / prefill shape.
+    "causal_decay_bf16_b8h16n8192d128": Workload("causal_decay_bf16_b8h16n8192d128",
+                                                 "causal_decay", 8, 16, 8192, 128, 128,
+                                                 torch.bfloat16, 1.0 / math.sqrt(128)),
+    # recurrent decode with a per-head decay from a 1024-token prefill.
+    "decode_decay_bf16_b256h32d128": Workload("decode_decay_bf16_b256h32d128", "decode_decay",
+                                              256, 32, 1024, 128, 128, torch.bfloat16, 1.0,
+                                              steps=4096, step_scale=1.0 / math.sqrt(128)),
     # recurrent decode from a 1024-token prefill.
     "decode_bf16_b256h32d128": Workload("decode_bf16_b256h32d128", "decode", 256, 32, 1024, 128,
                                         128, torch.bfloat16, 1.0, steps=4096,
@@ -101,6 +112,12 @@ def make_backward_inputs(w: Workload, device="cpu", gen_device="cpu"):
     v = _draw(g, (w.B, w.H, w.N, w.dv), w.scale, w.dtype, device)
     dy = _draw(g, (w.B, w.H, w.N, w.dv), 1.0, torch.float32, device)
     return q, k, v, dy
+
+
+def head_decays(H: int) -> torch.Tensor:
+    """The decay workloads' per-head gamma_h = 1 - 2^(-5 - 8 h / H) (float32, CPU)."""
+    h = torch.arange(H, dtype=torch.float64)
+    return (1.0 - torch.pow(2.0, -5.0 - 8.0 * h / H)).to(torch.float32)
 
 
 def decode_step_generator(w: Workload, gen_device="cpu") -> torch.Generator:

@@ -181,3 +181,23 @@ def test_backward_rejects_bad_arguments():
     assert call(gq=ctypes.c_void_p(gq.value + 4)) == la.LA_ERR_INVALID_ARG     # misaligned
     assert call(wsb=need - 1) == la.LA_ERR_WORKSPACE
     assert call(ws=ctypes.c_void_p(ws.value + 16)) == la.LA_ERR_WORKSPACE      # not 256-aligned
+
+
+def test_decay_entry_points_reject_bad_arguments():
+    L = la.lib()
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(8)]
+    q, k, v, y, S, z, g, _ = p
+    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 1e-6, None, None, None,
+                                     None, None, None) == la.LA_ERR_INVALID_ARG   # no gamma
+    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 48, 64, 1, 1e-6, g, None, None,
+                                     None, None, None) == la.LA_ERR_UNSUPPORTED
+    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 0.0, g, None, None,
+                                     None, None, None) == la.LA_ERR_INVALID_ARG
+    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 1e-6, g, S, None,
+                                     None, None, None) == la.LA_ERR_INVALID_ARG   # S_in alone
+    assert L.la_decode_step_decay(q, k, v, y, S, z, 1, 2, 64, 64, 1, 1e-6, None,
+                                  None) == la.LA_ERR_INVALID_ARG
+    assert L.la_decode_step_decay(q, k, v, y, None, z, 1, 2, 64, 64, 1, 1e-6, g,
+                                  None) == la.LA_ERR_INVALID_ARG
+    assert L.la_decode_step_decay(q, k, v, y, S, ctypes.c_void_p(S.value + 64), 1, 2, 64, 64, 1,
+                                  1e-6, g, None) == la.LA_ERR_INVALID_ARG        # S overlaps z

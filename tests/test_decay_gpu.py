@@ -1,0 +1,144 @@
+"""GPU parity of the decay entry points against the fp64 oracle.
+
+la_forward_causal_decay and la_decode_step_decay (RetNet's update,
+"Linear Attention/es", "Variantes y extensiones") on seeded inputs: every
+(d, dv) pair, both input dtypes, ragged tails, per-head gamma, initial and
+final state; the limits gamma = 1 (the plain form) and gamma = 0 (y = v);
+decode steps continuing a decayed prefill; sampled heads of the full-size
+workloads.  Both kernels compute in fp32, so the float32 bound applies to
+both input dtypes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_rnn_sequence_gb300 import linattn as la
+from linear_rnn_sequence_gb300.workloads import (WORKLOADS, head_decays, make_qkv,
+                                                 next_decode_inputs, decode_step_generator,
+                                                 random_qkv)
+from metrics import TOL_F32, rel_max_err
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # B, H, N, d, dv, dtype, scale
+    (1, 2, 256, 32, 32, torch.float32, 1.0),
+    (1, 3, 333, 64, 64, torch.float32, 1.0),
+    (2, 2, 517, 128, 128, torch.float32, 0.2),
+    (1, 2, 1000, 64, 128, torch.float32, 0.5),
+    (2, 3, 1031, 64, 64, torch.bfloat16, 0.125),
+    (1, 4, 777, 128, 128, torch.bfloat16, 0.0884),
+    (1, 2, 129, 128, 32, torch.bfloat16, 1.0),
+    (1, 2, 385, 32, 128, torch.bfloat16, 1.0),
+]
+
+
+def _ids(c):
+    B, H, N, d, dv, dt, s = c
+    return f"B{B}H{H}N{N}d{d}dv{dv}{'bf16' if dt == torch.bfloat16 else 'f32'}"
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_causal_decay_matches_oracle(case, with_state, cuda_device):
+    B, H, N, d, dv, dt, s = case
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=dt, scale=s, seed=N + 9)
+    gam = head_decays(H)
+    S_in = z_in = None
+    if with_state:
+        qp, kp, vp = random_qkv(B, H, 40, d, dv, dtype=dt, scale=0.5, seed=N)
+        _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: None if t is None else torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    y, S, z = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                      gam.to(cuda_device), S_in=dev(S_in), z_in=dev(z_in),
+                                      return_state=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.causal_recurrent_decay(q, k, v, gam, S_in=S_in, z_in=z_in,
+                                               return_state=True)
+    for name, g, w in (("y", y, yo), ("S", S, So), ("z", z, zo)):
+        err = rel_max_err(g, w)
+        assert err <= TOL_F32, f"{name}: {err:.3e}"
+
+
+def test_decay_limits(cuda_device):
+    """gamma = 1 is the plain causal form; gamma = 0 returns v."""
+    q, k, v = random_qkv(2, 3, 300, 64, 64, dtype=torch.bfloat16, scale=0.125, seed=2)
+    qd, kd, vd = (t.to(cuda_device) for t in (q, k, v))
+    y1 = la.forward_causal_decay(qd, kd, vd, torch.ones(3, device=cuda_device))
+    y0 = la.forward_causal_decay(qd, kd, vd, torch.zeros(3, device=cuda_device))
+    torch.cuda.synchronize()
+    assert rel_max_err(y1, oracle.causal_recurrent(q, k, v)) <= TOL_F32
+    assert rel_max_err(y0, v.double().numpy()) <= 1e-6
+
+
+def test_decay_empty_sequence_copies_state(cuda_device):
+    S_in = torch.randn(1, 2, 64, 64, device=cuda_device)
+    z_in = torch.rand(1, 2, 64, device=cuda_device) + 1
+    q = torch.zeros(1, 2, 0, 64, dtype=torch.bfloat16, device=cuda_device)
+    y, S, z = la.forward_causal_decay(q, q, q, head_decays(2).to(cuda_device), S_in=S_in,
+                                      z_in=z_in, return_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S_in) and torch.equal(z, z_in)
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d,dv", [(32, 32), (64, 128), (128, 128), (128, 64)])
+def test_decode_decay_steps_match_oracle(dt, d, dv, cuda_device):
+    B, H, Np, steps = 2, 3, 100, 20
+    gam = head_decays(H)
+    q, k, v = random_qkv(B, H, Np, d, dv, dtype=dt, scale=0.5, seed=7)
+    _, So, zo = oracle.causal_recurrent_decay(q, k, v, gam, return_state=True)
+    S = torch.tensor(So, dtype=torch.float32, device=cuda_device)
+    z = torch.tensor(zo, dtype=torch.float32, device=cuda_device)
+    Sref, zref = So, zo
+    g = torch.Generator().manual_seed(11)
+    for _ in range(steps):
+        qs, ks, vs = ((torch.randn(B, H, n, generator=g) * 0.3).to(dt) for n in (d, d, dv))
+        y = la.decode_step_decay(qs.to(cuda_device), ks.to(cuda_device), vs.to(cuda_device), S, z,
+                                 gam.to(cuda_device))
+        yo, Sref, zref = oracle.causal_recurrent_decay(qs[:, :, None], ks[:, :, None],
+                                                       vs[:, :, None], gam, S_in=Sref, z_in=zref,
+                                                       return_state=True)
+        torch.cuda.synchronize()
+        assert rel_max_err(y, yo[:, :, 0]) <= TOL_F32
+    assert rel_max_err(S, Sref) <= TOL_F32
+    assert rel_max_err(z, zref) <= TOL_F32
+
+
+def test_causal_decay_workload_sampled_heads(cuda_device):
+    """Full-size prefill shape; whole heads checked against the oracle."""
+    w = WORKLOADS["causal_decay_bf16_b8h16n8192d128"]
+    q, k, v = make_qkv(w)
+    gam = head_decays(w.H)
+    y = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                gam.to(cuda_device))
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (3, 7), (7, 15)):
+        yo = oracle.causal_recurrent_decay(q[b, h][None], k[b, h][None], v[b, h][None],
+                                           gam[h:h + 1])
+        assert rel_max_err(y[b, h], yo[0]) <= TOL_F32
+
+
+def test_decode_decay_workload_steps(cuda_device):
+    """Decode shape B256 H32 d128: 1024-token decayed prefill, then 16 steps,
+    each step's output and the final state checked on sampled heads."""
+    w = WORKLOADS["decode_decay_bf16_b256h32d128"]
+    q, k, v = make_qkv(w, device=cuda_device, gen_device=cuda_device)
+    gam = head_decays(w.H).to(cuda_device)
+    _, S, z = la.forward_causal_decay(q, k, v, gam, return_state=True)
+    heads = [(0, 0), (100, 17), (255, 31)]
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads]).cpu()
+    g32 = head_decays(w.H)
+    gsel = torch.stack([g32[h] for _, h in heads])
+    _, Sref, zref = oracle.causal_recurrent_decay(sel(q), sel(k), sel(v), gsel, return_state=True)
+    gen = decode_step_generator(w, gen_device=cuda_device)
+    for _ in range(16):
+        qs, ks, vs = next_decode_inputs(w, gen)
+        y = la.decode_step_decay(qs, ks, vs, S, z, gam)
+        yo, Sref, zref = oracle.causal_recurrent_decay(sel(qs)[:, None], sel(ks)[:, None],
+                                                       sel(vs)[:, None], gsel, S_in=Sref,
+                                                       z_in=zref, return_state=True)
+        torch.cuda.synchronize()
+        assert rel_max_err(sel(y), yo[:, 0]) <= TOL_F32
+    assert rel_max_err(sel(S), Sref) <= TOL_F32

@@ -1,206 +1,170 @@
-// causal_simt.cu -- chunked causal linear attention on CUDA cores, fp32.
+// causal_simt.cu -- causal linear attention on CUDA cores, fp32, token by
+// token, with an optional per-head decay.
 //
-// Blockwise form of "Linear Attention/es", "Entrenamiento: forma paralela":
-// per block of C tokens, y_i = [sum_{j<=i in block} w_ij v_j + phi(q_i)^T S_prev]
-//                            / max(sum_{j<=i in block} w_ij + phi(q_i)^T z_prev, eps)
-// with w_ij = phi(q_i)^T phi(k_j), followed by S_prev += sum_j phi(k_j) v_j^T
-// and z_prev += sum_j phi(k_j).  Everything is fp32 (FFMA), so this is the
-// path for float32 inputs and for sizes the tensor-core kernel does not take.
+// The recurrence of "Linear Attention/es", "Forma recurrente e inferencia
+// autorregresiva":
+//   S_t = gamma S_{t-1} + phi(k_t) v_t^T,  z_t = gamma z_{t-1} + phi(k_t),
+//   y_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps)
+// with gamma = 1 for the plain form and one gamma per head for RetNet's
+// decay ("Variantes y extensiones"; z is decayed like S so that y stays a
+// normalised average).  Everything is fp32 FMA, so this is the path for
+// float32 inputs, for d or dv = 32, and for the decay.
 //
-// One CTA owns one head and one block of 32 value columns (columns of S and
-// y are independent; the denominator is recomputed by each column block).
-// The state S[:, cols] (d x 32) and z live in shared memory for the whole
-// sequence; only q, k, v are read and y written.
-//
-// With a per-head decay gamma (RetNet in "Variantes y extensiones":
-// S_t = gamma S_{t-1} + phi(k_t) v_t^T, z alike) token i of a block sees the
-// pairs j <= i weighted by gamma^(i-j) and the state of the previous blocks
-// by gamma^(i+1); after a block of L tokens the state becomes
-// gamma^L S_prev + sum_j gamma^(L-1-j) phi(k_j) v_j^T.
+// One CTA owns one head for the whole sequence.  Its state S lives in
+// registers: warp w owns a band of value columns and lane l a few feature
+// rows of each, so phi(q_t)^T S_t (a sum over rows) is a reduce-scatter
+// inside the warp and every lane finishes one column of y_t.  z_t and the
+// denominators of a 32-token chunk are formed before its token loop (one
+// thread per feature walks the chunk; one warp per token takes the dot
+// product), and the next chunk's q, k, v are in flight from HBM during the
+// current chunk's tokens.  Per token and state element: one multiply (decay
+// only) and two FMAs.
 #include "la_device.cuh"
 #include "la_internal.h"
+#include "simt_tiles.cuh"
 
 namespace la {
 namespace {
 
-constexpr int kC = 32;        // tokens per block
-constexpr int kCols = 32;     // value columns per CTA
-constexpr int kThreads = 256;
+using namespace tiles;
 
-template <int D>
-struct SimtSmem {
-    static constexpr int QS = D + 1;  // padded row stride for phi(Q), phi(K)
-    static constexpr size_t bytes =
-        sizeof(float) * (2 * kC * QS + kC * kCols + D * kCols + D + kC * (kC + 1) + 2 * kC + kC + 1);
+template <int D, int DV>
+struct FwdCfg {
+    static constexpr int kNT = D * DV >= 2048 ? 512 : 256;   // threads per CTA
+    static constexpr size_t kSmemFloats = 3 * (size_t)kBC * D + 2 * (size_t)kBC * DV + kBC;
 };
 
-template <int D, typename T, bool DECAY>
-__global__ void __launch_bounds__(kThreads)
-causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                   float *__restrict__ y, int N, int DV, float eps,
-                   const float *__restrict__ S_in, const float *__restrict__ z_in,
-                   float *__restrict__ S_out, float *__restrict__ z_out,
-                   const float *__restrict__ gamma, int H)
+template <int D, int DV, typename T, bool DECAY>
+__global__ void __launch_bounds__(FwdCfg<D, DV>::kNT, 1)
+causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                  float *__restrict__ y, int N, int H, float eps,
+                  const float *__restrict__ gamma, const float *__restrict__ S_in,
+                  const float *__restrict__ z_in, float *__restrict__ S_out,
+                  float *__restrict__ z_out)
 {
-    constexpr int QS = SimtSmem<D>::QS;
-    extern __shared__ float sm[];
-    float *Qs = sm;                       // [kC][QS]  phi(q)
-    float *Ks = Qs + kC * QS;             // [kC][QS]  phi(k)
-    float *Vs = Ks + kC * QS;             // [kC][kCols]
-    float *Ss = Vs + kC * kCols;          // [D][kCols]
-    float *zs = Ss + D * kCols;           // [D]
-    float *Ps = zs + D;                   // [kC][kC+1] masked w_ij
-    float *dinter = Ps + kC * (kC + 1);   // [kC] phi(q_i)^T z_prev
-    float *dens = dinter + kC;            // [kC] clamped denominators
-    float *pw = dens + kC;                // [kC+1] gamma^m
-
+    constexpr int NT = FwdCfg<D, DV>::kNT, NW = NT / 32;
+    using CT = WarpRows<NT, DV, D>;   // warp: CT::RPW value columns; lane: CT::CPL features
+    static_assert(NT >= D, "one thread per feature");
+    extern __shared__ float4 smem4[];
+    float *sFq = reinterpret_cast<float *>(smem4);  // [kBC][D] phi(q)
+    float *sFk = sFq + kBC * D;                     // [kBC][D] phi(k)
+    float *sZt = sFk + kBC * D;                     // [kBC][D] z_t
+    float *sV = sZt + kBC * D;                      // [kBC][DV]
+    float *sY = sV + kBC * DV;                      // [kBC][DV]
+    float *sDinv = sY + kBC * DV;                   // [kBC] 1 / max(den_t, eps)
     const int head = blockIdx.x;
-    const int col0 = blockIdx.y * kCols;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const T *qh = q + (long)head * N * D;
-    const T *kh = k + (long)head * N * D;
-    const T *vh = v + (long)head * N * DV;
-    float *yh = y + (long)head * N * DV;
+    const int b0 = warp * CT::RPW, a0 = lane * CT::CPL;
+    const int my_col = b0 + CT::row_of(lane);
+    const bool writer = CT::writer(lane);
+    const float g = DECAY ? gamma[head % H] : 1.f;
 
-    for (int i = tid; i < D * kCols; i += kThreads) {
-        const int a = i / kCols, c = i % kCols;
-        Ss[i] = S_in ? S_in[((long)head * D + a) * DV + col0 + c] : 0.f;
-    }
-    for (int a = tid; a < D; a += kThreads) zs[a] = z_in ? z_in[(long)head * D + a] : 0.f;
-    if (DECAY && tid == 0) {
-        const float g = gamma[head % H];
-        float p = 1.f;
-        for (int m = 0; m <= kC; ++m) {
-            pw[m] = p;
-            p *= g;
-        }
-    }
+    // S[a0 + j][b0 + i] in S2[i][j]; S_in is read in full before S_out is written
+    float S2[CT::RPW][CT::CPL];
+    const float *Sh_in = S_in ? S_in + (size_t)head * D * DV : nullptr;
+#pragma unroll
+    for (int i = 0; i < CT::RPW; ++i)
+#pragma unroll
+        for (int j = 0; j < CT::CPL; ++j) S2[i][j] = Sh_in ? Sh_in[(a0 + j) * DV + b0 + i] : 0.f;
+    float z = (tid < D && z_in) ? z_in[(size_t)head * D + tid] : 0.f;   // thread a < D: z[a]
 
-    for (int t0 = 0; t0 < N; t0 += kC) {
-        const int L = min(kC, N - t0);
-        __syncthreads();  // previous block's state update is complete
-        for (int e = tid; e < kC * D; e += kThreads) {
-            const int i = e / D, a = e % D;
-            float fq = 0.f, fk = 0.f;  // rows past the end contribute nothing
-            if (i < L) {
-                fq = phi_f(to_f(qh[(long)(t0 + i) * D + a]));
-                fk = phi_f(to_f(kh[(long)(t0 + i) * D + a]));
-            }
-            Qs[i * QS + a] = fq;
-            Ks[i * QS + a] = fk;
-        }
-        for (int e = tid; e < kC * kCols; e += kThreads) {
-            const int j = e / kCols, c = e % kCols;
-            Vs[e] = j < L ? to_f(vh[(long)(t0 + j) * DV + col0 + c]) : 0.f;
-        }
+    const T *qh = q + (size_t)head * N * D, *kh = k + (size_t)head * N * D;
+    const T *vh = v + (size_t)head * N * DV;
+    float *yh = y + (size_t)head * N * DV;
+    ChunkLoad<D, T, NT> lq, lk;
+    ChunkLoad<DV, T, NT> lv;
+    if (N > 0) {
+        const int L = min(kBC, N);
+        lq.load(qh, L); lk.load(kh, L); lv.load(vh, L);
+    }
+    for (int t0 = 0; t0 < N; t0 += kBC) {
+        const int L = min(kBC, N - t0);
+        __syncthreads();   // the previous chunk is consumed and its y written
+        lq.store(sFq, L, Phi());
+        lk.store(sFk, L, Phi());
+        lv.store(sV, L, Ident());
         __syncthreads();
-
-        // w_ij for j <= i (thread: column j = lane, rows 4*warp .. 4*warp+3)
-        {
-            const int j = lane, i0 = warp * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int a = 0; a < D; ++a) {
-                const float kv = Ks[j * QS + a];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] = fmaf(Qs[(i0 + r) * QS + a], kv, acc[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                Ps[(i0 + r) * (kC + 1) + j] =
-                    (j <= i0 + r) ? (DECAY ? acc[r] * pw[i0 + r - j] : acc[r]) : 0.f;
+        if (t0 + kBC < N) {   // the next chunk flies in during this one
+            const int n0 = t0 + kBC, nL = min(kBC, N - n0);
+            lq.load(qh + (size_t)n0 * D, nL); lk.load(kh + (size_t)n0 * D, nL);
+            lv.load(vh + (size_t)n0 * DV, nL);
         }
-        if (tid < kC) {
+        // z_t for every token of the chunk (z_t includes token t)
+        if (tid < D)
+            for (int t = 0; t < L; ++t) {
+                z = DECAY ? fmaf(g, z, sFk[t * D + tid]) : z + sFk[t * D + tid];
+                sZt[t * D + tid] = z;
+            }
+        __syncthreads();
+        // den_t = phi(q_t) . z_t, one warp per token
+        for (int t = warp; t < L; t += NW) {
             float s = 0.f;
-            for (int a = 0; a < D; ++a) s = fmaf(Qs[tid * QS + a], zs[a], s);
-            dinter[tid] = DECAY ? s * pw[tid + 1] : s;
+            for (int x = lane; x < D; x += 32) s = fmaf(sFq[t * D + x], sZt[t * D + x], s);
+            s = warp_sum(s);
+            if (lane == 0) sDinv[t] = 1.f / fmaxf(s, eps);
         }
         __syncthreads();
-        if (tid < kC) {
-            float s = dinter[tid];
-            for (int j = 0; j <= tid; ++j) s += Ps[tid * (kC + 1) + j];
-            dens[tid] = fmaxf(s, eps);
+        // S_t = gamma S_{t-1} + phi(k_t) v_t^T, then y_t = phi(q_t)^T S_t / D_t
+        for (int t = 0; t < L; ++t) {
+            float fk[CT::CPL], fq[CT::CPL], vv[CT::RPW], acc[CT::RPW];
+            ldn(sFk + t * D + a0, fk);
+            ldn(sFq + t * D + a0, fq);
+            ldn(sV + t * DV + b0, vv);   // warp-uniform
+#pragma unroll
+            for (int i = 0; i < CT::RPW; ++i) {
+                acc[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < CT::CPL; ++j) {
+                    S2[i][j] = fmaf(fk[j], vv[i], DECAY ? g * S2[i][j] : S2[i][j]);
+                    acc[i] = fmaf(S2[i][j], fq[j], acc[i]);
+                }
+            }
+            const float num = reduce_scatter<CT::RPW>(acc, lane);
+            if (writer) sY[t * DV + my_col] = num * sDinv[t];
         }
         __syncthreads();
-
-        // numerators and outputs (thread: column c = lane, rows 4*warp ..)
-        {
-            const int c = lane, i0 = warp * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int a = 0; a < D; ++a) {
-                const float s = Ss[a * kCols + c];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] = fmaf(Qs[(i0 + r) * QS + a], s, acc[r]);
-            }
-            if (DECAY)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] *= pw[i0 + r + 1];
-            for (int j = 0; j < kC; ++j) {
-                const float vj = Vs[j * kCols + c];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] = fmaf(Ps[(i0 + r) * (kC + 1) + j], vj, acc[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (i0 + r < L) yh[(long)(t0 + i0 + r) * DV + col0 + c] = acc[r] / dens[i0 + r];
-        }
-        __syncthreads();
-
-        // state update: S[a][c] += sum_j phi(k_j)[a] v_j[c];  z += sum_j phi(k_j)
-        if (DECAY) {   // gamma^L S_prev + sum_{j<L} gamma^(L-1-j) phi(k_j) v_j^T
-            for (int e = tid; e < D * kCols; e += kThreads) {
-                const int a = e / kCols, c = e % kCols;
-                float s = Ss[e] * pw[L];
-                for (int j = 0; j < L; ++j) s = fmaf(Ks[j * QS + a] * pw[L - 1 - j], Vs[j * kCols + c], s);
-                Ss[e] = s;
-            }
-            for (int a = tid; a < D; a += kThreads) {
-                float s = zs[a] * pw[L];
-                for (int j = 0; j < L; ++j) s = fmaf(Ks[j * QS + a], pw[L - 1 - j], s);
-                zs[a] = s;
-            }
-        } else {
-            for (int e = tid; e < D * kCols; e += kThreads) {
-                const int a = e / kCols, c = e % kCols;
-                float s = Ss[e];
-                for (int j = 0; j < kC; ++j) s = fmaf(Ks[j * QS + a], Vs[j * kCols + c], s);
-                Ss[e] = s;
-            }
-            for (int a = tid; a < D; a += kThreads) {
-                float s = zs[a];
-                for (int j = 0; j < kC; ++j) s += Ks[j * QS + a];
-                zs[a] = s;
-            }
-        }
+        for (int e = tid * 4; e < L * DV; e += NT * 4) st4(yh + (size_t)t0 * DV + e, ld4(sY + e));
     }
-    __syncthreads();
-    if (S_out)
-        for (int i = tid; i < D * kCols; i += kThreads) {
-            const int a = i / kCols, c = i % kCols;
-            S_out[((long)head * D + a) * DV + col0 + c] = Ss[i];
-        }
-    if (z_out && blockIdx.y == 0)
-        for (int a = tid; a < D; a += kThreads) z_out[(long)head * D + a] = zs[a];
+    if (S_out) {
+        float *So = S_out + (size_t)head * D * DV;
+#pragma unroll
+        for (int i = 0; i < CT::RPW; ++i)
+#pragma unroll
+            for (int j = 0; j < CT::CPL; ++j) So[(a0 + j) * DV + b0 + i] = S2[i][j];
+    }
+    if (z_out && tid < D) z_out[(size_t)head * D + tid] = z;
 }
 
-template <int D, typename T, bool DECAY>
-cudaError_t launch_t(const FwdArgs &a) {
-    const size_t smem = SimtSmem<D>::bytes;
-    auto kern = causal_simt_kernel<D, T, DECAY>;
+template <int D, int DV, typename T, bool DECAY>
+cudaError_t launch_typed(const FwdArgs &a) {
+    constexpr size_t smem = FwdCfg<D, DV>::kSmemFloats * sizeof(float);
+    auto kern = causal_rec_kernel<D, DV, T, DECAY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.BH(), a.dv / kCols);
-    kern<<<grid, kThreads, smem, a.stream>>>((const T *)a.q, (const T *)a.k, (const T *)a.v,
-                                             a.y, a.N, a.dv, a.eps, a.S_in, a.z_in, a.S_out,
-                                             a.z_out, a.gamma, a.H);
+    kern<<<a.BH(), FwdCfg<D, DV>::kNT, smem, a.stream>>>(
+        (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.N, a.H, a.eps, a.gamma, a.S_in,
+        a.z_in, a.S_out, a.z_out);
     return cudaGetLastError();
+}
+
+template <int D, int DV>
+cudaError_t launch_dims(const FwdArgs &a) {
+    if (a.gamma)
+        return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16, true>(a)
+                                     : launch_typed<D, DV, float, true>(a);
+    return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16, false>(a)
+                                 : launch_typed<D, DV, float, false>(a);
 }
 
 template <int D>
 cudaError_t launch_d(const FwdArgs &a) {
-    if (a.gamma)
-        return a.dt == LA_DTYPE_BF16 ? launch_t<D, __nv_bfloat16, true>(a) : launch_t<D, float, true>(a);
-    return a.dt == LA_DTYPE_BF16 ? launch_t<D, __nv_bfloat16, false>(a) : launch_t<D, float, false>(a);
+    switch (a.dv) {
+    case 32: return launch_dims<D, 32>(a);
+    case 64: return launch_dims<D, 64>(a);
+    case 128: return launch_dims<D, 128>(a);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

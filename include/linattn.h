@@ -130,9 +130,9 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
  *   y_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps),
  * one gamma per head for the multi-scale retention the section mentions; z
  * is decayed like S so that y stays a normalised average).  gamma is a DEVICE
- * array of H floats in [0, 1], shared by the B batch rows; its values are
- * not checked (a value outside [0, 1] gives a meaningless result, not an
- * error).  Arguments, layouts and the initial / final state as in
+ * array of H floats in [0, 1], 4-byte aligned, shared by the B batch rows;
+ * its values are not checked (a value outside [0, 1] gives a meaningless
+ * result, not an error).  Arguments, layouts and the initial / final state as in
  * la_forward_causal; no workspace is needed.  Computed blockwise in fp32 on
  * the CUDA cores (the blocks' pairs weighted by gamma^(i-j), the carried
  * state by gamma^(i+1)), for both input dtypes.  NULL gamma:

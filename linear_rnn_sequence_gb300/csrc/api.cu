@@ -186,7 +186,7 @@ la_status la_forward_causal_decay(const void *q, const void *k, const void *v, f
                                   float *S_out, float *z_out, void *stream) {
     la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
     if (st != LA_OK) return st;
-    if (!gamma) return LA_ERR_INVALID_ARG;
+    if (!gamma || (reinterpret_cast<uintptr_t>(gamma) & 3u) != 0) return LA_ERR_INVALID_ARG;
     if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
     if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
     const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
@@ -220,7 +220,7 @@ la_status la_decode_step_decay(const void *q, const void *k, const void *v, floa
                                const float *gamma, void *stream) {
     la_status st = check_common(q, k, v, y, B, H, 1, d, dv, dt, eps);
     if (st != LA_OK) return st;
-    if (!gamma) return LA_ERR_INVALID_ARG;
+    if (!gamma || (reinterpret_cast<uintptr_t>(gamma) & 3u) != 0) return LA_ERR_INVALID_ARG;
     if ((st = check_state(S, z, true)) != LA_OK) return st;
     const size_t yb = (size_t)B * H * dv * 4, sb = (size_t)B * H * d * dv * 4,
                  zb = (size_t)B * H * d * 4;

@@ -637,10 +637,6 @@ size_t causal_backward_workspace(int BH, int N, int d, int dv) {
     return make_plan(BH, N, d, dv).total;
 }
 
-int causal_backward_launches(int BH, int N, int d, int dv, bool with_state) {
-    return 4 + (make_plan(BH, N, d, dv).P > 1 ? 1 : 0) + (with_state ? 1 : 0);
-}
-
 cudaError_t launch_causal_backward(const BwdArgs &a) {
     const BwdPlan pl = make_plan(a.B * a.H, a.N, a.d, a.dv);
     if (a.ws_bytes < pl.total) return cudaErrorInvalidValue;

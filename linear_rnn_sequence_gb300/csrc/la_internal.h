@@ -85,7 +85,6 @@ cudaError_t launch_noncausal_tc(const FwdArgs &a);
 
 // gradients of the causal form (CUDA cores, fp32)
 size_t causal_backward_workspace(int BH, int N, int d, int dv);
-int causal_backward_launches(int BH, int N, int d, int dv, bool with_state);
 cudaError_t launch_causal_backward(const BwdArgs &a);
 
 }  // namespace la

@@ -201,3 +201,5 @@ def test_decay_entry_points_reject_bad_arguments():
                                   None) == la.LA_ERR_INVALID_ARG
     assert L.la_decode_step_decay(q, k, v, y, S, ctypes.c_void_p(S.value + 64), 1, 2, 64, 64, 1,
                                   1e-6, g, None) == la.LA_ERR_INVALID_ARG        # S overlaps z
+    assert L.la_decode_step_decay(q, k, v, y, S, z, 1, 2, 64, 64, 1, 1e-6,
+                                  ctypes.c_void_p(g.value + 2), None) == la.LA_ERR_INVALID_ARG

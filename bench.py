@@ -551,7 +551,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "steps_timed": nsteps, "l2": "state (512 MB) larger than L2",
                      "roofline": roofline(w.BH * decode_bytes_per_head_step(w),
                                           w.BH * decay_flops_per_token_head(w.d, w.dv),
-                                          sum(per) / len(per), peaks, peak_kind, None)}
+                                          sum(per) / len(per), peaks, peak_kind,
+                                          load_traffic(w.name))}
     del qs, ks, vs, S, z
     torch.cuda.empty_cache()
     return modes

@@ -81,6 +81,9 @@ def _bind(lib):
     lib.oracle_causal_recurrent_decay.restype = i
     lib.oracle_causal_backward.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, P, P, P, P, i]
     lib.oracle_causal_backward.restype = i
+    lib.oracle_causal_backward_decay.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, P, P, P,
+                                                 P, P, i]
+    lib.oracle_causal_backward_decay.restype = i
     return lib
 
 
@@ -205,13 +208,25 @@ def decode_step(q, k, v, S, z, eps: float = 1e-6, nthreads: int | None = None):
     return y, S, z
 
 
+def _head_gammas(gamma, lead, BH):
+    g = _f64(gamma).reshape(-1)
+    if g.size != BH:
+        if len(lead) >= 1 and g.size == lead[-1]:
+            g = np.broadcast_to(g, lead).reshape(-1)
+        else:
+            raise ValueError(f"gamma has {g.size} values for {BH} heads")
+    return np.ascontiguousarray(g, dtype=np.float64)
+
+
 def causal_backward(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
-                    return_state_grad: bool = False, nthreads: int | None = None):
-    """Gradients of L = sum_t dy_t . y_t, y the causal output of (q, k, v).
+                    return_state_grad: bool = False, nthreads: int | None = None, gamma=None):
+    """Gradients of L = sum_t dy_t . y_t, y the causal output of (q, k, v)
+    (with the per-head decay ``gamma`` when given, as ``causal_recurrent_decay``).
 
     Returns (dq, dk, dv), plus (dS_in, dz_in) when ``return_state_grad``.
     """
     q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    g = None if gamma is None else _head_gammas(gamma, lead, BH)
     dy = _f64(dy)
     if dy.shape != v.shape:
         raise ValueError(f"dy{dy.shape} must match v{v.shape}")
@@ -220,10 +235,10 @@ def causal_backward(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
     z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
     gS = np.empty(lead + (d, dv)) if return_state_grad else None
     gz = np.empty(lead + (d,)) if return_state_grad else None
-    rc = _load().oracle_causal_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq), _ptr(gk),
-                                        _ptr(gv), BH, N, d, dv, float(eps), _ptr(S_in),
-                                        _ptr(z_in), _ptr(gS), _ptr(gz),
-                                        nthreads or default_threads())
+    rc = _load().oracle_causal_backward_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq),
+                                              _ptr(gk), _ptr(gv), BH, N, d, dv, float(eps),
+                                              _ptr(g), _ptr(S_in), _ptr(z_in), _ptr(gS), _ptr(gz),
+                                              nthreads or default_threads())
     if rc:
         raise RuntimeError("oracle_causal_backward failed")
     return (gq, gk, gv, gS, gz) if return_state_grad else (gq, gk, gv)
@@ -235,13 +250,7 @@ def causal_recurrent_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=No
     for q of shape [B, H, N, d] (broadcast over B), or one value per head of
     the flattened leading shape."""
     q, k, v, lead, BH, N, d, dv = _split(q, k, v)
-    g = _f64(gamma).reshape(-1)
-    if g.size != BH:
-        if len(lead) >= 1 and g.size == lead[-1]:
-            g = np.broadcast_to(g, lead).reshape(-1)
-        else:
-            raise ValueError(f"gamma has {g.size} values for {BH} heads")
-    g = np.ascontiguousarray(g, dtype=np.float64)
+    g = _head_gammas(gamma, lead, BH)
     y = np.empty(lead + (N, dv))
     S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
     z_in = None if z_in is None else _f64(z_in).reshape(BH, d)

@@ -375,6 +375,7 @@ typedef struct {
     double *dS_in, *dz_in;
     int BH, N, d, dv;
     double eps;
+    const double *gamma;   /* nullable: per-head decay */
     int h_begin, h_end;
 } bjob_t;
 
@@ -393,9 +394,15 @@ static void head_backward(const bjob_t *J, int h)
     double *e = malloc(sizeof(double) * ((size_t)N + 1));       /* e_t for every t */
     if (J->S_in) memcpy(S, J->S_in + (long)h * d * dv, sizeof(double) * d * dv);
     if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
+    const double gam = J->gamma ? J->gamma[h] : 1.0;
     /* forward in t: the state after token t, then dL/dphi(q_t) */
     for (int t = 0; t < N; ++t) {
         for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        if (J->gamma)
+            for (int a = 0; a < d; ++a) {
+                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= gam;
+                z[a] *= gam;
+            }
         for (int a = 0; a < d; ++a) {
             for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];
             z[a] += fk[a];
@@ -419,11 +426,18 @@ static void head_backward(const bjob_t *J, int h)
             dq[(long)t * d + a] = s * dphi(q[(long)t * d + a]);
         }
     }
-    /* backward in t: Sh, zh include token t itself (y_s reads S_s for s >= t) */
+    /* backward in t: Sh, zh include token t itself (y_s reads S_s for s >= t);
+     * with a decay, S_s holds phi(k_t) v_t^T times gamma^(s-t), so
+     * Sh_t = phi(q_t) g_t^T + gamma Sh_{t+1}                                  */
     memset(S, 0, sizeof(double) * d * dv);
     memset(z, 0, sizeof(double) * d);
     for (int t = N - 1; t >= 0; --t) {
         for (int a = 0; a < d; ++a) fq[a] = phi(q[(long)t * d + a]);
+        if (J->gamma)
+            for (int a = 0; a < d; ++a) {
+                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= gam;
+                z[a] *= gam;
+            }
         for (int a = 0; a < d; ++a) {
             for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a] * g[(long)t * dv + b];
             z[a] += fq[a] * e[t];
@@ -440,8 +454,11 @@ static void head_backward(const bjob_t *J, int h)
             dvv[(long)t * dv + b] = s;
         }
     }
-    if (J->dS_in) memcpy(J->dS_in + (long)h * d * dv, S, sizeof(double) * d * dv);
-    if (J->dz_in) memcpy(J->dz_in + (long)h * d, z, sizeof(double) * d);
+    /* S_t holds S_in times gamma^(t+1): dL/dS_in = gamma Sh_1 */
+    if (J->dS_in)
+        for (long i = 0; i < (long)d * dv; ++i) J->dS_in[(long)h * d * dv + i] = gam * S[i];
+    if (J->dz_in)
+        for (int a = 0; a < d; ++a) J->dz_in[(long)h * d + a] = gam * z[a];
     free(S); free(z); free(fk); free(fq); free(y); free(g); free(e);
 }
 
@@ -455,17 +472,36 @@ static void *bworker(void *arg)
 /* Gradients of sum_t dy_t . y_t for the causal recurrent form.  q, k, dq, dk:
  * [BH][N][d]; v, dy, dvv: [BH][N][dv].  S_in/z_in may be NULL (zero state);
  * dS_in [BH][d][dv] and dz_in [BH][d] may be NULL.  Returns 0 on success.   */
+int oracle_causal_backward_decay(const double *q, const double *k, const double *v,
+                                 const double *dy, double *dq, double *dk, double *dvv,
+                                 int BH, int N, int d, int dv, double eps, const double *gamma,
+                                 const double *S_in, const double *z_in,
+                                 double *dS_in, double *dz_in, int nthreads);
+
 int oracle_causal_backward(const double *q, const double *k, const double *v,
                            const double *dy, double *dq, double *dk, double *dvv,
                            int BH, int N, int d, int dv, double eps,
                            const double *S_in, const double *z_in,
                            double *dS_in, double *dz_in, int nthreads)
 {
+    return oracle_causal_backward_decay(q, k, v, dy, dq, dk, dvv, BH, N, d, dv, eps, NULL,
+                                        S_in, z_in, dS_in, dz_in, nthreads);
+}
+
+/* The same with a per-head decay gamma[BH] (NULL: none), the gradients of
+ * the recurrence S_t = gamma S_{t-1} + phi(k_t) v_t^T, z_t likewise.        */
+int oracle_causal_backward_decay(const double *q, const double *k, const double *v,
+                                 const double *dy, double *dq, double *dk, double *dvv,
+                                 int BH, int N, int d, int dv, double eps, const double *gamma,
+                                 const double *S_in, const double *z_in,
+                                 double *dS_in, double *dz_in, int nthreads)
+{
     if (BH < 0 || N < 0 || d <= 0 || dv <= 0) return 1;
     bjob_t base = {0};
     base.q = q; base.k = k; base.v = v; base.dy = dy; base.dq = dq; base.dk = dk;
     base.dvv = dvv; base.S_in = S_in; base.z_in = z_in; base.dS_in = dS_in;
     base.dz_in = dz_in; base.BH = BH; base.N = N; base.d = d; base.dv = dv; base.eps = eps;
+    base.gamma = gamma;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > BH) nthreads = BH > 0 ? BH : 1;
     bjob_t *jobs = malloc(sizeof(bjob_t) * nthreads);

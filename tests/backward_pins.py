@@ -15,12 +15,16 @@ import numpy as np
 import oracle
 
 
-def loss(q, k, v, dy, eps, S_in=None, z_in=None) -> float:
-    y = oracle.causal_recurrent(q, k, v, eps=eps, S_in=S_in, z_in=z_in, nthreads=1)
+def loss(q, k, v, dy, eps, S_in=None, z_in=None, gamma=None) -> float:
+    if gamma is None:
+        y = oracle.causal_recurrent(q, k, v, eps=eps, S_in=S_in, z_in=z_in, nthreads=1)
+    else:
+        y = oracle.causal_recurrent_decay(q, k, v, gamma, eps=eps, S_in=S_in, z_in=z_in,
+                                          nthreads=1)
     return float((y * dy).sum())
 
 
-def finite_difference_grads(q, k, v, dy, eps, S_in=None, z_in=None, h=1e-6):
+def finite_difference_grads(q, k, v, dy, eps, S_in=None, z_in=None, h=1e-6, gamma=None):
     """Central differences of the loss for every element of q, k, v (and S_in, z_in)."""
     args = [np.array(a, dtype=np.float64) for a in (q, k, v)]
     state = [None if a is None else np.array(a, dtype=np.float64) for a in (S_in, z_in)]
@@ -35,9 +39,9 @@ def finite_difference_grads(q, k, v, dy, eps, S_in=None, z_in=None, h=1e-6):
         for i in range(flat.size):
             old = flat[i]
             flat[i] = old + h
-            lp = loss(*args, dy, eps, *state)
+            lp = loss(*args, dy, eps, *state, gamma=gamma)
             flat[i] = old - h
-            lm = loss(*args, dy, eps, *state)
+            lm = loss(*args, dy, eps, *state, gamma=gamma)
             flat[i] = old
             gflat[i] = (lp - lm) / (2 * h)
         grads.append(g)
@@ -93,6 +97,23 @@ def eps_between_dens(q, k, z_in=None, margin=1e-3) -> float:
         if gaps[i] > 2 * margin:
             return float((dd[i] + dd[i + 1]) / 2)
     raise ValueError("no gap between denominators")
+
+
+def fd_decay_pin_passes(seed=5, rtol=1e-6) -> bool:
+    """One small case with per-head decays and an initial state."""
+    r = np.random.default_rng(seed)
+    q, k = r.standard_normal((2, 2, 6, 3))
+    v, dy = r.standard_normal((2, 2, 6, 2))
+    S_in = r.standard_normal((2, 3, 2))
+    z_in = np.abs(r.standard_normal((2, 3))) + 0.5
+    gam = np.array([0.6, 0.95])
+    want = finite_difference_grads(q, k, v, dy, 1e-6, S_in, z_in, gamma=gam)
+    got = oracle.causal_backward(q, k, v, dy, eps=1e-6, S_in=S_in, z_in=z_in,
+                                 return_state_grad=True, nthreads=1, gamma=gam)
+    for g, w in zip(got, want):
+        if not np.abs(g - w).max() <= rtol * max(np.abs(w).max(), 1e-12):
+            return False
+    return True
 
 
 def fd_pin_passes(seed=3, rtol=1e-6) -> bool:

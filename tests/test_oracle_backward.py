@@ -118,3 +118,38 @@ def test_backward_threads_do_not_change_results():
     b = oracle.causal_backward(q, k, v, dy, nthreads=4)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_backward_with_decay_matches_finite_differences(seed):
+    """With per-head decays (RetNet's update) and an initial state."""
+    assert bp.fd_decay_pin_passes(seed=seed)
+
+
+def test_backward_with_decay_one_is_the_plain_backward():
+    r = np.random.default_rng(8)
+    q, k = r.standard_normal((2, 2, 3, 15, 4))
+    v, dy = r.standard_normal((2, 2, 3, 15, 5))
+    a = oracle.causal_backward(q, k, v, dy)
+    b = oracle.causal_backward(q, k, v, dy, gamma=np.ones(3))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_backward_with_decay_matches_autograd():
+    """The pairwise form with gamma^(t-j) weights, differentiated by torch."""
+    import torch
+    r = np.random.default_rng(9)
+    N, d, dv, gam = 14, 4, 3, 0.8
+    q, k = 0.7 * r.standard_normal((2, N, d))
+    v, dy = r.standard_normal((2, N, dv))
+    t = [torch.tensor(x, requires_grad=True) for x in (q, k, v)]
+    phi = lambda x: torch.where(x > 0, x + 1.0, torch.exp(torch.clamp(x, max=0.0)))
+    i = torch.arange(N, dtype=torch.float64)
+    mask = torch.tril(torch.pow(gam, (i[:, None] - i[None, :]).clamp(min=0)))
+    w = (phi(t[0]) @ phi(t[1]).T) * mask
+    y = (w @ t[2]) / w.sum(-1).clamp_min(1e-6)[:, None]
+    (y * torch.tensor(dy)).sum().backward()
+    got = oracle.causal_backward(q, k, v, dy, gamma=[gam])
+    for g, x in zip(got, t):
+        np.testing.assert_allclose(g, x.grad.numpy(), rtol=1e-10, atol=1e-12)

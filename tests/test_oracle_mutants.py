@@ -45,6 +45,10 @@ MUTANTS = {
     "decay_skips_z": ("                z[a] *= g;\n", ""),
     "decay_squared_on_S": ("for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;",
                            "for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g * g;"),
+    "bwd_decay_state_grad_unscaled": ("J->dS_in[(long)h * d * dv + i] = gam * S[i];",
+                                      "J->dS_in[(long)h * d * dv + i] = S[i];"),
+    "bwd_decay_skips_reverse_z": ("                z[a] *= gam;\n            }\n        for (int a = 0; a < d; ++a) {\n            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a]",
+                                  "            }\n        for (int a = 0; a < d; ++a) {\n            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a]"),
 }
 
 
@@ -94,6 +98,8 @@ def _pins_pass() -> bool:
     # gradients: central differences of the forward, with an initial state
     # and a clamp that is active for some tokens only
     if not (backward_pins.fd_pin_passes(seed=3) and backward_pins.fd_pin_passes(seed=4)):
+        return False
+    if not backward_pins.fd_decay_pin_passes(seed=5):
         return False
     # decay: the pairwise form with gamma^(t-j) weights
     from tests.test_oracle_decay import brute_decay

@@ -195,6 +195,23 @@ LA_API la_status la_backward_causal(const void *q, const void *k, const void *v,
                                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Gradients of la_forward_causal_decay: as la_backward_causal for the
+ * decayed recurrence S_t = gamma_h S_{t-1} + phi(k_t) v_t^T (z alike), with
+ * gamma as in la_forward_causal_decay (DEVICE array of H floats in [0, 1],
+ * 4-byte aligned; NULL: LA_ERR_INVALID_ARG).  The reverse state then obeys
+ * Sh_t = phi(q_t) g_t^T + gamma_h Sh_{t+1}, and dL/dS_in = gamma_h Sh_1.
+ * The gradient with respect to gamma is not computed.  Workspace: the size
+ * la_causal_backward_workspace_bytes returns.
+ */
+LA_API la_status la_backward_causal_decay(const void *q, const void *k, const void *v,
+                                          const float *dy, float *grad_q, float *grad_k,
+                                          float *grad_v, int B, int H, int N, int d, int dv,
+                                          la_dtype dt, float eps, const float *gamma,
+                                          const float *S_in, const float *z_in,
+                                          float *grad_S_in, float *grad_z_in, void *workspace,
+                                          size_t workspace_bytes, void *stream);
+
+/*
  * Device staging memory, in bytes, that la_forward_causal_host needs for
  * these sizes (0 for N == 0 or unsupported sizes).  Like the workspace size,
  * it depends on the current device's SM count.

@@ -240,11 +240,17 @@ size_t la_causal_backward_workspace_bytes(int B, int H, int N, int d, int dv, la
     return causal_backward_workspace(B * H, N, d, dv);
 }
 
-la_status la_backward_causal(const void *q, const void *k, const void *v, const float *dy,
-                             float *grad_q, float *grad_k, float *grad_v, int B, int H, int N,
-                             int d, int dv, la_dtype dt, float eps, const float *S_in,
-                             const float *z_in, float *grad_S_in, float *grad_z_in,
-                             void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace la {
+namespace {
+
+// la_backward_causal and la_backward_causal_decay (gamma null: no decay).
+la_status backward_impl(const void *q, const void *k, const void *v, const float *dy,
+                        float *grad_q, float *grad_k, float *grad_v, int B, int H, int N, int d,
+                        int dv, la_dtype dt, float eps, const float *gamma, const float *S_in,
+                        const float *z_in, float *grad_S_in, float *grad_z_in, void *workspace,
+                        size_t workspace_bytes, void *stream) {
     la_status st = check_common(q, k, v, grad_v, B, H, N, d, dv, dt, eps);
     if (st != LA_OK) return st;
     if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
@@ -282,8 +288,41 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
     if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
     BwdArgs a{q, k, v, dy, grad_q, grad_k, grad_v, B, H, N, d, dv, dt, eps, S_in, z_in,
               grad_S_in, grad_z_in, workspace, workspace_bytes, s};
+    a.gamma = gamma;
     return from_cuda(launch_causal_backward(a));
 }
+
+}  // namespace
+}  // namespace la
+
+extern "C" {
+
+la_status la_backward_causal(const void *q, const void *k, const void *v, const float *dy,
+                             float *grad_q, float *grad_k, float *grad_v, int B, int H, int N,
+                             int d, int dv, la_dtype dt, float eps, const float *S_in,
+                             const float *z_in, float *grad_S_in, float *grad_z_in,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_impl(q, k, v, dy, grad_q, grad_k, grad_v, B, H, N, d, dv, dt, eps, nullptr,
+                         S_in, z_in, grad_S_in, grad_z_in, workspace, workspace_bytes, stream);
+}
+
+la_status la_backward_causal_decay(const void *q, const void *k, const void *v,
+                                   const float *dy, float *grad_q, float *grad_k,
+                                   float *grad_v, int B, int H, int N, int d, int dv,
+                                   la_dtype dt, float eps, const float *gamma,
+                                   const float *S_in, const float *z_in, float *grad_S_in,
+                                   float *grad_z_in, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (!gamma || (reinterpret_cast<uintptr_t>(gamma) & 3u) != 0) return LA_ERR_INVALID_ARG;
+    const size_t T = (size_t)B * H * (N > 0 ? N : 0);
+    if (overlap(gamma, (size_t)H * 4, grad_q, T * d * 4) ||
+        overlap(gamma, (size_t)H * 4, grad_k, T * d * 4) ||
+        overlap(gamma, (size_t)H * 4, grad_v, T * dv * 4))
+        return LA_ERR_INVALID_ARG;
+    return backward_impl(q, k, v, dy, grad_q, grad_k, grad_v, B, H, N, d, dv, dt, eps, gamma,
+                         S_in, z_in, grad_S_in, grad_z_in, workspace, workspace_bytes, stream);
+}
+
 
 la_status la_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
     if (!workspace || workspace_bytes < sizeof(WsHeader)) return LA_ERR_WORKSPACE;

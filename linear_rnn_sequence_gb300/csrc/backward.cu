@@ -49,6 +49,7 @@
 // is processed the next one is already in flight from global memory into
 // registers.
 #include <algorithm>
+#include <type_traits>
 
 #include "la_device.cuh"
 #include "la_internal.h"
@@ -58,6 +59,10 @@ namespace la {
 namespace {
 
 using namespace tiles;
+
+// Accumulator type of the decayed token count (see bwd_dq_kernel).
+template <bool DECAY>
+using NAcc = typename std::conditional<DECAY, double, float>::type;
 
 template <int D, int DV>
 struct Cfg {
@@ -109,10 +114,13 @@ __global__ void bwd_seed_kernel(const float *__restrict__ S_in, const float *__r
 }
 
 // ---- 1. per-segment sums (R, zeta, u, n) ------------------------------------
-template <int D, int DV, typename T>
+// DECAY: the sums are of the decayed recurrence, each token weighted by
+// gamma^(segment end - 1 - token).
+template <int D, int DV, typename T, bool DECAY>
 __global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
 bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, int P,
-                     int seg_chunks, float *__restrict__ states)
+                     int seg_chunks, float *__restrict__ states, const float *__restrict__ gamma,
+                     int H)
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT;
@@ -124,6 +132,7 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
     if (sg.p == P - 1) return;   // no later segment reads the last one's sums
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
+    const float gm = DECAY ? gamma[sg.h % H] : 1.f;
     float R[RT::RPW][RT::CPL];
 #pragma unroll
     for (int r = 0; r < RT::RPW; ++r)
@@ -147,9 +156,11 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
             lv.load(v + nrow * DV, nL);
         }
         if (tid < D)
-            for (int t = 0; t < L; ++t) zeta += sPk[t * D + tid];
+            for (int t = 0; t < L; ++t)
+                zeta = DECAY ? fmaf(gm, zeta, sPk[t * D + tid]) : zeta + sPk[t * D + tid];
         else if (tid < D + DV)
-            for (int t = 0; t < L; ++t) u += sV[t * DV + tid - D];
+            for (int t = 0; t < L; ++t)
+                u = DECAY ? fmaf(gm, u, sV[t * DV + tid - D]) : u + sV[t * DV + tid - D];
         for (int t = 0; t < L; ++t) {
             float pk[RT::RPW], x[RT::CPL];
             ldn(sPk + t * D + r0, pk);
@@ -157,7 +168,8 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
 #pragma unroll
             for (int r = 0; r < RT::RPW; ++r)
 #pragma unroll
-                for (int c = 0; c < RT::CPL; ++c) R[r][c] = fmaf(pk[r], x[c], R[r][c]);
+                for (int c = 0; c < RT::CPL; ++c)
+                    R[r][c] = fmaf(pk[r], x[c], DECAY ? gm * R[r][c] : R[r][c]);
         }
     }
     float *out = states + ((size_t)sg.h * P + sg.p) * C::kE;
@@ -167,18 +179,31 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
         for (int c = 0; c < RT::CPL; ++c) out[(r0 + r) * DV + c0 + c] = R[r][c];
     if (tid < D) out[C::kOffZ + tid] = zeta;
     else if (tid < D + DV) out[C::kOffU + tid - D] = u;
-    if (tid < 4) out[C::kOffN + tid] = tid == 0 ? (float)(sg.t1 - sg.t0) : 0.f;
+    if (tid < 4) {
+        // the (decayed) token count; with a decay in fp64: near its steady
+        // state 1/(1 - gamma) every fp32 rounding of gamma n + 1 leans the
+        // same way, a bias of up to 2^-24 / (1 - gamma)
+        NAcc<DECAY> n = 0;
+        if (tid == 0)
+            for (int t = sg.t0; t < sg.t1; ++t) n = DECAY ? fma((NAcc<DECAY>)gm, n, NAcc<DECAY>(1)) : n + 1;
+        out[C::kOffN + tid] = (float)n;
+    }
 }
 
 // ---- 2./4. exclusive scan over segments, one thread per state element -----
-// Forward (reverse == 0): entry p becomes seed + sum_{p' < p} entry p' (the
-// last segment's entry is never read).  Reverse: sum_{p' > p} entry p'.
+// Forward (reverse == 0): entry p becomes the state before segment p, from
+// the seed: run_{p+1} = decay run_p + entry p (the last segment's entry is
+// never read).  Reverse: entry p becomes the reverse state after segment p,
+// run_{p-1} = entry p + decay run_p.  decay = gamma^(segment length) with a
+// decay (every segment that contributes is full), else 1.
 __global__ void bwd_scan_kernel(float *__restrict__ states, int P, int E, int blocks_per_head,
-                                const float *__restrict__ seed, int reverse)
+                                const float *__restrict__ seed, int reverse,
+                                const float *__restrict__ gamma, int H, int seg_len)
 {
     const int h = blockIdx.x / blocks_per_head;
     const int e = (blockIdx.x % blocks_per_head) * blockDim.x + threadIdx.x;
     if (e >= E) return;
+    const float f = gamma ? powf(gamma[h % H], (float)seg_len) : 1.f;
     float *col = states + (size_t)h * P * E + e;
     float run = 0.f;
     if (!reverse) {
@@ -186,13 +211,13 @@ __global__ void bwd_scan_kernel(float *__restrict__ states, int P, int E, int bl
         for (int p = 0; p < P; ++p) {
             const float x = p < P - 1 ? col[(size_t)p * E] : 0.f;
             col[(size_t)p * E] = run;
-            run += x;
+            run = fmaf(f, run, x);
         }
     } else {
         for (int p = P - 1; p >= 0; --p) {
             const float x = col[(size_t)p * E];
             col[(size_t)p * E] = run;
-            run += x;
+            run = fmaf(f, run, x);
         }
     }
 }
@@ -200,19 +225,22 @@ __global__ void bwd_scan_kernel(float *__restrict__ states, int P, int E, int bl
 // ---- 3. dq, 1/D_t, e_t, and the segment's sums of phi(q) g^T, phi(q) e ----
 template <int D, int DV>
 struct DqSmem {
-    static constexpr size_t floats = 4 * (size_t)kBC * D + 3 * (size_t)kBC * DV + D + DV + 8 * kBC;
+    static constexpr size_t floats = 4 * (size_t)kBC * D + 3 * (size_t)kBC * DV + DV + 9 * kBC;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
 // SEG: the sequence is split (P > 1), so the segment's sums of phi(q) g^T
 // and phi(q) e are needed by the reverse scan; with one segment the reverse
-// pass starts from zero and they are skipped.
-template <int D, int DV, typename T, bool SEG>
+// pass starts from zero and they are skipped.  DECAY: the recurrence carries
+// a per-head decay; the segment sums are then weighted by gamma^(token -
+// segment start), as the reverse state they feed decays towards earlier tokens.
+template <int D, int DV, typename T, bool SEG, bool DECAY>
 __global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
 bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ dy, float *__restrict__ dq, int N, int P, int seg_chunks,
               float eps, const float *__restrict__ prefix, float *__restrict__ rev_local,
-              float *__restrict__ dinv_out, float *__restrict__ e_out)
+              float *__restrict__ dinv_out, float *__restrict__ e_out,
+              const float *__restrict__ gamma, int H)
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT, NW = NT / 32;
@@ -226,8 +254,7 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float *sV = sH + kBC * D;                       // [kBC][DV]
     float *sG = sV + kBC * DV;                      // [kBC][DV] dy_t, then g_t
     float *sUt = sG + kBC * DV;                     // [kBC][DV] u_t
-    float *sZrun = sUt + kBC * DV;                  // [D]  zeta before the chunk
-    float *sUrun = sZrun + D;                       // [DV] u before the chunk
+    float *sUrun = sUt + kBC * DV;                  // [DV] u before the chunk
     float *sDinv = sUrun + DV;                      // [kBC] 1 / D_t
     float *sAct = sDinv + kBC;                      // [kBC] 1 where den_t >= eps
     float *sSq = sAct + kBC;                        // [kBC] sum of phi(q_t)
@@ -236,6 +263,7 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float *sNt = sUg + kBC;                         // [kBC] n_t
     float *sE = sNt + kBC;                          // [kBC] e_t
     float *sC = sE + kBC;                           // [kBC] c_t
+    float *sPw = sC + kBC;                          // [kBC] gamma^(token - segment start)
     const Seg sg = segment(P, seg_chunks, N);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
@@ -250,10 +278,12 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 #pragma unroll
         for (int c = 0; c < RT::CPL; ++c) Sh[r][c] = 0.f;
     }
-    if (tid < D) sZrun[tid] = pre[C::kOffZ + tid];
-    else if (tid < D + DV) sUrun[tid - D] = pre[C::kOffU + tid - D];
-    float n_run = pre[C::kOffN];
+    float zeta_run = tid < D ? pre[C::kOffZ + tid] : 0.f;   // thread a < D: zeta[a]
+    if (tid >= D && tid < D + DV) sUrun[tid - D] = pre[C::kOffU + tid - D];
+    NAcc<DECAY> n_acc = pre[C::kOffN];   // advanced by thread NT - 1
+    NAcc<DECAY> pw_acc = 1;              // gamma^(token - segment start), thread NT - 1
     float zh = 0.f;
+    const float gm = DECAY ? gamma[sg.h % H] : 1.f;
 
     ChunkLoad<D, T, NT> lq, lk;
     ChunkLoad<DV, T, NT> lv;
@@ -279,26 +309,37 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             lq.load(q + nrow * D, nL); lk.load(k + nrow * D, nL);
             lv.load(v + nrow * DV, nL); ldy.load(dy + nrow * DV, nL);
         }
-        // zeta_t and u_t for every token of the chunk (both include token t)
+        // zeta_t, u_t and n_t for every token of the chunk (all include token t)
         if (tid < D) {
-            float run = sZrun[tid];
-            for (int t = 0; t < kBC; ++t) {
-                run += sPk[t * D + tid];
+            float run = zeta_run;
+            for (int t = 0; t < L; ++t) {
+                run = DECAY ? fmaf(gm, run, sPk[t * D + tid]) : run + sPk[t * D + tid];
                 sZt[t * D + tid] = run;
             }
-            sZrun[tid] = run;
+            zeta_run = run;
         } else if (tid < D + DV) {
             const int b = tid - D;
             float run = sUrun[b];
-            for (int t = 0; t < kBC; ++t) {
-                run += sV[t * DV + b];
+            for (int t = 0; t < L; ++t) {
+                run = DECAY ? fmaf(gm, run, sV[t * DV + b]) : run + sV[t * DV + b];
                 sUt[t * DV + b] = run;
             }
             sUrun[b] = run;
+        } else if (tid == NT - 1) {
+            // the (decayed) token count; with a decay in fp64: near its
+            // steady state 1/(1 - gamma) every fp32 rounding of gamma n + 1
+            // leans the same way, a bias of up to 2^-24 / (1 - gamma) that dq
+            // would inherit (zeta's increments are small, its bias is not)
+            for (int t = 0; t < L; ++t) {
+                n_acc = DECAY ? fma((NAcc<DECAY>)gm, n_acc, NAcc<DECAY>(1)) : n_acc + 1;
+                sNt[t] = (float)n_acc;
+                sPw[t] = (float)pw_acc;
+                pw_acc *= gm;
+            }
         }
         __syncthreads();
         // per token: den_t = n_t sum(phi(q_t)) + phi(q_t).zeta_t, u_t.dy_t; one warp per token
-        for (int t = warp; t < kBC; t += NW) {
+        for (int t = warp; t < L; t += NW) {
             float sq = 0.f, fz = 0.f, ug = 0.f;
             for (int x = lane; x < D; x += 32) {
                 const float f = sFq[t * D + x];
@@ -310,19 +351,17 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             fz = warp_sum(fz);
             ug = warp_sum(ug);
             if (lane == 0) {
-                const float nt = n_run + (float)min(t + 1, L);
-                const float den = fmaf(nt, sq, fz);
+                const float den = fmaf(sNt[t], sq, fz);
                 const float dinv = 1.f / fmaxf(den, eps);
                 sDinv[t] = dinv;
-                sAct[t] = t < L && den >= eps ? 1.f : 0.f;
+                sAct[t] = den >= eps ? 1.f : 0.f;
                 sSq[t] = sq;
                 sFz[t] = fz;
                 sUg[t] = ug * dinv;
-                sNt[t] = nt;
             }
         }
         __syncthreads();
-        for (int e = tid; e < kBC * DV; e += NT) sG[e] *= sDinv[e / DV];
+        for (int e = tid; e < L * DV; e += NT) sG[e] *= sDinv[e / DV];
         __syncthreads();
         // the recurrence: R_t = R_{t-1} + psi(k_t) v_t^T, hR_t = R_t g_t;
         // and the segment's sum of phi(q_t) g_t^T
@@ -332,12 +371,17 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             ldn(sFq + t * D + r0, fq);      // warp-uniform
             ldn(sV + t * DV + c0, x);
             ldn(sG + t * DV + c0, g);
+            if constexpr (SEG && DECAY) {
+                const float w = sPw[t];
+#pragma unroll
+                for (int r = 0; r < RT::RPW; ++r) fq[r] *= w;
+            }
 #pragma unroll
             for (int r = 0; r < RT::RPW; ++r) {
                 acc[r] = 0.f;
 #pragma unroll
                 for (int c = 0; c < RT::CPL; ++c) {
-                    R[r][c] = fmaf(pk[r], x[c], R[r][c]);
+                    R[r][c] = fmaf(pk[r], x[c], DECAY ? gm * R[r][c] : R[r][c]);
                     acc[r] = fmaf(R[r][c], g[c], acc[r]);
                     if constexpr (SEG) Sh[r][c] = fmaf(fq[r], g[c], Sh[r][c]);
                 }
@@ -347,12 +391,12 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         }
         __syncthreads();
         // e_t and c_t (see the header: the leading terms cancel algebraically)
-        for (int t = warp; t < kBC; t += NW) {
+        for (int t = warp; t < L; t += NW) {
             float fh = 0.f;
             for (int x = lane; x < D; x += 32) fh = fmaf(sFq[t * D + x], sH[t * D + x], fh);
             fh = warp_sum(fh);
             if (lane == 0) {
-                float e = 0.f, c = t < L ? sUg[t] : 0.f;
+                float e = 0.f, c = sUg[t];
                 if (sAct[t] != 0.f) {
                     e = -fmaf(sSq[t], sUg[t], fh) * sDinv[t];
                     c = fmaf(sUg[t], sFz[t], -sNt[t] * fh) * sDinv[t];
@@ -372,8 +416,8 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             e_out[row0 + tid] = sE[tid];
         }
         if (SEG && tid < D)
-            for (int t = 0; t < L; ++t) zh = fmaf(sFq[t * D + tid], sE[t], zh);
-        n_run += (float)L;
+            for (int t = 0; t < L; ++t)
+                zh = fmaf(DECAY ? sFq[t * D + tid] * sPw[t] : sFq[t * D + tid], sE[t], zh);
     }
     if constexpr (SEG) {
         float *out = rev_local + ((size_t)sg.h * P + sg.p) * C::kE;
@@ -395,13 +439,16 @@ struct DkdvSmem {
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
-template <int D, int DV, typename T>
+// DECAY: Sh_t = phi(q_t) g_t^T + gamma Sh_{t+1} (zh alike), and the state
+// gradient gains the factor gamma of the first token's update.
+template <int D, int DV, typename T, bool DECAY>
 __global__ void __launch_bounds__(Cfg<D, DV>::kNT, 1)
 bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                 const float *__restrict__ dy, float *__restrict__ dk, float *__restrict__ dvg,
                 int N, int P, int seg_chunks, const float *__restrict__ suffix,
                 const float *__restrict__ dinv, const float *__restrict__ e_in,
-                float *__restrict__ grad_S, float *__restrict__ grad_z)
+                float *__restrict__ grad_S, float *__restrict__ grad_z,
+                const float *__restrict__ gamma, int H)
 {
     using C = Cfg<D, DV>;
     constexpr int NT = C::kNT;
@@ -428,6 +475,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
 #pragma unroll
     for (int r = 0; r < RT::RPW; ++r) ldn(suf + (r0 + r) * DV + c0, S1[r]);
     float zh = tid < D ? suf[C::kOffZ + tid] : 0.f;   // thread a < D carries zh[a]
+    const float gm = DECAY ? gamma[sg.h % H] : 1.f;
 
     ChunkLoad<D, T, NT> lq, lk;
     ChunkLoad<DV, T, NT> lv;
@@ -461,7 +509,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
         // zh_t = zh_{t+1} + phi(q_t) e_t for every token of the chunk, last first
         if (tid < D)
             for (int t = L - 1; t >= 0; --t) {
-                zh = fmaf(sFq[t * D + tid], sE[t], zh);
+                zh = DECAY ? fmaf(gm, zh, sFq[t * D + tid] * sE[t]) : fmaf(sFq[t * D + tid], sE[t], zh);
                 sDK[t * D + tid] = zh;
             }
         __syncthreads();
@@ -482,7 +530,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 acc[r] = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < RT::CPL; ++cc) {
-                    S1[r][cc] = fmaf(fq[r], g[cc], S1[r][cc]);
+                    S1[r][cc] = fmaf(fq[r], g[cc], DECAY ? gm * S1[r][cc] : S1[r][cc]);
                     acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
                     pv[cc] = fmaf(S1[r][cc], fk[r], pv[cc]);
                 }
@@ -514,8 +562,8 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
 #pragma unroll
         for (int r = 0; r < RT::RPW; ++r)
 #pragma unroll
-            for (int cc = 0; cc < RT::CPL; ++cc) gS[(r0 + r) * DV + c0 + cc] = S1[r][cc];
-        if (tid < D) grad_z[(size_t)sg.h * D + tid] = zh;
+            for (int cc = 0; cc < RT::CPL; ++cc) gS[(r0 + r) * DV + c0 + cc] = gm * S1[r][cc];
+        if (tid < D) grad_z[(size_t)sg.h * D + tid] = gm * zh;
     }
 }
 
@@ -562,7 +610,7 @@ BwdPlan make_plan(int BH, int N, int d, int dv) {
     return pl;
 }
 
-template <int D, int DV, typename T>
+template <int D, int DV, typename T, bool DECAY>
 cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
     using C = Cfg<D, DV>;
     const int BH = a.B * a.H;
@@ -578,11 +626,11 @@ cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
     constexpr size_t kv_smem = sizeof(float) * kBC * (D + DV);
     constexpr size_t dq_smem = DqSmem<D, DV>::bytes, dkdv_smem = DkdvSmem<D, DV>::bytes;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, true>,
+    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, true, DECAY>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, false>,
+        (e = cudaFuncSetAttribute(bwd_dq_kernel<D, DV, T, false, DECAY>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, DV, T>,
+        (e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, DV, T, DECAY>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv_smem)) != cudaSuccess)
         return e;
     if (a.S_in) {
@@ -590,36 +638,41 @@ cudaError_t launch_typed(const BwdArgs &a, const BwdPlan &pl) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pl.P > 1) {
-        bwd_kv_states_kernel<D, DV, T><<<grid, C::kNT, kv_smem, a.stream>>>(k, v, a.N, pl.P,
-                                                                           pl.seg_chunks, fwd);
+        bwd_kv_states_kernel<D, DV, T, DECAY><<<grid, C::kNT, kv_smem, a.stream>>>(
+            k, v, a.N, pl.P, pl.seg_chunks, fwd, a.gamma, a.H);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(fwd, pl.P, pl.E, bph, a.S_in ? seed : nullptr, 0);
+    const int seg_len = pl.seg_chunks * kBC;
+    bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(fwd, pl.P, pl.E, bph, a.S_in ? seed : nullptr, 0,
+                                                    a.gamma, a.H, seg_len);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pl.P > 1) {
-        bwd_dq_kernel<D, DV, T, true><<<grid, C::kNT, dq_smem, a.stream>>>(
-            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev);
+        bwd_dq_kernel<D, DV, T, true, DECAY><<<grid, C::kNT, dq_smem, a.stream>>>(
+            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev, a.gamma, a.H);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(rev, pl.P, pl.E, bph, nullptr, 1);
+        bwd_scan_kernel<<<BH * bph, 256, 0, a.stream>>>(rev, pl.P, pl.E, bph, nullptr, 1, a.gamma,
+                                                        a.H, seg_len);
     } else {   // one segment: the reverse pass starts from the zero state
-        bwd_dq_kernel<D, DV, T, false><<<grid, C::kNT, dq_smem, a.stream>>>(
-            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev);
+        bwd_dq_kernel<D, DV, T, false, DECAY><<<grid, C::kNT, dq_smem, a.stream>>>(
+            q, k, v, a.dy, a.dq, a.N, pl.P, pl.seg_chunks, a.eps, fwd, rev, dinv, ev, a.gamma, a.H);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(rev, 0, (size_t)BH * pl.E * sizeof(float), a.stream)) != cudaSuccess)
             return e;
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_dkdv_kernel<D, DV, T><<<grid, C::kNT, dkdv_smem, a.stream>>>(q, k, v, a.dy, a.dk, a.dv_grad,
-                                                                    a.N, pl.P, pl.seg_chunks, rev,
-                                                                    dinv, ev, a.grad_S_in,
-                                                                    a.grad_z_in);
+    bwd_dkdv_kernel<D, DV, T, DECAY><<<grid, C::kNT, dkdv_smem, a.stream>>>(
+        q, k, v, a.dy, a.dk, a.dv_grad, a.N, pl.P, pl.seg_chunks, rev, dinv, ev, a.grad_S_in,
+        a.grad_z_in, a.gamma, a.H);
     return cudaGetLastError();
 }
 
 template <int D, int DV>
 cudaError_t launch_dims(const BwdArgs &a, const BwdPlan &pl) {
-    return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16>(a, pl)
-                                 : launch_typed<D, DV, float>(a, pl);
+    if (a.gamma)
+        return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16, true>(a, pl)
+                                     : launch_typed<D, DV, float, true>(a, pl);
+    return a.dt == LA_DTYPE_BF16 ? launch_typed<D, DV, __nv_bfloat16, false>(a, pl)
+                                 : launch_typed<D, DV, float, false>(a, pl);
 }
 
 template <int D>

@@ -19,6 +19,12 @@
 // product), and the next chunk's q, k, v are in flight from HBM during the
 // current chunk's tokens.  Per token and state element: one multiply (decay
 // only) and two FMAs.
+//
+// With a decay the normaliser is carried split, z = n 1 + zeta with n the
+// decayed token count (in fp64, one thread) and zeta = sum gamma^(t-j)
+// psi(k_j): z settles near 1/(1 - gamma), where fp32 roundings of
+// gamma z + phi(k) all lean the same way and would bias it by up to
+// 2^-24 / (1 - gamma); the increments of zeta are small, so its bias is not.
 #include "la_device.cuh"
 #include "la_internal.h"
 #include "simt_tiles.cuh"
@@ -66,7 +72,19 @@ causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     for (int i = 0; i < CT::RPW; ++i)
 #pragma unroll
         for (int j = 0; j < CT::CPL; ++j) S2[i][j] = Sh_in ? Sh_in[(a0 + j) * DV + b0 + i] : 0.f;
-    float z = (tid < D && z_in) ? z_in[(size_t)head * D + tid] : 0.f;   // thread a < D: z[a]
+    // thread a < D carries z[a] (with a decay: zeta[a]); thread NT - 1 the
+    // decayed count n, which starts at the mean of z_in
+    float z = (tid < D && z_in) ? z_in[(size_t)head * D + tid] : 0.f;
+    double n = 0.0;
+    if constexpr (DECAY) {
+        if (tid == NT - 1 && z_in) {
+            for (int a = 0; a < D; ++a) n += z_in[(size_t)head * D + a];
+            n /= D;
+            sDinv[0] = (float)n;
+        }
+        __syncthreads();
+        if (tid < D && z_in) z -= sDinv[0];
+    }
 
     const T *qh = q + (size_t)head * N * D, *kh = k + (size_t)head * N * D;
     const T *vh = v + (size_t)head * N * DV;
@@ -89,18 +107,27 @@ causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
             lq.load(qh + (size_t)n0 * D, nL); lk.load(kh + (size_t)n0 * D, nL);
             lv.load(vh + (size_t)n0 * DV, nL);
         }
-        // z_t for every token of the chunk (z_t includes token t)
+        // z_t (with a decay: zeta_t and n_t) for every token of the chunk
         if (tid < D)
             for (int t = 0; t < L; ++t) {
-                z = DECAY ? fmaf(g, z, sFk[t * D + tid]) : z + sFk[t * D + tid];
+                z = DECAY ? fmaf(g, z, sFk[t * D + tid] - 1.f) : z + sFk[t * D + tid];
                 sZt[t * D + tid] = z;
             }
+        if (DECAY && tid == NT - 1)
+            for (int t = 0; t < L; ++t) {
+                n = fma((double)g, n, 1.0);
+                sY[t] = (float)n;   // sY is free until the token loop
+            }
         __syncthreads();
-        // den_t = phi(q_t) . z_t, one warp per token
+        // den_t = phi(q_t) . z_t (with a decay: n_t sum(phi(q_t)) + phi(q_t) . zeta_t)
         for (int t = warp; t < L; t += NW) {
-            float s = 0.f;
-            for (int x = lane; x < D; x += 32) s = fmaf(sFq[t * D + x], sZt[t * D + x], s);
+            float s = 0.f, sq = 0.f;
+            for (int x = lane; x < D; x += 32) {
+                s = fmaf(sFq[t * D + x], sZt[t * D + x], s);
+                if (DECAY) sq += sFq[t * D + x];
+            }
             s = warp_sum(s);
+            if (DECAY) s = fmaf(sY[t], warp_sum(sq), s);
             if (lane == 0) sDinv[t] = 1.f / fmaxf(s, eps);
         }
         __syncthreads();
@@ -131,6 +158,12 @@ causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         for (int i = 0; i < CT::RPW; ++i)
 #pragma unroll
             for (int j = 0; j < CT::CPL; ++j) So[(a0 + j) * DV + b0 + i] = S2[i][j];
+    }
+    if constexpr (DECAY) {
+        __syncthreads();
+        if (tid == NT - 1) sDinv[0] = (float)n;
+        __syncthreads();
+        z += sDinv[0];
     }
     if (z_out && tid < D) z_out[(size_t)head * D + tid] = z;
 }

@@ -50,6 +50,7 @@ struct BwdArgs {
     void *ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    const float *gamma = nullptr;  // per-head decay [H] (device), null: none
 };
 
 // Workspace header written at the start of every workspace (256 bytes).

@@ -80,6 +80,9 @@ def lib():
             L.la_backward_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
                                              vp, vp, vp, vp, vp, sz, vp]
             L.la_backward_causal.restype = i
+            L.la_backward_causal_decay.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                                   f, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.la_backward_causal_decay.restype = i
             L.la_workspace_status.argtypes = [vp, sz, vp]
             L.la_workspace_status.restype = i
             L.la_debug_set_fault.argtypes = [i, ctypes.c_longlong]
@@ -226,14 +229,16 @@ def causal_backward_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16) -> int
 
 
 def backward_causal(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
-                    return_state_grad=False, out=None, workspace=None, stream=None):
+                    return_state_grad=False, out=None, workspace=None, stream=None, gamma=None):
     """Gradients of the causal forward for the upstream gradient ``dy``.
 
     q, k: [B,H,N,d]; v: [B,H,N,dv] (bf16 or fp32); dy: [B,H,N,dv] float32.
+    With ``gamma`` (float32 CUDA tensor [H]) the gradients are those of the
+    decayed forward (``forward_causal_decay``).
     Returns (dq, dk, dv) float32, plus (dS_in, dz_in) when ``return_state_grad``.
     ``out`` may be a preallocated (dq, dk, dv) triple.
     """
-    _check_cuda(q, k, v, dy, S_in, z_in, workspace)
+    _check_cuda(q, k, v, dy, S_in, z_in, workspace, gamma)
     B, H, N, d = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -255,11 +260,21 @@ def backward_causal(q, k, v, dy, eps: float = 1e-6, S_in=None, z_in=None,
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().la_backward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq), _ptr(gk),
-                                  _ptr(gv), B, H, N, d, dv, dt, float(eps), _ptr(S_in),
-                                  _ptr(z_in), _ptr(gS), _ptr(gz), _ptr(workspace), wbytes,
-                                  _stream_handle(stream, q.device))
-    _raise(st, "la_backward_causal")
+    if gamma is None:
+        st = lib().la_backward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq), _ptr(gk),
+                                      _ptr(gv), B, H, N, d, dv, dt, float(eps), _ptr(S_in),
+                                      _ptr(z_in), _ptr(gS), _ptr(gz), _ptr(workspace), wbytes,
+                                      _stream_handle(stream, q.device))
+        _raise(st, "la_backward_causal")
+    else:
+        if gamma.shape != (H,) or gamma.dtype != torch.float32:
+            raise ValueError("gamma must be a float32 tensor of shape [H]")
+        st = lib().la_backward_causal_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(gq),
+                                            _ptr(gk), _ptr(gv), B, H, N, d, dv, dt, float(eps),
+                                            _ptr(gamma), _ptr(S_in), _ptr(z_in), _ptr(gS),
+                                            _ptr(gz), _ptr(workspace), wbytes,
+                                            _stream_handle(stream, q.device))
+        _raise(st, "la_backward_causal_decay")
     return (gq, gk, gv, gS, gz) if return_state_grad else (gq, gk, gv)
 
 

@@ -203,3 +203,16 @@ def test_decay_entry_points_reject_bad_arguments():
                                   1e-6, g, None) == la.LA_ERR_INVALID_ARG        # S overlaps z
     assert L.la_decode_step_decay(q, k, v, y, S, z, 1, 2, 64, 64, 1, 1e-6,
                                   ctypes.c_void_p(g.value + 2), None) == la.LA_ERR_INVALID_ARG
+
+
+def test_backward_decay_rejects_bad_arguments():
+    L = la.lib()
+    need = L.la_causal_backward_workspace_bytes(1, 2, 8, 64, 64, 1)
+    p = [ctypes.c_void_p((i + 1) << 24) for i in range(10)]
+    q, k, v, dy, gq, gk, gv, g, ws, _ = p
+    call = lambda gamma: L.la_backward_causal_decay(q, k, v, dy, gq, gk, gv, 1, 2, 8, 64, 64, 1,
+                                                    1e-6, gamma, None, None, None, None, ws,
+                                                    need, None)
+    assert call(None) == la.LA_ERR_INVALID_ARG
+    assert call(ctypes.c_void_p(g.value + 1)) == la.LA_ERR_INVALID_ARG      # misaligned
+    assert call(ctypes.c_void_p(gq.value + 64)) == la.LA_ERR_INVALID_ARG    # gamma inside dq

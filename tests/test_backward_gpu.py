@@ -121,3 +121,49 @@ def test_backward_long_sequence_sampled_heads(cuda_device):
     for h in (0, 31):
         want = oracle.causal_backward(flat(q)[h], flat(k)[h], flat(v)[h], flat(dy)[h])
         _check([flat(dq)[h], flat(dk)[h], flat(dvv)[h]], want)
+
+
+DECAY_CASES = [
+    (1, 2, 256, 32, 32, torch.float32, 1.0),
+    (2, 2, 517, 128, 128, torch.float32, 0.2),
+    (1, 3, 1031, 64, 64, torch.bfloat16, 0.125),
+    (1, 2, 385, 32, 128, torch.bfloat16, 1.0),
+    (1, 1, 4000, 128, 128, torch.bfloat16, 0.0884),
+]
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+@pytest.mark.parametrize("case", DECAY_CASES, ids=_ids)
+def test_backward_decay_matches_oracle(case, with_state, cuda_device):
+    """Gradients of the decayed forward, per-head gamma; split sequences too."""
+    from linear_rnn_sequence_gb300.workloads import head_decays
+    B, H, N, d, dv, dt, s = case
+    q, k, v, dy = random_qkv_dy(B, H, N, d, dv, dtype=dt, scale=s, seed=N + 17)
+    gam = head_decays(H)
+    S_in = z_in = None
+    if with_state:
+        qp, kp, vp = random_qkv(B, H, 50, d, dv, dtype=dt, scale=0.5, seed=N)
+        _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: None if t is None else torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    got = la.backward_causal(*(t.to(cuda_device) for t in (q, k, v, dy)), S_in=dev(S_in),
+                             z_in=dev(z_in), return_state_grad=True, gamma=gam.to(cuda_device))
+    torch.cuda.synchronize()
+    want = oracle.causal_backward(q, k, v, dy, S_in=S_in, z_in=z_in, return_state_grad=True,
+                                  gamma=gam)
+    _check(got, want)
+
+
+def test_backward_decay_long_sequence_sampled_heads(cuda_device):
+    """B1 H32 N131072 d64 with decays: split into segments, decayed scans."""
+    from linear_rnn_sequence_gb300.workloads import head_decays
+    w = WORKLOADS["causal_bf16_b1h32n131072d64"]
+    q, k, v, dy = make_backward_inputs(w.with_(mode="backward"))
+    gam = head_decays(w.H)
+    dq, dk, dvv = la.backward_causal(*(t.to(cuda_device) for t in (q, k, v, dy)),
+                                     gamma=gam.to(cuda_device))
+    torch.cuda.synchronize()
+    flat = lambda t: t.reshape(w.BH, w.N, t.shape[-1])
+    for h in (0, 31):
+        want = oracle.causal_backward(flat(q)[h], flat(k)[h], flat(v)[h], flat(dy)[h],
+                                      gamma=gam[h:h + 1])
+        _check([flat(dq)[h], flat(dk)[h], flat(dvv)[h]], want)

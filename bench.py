@@ -502,6 +502,23 @@ def run_modes(args, world, dev, peaks, peak_kind):
                                   "traffic": None,
                                   "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
                                   "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
+    # the same gradients for the decayed forward (per-head gamma)
+    gam = head_decays(w.H).to(dev)
+    total, per = time_steps(lambda: la.backward_causal(q, k, v, dy, eps=w.eps, out=outs,
+                                                       workspace=ws, gamma=gam),
+                            max(3, min(args.steps, 10)), args.warmup, world)
+    ms = sum(per) / len(per)
+    # the decayed recurrence adds one multiply per state element in each
+    # direction: 12 d dv instead of 10 d dv
+    alg_flops = T * (bwd_flops_per_token_head(w.d, w.dv) + 2 * w.d * w.dv)
+    tflops = alg_flops / (ms * 1e-3) / 1e12
+    modes["causal_backward_decay_bf16_b8h16n8192d128"] = {
+        "tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+        "l2": "inputs larger than L2",
+        "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
+                     "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": None,
+                     "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
+                     "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
     del q, k, v, dy, outs, ws
     torch.cuda.empty_cache()
 

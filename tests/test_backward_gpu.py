@@ -167,3 +167,34 @@ def test_backward_decay_long_sequence_sampled_heads(cuda_device):
         want = oracle.causal_backward(flat(q)[h], flat(k)[h], flat(v)[h], flat(dy)[h],
                                       gamma=gam[h:h + 1])
         _check([flat(dq)[h], flat(dk)[h], flat(dvv)[h]], want)
+
+
+@pytest.mark.parametrize("decay", [False, True])
+def test_backward_outputs_stay_in_bounds_and_are_deterministic(decay, cuda_device):
+    """Canary-padded gradient buffers (a split, ragged sequence with an initial
+    state): nothing is written past any output, and two runs agree bitwise."""
+    from linear_rnn_sequence_gb300.workloads import head_decays
+    B, H, N, d, dv = 1, 2, 1000, 64, 128
+    q, k, v, dy = (t.to(cuda_device) for t in random_qkv_dy(B, H, N, d, dv,
+                                                            dtype=torch.bfloat16, scale=0.2,
+                                                            seed=21))
+    S_in = torch.randn(B, H, d, dv, device=cuda_device)
+    z_in = torch.rand(B, H, d, device=cuda_device) + 1.0
+    gam = head_decays(H).to(cuda_device) if decay else None
+    pad = 4096
+    sizes = (B * H * N * d, B * H * N * d, B * H * N * dv, B * H * d * dv, B * H * d)
+    bufs = [torch.full((n + pad,), 12345.0, device=cuda_device) for n in sizes]
+    views = [b[:n] for b, n in zip(bufs, sizes)]
+    gq, gk, gv = (views[0].view(B, H, N, d), views[1].view(B, H, N, d),
+                  views[2].view(B, H, N, dv))
+    ws = la.alloc_workspace(la.causal_backward_workspace_bytes(B, H, N, d, dv), cuda_device)
+    out = la.backward_causal(q, k, v, dy, S_in=S_in, z_in=z_in, return_state_grad=True,
+                             out=(gq, gk, gv), workspace=ws, gamma=gam)
+    torch.cuda.synchronize()
+    for b in bufs[:3]:
+        assert (b[-pad:] == 12345.0).all()
+    again = la.backward_causal(q, k, v, dy, S_in=S_in, z_in=z_in, return_state_grad=True,
+                               workspace=ws, gamma=gam)
+    torch.cuda.synchronize()
+    for x, y in zip(out, again):
+        assert torch.equal(x, y)

@@ -142,3 +142,25 @@ def test_decode_decay_workload_steps(cuda_device):
         torch.cuda.synchronize()
         assert rel_max_err(sel(y), yo[:, 0]) <= TOL_F32
     assert rel_max_err(sel(S), Sref) <= TOL_F32
+
+
+def test_decay_outputs_stay_in_bounds(cuda_device):
+    """Canary-padded y, S, z for the decayed forward and decode step."""
+    B, H, N, d, dv = 1, 2, 130, 64, 64
+    q, k, v = (t.to(cuda_device) for t in random_qkv(B, H, N, d, dv, dtype=torch.bfloat16,
+                                                     scale=0.2, seed=5))
+    gam = head_decays(H).to(cuda_device)
+    pad = 4096
+    ybuf = torch.full((B * H * N * dv + pad,), 12345.0, device=cuda_device)
+    Sbuf = torch.full((B * H * d * dv + pad,), 12345.0, device=cuda_device)
+    zbuf = torch.full((B * H * d + pad,), 12345.0, device=cuda_device)
+    y = ybuf[: B * H * N * dv].view(B, H, N, dv)
+    S = Sbuf[: B * H * d * dv].view(B, H, d, dv)
+    z = zbuf[: B * H * d].view(B, H, d)
+    la.forward_causal_decay(q, k, v, gam, out=y, S_out=S, z_out=z, return_state=True)
+    yd = ybuf[: B * H * dv].view(B, H, dv)
+    la.decode_step_decay(q[:, :, 0].contiguous(), k[:, :, 0].contiguous(),
+                         v[:, :, 0].contiguous(), S, z, gam, out=yd)
+    torch.cuda.synchronize()
+    for buf in (ybuf, Sbuf, zbuf):
+        assert (buf[-pad:] == 12345.0).all()

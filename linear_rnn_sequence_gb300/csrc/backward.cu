@@ -225,7 +225,7 @@ __global__ void bwd_scan_kernel(float *__restrict__ states, int P, int E, int bl
 // ---- 3. dq, 1/D_t, e_t, and the segment's sums of phi(q) g^T, phi(q) e ----
 template <int D, int DV>
 struct DqSmem {
-    static constexpr size_t floats = 4 * (size_t)kBC * D + 3 * (size_t)kBC * DV + DV + 9 * kBC;
+    static constexpr size_t floats = 4 * (size_t)kBC * D + 3 * (size_t)kBC * DV + DV + 11 * kBC + 8;
     static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -264,6 +264,8 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float *sE = sNt + kBC;                          // [kBC] e_t
     float *sC = sE + kBC;                           // [kBC] c_t
     float *sPw = sC + kBC;                          // [kBC] gamma^(token - segment start)
+    float *sGp = sPw + kBC;                         // [kBC + 1] gamma^m
+    float *sGip = sGp + kBC + 4;                    // [kBC + 1] gamma^-m
     const Seg sg = segment(P, seg_chunks, N);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
@@ -284,6 +286,20 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     NAcc<DECAY> pw_acc = 1;              // gamma^(token - segment start), thread NT - 1
     float zh = 0.f;
     const float gm = DECAY ? gamma[sg.h % H] : 1.f;
+    // For gamma >= 1/4 the decay costs no multiply per state element: within
+    // a chunk R_t = gamma^(i+1) Rt_i with Rt_i = R_prev + sum_{j<=i}
+    // gamma^-(j+1) psi(k_j) v_j^T (i, j counted in the chunk, so
+    // gamma^-(j+1) <= 2^64), R g scaled by gamma^(i+1), R rescaled per chunk.
+    const bool scaled = DECAY && gm >= 0.25f;
+    if (scaled && tid == 0) {
+        float p = 1.f, ip = 1.f;
+        for (int m = 0; m <= kBC; ++m) {
+            sGp[m] = p;
+            sGip[m] = ip;
+            p *= gm;
+            ip /= gm;
+        }
+    }
 
     ChunkLoad<D, T, NT> lq, lk;
     ChunkLoad<DV, T, NT> lv;
@@ -365,30 +381,48 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         __syncthreads();
         // the recurrence: R_t = R_{t-1} + psi(k_t) v_t^T, hR_t = R_t g_t;
         // and the segment's sum of phi(q_t) g_t^T
-        for (int t = 0; t < L; ++t) {
-            float pk[RT::RPW], fq[RT::RPW], x[RT::CPL], g[RT::CPL], acc[RT::RPW];
-            ldn(sPk + t * D + r0, pk);      // warp-uniform
-            ldn(sFq + t * D + r0, fq);      // warp-uniform
-            ldn(sV + t * DV + c0, x);
-            ldn(sG + t * DV + c0, g);
-            if constexpr (SEG && DECAY) {
-                const float w = sPw[t];
+        auto token_loop = [&](auto scaled_tag) {
+            constexpr bool SC = decltype(scaled_tag)::value;
+            for (int t = 0; t < L; ++t) {
+                float pk[RT::RPW], fq[RT::RPW], x[RT::CPL], g[RT::CPL], acc[RT::RPW];
+                ldn(sPk + t * D + r0, pk);      // warp-uniform
+                ldn(sFq + t * D + r0, fq);      // warp-uniform
+                ldn(sV + t * DV + c0, x);
+                ldn(sG + t * DV + c0, g);
+                if constexpr (SC) {
+                    const float ip = sGip[t + 1];
 #pragma unroll
-                for (int r = 0; r < RT::RPW; ++r) fq[r] *= w;
-            }
-#pragma unroll
-            for (int r = 0; r < RT::RPW; ++r) {
-                acc[r] = 0.f;
-#pragma unroll
-                for (int c = 0; c < RT::CPL; ++c) {
-                    R[r][c] = fmaf(pk[r], x[c], DECAY ? gm * R[r][c] : R[r][c]);
-                    acc[r] = fmaf(R[r][c], g[c], acc[r]);
-                    if constexpr (SEG) Sh[r][c] = fmaf(fq[r], g[c], Sh[r][c]);
+                    for (int r = 0; r < RT::RPW; ++r) pk[r] *= ip;
                 }
+                if constexpr (SEG && DECAY) {
+                    const float w = sPw[t];
+#pragma unroll
+                    for (int r = 0; r < RT::RPW; ++r) fq[r] *= w;
+                }
+#pragma unroll
+                for (int r = 0; r < RT::RPW; ++r) {
+                    acc[r] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < RT::CPL; ++c) {
+                        R[r][c] = fmaf(pk[r], x[c], (DECAY && !SC) ? gm * R[r][c] : R[r][c]);
+                        acc[r] = fmaf(R[r][c], g[c], acc[r]);
+                        if constexpr (SEG) Sh[r][c] = fmaf(fq[r], g[c], Sh[r][c]);
+                    }
+                }
+                float hsum = reduce_scatter<RT::RPW>(acc, lane);
+                if constexpr (SC) hsum *= sGp[t + 1];
+                if (writer) sH[t * D + my_row] = hsum;
             }
-            const float hsum = reduce_scatter<RT::RPW>(acc, lane);
-            if (writer) sH[t * D + my_row] = hsum;
-        }
+            if constexpr (SC) {
+                const float pL = sGp[L];
+#pragma unroll
+                for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+                    for (int c = 0; c < RT::CPL; ++c) R[r][c] *= pL;
+            }
+        };
+        if (scaled) token_loop(std::true_type{});
+        else token_loop(std::false_type{});
         __syncthreads();
         // e_t and c_t (see the header: the leading terms cancel algebraically)
         for (int t = warp; t < L; t += NW) {
@@ -434,7 +468,7 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 template <int D, int DV>
 struct DkdvSmem {
     static constexpr int kGrp = 8;   // tokens whose dv partial sums are reduced together
-    static constexpr size_t floats = 3 * (size_t)kBC * D + 3 * (size_t)kBC * DV + 2 * kBC +
+    static constexpr size_t floats = 3 * (size_t)kBC * D + 3 * (size_t)kBC * DV + 4 * kBC + 8 +
                                      (size_t)kGrp * (Cfg<D, DV>::kNT / 32) * DV;
     static constexpr size_t bytes = floats * sizeof(float);
 };
@@ -463,7 +497,9 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     float *sDV = sG + kBC * DV;                     // [kBC][DV]
     float *sE = sDV + kBC * DV;                     // [kBC]
     float *sDinv = sE + kBC;                        // [kBC]
-    float *sPart = sDinv + kBC;                     // [kGrp][NW][DV] per-warp partial dv
+    float *sGp = sDinv + kBC;                       // [kBC + 1] gamma^m (kBC + 4 keeps sPart 16-byte aligned)
+    float *sGip = sGp + kBC + 4;                    // [kBC + 1] gamma^-m
+    float *sPart = sGip + kBC + 4;                  // [kGrp][NW][DV] per-warp partial dv
     const Seg sg = segment(P, seg_chunks, N);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
@@ -476,6 +512,18 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     for (int r = 0; r < RT::RPW; ++r) ldn(suf + (r0 + r) * DV + c0, S1[r]);
     float zh = tid < D ? suf[C::kOffZ + tid] : 0.f;   // thread a < D carries zh[a]
     const float gm = DECAY ? gamma[sg.h % H] : 1.f;
+    // gamma >= 1/4: Sh carried rescaled within a chunk, as in bwd_dq_kernel
+    // (counted from the chunk's last token backwards)
+    const bool scaled = DECAY && gm >= 0.25f;
+    if (scaled && tid == 0) {
+        float p = 1.f, ip = 1.f;
+        for (int m = 0; m <= kBC; ++m) {
+            sGp[m] = p;
+            sGip[m] = ip;
+            p *= gm;
+            ip /= gm;
+        }
+    }
 
     ChunkLoad<D, T, NT> lq, lk;
     ChunkLoad<DV, T, NT> lv;
@@ -513,46 +561,70 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 sDK[t * D + tid] = zh;
             }
         __syncthreads();
-        int slot = 0;
-        for (int t = L - 1; t >= 0; --t) {
-            // Sh_t = Sh_{t+1} + phi(q_t) g_t^T; dk_t from Sh_t v_t (a reduction over
-            // columns, inside the warp); dv_t = Sh_t^T phi(k_t) from per-warp partial
-            // sums over the warp's rows, added across warps every kGrp tokens
-            float fq[RT::RPW], fk[RT::RPW], g[RT::CPL], x[RT::CPL], acc[RT::RPW], pv[RT::CPL];
-            ldn(sFq + t * D + r0, fq);       // warp-uniform
-            ldn(sFk + t * D + r0, fk);       // warp-uniform
-            ldn(sG + t * DV + c0, g);
-            ldn(sV + t * DV + c0, x);
+        auto token_loop = [&](auto scaled_tag) {
+            constexpr bool SC = decltype(scaled_tag)::value;
+            int slot = 0;
+            for (int t = L - 1; t >= 0; --t) {
+                // Sh_t = Sh_{t+1} + phi(q_t) g_t^T; dk_t from Sh_t v_t (a reduction
+                // over columns, inside the warp); dv_t = Sh_t^T phi(k_t) from per-warp
+                // partial sums over the warp's rows, added across warps every kGrp tokens
+                float fq[RT::RPW], fk[RT::RPW], g[RT::CPL], x[RT::CPL], acc[RT::RPW], pv[RT::CPL];
+                ldn(sFq + t * D + r0, fq);       // warp-uniform
+                ldn(sFk + t * D + r0, fk);       // warp-uniform
+                ldn(sG + t * DV + c0, g);
+                ldn(sV + t * DV + c0, x);
+                const int m = L - t;             // tokens of the chunk processed, this one included
+                if constexpr (SC) {
+                    const float ip = sGip[m];
 #pragma unroll
-            for (int cc = 0; cc < RT::CPL; ++cc) pv[cc] = 0.f;
+                    for (int r = 0; r < RT::RPW; ++r) fq[r] *= ip;
+                }
 #pragma unroll
-            for (int r = 0; r < RT::RPW; ++r) {
-                acc[r] = 0.f;
+                for (int cc = 0; cc < RT::CPL; ++cc) pv[cc] = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < RT::CPL; ++cc) {
-                    S1[r][cc] = fmaf(fq[r], g[cc], DECAY ? gm * S1[r][cc] : S1[r][cc]);
-                    acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
-                    pv[cc] = fmaf(S1[r][cc], fk[r], pv[cc]);
+                for (int r = 0; r < RT::RPW; ++r) {
+                    acc[r] = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < RT::CPL; ++cc) {
+                        S1[r][cc] = fmaf(fq[r], g[cc], (DECAY && !SC) ? gm * S1[r][cc] : S1[r][cc]);
+                        acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
+                        pv[cc] = fmaf(S1[r][cc], fk[r], pv[cc]);
+                    }
+                }
+                float dfk = reduce_scatter<RT::RPW>(acc, lane);
+                if constexpr (SC) {
+                    const float p = sGp[m];
+                    dfk *= p;
+#pragma unroll
+                    for (int cc = 0; cc < RT::CPL; ++cc) pv[cc] *= p;
+                }
+                if (wr1)   // dk_t = (Sh_t v_t + zh_t) * phi'(k_t)
+                    sDK[t * D + my_row] = (dfk + sDK[t * D + my_row]) * fminf(sFk[t * D + my_row], 1.f);
+                stn(sPart + (slot * NW + warp) * DV + c0, pv);
+                if (++slot == kGrp || t == 0) {   // uniform across the CTA
+                    __syncthreads();
+                    // slot s holds token t + slot - 1 - s
+                    for (int e = tid; e < slot * DV; e += NT) {
+                        const int s = e / DV, b = e % DV;
+                        float sum = 0.f;
+#pragma unroll
+                        for (int w = 0; w < NW; ++w) sum += sPart[(s * NW + w) * DV + b];
+                        sDV[(t + slot - 1 - s) * DV + b] = sum;
+                    }
+                    __syncthreads();
+                    slot = 0;
                 }
             }
-            const float dfk = reduce_scatter<RT::RPW>(acc, lane);
-            if (wr1)   // dk_t = (Sh_t v_t + zh_t) * phi'(k_t)
-                sDK[t * D + my_row] = (dfk + sDK[t * D + my_row]) * fminf(sFk[t * D + my_row], 1.f);
-            stn(sPart + (slot * NW + warp) * DV + c0, pv);
-            if (++slot == kGrp || t == 0) {   // uniform across the CTA
-                __syncthreads();
-                // slot s holds token t + slot - 1 - s
-                for (int e = tid; e < slot * DV; e += NT) {
-                    const int s = e / DV, b = e % DV;
-                    float sum = 0.f;
+            if constexpr (SC) {
+                const float pL = sGp[L];
 #pragma unroll
-                    for (int w = 0; w < NW; ++w) sum += sPart[(s * NW + w) * DV + b];
-                    sDV[(t + slot - 1 - s) * DV + b] = sum;
-                }
-                __syncthreads();
-                slot = 0;
+                for (int r = 0; r < RT::RPW; ++r)
+#pragma unroll
+                    for (int cc = 0; cc < RT::CPL; ++cc) S1[r][cc] *= pL;
             }
-        }
+        };
+        if (scaled) token_loop(std::true_type{});
+        else token_loop(std::false_type{});
         __syncthreads();
         for (int e = tid * 4; e < L * D; e += NT * 4) st4(dk + row0 * D + e, ld4(sDK + e));
         for (int e = tid * 4; e < L * DV; e += NT * 4) st4(dvg + row0 * DV + e, ld4(sDV + e));

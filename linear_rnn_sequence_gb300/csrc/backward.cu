@@ -383,6 +383,9 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         // and the segment's sum of phi(q_t) g_t^T
         auto token_loop = [&](auto scaled_tag) {
             constexpr bool SC = decltype(scaled_tag)::value;
+            // two tokens per iteration overlap one token's reduce-scatter with the
+            // next token's FMAs (not with the segment sums: too many registers)
+#pragma unroll (SEG ? 1 : 2)
             for (int t = 0; t < L; ++t) {
                 float pk[RT::RPW], fq[RT::RPW], x[RT::CPL], g[RT::CPL], acc[RT::RPW];
                 ldn(sPk + t * D + r0, pk);      // warp-uniform
@@ -564,6 +567,9 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
         auto token_loop = [&](auto scaled_tag) {
             constexpr bool SC = decltype(scaled_tag)::value;
             int slot = 0;
+            // two tokens per iteration overlap one token's reduce-scatter with the
+            // next token's FMAs
+#pragma unroll 2
             for (int t = L - 1; t >= 0; --t) {
                 // Sh_t = Sh_{t+1} + phi(q_t) g_t^T; dk_t from Sh_t v_t (a reduction
                 // over columns, inside the warp); dv_t = Sh_t^T phi(k_t) from per-warp

@@ -198,3 +198,42 @@ def test_backward_outputs_stay_in_bounds_and_are_deterministic(decay, cuda_devic
     torch.cuda.synchronize()
     for x, y in zip(out, again):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("gammas", [(0.0, 0.1, 0.2, 0.24), (0.25, 0.5, 0.9, 1.0)])
+def test_backward_decay_both_state_paths(gammas, cuda_device):
+    """gamma < 1/4 multiplies the state per element; gamma >= 1/4 carries it
+    rescaled within each chunk.  Both, including the limits 0 and 1, on a
+    split sequence with an initial state."""
+    B, H, N, d, dv = 1, 4, 2000, 64, 64
+    q, k, v, dy = random_qkv_dy(B, H, N, d, dv, dtype=torch.float32, scale=0.5, seed=31)
+    gam = torch.tensor(gammas, dtype=torch.float32)
+    qp, kp, vp = random_qkv(B, H, 30, d, dv, dtype=torch.float32, scale=0.5, seed=32)
+    _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    got = la.backward_causal(*(t.to(cuda_device) for t in (q, k, v, dy)), S_in=dev(S_in),
+                             z_in=dev(z_in), return_state_grad=True, gamma=gam.to(cuda_device))
+    y = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                gam.to(cuda_device), S_in=dev(S_in), z_in=dev(z_in))
+    torch.cuda.synchronize()
+    want = oracle.causal_backward(q, k, v, dy, S_in=S_in, z_in=z_in, return_state_grad=True,
+                                  gamma=gam)
+    _check(got, want)
+    assert rel_max_err(y, oracle.causal_recurrent_decay(q, k, v, gam, S_in=S_in,
+                                                        z_in=z_in)) <= TOL_BWD
+
+
+def test_backward_with_partly_active_clamp(cuda_device):
+    """eps between the denominators (away from all of them): tokens below it
+    pass no gradient through the denominator."""
+    from tests import backward_pins as bp
+    B, H, N, d, dv = 1, 2, 300, 32, 32
+    q, k, v, dy = random_qkv_dy(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=33)
+    dd = np.sort(bp.dens(q.double().numpy(), k.double().numpy()).reshape(-1))
+    gaps = np.diff(dd)
+    i = int(np.argmax(gaps[: len(gaps) // 2]))   # a wide gap among the smaller dens
+    eps = float((dd[i] + dd[i + 1]) / 2)
+    assert 0 < i and gaps[i] > 1e-3 * dd[i]
+    got = la.backward_causal(*(t.to(cuda_device) for t in (q, k, v, dy)), eps=eps)
+    torch.cuda.synchronize()
+    _check(got, oracle.causal_backward(q, k, v, dy, eps=eps))

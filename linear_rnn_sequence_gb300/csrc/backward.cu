@@ -29,6 +29,14 @@
 //   e_t = -(sum(phi(q_t)) (u_t.g_t) + phi(q_t).hR) / D_t
 // (when the clamp is active e_t = 0 and c_t = u_t.g_t).  Everything is fp32 FMA.
 //
+// Decay.  With RetNet's per-head decay ("Variantes y extensiones":
+// S_t = gamma S_{t-1} + phi(k_t) v_t^T, z alike) every recurrence above
+// carries gamma (Sh_t = phi(q_t) g_t^T + gamma Sh_{t+1}), the split holds with
+// decayed u, n, zeta and R, and dL/dS_in = gamma Sh_1.  The decayed count n
+// is kept in fp64: near its steady state 1/(1 - gamma) every fp32 rounding
+// of gamma n + 1 leans the same way.  For gamma >= 1/4 the states are carried
+// rescaled within each chunk, so the decay costs no multiply per element.
+//
 // Work split: the sequence of each head is cut into P segments of whole
 // 32-token chunks.  Up to six launches:
 //   0. seed        split S_in, z_in into (R, zeta, u, n)         (S_in only)
@@ -37,7 +45,8 @@
 //   3. dq          per (head, segment), tokens in order from the prefix:
 //                  dq; per token 1/D_t and e_t into the workspace; the
 //                  segment's own sums of phi(q) g^T and phi(q) e
-//   4. scan        exclusive suffix over segments of those sums
+//   4. scan        exclusive suffix over segments of those sums (P > 1;
+//                  with one segment the reverse pass starts from zero)
 //   5. dkdv        per (head, segment), tokens in reverse from the suffix:
 //                  dk, dv; segment 0 ends with dL/dS_in, dL/dz_in
 // Inside a CTA the state lives in registers: warp w owns a band of rows and

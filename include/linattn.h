@@ -229,7 +229,7 @@ LA_API size_t la_causal_host_buffer_bytes(int B, int H, int N, int d, int dv, la
  * once, on two streams the call creates and destroys plus `stream`, which the
  * work is ordered after.  It returns when the results are in host memory.
  * Page-locked host memory gives asynchronous full-speed copies; pageable
- * memory works but its copies are staged by the driver and do not overlap.
+ * memory works but its copies are staged by the CUDA runtime and do not overlap.
  * dev_buf is caller-owned device memory of at least
  * la_causal_host_buffer_bytes(...) bytes, 256-byte aligned; its contents are
  * scratch.  Errors: as la_forward_causal (checked per group), LA_ERR_WORKSPACE

@@ -351,11 +351,15 @@ def launches_per_call(mode, w):
     from linear_rnn_sequence_gb300 import linattn as la
     if mode == "causal":
         return 3 if la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 256 else 1
+    tc = w.dtype == torch.bfloat16 and w.d in (64, 128) and w.dv in (64, 128)
     if mode == "noncausal":
         # tensor-core path (bf16, d and dv in {64, 128}): segment states, their
         # per-head sum, the query kernel; otherwise two CUDA-core kernels
-        tc = w.dtype == torch.bfloat16 and w.d in (64, 128) and w.dv in (64, 128)
         return 3 if tc else 2
+    if mode == "causal_decay":
+        # tensor-core kernel for the heads it takes, then the CUDA-core kernel
+        # for the rest (its CTAs for the first kind return at once)
+        return 2 if tc else 1
     return 1
 
 
@@ -522,25 +526,26 @@ def run_modes(args, world, dev, peaks, peak_kind):
     del q, k, v, dy, outs, ws
     torch.cuda.empty_cache()
 
-    # causal with a per-head decay (CUDA cores, fp32)
+    # causal with a per-head decay (every head of this workload has
+    # gamma >= 2^-1/2, so the tensor-core kernel computes all of them; the
+    # CUDA-core pass that follows only returns)
     w = WORKLOADS["causal_decay_bf16_b8h16n8192d128"]
     q, k, v = make_qkv(w, device=dev, gen_device=dev)
     gam = head_decays(w.H).to(dev)
     y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
-    total, per = time_steps(lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y),
+    ws = la.alloc_workspace(la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+    total, per = time_steps(lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y,
+                                                            workspace=ws),
                             max(3, min(args.steps, 10)), args.warmup, world)
     T = w.BH * w.N
     ms = sum(per) / len(per)
-    tflops = T * decay_flops_per_token_head(w.d, w.dv) / (ms * 1e-3) / 1e12
     modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
                      "l2": "inputs larger than L2",
-                     "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
-                                  "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
-                                  "traffic": None,
-                                  "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
-                                  "hbm_roof_fraction": T * alg_bytes_per_token_head(w)
-                                  / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
-    del q, k, v, y
+                     "kernels_per_call": launches_per_call("causal_decay", w),
+                     "roofline": roofline(T * alg_bytes_per_token_head(w),
+                                          T * decay_flops_per_token_head(w.d, w.dv), ms, peaks,
+                                          peak_kind, load_traffic(w.name))}
+    del q, k, v, y, ws
     torch.cuda.empty_cache()
 
     # decode with a per-head decay: state from a decayed 1024-token prefill

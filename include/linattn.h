@@ -132,16 +132,24 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
  * is decayed like S so that y stays a normalised average).  gamma is a DEVICE
  * array of H floats in [0, 1], 4-byte aligned, shared by the B batch rows;
  * its values are not checked (a value outside [0, 1] gives a meaningless
- * result, not an error).  Arguments, layouts and the initial / final state as in
- * la_forward_causal; no workspace is needed.  Computed blockwise in fp32 on
- * the CUDA cores (the blocks' pairs weighted by gamma^(i-j), the carried
- * state by gamma^(i+1)), for both input dtypes.  NULL gamma:
- * LA_ERR_INVALID_ARG.
+ * result, not an error).  Arguments, layouts, the initial / final state and
+ * the workspace (size: la_causal_workspace_bytes; only its 256-byte status
+ * header is used, and it may be NULL when that size is 0) as in
+ * la_forward_causal.
+ * bf16 inputs with d, dv in {64, 128}: heads with gamma in [2^-1/2, 1] run on
+ * the tensor cores, 128-token blocks as in la_forward_causal with key j of a
+ * block of L tokens weighted by gamma^(L-1-j), the block's weights by
+ * gamma^-L, and the carried state multiplied by gamma^L per block (same
+ * precision scheme and bound as la_forward_causal); a second kernel then
+ * computes the other heads on the CUDA cores.  Otherwise (float32 inputs,
+ * d or dv = 32) every head runs on the CUDA cores, token by token in fp32.
+ * The split needs no host read of gamma.  NULL gamma: LA_ERR_INVALID_ARG.
  */
 LA_API la_status la_forward_causal_decay(const void *q, const void *k, const void *v, float *y,
                                          int B, int H, int N, int d, int dv, la_dtype dt,
                                          float eps, const float *gamma, const float *S_in,
                                          const float *z_in, float *S_out, float *z_out,
+                                         void *workspace, size_t workspace_bytes,
                                          void *stream);
 
 /*

@@ -183,7 +183,8 @@ la_status la_decode_step(const void *q, const void *k, const void *v, float *y, 
 la_status la_forward_causal_decay(const void *q, const void *k, const void *v, float *y, int B,
                                   int H, int N, int d, int dv, la_dtype dt, float eps,
                                   const float *gamma, const float *S_in, const float *z_in,
-                                  float *S_out, float *z_out, void *stream) {
+                                  float *S_out, float *z_out, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
     la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
     if (st != LA_OK) return st;
     if (!gamma || (reinterpret_cast<uintptr_t>(gamma) & 3u) != 0) return LA_ERR_INVALID_ARG;
@@ -194,7 +195,12 @@ la_status la_forward_causal_decay(const void *q, const void *k, const void *v, f
         overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb) ||
         overlap(y, T * dv * 4, gamma, (size_t)H * 4))
         return LA_ERR_INVALID_ARG;
+    const size_t need = causal_ws(B, H, N, d, dv, dt);
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (need > 0) {  // a fresh run-time status for every call that uses the workspace
+        if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
+    }
     if (N == 0) {  // no tokens: the final state is the initial state
         if (S_out) {
             cudaError_t e = cudaSuccess;
@@ -210,8 +216,17 @@ la_status la_forward_causal_decay(const void *q, const void *k, const void *v, f
         }
         return LA_OK;
     }
-    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out, nullptr, 0, s};
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out,
+              workspace, workspace_bytes, s};
     a.gamma = gamma;
+    // heads with decay_on_tensor_cores(gamma) on the tensor cores, then the
+    // rest on the CUDA cores (the second kernel's CTAs for the first kind
+    // return at once); no host read of gamma is needed to split them
+    if (causal_tc_supported(a)) {
+        const cudaError_t e = launch_causal_tc(a);
+        if (e != cudaSuccess) return from_cuda(e);
+        a.skip_tc_heads = true;
+    }
     return from_cuda(launch_causal_simt(a));
 }
 

@@ -46,7 +46,7 @@ causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
                   float *__restrict__ y, int N, int H, float eps,
                   const float *__restrict__ gamma, const float *__restrict__ S_in,
                   const float *__restrict__ z_in, float *__restrict__ S_out,
-                  float *__restrict__ z_out)
+                  float *__restrict__ z_out, bool skip_tc_heads)
 {
     constexpr int NT = FwdCfg<D, DV>::kNT, NW = NT / 32;
     using CT = WarpRows<NT, DV, D>;   // warp: CT::RPW value columns; lane: CT::CPL features
@@ -64,6 +64,8 @@ causal_rec_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     const int my_col = b0 + CT::row_of(lane);
     const bool writer = CT::writer(lane);
     const float g = DECAY ? gamma[head % H] : 1.f;
+    // heads the tensor-core kernel has already computed (whole CTA leaves)
+    if (DECAY && skip_tc_heads && decay_on_tensor_cores(g)) return;
 
     // S[a0 + j][b0 + i] in S2[i][j]; S_in is read in full before S_out is written
     float S2[CT::RPW][CT::CPL];
@@ -177,7 +179,7 @@ cudaError_t launch_typed(const FwdArgs &a) {
     if (e != cudaSuccess) return e;
     kern<<<a.BH(), FwdCfg<D, DV>::kNT, smem, a.stream>>>(
         (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.N, a.H, a.eps, a.gamma, a.S_in,
-        a.z_in, a.S_out, a.z_out);
+        a.z_in, a.S_out, a.z_out, a.skip_tc_heads);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,21 @@
 // The result is the exact attention of the features 1 + bf16(psi(x)); the
 // outputs are float32.
 //
+// Decay (DECAY = true; RetNet's S_t = gamma S_{t-1} + phi(k_t) v_t^T, z alike,
+// "Linear Attention/es", "Variantes y extensiones").  For query i of a block
+// of L tokens starting from state (S_b, z_b),
+//   num_i = gamma^(i+1) [ phi(q_i)^T S_b + sum_{j <= i} gamma^-(j+1) w_ij v_j ]
+// and den_i alike, so the common factor gamma^(i+1) cancels in y_i except in
+// the clamp, which becomes max(den', eps gamma^-(i+1)).  Key j enters scaled
+// by s_j = gamma^(L-1-j) <= 1 (psi(k_j) before its bf16 rounding, and the
+// 1 and beta parts as bf16 hi/lo pairs), which is its weight in the state
+// after the block; the weight epilogue multiplies G = s_j w_ij by gamma^-L to
+// get gamma^-(j+1) w_ij.  The inter-block terms use S_b unscaled, and the
+// state export multiplies the TMEM state by gamma^L of the next block before
+// that block's update adds to it.  All factors are at most 2^64 for
+// gamma >= 2^-1/2; smaller decays are left to the CUDA-core kernel.  One work
+// item per head (no sequence split).
+//
 // One CTA owns one (head, segment) work item and walks its blocks in order.
 // Warp roles (18 warps):
 //   warp 0       TMA producer: Q (1 stage), K and V (2 stages) tiles, 128B swizzle
@@ -105,7 +120,9 @@ __device__ __forceinline__ uint32_t k16_off(int n, int k) {
     return (uint32_t)((n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2);
 }
 
-template <int D, int DV>
+constexpr int kSmallBytes = 6 * 1024;   // the Small area of every layout
+
+template <int D, int DV, bool DECAY = false>
 struct Layout {
     static constexpr int kQ = kC * D * 2;           // one Q stage
     static constexpr int kK = kC * D * 2;
@@ -126,10 +143,13 @@ struct Layout {
     static constexpr int oYB = oGB + 2 * kGB;
     static constexpr int oZB = oYB + kYB;
     static constexpr int oSmall = oZB + kZB;
-    static constexpr int kSmall = 6 * 1024;
-    static constexpr int bytes = oSmall + kSmall;
+    static constexpr int kSmall = kSmallBytes;
+    static constexpr int oDecay = oSmall + kSmall;  // decay kernel only: DecaySmall
+    static constexpr int kDecay = DECAY ? 2 * 1024 : 0;
+    static constexpr int bytes = oDecay + kDecay;
     // request enough that only one CTA fits per SM (TMEM: 512 columns each)
     static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
+    static_assert(request <= 227 * 1024, "shared memory per CTA");
 };
 
 // Small shared-memory area.  Per-block values are kept by block parity:
@@ -153,7 +173,18 @@ struct Small {
 };
 static_assert(offsetof(Small, u) % 16 == 0 && offsetof(Small, q_full) % 8 == 0,
               "vector loads and mbarriers need aligned fields");
-static_assert(sizeof(Small) <= 6 * 1024, "small area");
+static_assert(sizeof(Small) <= kSmallBytes, "small area");
+
+// Shared values of the decay kernel only (after Small; the plain kernel's
+// layout does not have them).
+struct DecaySmall {
+    alignas(16) float s_part[2][4];    // per-warp sums of the key weights s_j
+    alignas(16) float gpow[2][kC + 2]; // [0][m] = gamma^m, [1][m] = gamma^-m
+};
+static_assert(sizeof(DecaySmall) <= 2 * 1024, "decay area");
+__device__ __forceinline__ DecaySmall &decay_area(Small &S) {
+    return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
+}
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -316,12 +347,13 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
 // alpha_i = sum of the rounded psi(q_i) over both halves, and d).  Once
 // G = w is ready, every other 16-column group each: w_ij (j <= i, else 0)
 // split into bf16 hi + lo pairs written back over G, and the partial row sums.
-template <int D, int DV>
+template <int D, int DV, bool DECAY>
 __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
-                                             int nchunks, const Guard &g) {
+                                             int nchunks, int nloc, const Guard &g) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpA) >> 2;
+    DecaySmall &X = decay_area(S);   // touched only with DECAY
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const float dd = (float)D;
     // groups entirely above this warp's rows are all zero (causal mask)
@@ -385,6 +417,10 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         if (ok) {
             tc_fence_after();
             if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 2);
+            // decay: G holds gamma^(L-1-j) w_ij (keys pre-scaled), so
+            // gamma^-L G = gamma^-(j+1) w_ij, the weight relative to row i's
+            // common factor gamma^(i+1)
+            const float gsc = DECAY ? X.gpow[1][min(kC, nloc - c * kC)] : 1.f;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
             // (hi + lo equals w to within about 2^-17 w)
             float rowsum = 0.f;
@@ -398,8 +434,10 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                     const int lim = (wq * 32 >= grp * 16 + 15) ? 15 : row - grp * 16;
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 2) {
-                        const float w0 = (jj <= lim) ? u2f(gc[jj]) : 0.f;
-                        const float w1 = (jj + 1 <= lim) ? u2f(gc[jj + 1]) : 0.f;
+                        const float g0 = DECAY ? u2f(gc[jj]) * gsc : u2f(gc[jj]);
+                        const float g1 = DECAY ? u2f(gc[jj + 1]) * gsc : u2f(gc[jj + 1]);
+                        const float w0 = (jj <= lim) ? g0 : 0.f;
+                        const float w1 = (jj + 1 <= lim) ? g1 : 0.f;
                         const uint32_t hi = pack_bf16x2(w0, w1);
                         const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
                         rowsum += w0 + w1;
@@ -443,7 +481,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
 // Eight warps, two per TMEM lane quarter, the two threads of a row (halves
 // h = 0, 1) sharing its work: psi(k) in place over half of the features,
 // the state export of half of R's columns, half of the output columns.
-template <int D, int DV>
+template <int D, int DV, bool DECAY>
 __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
                                              uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
                                              uint8_t *sYB, uint8_t *sZB,
@@ -454,6 +492,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpB) >> 2;
+    DecaySmall &X = decay_area(S);   // touched only with DECAY
     const int wtid = tid - kWarpB * 32;   // 0..255
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const int N = nloc;   // tokens of this work item (segment)
@@ -490,6 +529,9 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // head, or the exclusive prefix of this segment
         const float *Sin = p.S_in ? p.S_in + (size_t)item * D * DV : nullptr;
         const float *zin = p.z_in ? p.z_in + (size_t)item * D : nullptr;
+        // decay: the TMEM state is multiplied by gamma^L before each block's
+        // update adds to it (block 0: here); the exported operands are not
+        const float g0 = DECAY ? X.gpow[0][min(kC, N)] : 1.f;
 #pragma unroll
         for (int gq = 0; gq < kRGroups; ++gq) {
             const int grp = h * kRGroups + gq;
@@ -499,8 +541,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 const int b = grp * 16 + jj;
                 v[jj] = f2u((Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f);
             }
-            tmem_st16(tb + lb + kColR + grp * 16, v);
             if (row < D) export_row_bf16<D, DV>(sRt, row, grp, v);
+            if (DECAY) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) v[jj] = f2u(u2f(v[jj]) * g0);
+            }
+            tmem_st16(tb + lb + kColR + grp * 16, v);
         }
         float zeta0 = 0.f;
         if (h == 0) {
@@ -512,10 +558,17 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 #pragma unroll 16
                 for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
             }
-            const uint32_t zv[4] = {f2u(zeta0), 0u, 0u, 0u};
-            const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
+            const uint32_t zv[4] = {f2u(zeta0 * g0), 0u, 0u, 0u};
             tmem_st4(tb + lb + kColZ, zv);
-            tmem_st4(tb + lb + kColUV, uv);
+            if (DECAY) {   // columns [sum v | r_hi | r_lo | u_hi | u_lo | 0 0 0]
+                const uint32_t uv[4] = {0u, f2u(r0 * g0), 0u, f2u(u0 * g0)};
+                const uint32_t uw[4] = {0u, 0u, 0u, 0u};
+                tmem_st4(tb + lb + kColUV, uv);
+                tmem_st4(tb + lb + kColUV + 4, uw);
+            } else {       // columns [u | r_hi | r_lo | 0]
+                const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
+                tmem_st4(tb + lb + kColUV, uv);
+            }
             S.zeta[row] = zeta0;
             S.u[1][row] = u0;
             if (row < DV) aug_row(sYB, row, r0, u0);
@@ -545,6 +598,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     // Returns false when the group gave up (agreed at the group barrier).
     auto phi_k = [&](int c) -> bool {
         const int s = c & 1, cb = c & 1;
+        // decay: key j of a block of L tokens enters with weight
+        // s_j = gamma^(L-1-j), its share of the state after the block
+        // (padding rows: 0)
+        const int L = min(kC, N - c * kC);
+        const float sc = DECAY ? (row < L ? X.gpow[0][L - 1 - row] : 0.f) : 1.f;
         const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
@@ -568,7 +626,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk = psi_bf16x2(w[hw]);
+                        const uint32_t pk =
+                            DECAY ? psi_scaled_bf16x2(w[hw], sc) : psi_bf16x2(w[hw]);
                         beta2 = acc_bf16x2(beta2, pk);
                         w[hw] = pk;
                     }
@@ -590,11 +649,25 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
-            // B' row of key j: [beta_hi, beta_lo, 1, 1, 1, 0, 0, 0]
-            *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) = make_uint4(
-                pack_bf16x2(bh, beta - bh), pack_bf16x2(1.f, 1.f), pack_bf16x2(1.f, 0.f), 0u);
+            // key weight s_j as a bf16 pair (exactly 1, 0 without a decay)
+            float sh = 1.f, sl = 0.f;
+            if (DECAY) {
+                sh = bf16_round(sc);
+                sl = bf16_round(sc - sh);
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 48) = __float2bfloat16_rn(sh);
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 64) = __float2bfloat16_rn(sl);
+            }
+            // B' row of key j: [beta_hi, beta_lo, s_hi, s_hi, s_hi, s_lo, s_lo, 0]
+            // (beta is the sum of the scaled psi(k_j) with a decay)
+            *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) =
+                make_uint4(pack_bf16x2(bh, beta - bh), pack_bf16x2(sh, sh), pack_bf16x2(sh, sl),
+                           pack_bf16x2(sl, 0.f));
             const float bsum = warp_sum_f(beta);
             if (lane == 0) S.rho_part[cb][wq] = bsum;
+            if (DECAY) {
+                const float ssum = warp_sum_f(sh + sl);
+                if (lane == 0) X.s_part[cb][wq] = ssum;
+            }
             fence_proxy_async();
             mbar_arrive(&S.phik_done[s]);
             if (lane == 0) LA_TRACE_POINT(c, 26 + wq);
@@ -608,6 +681,10 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     auto export_state = [&](int c) -> bool {
         const int cb = c & 1, pb = (c + 1) & 1;
         const int L = min(kC, N - c * kC);
+        // decay: once exported, the state is multiplied in TMEM by gamma^L of
+        // block c+1, before that block's update adds to it (not after the last)
+        const bool rescale = DECAY && c + 1 < nchunks;
+        const float gnext = rescale ? X.gpow[0][min(kC, N - (c + 1) * kC)] : 1.f;
         if (!wait_warp(&S.st_full, c & 1, g, 51) || !wait_warp(&S.aq_free, c & 1, g, 54))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 4);
@@ -623,26 +700,57 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 export_row_bf16<D, DV>(sRt, row, grp, rv0);
                 export_row_bf16<D, DV>(sRt, row, grp + 1, rv1);
             }
+            if (rescale) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    rv0[m] = f2u(u2f(rv0[m]) * gnext);
+                    rv1[m] = f2u(u2f(rv1[m]) * gnext);
+                }
+                tmem_st16(tb + lb + kColR + grp * 16, rv0);
+                tmem_st16(tb + lb + kColR + (grp + 1) * 16, rv1);
+            }
         }
         if (h == 0) {
-            uint32_t zv[4], uv[4];
+            uint32_t zv[4], uv[4], uw[4];
             tmem_ld4(tb + lb + kColZ, zv);
             tmem_ld4(tb + lb + kColUV, uv);
+            if (DECAY) tmem_ld4(tb + lb + kColUV + 4, uw);
             tmem_wait_ld();
+            const float u = DECAY ? u2f(uv[3]) + u2f(uw[0]) : u2f(uv[0]);
             if (row < D) {
                 S.zeta[row] = u2f(zv[0]);
                 *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
                     __float2bfloat16_rn(u2f(zv[0]));
             }
-            S.u[cb][row] = u2f(uv[0]);
-            if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u2f(uv[0]));
+            S.u[cb][row] = u;
+            if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u);
             if (wtid == 0) {
-                S.n_s[cb] = S.n_s[pb] + (float)L;
-                S.rho_s[cb] = S.rho_s[pb] + ((S.rho_part[cb][0] + S.rho_part[cb][1]) +
-                                             (S.rho_part[cb][2] + S.rho_part[cb][3]));
+                const float rsum = (S.rho_part[cb][0] + S.rho_part[cb][1]) +
+                                   (S.rho_part[cb][2] + S.rho_part[cb][3]);
+                if (DECAY) {   // n and rho decay like the state: x <- gamma^L x + sum_j s_j x_j
+                    const float gcur = X.gpow[0][L];
+                    S.n_s[cb] = fmaf(gcur, S.n_s[pb], (X.s_part[cb][0] + X.s_part[cb][1]) +
+                                                          (X.s_part[cb][2] + X.s_part[cb][3]));
+                    S.rho_s[cb] = fmaf(gcur, S.rho_s[pb], rsum);
+                } else {
+                    S.n_s[cb] = S.n_s[pb] + (float)L;
+                    S.rho_s[cb] = S.rho_s[pb] + rsum;
+                }
                 aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
             }
+            if (rescale) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    zv[m] = f2u(u2f(zv[m]) * gnext);
+                    uv[m] = f2u(u2f(uv[m]) * gnext);
+                    uw[m] = f2u(u2f(uw[m]) * gnext);
+                }
+                tmem_st4(tb + lb + kColZ, zv);
+                tmem_st4(tb + lb + kColUV, uv);
+                tmem_st4(tb + lb + kColUV + 4, uw);
+            }
         }
+        if (rescale) tmem_wait_st();
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&S.rt_ready);
@@ -665,9 +773,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         tc_fence_after();
         uint32_t yz[4];
         tmem_ld4(tb + lb + kColYz, yz);
+        // decay: row i's numerator and denominator are both carried divided by
+        // gamma^(i+1), so the clamp max(den, eps) becomes max(den', eps gamma^-(i+1))
+        const float eps_row = DECAY ? p.eps * X.gpow[1][row + 1] : p.eps;
         tmem_wait_ld();
         S.e_inv[h][row] =
-            1.f / fmaxf(u2f(yz[0]) + (S.rowsum[cb][0][row] + S.rowsum[cb][1][row]), p.eps);
+            1.f / fmaxf(u2f(yz[0]) + (S.rowsum[cb][0][row] + S.rowsum[cb][1][row]), eps_row);
         __syncwarp();
         float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
         const int tq = lane >> 2, tc = (lane & 3) * 2;
@@ -742,13 +853,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int DV>
+template <int D, int DV, bool DECAY>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap,
                  const TcParams p)
 {
-    using Lay = Layout<D, DV>;
+    using Lay = Layout<D, DV, DECAY>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -766,6 +877,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
     if (tid == 0) LA_TRACE_POINT(0, 15);
+    // decay (one segment per head): powers of the head's gamma, read by both
+    // row-worker groups (visible after the __syncthreads below)
+    if (DECAY && tid < kC + 2) {
+        DecaySmall &X = decay_area(S);
+        const float gam = p.gamma[head % p.H];
+        X.gpow[0][tid] = powf(gam, (float)tid);
+        X.gpow[1][tid] = powf(gam, -(float)tid);
+    }
 
     if (tid == 0) {
         S.abort_flag = 0;
@@ -812,10 +931,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     } else if (warp == 1) {
         if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
     } else if (warp < kWarpB) {
-        group_a_role<D, DV>(S, tb, sQ, nchunks, g);
+        group_a_role<D, DV, DECAY>(S, tb, sQ, nchunks, nloc, g);
     } else {
-        group_b_role<D, DV>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0, nloc,
-                            seg == p.nseg - 1, nchunks, g);
+        group_b_role<D, DV, DECAY>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0,
+                                   nloc, seg == p.nseg - 1, nchunks, g);
     }
     tc_fence_before();
     __syncthreads();
@@ -889,9 +1008,9 @@ size_t segment_workspace(int BH, int N, int d, int dv) {
     return sizeof(WsHeader) + 2 * sizeof(float) * (size_t)BH * nseg * ((size_t)d * dv + d);
 }
 
-template <int D, int DV>
+template <int D, int DV, bool DECAY>
 cudaError_t launch_dv(const FwdArgs &a) {
-    using Lay = Layout<D, DV>;
+    using Lay = Layout<D, DV, DECAY>;
     CUtensorMap qm, km, vm;
     const int BH = a.BH();
     if (!encode_3d(&qm, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
@@ -911,6 +1030,12 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.S_out = a.S_out;
     p.z_out = a.z_out;
     choose_segments(BH, a.N, p.nseg, p.seg_chunks);
+    if (DECAY) {   // one work item per head: the segment pass has no decay
+        p.nseg = 1;
+        p.seg_chunks = a.N > kC ? (a.N + kC - 1) / kC : 1;
+        p.gamma = a.gamma;
+        p.H = a.H;
+    }
     WsHeader *hdr = static_cast<WsHeader *>(a.ws);
     p.err = &hdr->error;
     p.err_where = &hdr->error_where;
@@ -918,7 +1043,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
     p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
-    if (p.nseg > 1) {
+    if (!DECAY && p.nseg > 1) {
         // segment states, then their exclusive prefixes, which become the
         // initial states of the (head, segment) items
         const size_t nS = (size_t)D * DV, cnt = (size_t)items;
@@ -941,11 +1066,11 @@ cudaError_t launch_dv(const FwdArgs &a) {
         p.S_in = S_pre;
         p.z_in = z_pre;
     }
-    auto kern = causal_tc_kernel<D, DV>;
+    auto kern = causal_tc_kernel<D, DV, DECAY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::request);
     if (e != cudaSuccess) return e;
-    if (p.nseg > 1)
+    if (!DECAY && p.nseg > 1)
         return launch_overlapped(kern, dim3(items), dim3(kThreads), Lay::request, a.stream, qm, km,
                                  vm, p);
     kern<<<items, kThreads, Lay::request, a.stream>>>(qm, km, vm, p);
@@ -966,12 +1091,17 @@ int causal_tc_launches(int BH, int N) {
     return nseg > 1 ? 3 : 1;
 }
 
-cudaError_t launch_causal_tc(const FwdArgs &a) {
-    if (a.d == 64 && a.dv == 64) return launch_dv<64, 64>(a);
-    if (a.d == 64 && a.dv == 128) return launch_dv<64, 128>(a);
-    if (a.d == 128 && a.dv == 64) return launch_dv<128, 64>(a);
-    if (a.d == 128 && a.dv == 128) return launch_dv<128, 128>(a);
+template <bool DECAY>
+cudaError_t launch_tc_dims(const FwdArgs &a) {
+    if (a.d == 64 && a.dv == 64) return launch_dv<64, 64, DECAY>(a);
+    if (a.d == 64 && a.dv == 128) return launch_dv<64, 128, DECAY>(a);
+    if (a.d == 128 && a.dv == 64) return launch_dv<128, 64, DECAY>(a);
+    if (a.d == 128 && a.dv == 128) return launch_dv<128, 128, DECAY>(a);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_causal_tc(const FwdArgs &a) {
+    return a.gamma ? launch_tc_dims<true>(a) : launch_tc_dims<false>(a);
 }
 
 }  // namespace la

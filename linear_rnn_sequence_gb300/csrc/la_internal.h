@@ -24,8 +24,19 @@ struct FwdArgs {
     size_t ws_bytes;
     cudaStream_t stream;
     const float *gamma = nullptr;   // per-head decay [H] (device), null: none
+    // decay only: heads whose gamma passes decay_on_tensor_cores were already
+    // computed by the tensor-core kernel; the CUDA-core kernel skips them
+    bool skip_tc_heads = false;
     int BH() const { return B * H; }
 };
+
+// The decayed tensor-core kernel scales block-local weights by gamma^-128 and
+// gamma^-(i+1); with gamma >= 2^-1/2 these stay below 2^64, far inside the
+// fp32 and bf16 range.  Smaller decays (and values outside [0, 1], NaN)
+// take the CUDA-core kernel, which multiplies the state token by token.
+__host__ __device__ inline bool decay_on_tensor_cores(float gamma) {
+    return gamma >= 0.70710678f && gamma <= 1.f;
+}
 
 struct DecodeArgs {
     const void *q, *k, *v;

@@ -35,6 +35,8 @@ struct TcParams {
     unsigned int *err_where;
     unsigned long long limit_ns;
     int drop_item;                 // test hook: this item's first K/V copy is never issued (-1: off)
+    const float *gamma;            // per-head decay [H] (causal kernel with DECAY only)
+    int H;
 };
 
 // Packed fp32 pairs (two floats in one 64-bit register; the f32x2 arithmetic
@@ -75,6 +77,21 @@ __device__ __forceinline__ uint32_t psi_bf16x2(uint32_t w) {
     f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), f2pack(-1.f, -1.f)), e0, e1);
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(fmaxf(x1, e1)), "f"(fmaxf(x0, e0)));
+    return r;
+}
+
+// sc * psi(x) for both bf16 halves of w, rounded once to bf16x2 (the decayed
+// causal kernel weights key j by sc = gamma^(L-1-j) before the tensor cores
+// see it).
+__device__ __forceinline__ uint32_t psi_scaled_bf16x2(uint32_t w, float sc) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1;
+    f2unpack(f2mul(f2pack(fminf(x0, 0.f), fminf(x1, 0.f)),
+                   f2pack(1.4426950408889634f, 1.4426950408889634f)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), f2pack(-1.f, -1.f)), e0, e1);
+    f2unpack(f2mul(f2pack(fmaxf(x0, e0), fmaxf(x1, e1)), f2pack(sc, sc)), e0, e1);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e1), "f"(e0));
     return r;
 }
 

@@ -71,7 +71,7 @@ def lib():
                                                  sz, vp]
             L.la_forward_causal_host.restype = i
             L.la_forward_causal_decay.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp,
-                                                  vp, vp, vp]
+                                                  vp, vp, vp, sz, vp]
             L.la_forward_causal_decay.restype = i
             L.la_decode_step_decay.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
             L.la_decode_step_decay.restype = i
@@ -183,13 +183,15 @@ def forward_causal(q, k, v, eps: float = 1e-6, S_in=None, z_in=None, return_stat
 
 
 def forward_causal_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=None,
-                         return_state=False, out=None, S_out=None, z_out=None, stream=None):
+                         return_state=False, out=None, S_out=None, z_out=None, workspace=None,
+                         stream=None, check_status=False):
     """Causal attention with a per-head decay ``gamma`` (float32 CUDA tensor [H]).
 
     q, k: [B,H,N,d]; v: [B,H,N,dv].  Returns y [B,H,N,dv] float32 (and the
-    final (S, z) when ``return_state``).
+    final (S, z) when ``return_state``).  The workspace and ``check_status``
+    are as in ``forward_causal``.
     """
-    _check_cuda(q, k, v, gamma, S_in, z_in, out, S_out, z_out)
+    _check_cuda(q, k, v, gamma, S_in, z_in, out, S_out, z_out, workspace)
     B, H, N, d = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -201,10 +203,19 @@ def forward_causal_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=None
     if return_state and S_out is None:
         S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
         z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = int(lib().la_causal_workspace_bytes(B, H, N, d, dv, dt))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().la_forward_causal_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
                                        float(eps), _ptr(gamma), _ptr(S_in), _ptr(z_in),
-                                       _ptr(S_out), _ptr(z_out), _stream_handle(stream, q.device))
+                                       _ptr(S_out), _ptr(z_out), _ptr(workspace), wbytes,
+                                       _stream_handle(stream, q.device))
     _raise(st, "la_forward_causal_decay")
+    if check_status and workspace is not None:
+        err, where = workspace_header(workspace)
+        if err != LA_OK:
+            raise LinAttnError(err, f"la_forward_causal_decay (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
 
 

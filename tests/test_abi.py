@@ -186,15 +186,22 @@ def test_backward_rejects_bad_arguments():
 def test_decay_entry_points_reject_bad_arguments():
     L = la.lib()
     p = [ctypes.c_void_p((i + 1) << 24) for i in range(8)]
-    q, k, v, y, S, z, g, _ = p
-    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 1e-6, None, None, None,
-                                     None, None, None) == la.LA_ERR_INVALID_ARG   # no gamma
-    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 48, 64, 1, 1e-6, g, None, None,
-                                     None, None, None) == la.LA_ERR_UNSUPPORTED
-    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 0.0, g, None, None,
-                                     None, None, None) == la.LA_ERR_INVALID_ARG
-    assert L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, 64, 64, 1, 1e-6, g, S, None,
-                                     None, None, None) == la.LA_ERR_INVALID_ARG   # S_in alone
+    q, k, v, y, S, z, g, ws = p
+    need = L.la_causal_workspace_bytes(1, 2, 8, 64, 64, 1)
+    assert need >= 256   # bf16, d = dv = 64: the tensor-core kernel's status header
+
+    def fwd(d=64, eps=1e-6, gam=g, S_in=None, ws_=ws, wsb=need):
+        return L.la_forward_causal_decay(q, k, v, y, 1, 2, 8, d, 64, 1, eps, gam, S_in, None,
+                                         None, None, ws_, wsb, None)
+    assert fwd(gam=None) == la.LA_ERR_INVALID_ARG                  # no gamma
+    assert fwd(d=48) == la.LA_ERR_UNSUPPORTED
+    assert fwd(eps=0.0) == la.LA_ERR_INVALID_ARG
+    assert fwd(S_in=S) == la.LA_ERR_INVALID_ARG                    # S_in alone
+    assert fwd(ws_=None, wsb=0) == la.LA_ERR_WORKSPACE
+    assert fwd(wsb=need - 1) == la.LA_ERR_WORKSPACE
+    assert fwd(ws_=ctypes.c_void_p(ws.value + 16)) == la.LA_ERR_WORKSPACE   # not 256-aligned
+    # float32 inputs take the CUDA-core kernel alone: no workspace
+    assert L.la_causal_workspace_bytes(1, 2, 8, 64, 64, 0) == 0
     assert L.la_decode_step_decay(q, k, v, y, S, z, 1, 2, 64, 64, 1, 1e-6, None,
                                   None) == la.LA_ERR_INVALID_ARG
     assert L.la_decode_step_decay(q, k, v, y, None, z, 1, 2, 64, 64, 1, 1e-6, g,

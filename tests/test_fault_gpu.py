@@ -23,11 +23,14 @@ LIMIT_NS = 5_000_000   # 5 ms per bounded wait while the hook is on
     ("causal", 4, 1000),     # sequence split into segments: state + scan + chunk kernels
     ("causal", 96, 256),     # one CTA per head
     ("noncausal", 4, 1000),
+    ("decay", 8, 600),       # decayed form: one CTA per head, then the CUDA-core pass
 ])
 def test_dropped_copy_times_out_and_context_survives(mode, H, N, cuda_device):
     q, k, v = random_qkv(1, H, N, 64, 64, dtype=torch.bfloat16, scale=0.125, seed=H + N)
     qd, kd, vd = q.to(cuda_device), k.to(cuda_device), v.to(cuda_device)
-    fn = la.forward_causal if mode == "causal" else la.forward_noncausal
+    gam = torch.full((H,), 0.95)
+    fn = {"causal": la.forward_causal, "noncausal": la.forward_noncausal,
+          "decay": lambda *a, **kw: la.forward_causal_decay(*a, gam.to(cuda_device), **kw)}[mode]
     try:
         la.set_fault(drop_load_item=1, wait_limit_ns=LIMIT_NS)
         with pytest.raises(la.LinAttnError) as ei:
@@ -37,7 +40,9 @@ def test_dropped_copy_times_out_and_context_survives(mode, H, N, cuda_device):
         la.set_fault(-1, 0)
     y = fn(qd, kd, vd, check_status=True)
     torch.cuda.synchronize()
-    ref = oracle.causal_recurrent(q, k, v) if mode == "causal" else oracle.noncausal(q, k, v)
+    ref = {"causal": lambda: oracle.causal_recurrent(q, k, v),
+           "noncausal": lambda: oracle.noncausal(q, k, v),
+           "decay": lambda: oracle.causal_recurrent_decay(q, k, v, gam)}[mode]()
     assert rel_max_err(y, ref) <= TOL_BF16
 
 

@@ -37,12 +37,15 @@
 // the clamp, which becomes max(den', eps gamma^-(i+1)).  Key j enters scaled
 // by s_j = gamma^(L-1-j) <= 1 (psi(k_j) before its bf16 rounding, and the
 // 1 and beta parts as bf16 hi/lo pairs), which is its weight in the state
-// after the block; the weight epilogue multiplies G = s_j w_ij by gamma^-L to
-// get gamma^-(j+1) w_ij.  The inter-block terms use S_b unscaled, and the
-// state export multiplies the TMEM state by gamma^L of the next block before
-// that block's update adds to it.  All factors are at most 2^64 for
-// gamma >= 2^-1/2; smaller decays are left to the CUDA-core kernel.  One work
-// item per head (no sequence split).
+// after the block.  The inter-block terms use S_b unscaled.  The carried
+// state is decayed without touching TMEM on most blocks: TMEM holds it
+// divided by a running scale G (DecayScale below) that shrinks by gamma^L per
+// block, the keys enter multiplied by s_j / G, and the export multiplies by G.
+// The weight tile then holds s_j w_ij / G, and the weight epilogue multiplies
+// it by gamma^-L G to get gamma^-(j+1) w_ij.  Only when G would fall below
+// 2^-48 is the state rescaled in TMEM.  All factors stay within 2^+-112 for gamma >= 2^-1/2; smaller
+// decays are left to the CUDA-core kernel.  One work item per head (no
+// sequence split).
 //
 // One CTA owns one (head, segment) work item and walks its blocks in order.
 // Warp roles (18 warps):
@@ -185,6 +188,29 @@ static_assert(sizeof(DecaySmall) <= 2 * 1024, "decay area");
 __device__ __forceinline__ DecaySmall &decay_area(Small &S) {
     return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
 }
+
+// Decay: the TMEM state (R, zeta, u, r) is held divided by a scale G that
+// shrinks by gamma^L with every block, so a block's update only adds to it
+// (its keys enter multiplied by 1/G) and the export multiplies by G.  When
+// gamma^L G would fall below 2^-48, the state is instead rescaled in TMEM
+// before the block and G restarts at G0.  G0 = 3/4 (1 when gamma = 1): the
+// first keys after a restart then carry scales near 4/3 rather than just
+// above 1, where bf16(scale * x) would round most bf16 values x back to x and
+// drop the scale from their psi part in the same direction for every
+// feature.  Each role steps its own copy through the blocks in order; the
+// copies agree bit for bit.
+struct DecayScale {
+    float G0;              // restart value
+    float G;               // scale of the state after the current block
+    bool renorm = false;   // the state is rescaled in TMEM before the current block
+    __device__ __forceinline__ explicit DecayScale(float gamma)
+        : G0(gamma == 1.f ? 1.f : 0.75f), G(G0) {}
+    __device__ __forceinline__ void step(float gL) {
+        const float cand = gL * G;
+        renorm = cand < 0x1p-48f;
+        G = renorm ? G0 : cand;
+    }
+};
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -354,12 +380,15 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpA) >> 2;
     DecaySmall &X = decay_area(S);   // touched only with DECAY
+    // state scale G of block c (gpow[0][1] = gamma; the plain layout has no table)
+    DecayScale ds(DECAY ? X.gpow[0][1] : 1.f);
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const float dd = (float)D;
     // groups entirely above this warp's rows are all zero (causal mask)
     const int last_grp = (wq * 32 + 31) >> 4;
     for (int c = 0; c < nchunks; ++c) {
         const int cb = c & 1;
+        if (DECAY) ds.step(X.gpow[0][min(kC, nloc - c * kC)]);
         bool ok = wait_warp(&S.q_full, c & 1, g, 40);
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
@@ -417,10 +446,10 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         if (ok) {
             tc_fence_after();
             if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 2);
-            // decay: G holds gamma^(L-1-j) w_ij (keys pre-scaled), so
-            // gamma^-L G = gamma^-(j+1) w_ij, the weight relative to row i's
-            // common factor gamma^(i+1)
-            const float gsc = DECAY ? X.gpow[1][min(kC, nloc - c * kC)] : 1.f;
+            // decay: the weight tile holds gamma^(L-1-j) w_ij / G (keys
+            // pre-scaled), so multiplying by gamma^-L G gives gamma^-(j+1) w_ij,
+            // the weight relative to row i's common factor gamma^(i+1)
+            const float gsc = DECAY ? X.gpow[1][min(kC, nloc - c * kC)] * ds.G : 1.f;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
             // (hi + lo equals w to within about 2^-17 w)
             float rowsum = 0.f;
@@ -493,6 +522,10 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpB) >> 2;
     DecaySmall &X = decay_area(S);   // touched only with DECAY
+    // scales of the block whose keys phi_k prepares and of the state in TMEM
+    // (the export's block); the plain layout has no table
+    DecayScale ks(DECAY ? X.gpow[0][1] : 1.f);
+    DecayScale xs(DECAY ? X.gpow[0][1] : 1.f);
     const int wtid = tid - kWarpB * 32;   // 0..255
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const int N = nloc;   // tokens of this work item (segment)
@@ -529,9 +562,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // head, or the exclusive prefix of this segment
         const float *Sin = p.S_in ? p.S_in + (size_t)item * D * DV : nullptr;
         const float *zin = p.z_in ? p.z_in + (size_t)item * D : nullptr;
-        // decay: the TMEM state is multiplied by gamma^L before each block's
-        // update adds to it (block 0: here); the exported operands are not
-        const float g0 = DECAY ? X.gpow[0][min(kC, N)] : 1.f;
+        // decay: the initial state enters TMEM divided by G0, and already
+        // multiplied by gamma^L of block 0 when the scale restarts there
+        if (DECAY) xs.step(X.gpow[0][min(kC, N)]);
+        const float g0 =
+            DECAY ? (xs.renorm ? X.gpow[0][min(kC, N)] : 1.f) / xs.G0 : 1.f;
 #pragma unroll
         for (int gq = 0; gq < kRGroups; ++gq) {
             const int grp = h * kRGroups + gq;
@@ -602,7 +637,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // s_j = gamma^(L-1-j), its share of the state after the block
         // (padding rows: 0)
         const int L = min(kC, N - c * kC);
-        const float sc = DECAY ? (row < L ? X.gpow[0][L - 1 - row] : 0.f) : 1.f;
+        if (DECAY) ks.step(X.gpow[0][L]);
+        const float sc = DECAY ? (row < L ? X.gpow[0][L - 1 - row] / ks.G : 0.f) : 1.f;
         const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
@@ -649,7 +685,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
-            // key weight s_j as a bf16 pair (exactly 1, 0 without a decay)
+            // key weight s_j / G as a bf16 pair (exactly 1, 0 without a decay)
             float sh = 1.f, sl = 0.f;
             if (DECAY) {
                 sh = bf16_round(sc);
@@ -681,10 +717,18 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     auto export_state = [&](int c) -> bool {
         const int cb = c & 1, pb = (c + 1) & 1;
         const int L = min(kC, N - c * kC);
-        // decay: once exported, the state is multiplied in TMEM by gamma^L of
-        // block c+1, before that block's update adds to it (not after the last)
-        const bool rescale = DECAY && c + 1 < nchunks;
-        const float gnext = rescale ? X.gpow[0][min(kC, N - (c + 1) * kC)] : 1.f;
+        // decay: the state after block c is G times the TMEM contents; when
+        // the scale restarts at block c+1, the state is multiplied by gamma^L
+        // of block c+1 over G0 and written back before that block's update
+        const float G = DECAY ? xs.G : 1.f;
+        bool rescale = false;
+        float gnext = 1.f;
+        if (DECAY && c + 1 < nchunks) {
+            const float gL = X.gpow[0][min(kC, N - (c + 1) * kC)];
+            xs.step(gL);
+            rescale = xs.renorm;
+            gnext = gL / xs.G0;
+        }
         if (!wait_warp(&S.st_full, c & 1, g, 51) || !wait_warp(&S.aq_free, c & 1, g, 54))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 4);
@@ -696,6 +740,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             tmem_ld16(tb + lb + kColR + grp * 16, rv0);
             tmem_ld16(tb + lb + kColR + (grp + 1) * 16, rv1);
             tmem_wait_ld();
+            if (DECAY) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    rv0[m] = f2u(u2f(rv0[m]) * G);
+                    rv1[m] = f2u(u2f(rv1[m]) * G);
+                }
+            }
             if (row < D) {
                 export_row_bf16<D, DV>(sRt, row, grp, rv0);
                 export_row_bf16<D, DV>(sRt, row, grp + 1, rv1);
@@ -716,6 +767,14 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             tmem_ld4(tb + lb + kColUV, uv);
             if (DECAY) tmem_ld4(tb + lb + kColUV + 4, uw);
             tmem_wait_ld();
+            if (DECAY) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    zv[m] = f2u(u2f(zv[m]) * G);
+                    uv[m] = f2u(u2f(uv[m]) * G);
+                    uw[m] = f2u(u2f(uw[m]) * G);
+                }
+            }
             const float u = DECAY ? u2f(uv[3]) + u2f(uw[0]) : u2f(uv[0]);
             if (row < D) {
                 S.zeta[row] = u2f(zv[0]);
@@ -729,9 +788,9 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                                    (S.rho_part[cb][2] + S.rho_part[cb][3]);
                 if (DECAY) {   // n and rho decay like the state: x <- gamma^L x + sum_j s_j x_j
                     const float gcur = X.gpow[0][L];
-                    S.n_s[cb] = fmaf(gcur, S.n_s[pb], (X.s_part[cb][0] + X.s_part[cb][1]) +
-                                                          (X.s_part[cb][2] + X.s_part[cb][3]));
-                    S.rho_s[cb] = fmaf(gcur, S.rho_s[pb], rsum);
+                    S.n_s[cb] = fmaf(gcur, S.n_s[pb], G * ((X.s_part[cb][0] + X.s_part[cb][1]) +
+                                                           (X.s_part[cb][2] + X.s_part[cb][3])));
+                    S.rho_s[cb] = fmaf(gcur, S.rho_s[pb], G * rsum);
                 } else {
                     S.n_s[cb] = S.n_s[pb] + (float)L;
                     S.rho_s[cb] = S.rho_s[pb] + rsum;
@@ -830,6 +889,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     // ---- final state S = 1 u^T + R (R read back in fp32), z = n 1 + zeta
     if (!aborted && p.S_out && last_seg) {
         const int lbuf = (nchunks - 1) & 1;
+        const float Gl = DECAY ? xs.G : 1.f;   // the last block's state scale
         tc_fence_after();
 #pragma unroll
         for (int gq = 0; gq < kRGroups; ++gq) {
@@ -842,10 +902,10 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 4)
                     *reinterpret_cast<float4 *>(dst + jj) = make_float4(
-                        u2f(rv[jj]) + S.u[lbuf][grp * 16 + jj],
-                        u2f(rv[jj + 1]) + S.u[lbuf][grp * 16 + jj + 1],
-                        u2f(rv[jj + 2]) + S.u[lbuf][grp * 16 + jj + 2],
-                        u2f(rv[jj + 3]) + S.u[lbuf][grp * 16 + jj + 3]);
+                        fmaf(u2f(rv[jj]), Gl, S.u[lbuf][grp * 16 + jj]),
+                        fmaf(u2f(rv[jj + 1]), Gl, S.u[lbuf][grp * 16 + jj + 1]),
+                        fmaf(u2f(rv[jj + 2]), Gl, S.u[lbuf][grp * 16 + jj + 2]),
+                        fmaf(u2f(rv[jj + 3]), Gl, S.u[lbuf][grp * 16 + jj + 3]));
             }
         }
         if (h == 0 && row < D) p.z_out[(size_t)head * D + row] = S.n_s[lbuf] + S.zeta[row];

@@ -357,9 +357,13 @@ def launches_per_call(mode, w):
         # per-head sum, the query kernel; otherwise two CUDA-core kernels
         return 3 if tc else 2
     if mode == "causal_decay":
-        # tensor-core kernel for the heads it takes, then the CUDA-core kernel
-        # for the rest (its CTAs for the first kind return at once)
-        return 2 if tc else 1
+        # tensor-core kernel for the heads it takes (preceded by the segment
+        # states and their prefix scan when the sequence is split), then the
+        # CUDA-core kernel for the rest (its CTAs for the first kind return)
+        if not tc:
+            return 1
+        split = la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 256
+        return 4 if split else 2
     return 1
 
 
@@ -548,6 +552,27 @@ def run_modes(args, world, dev, peaks, peak_kind):
     del q, k, v, y, ws
     torch.cuda.empty_cache()
 
+    # long-context causal with a per-head decay: few heads, so the sequence is
+    # split (decayed segment states, their decayed prefix scan, chunk kernel)
+    w = WORKLOADS["causal_decay_bf16_b1h32n131072d64"]
+    q, k, v = make_qkv(w, device=dev, gen_device=dev)
+    gam = head_decays(w.H).to(dev)
+    y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+    ws = la.alloc_workspace(la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+    total, per = time_steps(lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y,
+                                                            workspace=ws),
+                            steps, args.warmup, world)
+    T = w.BH * w.N
+    ms = sum(per) / len(per)
+    modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
+                     "l2": "inputs larger than L2",
+                     "kernels_per_call": launches_per_call("causal_decay", w),
+                     "roofline": roofline(T * alg_bytes_per_token_head(w),
+                                          T * decay_flops_per_token_head(w.d, w.dv), ms, peaks,
+                                          peak_kind, load_traffic(w.name))}
+    del q, k, v, y, ws
+    torch.cuda.empty_cache()
+
     # decode with a per-head decay: state from a decayed 1024-token prefill
     w = WORKLOADS["decode_decay_bf16_b256h32d128"]
     gam = head_decays(w.H).to(dev)
@@ -613,16 +638,17 @@ def run_reference(args, world, rank):
 def profile_case(args):
     """A few launches of one kernel on one workload, for ncu captures.
 
-    --profile-case causal|long|noncausal|decode|backward|causal_decay|decode_decay picks the workload
-    (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 / B256 H32 d128
-    decode / gradients at B8 H16 N8192 d128 / the decay variants of the causal
-    and decode workloads); --batch overrides B for a smaller capture.
+    --profile-case causal|long|noncausal|decode|backward|causal_decay|long_decay|decode_decay
+    picks the workload (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 /
+    B256 H32 d128 decode / gradients at B8 H16 N8192 d128 / the decay variants of
+    the causal, long and decode workloads); --batch overrides B for a smaller capture.
     """
     from linear_rnn_sequence_gb300 import linattn as la
     names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
              "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128",
              "backward": "causal_backward_bf16_b8h16n8192d128",
              "causal_decay": "causal_decay_bf16_b8h16n8192d128",
+             "long_decay": "causal_decay_bf16_b1h32n131072d64",
              "decode_decay": "decode_decay_bf16_b256h32d128"}
     w = WORKLOADS[names[args.profile_case]]
     if args.batch:
@@ -646,7 +672,8 @@ def profile_case(args):
         q, k, v = make_qkv(w, device=dev, gen_device=dev)
         y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
         gam = head_decays(w.H).to(dev)
-        fn = lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y)
+        ws = la.alloc_workspace(la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+        fn = lambda: la.forward_causal_decay(q, k, v, gam, eps=w.eps, out=y, workspace=ws)
     elif w.mode == "backward":
         q, k, v, dy = make_backward_inputs(w, device=dev, gen_device=dev)
         outs = (torch.empty(w.B, w.H, w.N, w.d, device=dev),
@@ -687,7 +714,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward",
-                                               "causal_decay", "decode_decay"])
+                                               "causal_decay", "long_decay", "decode_decay"])
     ap.add_argument("--batch", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -189,29 +189,6 @@ __device__ __forceinline__ DecaySmall &decay_area(Small &S) {
     return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
 }
 
-// Decay: the TMEM state (R, zeta, u, r) is held divided by a scale G that
-// shrinks by gamma^L with every block, so a block's update only adds to it
-// (its keys enter multiplied by 1/G) and the export multiplies by G.  When
-// gamma^L G would fall below 2^-48, the state is instead rescaled in TMEM
-// before the block and G restarts at G0.  G0 = 3/4 (1 when gamma = 1): the
-// first keys after a restart then carry scales near 4/3 rather than just
-// above 1, where bf16(scale * x) would round most bf16 values x back to x and
-// drop the scale from their psi part in the same direction for every
-// feature.  Each role steps its own copy through the blocks in order; the
-// copies agree bit for bit.
-struct DecayScale {
-    float G0;              // restart value
-    float G;               // scale of the state after the current block
-    bool renorm = false;   // the state is rescaled in TMEM before the current block
-    __device__ __forceinline__ explicit DecayScale(float gamma)
-        : G0(gamma == 1.f ? 1.f : 0.75f), G(G0) {}
-    __device__ __forceinline__ void step(float gL) {
-        const float cand = gL * G;
-        renorm = cand < 0x1p-48f;
-        G = renorm ? G0 : cand;
-    }
-};
-
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
 __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
@@ -1006,15 +983,17 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 
 // ------------------------------------------------------------------ segment prefix scan
 // Exclusive prefix over the segments of each head, in a fixed order:
-// P_0 = S_in (or 0), P_s = P_{s-1} + S_{s-1}; the same for z.  One thread per
-// state element (grid: heads x element blocks); the segment loop issues its
-// loads ahead of the running sum.
+// P_0 = S_in (or 0), P_s = f P_{s-1} + S_{s-1}; the same for z.  f = 1, or
+// with a per-head decay gamma^(segment length) (every segment but the last,
+// which no prefix uses, has the same length).  One thread per state element
+// (grid: heads x element blocks); the segment loop issues its loads ahead of
+// the running sum.
 constexpr int kScanThreads = 128;
 __global__ void __launch_bounds__(kScanThreads)
 scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_seg,
                    float *__restrict__ S_pre, float *__restrict__ z_pre,
                    const float *__restrict__ S_in, const float *__restrict__ z_in, int nseg,
-                   int D, int DV)
+                   int D, int DV, const float *__restrict__ gamma, int H, int seg_len)
 {
     griddep_launch_dependents();
     griddep_wait();   // S_seg, z_seg come from the state pass
@@ -1030,19 +1009,20 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
     float acc = 0.f;
     if (isS && S_in) acc = S_in[(size_t)head * nS + o];
     if (!isS && z_in) acc = z_in[(size_t)head * D + o];
+    const float f = gamma ? powf(gamma[head % H], (float)seg_len) : 1.f;
     const size_t base = (size_t)head * nseg * stride + o;
     int sg = 0;
     for (; sg + 4 <= nseg; sg += 4) {
         const float s0 = src[base + (sg + 0) * stride], s1 = src[base + (sg + 1) * stride];
         const float s2 = src[base + (sg + 2) * stride], s3 = src[base + (sg + 3) * stride];
-        dst[base + (sg + 0) * stride] = acc; acc += s0;
-        dst[base + (sg + 1) * stride] = acc; acc += s1;
-        dst[base + (sg + 2) * stride] = acc; acc += s2;
-        dst[base + (sg + 3) * stride] = acc; acc += s3;
+        dst[base + (sg + 0) * stride] = acc; acc = fmaf(f, acc, s0);
+        dst[base + (sg + 1) * stride] = acc; acc = fmaf(f, acc, s1);
+        dst[base + (sg + 2) * stride] = acc; acc = fmaf(f, acc, s2);
+        dst[base + (sg + 3) * stride] = acc; acc = fmaf(f, acc, s3);
     }
     for (; sg < nseg; ++sg) {
         dst[base + sg * stride] = acc;
-        acc += src[base + sg * stride];
+        acc = fmaf(f, acc, src[base + sg * stride]);
     }
 }
 
@@ -1090,9 +1070,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.S_out = a.S_out;
     p.z_out = a.z_out;
     choose_segments(BH, a.N, p.nseg, p.seg_chunks);
-    if (DECAY) {   // one work item per head: the segment pass has no decay
-        p.nseg = 1;
-        p.seg_chunks = a.N > kC ? (a.N + kC - 1) / kC : 1;
+    if (DECAY) {
         p.gamma = a.gamma;
         p.H = a.H;
     }
@@ -1103,7 +1081,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
     p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
-    if (!DECAY && p.nseg > 1) {
+    if (p.nseg > 1) {
         // segment states, then their exclusive prefixes, which become the
         // initial states of the (head, segment) items
         const size_t nS = (size_t)D * DV, cnt = (size_t)items;
@@ -1111,8 +1089,8 @@ cudaError_t launch_dv(const FwdArgs &a) {
         float *z_seg = S_seg + cnt * nS;
         float *S_pre = z_seg + cnt * D;
         float *z_pre = S_pre + cnt * nS;
-        using SL = StateLayout<D, DV>;
-        auto skern = causal_state_kernel<D, DV>;
+        using SL = StateLayout<D, DV, DECAY>;
+        auto skern = causal_state_kernel<D, DV, DECAY>;
         cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::request);
         if (e != cudaSuccess) return e;
@@ -1121,7 +1099,8 @@ cudaError_t launch_dv(const FwdArgs &a) {
         const dim3 sgrid(BH, (D * DV + D + kScanThreads - 1) / kScanThreads);
         e = launch_overlapped(scan_states_kernel, sgrid, dim3(kScanThreads), 0, a.stream,
                               (const float *)S_seg, (const float *)z_seg, S_pre, z_pre, a.S_in,
-                              a.z_in, p.nseg, D, DV);
+                              a.z_in, p.nseg, D, DV, DECAY ? a.gamma : (const float *)nullptr,
+                              a.H, p.seg_chunks * kC);
         if (e != cudaSuccess) return e;
         p.S_in = S_pre;
         p.z_in = z_pre;
@@ -1130,7 +1109,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::request);
     if (e != cudaSuccess) return e;
-    if (!DECAY && p.nseg > 1)
+    if (p.nseg > 1)
         return launch_overlapped(kern, dim3(items), dim3(kThreads), Lay::request, a.stream, qm, km,
                                  vm, p);
     kern<<<items, kThreads, Lay::request, a.stream>>>(qm, km, vm, p);

@@ -39,6 +39,31 @@ struct TcParams {
     int H;
 };
 
+// Decay: the TMEM state (the causal kernel's R, zeta, u, r; the segment
+// sums of the state pass) is held divided by a scale G that
+// shrinks by gamma^L with every block, so a block's update only adds to it
+// (its keys enter multiplied by 1/G) and the export multiplies by G.  When
+// gamma^L G would fall below 2^-48, the state is instead rescaled in TMEM
+// before the block and G restarts at G0.  G0 = 3/4 (1 when gamma = 1): the
+// first keys after a restart then carry scales near 4/3 rather than just
+// above 1, where bf16(scale * x) would round most bf16 values x back to x and
+// drop the scale from their psi part in the same direction for every
+// feature.  Each role steps its own copy through the blocks in order; the
+// copies agree bit for bit.
+struct DecayScale {
+    float G0;              // restart value
+    float G;               // scale of the state after the current block
+    bool renorm = false;   // the state is rescaled in TMEM before the current block
+    __device__ __forceinline__ explicit DecayScale(float gamma)
+        : G0(gamma == 1.f ? 1.f : 0.75f), G(G0) {}
+    __device__ __forceinline__ void step(float gL) {
+        const float cand = gL * G;
+        renorm = cand < 0x1p-48f;
+        G = renorm ? G0 : cand;
+    }
+};
+
+
 // Packed fp32 pairs (two floats in one 64-bit register; the f32x2 arithmetic
 // of sm_100 and later does both lanes in one instruction).
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {

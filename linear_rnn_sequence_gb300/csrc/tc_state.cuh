@@ -21,20 +21,29 @@ namespace {
 // The state pass reuses the split form of the main kernel: R = psi(K)^T V,
 // zeta = psi(K)^T 1 and u = V^T 1 accumulate in TMEM, and the plain state is
 // S = 1 u^T + R, z = n 1 + zeta.
+// With a per-head decay (DECAY) the segment's state is the decayed sum
+// S_s = sum_j gamma^(end-1-j) phi(k_j) v_j^T (z alike), as the causal
+// kernel's: key j of a block of L tokens carries s_j = gamma^(L-1-j), the
+// TMEM sums are held divided by a running scale G that shrinks by gamma^L per
+// block (keys enter multiplied by s_j / G; the export multiplies by G), and
+// they are rescaled in TMEM only when G would fall below 2^-48.
 constexpr int kStateThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 psi(k) / export
 constexpr uint32_t kStColR = 0, kStColZ = 128, kStColU = 144, kStTmemCols = 256;
 
-template <int D, int DV>
+template <int D, int DV, bool DECAY = false>
 struct StateLayout {
     static constexpr int kK = kC * D * 2;
     static constexpr int kV = kC * DV * 2;
-    static constexpr int kOnes = 16 * kC * 2;      // [16 x C] operand, row 0 = ones
+    // [16 x C] operand, row 0 = ones; with a decay one per stage, rows 1, 2 =
+    // the block's key weights s_j / G as bf16 hi, lo
+    static constexpr int kOnes = 16 * kC * 2;
     static constexpr int oK = 0;                   // 2 stages
     static constexpr int oV = oK + 2 * kK;         // 2 stages
     static constexpr int oOnes = oV + 2 * kV;
-    static constexpr int oPad = oOnes + kOnes;     // 16 KB the padded M = 128 operands may touch
+    static constexpr int oPad = oOnes + (DECAY ? 2 : 1) * kOnes;   // 16 KB the padded M = 128 operands may touch
     static constexpr int oSmall = oPad + 16384;
-    static constexpr int bytes = oSmall + 2048;
+    static constexpr int oDecay = oSmall + 2048;   // decay only: StateDecay
+    static constexpr int bytes = oDecay + (DECAY ? 1024 : 0);
     static constexpr int request = bytes + 1024;
 };
 
@@ -44,17 +53,25 @@ struct StateSmall {
     uint32_t tmem_base;
     int abort_flag;
 };
+static_assert(sizeof(StateSmall) <= 2048, "state small area");
 
-template <int D, int DV>
+struct StateDecay {
+    alignas(16) float gpow[kC + 1];   // gamma^m
+    alignas(16) float n_part[4];      // per-warp sums of the decayed token counts
+};
+static_assert(sizeof(StateDecay) <= 1024, "state decay area");
+
+template <int D, int DV, bool DECAY = false>
 __global__ void __launch_bounds__(kStateThreads)
 causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const TcParams p, float *__restrict__ S_seg, float *__restrict__ z_seg)
 {
-    using Lay = StateLayout<D, DV>;
+    using Lay = StateLayout<D, DV, DECAY>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
     StateSmall &S = *reinterpret_cast<StateSmall *>(sm + Lay::oSmall);
+    StateDecay &X = *reinterpret_cast<StateDecay *>(sm + Lay::oDecay);   // DECAY only
     uint8_t *sK = sm + Lay::oK, *sV = sm + Lay::oV, *sOnes = sm + Lay::oOnes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item = blockIdx.x;
@@ -79,6 +96,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
     }
+    if (DECAY && tid < kC + 1) X.gpow[tid] = powf(p.gamma[head % p.H], (float)tid);
     if (warp == 1) {
         tmem_alloc(&S.tmem_base, kStTmemCols);
         tmem_relinquish();
@@ -110,7 +128,6 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         if (lane == 0) {   // MMA: R += psi(K)^T V, zeta += psi(K)^T 1, u += V^T 1
             constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);
             constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);
-            const uint32_t ob = smem_u32(sOnes);
             bool ok = mbar_wait(&S.init_done, 0, g, 61);
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int s = c & 1;
@@ -118,6 +135,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 63)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
+                const uint32_t ob = smem_u32(sOnes + (DECAY ? s * Lay::kOnes : 0));
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
@@ -135,11 +153,11 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     } else {
         const int wq = warp & 3, row = wq * 32 + lane, wtid = tid - 64;
         const uint32_t lb = (uint32_t)(wq * 32) << 16;
-        // ones operand (row 0 = 1, rows 1..15 = 0) and a zeroed pad region
-        for (int e = wtid; e < 16 * kC; e += kWG) {
-            const int n = e / kC, k = e % kC;
-            *reinterpret_cast<__nv_bfloat16 *>(sOnes + (n >> 3) * 2048 + (k >> 3) * 128 +
-                                               (n & 7) * 16 + (k & 7) * 2) =
+        // ones operand(s) (row 0 = 1, rows 1..15 = 0) and a zeroed pad region
+        for (int e = wtid; e < (DECAY ? 2 : 1) * 16 * kC; e += kWG) {
+            const int st = e / (16 * kC), n = (e / kC) % 16, k = e % kC;
+            *reinterpret_cast<__nv_bfloat16 *>(sOnes + st * Lay::kOnes + (n >> 3) * 2048 +
+                                               (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
                 __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
         }
         for (int e = wtid; e < 16384 / 16; e += kWG)
@@ -158,8 +176,37 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         tc_fence_before();
         mbar_arrive(&S.init_done);
         bool ok = true;
+        DecayScale ks(DECAY ? X.gpow[1] : 1.f);   // X.gpow[1] = gamma
+        float nrow = 0.f;   // decay: this token row's share of the decayed count, over G
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
+            const int L = min(kC, nloc - c * kC);
+            float sc = 1.f;
+            if (DECAY) {
+                const float Gp = ks.G, gL = X.gpow[L];
+                ks.step(gL);
+                nrow *= gL * Gp / ks.G;   // the count is carried over the new scale too
+                if (ks.renorm && c > 0) {
+                    // the previous block's MMAs must be done before the sums are rescaled
+                    ok = wait_warp(&S.kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1, g, 66);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float f = gL * Gp / ks.G0;
+#pragma unroll 1
+                    for (int grp = 0; grp < DV / 16 + 2; ++grp) {
+                        const uint32_t col = grp < DV / 16 ? kStColR + grp * 16
+                                                           : (grp == DV / 16 ? kStColZ : kStColU);
+                        uint32_t rv[16];
+                        tmem_ld16(tb + lb + col, rv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) rv[m] = f2u(u2f(rv[m]) * f);
+                        tmem_st16(tb + lb + col, rv);
+                    }
+                    tmem_wait_st();
+                }
+                sc = row < L ? X.gpow[L - 1 - row] / ks.G : 0.f;
+            }
             ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 64);
             if (!ok) break;
             uint8_t *kt = sK + s * Lay::kK;
@@ -174,7 +221,8 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 for (int f = 0; f < 8; ++f) {
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) w[h] = psi_bf16x2(w[h]);
+                    for (int h = 0; h < 4; ++h)
+                        w[h] = DECAY ? psi_scaled_bf16x2(w[h], sc) : psi_bf16x2(w[h]);
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
 #pragma unroll
@@ -182,7 +230,15 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                     *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
                                                sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
             }
+            if (DECAY) {   // key weight s_j / G as a bf16 pair in rows 1, 2 of the ones operand
+                const float sh = bf16_round(sc), sl = bf16_round(sc - sh);
+                uint8_t *op = sOnes + s * Lay::kOnes + (row >> 3) * 128 + (row & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(op + 16) = __float2bfloat16_rn(sh);
+                *reinterpret_cast<__nv_bfloat16 *>(op + 32) = __float2bfloat16_rn(sl);
+                nrow += sh + sl;
+            }
             fence_proxy_async();
+            if (DECAY) tc_fence_before();   // after a rescale of the TMEM sums
             mbar_arrive(&S.phik_done[s]);
         }
         ok = ok && wait_warp(&S.st_done, 0, g, 65);
@@ -192,7 +248,13 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             tmem_ld4(tb + lb + kStColZ, zv);
             tmem_ld4(tb + lb + kStColU, uv);
             tmem_wait_ld();
-            S.u[row] = u2f(uv[0]);
+            // decay: the sums are held over G; u = v^T [s_hi + s_lo] (columns 1, 2)
+            const float G = DECAY ? ks.G : 1.f;
+            S.u[row] = DECAY ? G * (u2f(uv[1]) + u2f(uv[2])) : u2f(uv[0]);
+            if (DECAY) {
+                const float ns = warp_sum_f(nrow);
+                if (lane == 0) X.n_part[wq] = ns;
+            }
             named_bar(kBarA, kWG);
             float *dst = S_seg + (size_t)item * D * DV;
 #pragma unroll 1
@@ -204,12 +266,14 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4)
                         *reinterpret_cast<float4 *>(dst + (size_t)row * DV + grp * 16 + jj) =
-                            make_float4(u2f(rv[jj]) + S.u[grp * 16 + jj],
-                                        u2f(rv[jj + 1]) + S.u[grp * 16 + jj + 1],
-                                        u2f(rv[jj + 2]) + S.u[grp * 16 + jj + 2],
-                                        u2f(rv[jj + 3]) + S.u[grp * 16 + jj + 3]);
+                            make_float4(fmaf(u2f(rv[jj]), G, S.u[grp * 16 + jj]),
+                                        fmaf(u2f(rv[jj + 1]), G, S.u[grp * 16 + jj + 1]),
+                                        fmaf(u2f(rv[jj + 2]), G, S.u[grp * 16 + jj + 2]),
+                                        fmaf(u2f(rv[jj + 3]), G, S.u[grp * 16 + jj + 3]));
             }
-            if (row < D) z_seg[(size_t)item * D + row] = (float)nloc + u2f(zv[0]);
+            const float n = DECAY ? G * ((X.n_part[0] + X.n_part[1]) + (X.n_part[2] + X.n_part[3]))
+                                  : (float)nloc;
+            if (row < D) z_seg[(size_t)item * D + row] = fmaf(u2f(zv[0]), G, n);
         }
     }
     tc_fence_before();

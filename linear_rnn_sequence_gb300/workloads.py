@@ -70,6 +70,10 @@ WORKLOADS = {
     "causal_decay_bf16_b8h16n8192d128": Workload("causal_decay_bf16_b8h16n8192d128",
                                                  "causal_decay", 8, 16, 8192, 128, 128,
                                                  torch.bfloat16, 1.0 / math.sqrt(128)),
+    # long-context causal with a per-head decay (few heads: the sequence is split).
+    "causal_decay_bf16_b1h32n131072d64": Workload("causal_decay_bf16_b1h32n131072d64",
+                                                  "causal_decay", 1, 32, 131072, 64, 64,
+                                                  torch.bfloat16, 1.0 / math.sqrt(64)),
     # recurrent decode with a per-head decay from a 1024-token prefill.
     "decode_decay_bf16_b256h32d128": Workload("decode_decay_bf16_b256h32d128", "decode_decay",
                                               256, 32, 1024, 128, 128, torch.bfloat16, 1.0,

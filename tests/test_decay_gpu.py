@@ -99,6 +99,72 @@ def test_causal_decay_routes_each_head(d, dv, cuda_device):
             assert err <= tol, f"head {h} (gamma {float(gam[h])}) {name}: {err:.3e}"
 
 
+def test_causal_decay_long_sequence_state(cuda_device):
+    """33 blocks with an initial state: the tensor-core kernel restarts its
+    state scale every block (gamma 0.72), every few blocks (0.9, 0.97) or
+    never (0.9995); y on whole heads, and the final S and z, against the
+    oracle."""
+    B, H, N, d, dv = 1, 4, 4099, 64, 128
+    gam = torch.tensor([0.72, 0.9, 0.97, 0.9995])
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=d ** -0.5, seed=41)
+    qp, kp, vp = random_qkv(B, H, 64, d, dv, dtype=torch.bfloat16, scale=0.3, seed=42)
+    _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    y, S, z = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                      gam.to(cuda_device), S_in=dev(S_in), z_in=dev(z_in),
+                                      return_state=True, check_status=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.causal_recurrent_decay(q, k, v, gam, S_in=S_in, z_in=z_in,
+                                               return_state=True)
+    for h in range(H):
+        for name, g, w in (("y", y[:, h], yo[:, h]), ("S", S[:, h], So[:, h]),
+                           ("z", z[:, h], zo[:, h])):
+            err = rel_max_err(g, w)
+            assert err <= TOL_BF16, f"head {h} (gamma {float(gam[h])}) {name}: {err:.3e}"
+
+
+@pytest.mark.parametrize("B,H,N,d,dv,gammas", [
+    (1, 2, 20000, 64, 64, (0.72, 0.99)),            # 157 segments of one block each
+    (1, 3, 5000, 128, 64, (0.9, 0.999, 1.0)),
+    (2, 2, 3333, 64, 128, (0.97, 0.9995)),
+])
+def test_causal_decay_split_sequence(B, H, N, d, dv, gammas, cuda_device):
+    """Few heads: the sequence is cut into segments, whose decayed states
+    and decayed prefixes seed the chunk kernel.  Whole heads against the
+    oracle, with an initial and a final state."""
+    gam = torch.tensor(gammas)
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=d ** -0.5, seed=N)
+    qp, kp, vp = random_qkv(B, H, 64, d, dv, dtype=torch.bfloat16, scale=0.3, seed=7)
+    _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    assert la.causal_workspace_bytes(B, H, N, d, dv) > 256   # segment states: split
+    y, S, z = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                      gam.to(cuda_device), S_in=dev(S_in), z_in=dev(z_in),
+                                      return_state=True, check_status=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.causal_recurrent_decay(q, k, v, gam, S_in=S_in, z_in=z_in,
+                                               return_state=True)
+    for h in range(H):
+        for name, g, w in (("y", y[:, h], yo[:, h]), ("S", S[:, h], So[:, h]),
+                           ("z", z[:, h], zo[:, h])):
+            err = rel_max_err(g, w)
+            assert err <= TOL_BF16, f"head {h} (gamma {float(gam[h])}) {name}: {err:.3e}"
+
+
+def test_causal_decay_long_workload_sampled_heads(cuda_device):
+    """Full-size long-context shape with decay (B1 H32 N131072 d64, split into
+    segments): whole heads against the oracle."""
+    w = WORKLOADS["causal_decay_bf16_b1h32n131072d64"]
+    q, k, v = make_qkv(w, device=cuda_device, gen_device=cuda_device)
+    gam = head_decays(w.H)
+    y = la.forward_causal_decay(q, k, v, gam.to(cuda_device), check_status=True)
+    torch.cuda.synchronize()
+    for h in (0, 13, 31):
+        yo = oracle.causal_recurrent_decay(q[0, h][None].cpu(), k[0, h][None].cpu(),
+                                           v[0, h][None].cpu(), gam[h:h + 1])
+        assert rel_max_err(y[0, h], yo[0]) <= tol_decay(w.dtype, w.d, w.dv, gam[h])
+
+
 def test_causal_decay_gamma_one_is_the_plain_kernel(cuda_device):
     """gamma = 1 on the tensor cores: every key weight is 1 and every
     rescaling factor is 1 exactly, so the output and final state equal the

@@ -139,9 +139,11 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
  * bf16 inputs with d, dv in {64, 128}: heads with gamma in [2^-1/2, 1] run on
  * the tensor cores, 128-token blocks as in la_forward_causal with key j of a
  * block of L tokens weighted by gamma^(L-1-j), the block's weights by
- * gamma^-L, and the carried state multiplied by gamma^L per block (same
- * precision scheme and bound as la_forward_causal); a second kernel then
- * computes the other heads on the CUDA cores.  Otherwise (float32 inputs,
+ * gamma^-L, and the carried state decayed by gamma^L per block (same
+ * precision scheme and bound as la_forward_causal; long sequences with few
+ * heads are split into segments the same way, with decayed segment states
+ * and prefixes); a second kernel then computes the other heads on the CUDA
+ * cores.  Otherwise (float32 inputs,
  * d or dv = 32) every head runs on the CUDA cores, token by token in fp32.
  * The split needs no host read of gamma.  NULL gamma: LA_ERR_INVALID_ARG.
  */

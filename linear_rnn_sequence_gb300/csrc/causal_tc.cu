@@ -491,7 +491,7 @@ template <int D, int DV, bool DECAY>
 __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
                                              uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
                                              uint8_t *sYB, uint8_t *sZB,
-                                             const TcParams &p, int head, int item,
+                                             const TcParams &p, int head, int slot,
                                              int tok0, int nloc, bool last_seg, int nchunks,
                                              const Guard &g) {
     using Lay = Layout<D, DV>;
@@ -537,8 +537,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     {
         // initial state of this work item: the caller's state for a whole
         // head, or the exclusive prefix of this segment
-        const float *Sin = p.S_in ? p.S_in + (size_t)item * D * DV : nullptr;
-        const float *zin = p.z_in ? p.z_in + (size_t)item * D : nullptr;
+        const float *Sin = p.S_in ? p.S_in + (size_t)slot * D * DV : nullptr;
+        const float *zin = p.z_in ? p.z_in + (size_t)slot * D : nullptr;
         // decay: the initial state enters TMEM divided by G0, and already
         // multiplied by gamma^L of block 0 when the scale restarts there
         if (DECAY) xs.step(X.gpow[0][min(kC, N)]);
@@ -906,11 +906,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     uint8_t *sGB = sm + Lay::oGB, *sYB = sm + Lay::oYB, *sZB = sm + Lay::oZB;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // work item = (head, segment of seg_chunks blocks)
+    // work item = (head, segment of seg_chunks blocks); slot: the index of
+    // its initial state
     const int item = blockIdx.x;
     const int head = item / p.nseg, seg = item - head * p.nseg;
-    const int tok0 = seg * p.seg_chunks * kC;
-    const int nloc = min(p.N - tok0, p.seg_chunks * kC);
+    const int slot = item;
+    int tok0, nloc;
+    segment_range(p, seg, tok0, nloc);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
     if (tid == 0) LA_TRACE_POINT(0, 15);
@@ -970,7 +972,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     } else if (warp < kWarpB) {
         group_a_role<D, DV, DECAY>(S, tb, sQ, nchunks, nloc, g);
     } else {
-        group_b_role<D, DV, DECAY>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, item, tok0,
+        group_b_role<D, DV, DECAY>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, slot, tok0,
                                    nloc, seg == p.nseg - 1, nchunks, g);
     }
     tc_fence_before();
@@ -984,10 +986,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 // ------------------------------------------------------------------ segment prefix scan
 // Exclusive prefix over the segments of each head, in a fixed order:
 // P_0 = S_in (or 0), P_s = f P_{s-1} + S_{s-1}; the same for z.  f = 1, or
-// with a per-head decay gamma^(segment length) (every segment but the last,
-// which no prefix uses, has the same length).  One thread per state element
-// (grid: heads x element blocks); the segment loop issues its loads ahead of
-// the running sum.
+// with a per-head decay gamma^(segment length): every segment but the last
+// has the same length (seg_len), and the last one's state is neither used
+// nor computed.  One thread per state element (grid: heads x element
+// blocks); the segment loop issues its loads ahead of the running sum.
 constexpr int kScanThreads = 128;
 __global__ void __launch_bounds__(kScanThreads)
 scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_seg,
@@ -1012,7 +1014,7 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
     const float f = gamma ? powf(gamma[head % H], (float)seg_len) : 1.f;
     const size_t base = (size_t)head * nseg * stride + o;
     int sg = 0;
-    for (; sg + 4 <= nseg; sg += 4) {
+    for (; sg + 4 <= nseg - 1; sg += 4) {
         const float s0 = src[base + (sg + 0) * stride], s1 = src[base + (sg + 1) * stride];
         const float s2 = src[base + (sg + 2) * stride], s3 = src[base + (sg + 3) * stride];
         dst[base + (sg + 0) * stride] = acc; acc = fmaf(f, acc, s0);
@@ -1020,15 +1022,18 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
         dst[base + (sg + 2) * stride] = acc; acc = fmaf(f, acc, s2);
         dst[base + (sg + 3) * stride] = acc; acc = fmaf(f, acc, s3);
     }
-    for (; sg < nseg; ++sg) {
+    for (; sg < nseg - 1; ++sg) {
         dst[base + sg * stride] = acc;
         acc = fmaf(f, acc, src[base + sg * stride]);
     }
+    dst[base + (size_t)(nseg - 1) * stride] = acc;
 }
 
 // ------------------------------------------------------------------ host side
 // Split the sequence only when the heads alone leave SMs idle: then aim for
 // about four waves of (head, segment) items, at least one block per segment.
+// (A short-then-long split of one wave of heads, to fill the SMs it leaves
+// idle, measured slower on B8 H16 N8192 and is not used.)
 void choose_segments(int BH, int N, int &nseg, int &seg_chunks) {
     const int nch = (N + kC - 1) / kC;
     const int sms = num_sms();
@@ -1082,9 +1087,10 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
     if (p.nseg > 1) {
-        // segment states, then their exclusive prefixes, which become the
-        // initial states of the (head, segment) items
+        // states of every segment but each head's last, then their exclusive
+        // prefixes, which become the initial states of the (head, segment) items
         const size_t nS = (size_t)D * DV, cnt = (size_t)items;
+        p.state_segs = p.nseg - 1;
         float *S_seg = reinterpret_cast<float *>(static_cast<char *>(a.ws) + sizeof(WsHeader));
         float *z_seg = S_seg + cnt * nS;
         float *S_pre = z_seg + cnt * D;
@@ -1094,7 +1100,8 @@ cudaError_t launch_dv(const FwdArgs &a) {
         cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::request);
         if (e != cudaSuccess) return e;
-        skern<<<items, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg, z_seg);
+        skern<<<BH * p.state_segs, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg,
+                                                                             z_seg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const dim3 sgrid(BH, (D * DV + D + kScanThreads - 1) / kScanThreads);
         e = launch_overlapped(scan_states_kernel, sgrid, dim3(kScanThreads), 0, a.stream,

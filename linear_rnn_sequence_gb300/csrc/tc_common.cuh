@@ -37,7 +37,14 @@ struct TcParams {
     int drop_item;                 // test hook: this item's first K/V copy is never issued (-1: off)
     const float *gamma;            // per-head decay [H] (causal kernel with DECAY only)
     int H;
+    int state_segs;                // segments per head the state pass reduces (0: all)
 };
+
+// Token range of segment seg of a head (segments of seg_chunks blocks).
+__device__ __forceinline__ void segment_range(const TcParams &p, int seg, int &tok0, int &nloc) {
+    tok0 = seg * p.seg_chunks * kC;
+    nloc = min(p.N - tok0, p.seg_chunks * kC);
+}
 
 // Decay: the TMEM state (the causal kernel's R, zeta, u, r; the segment
 // sums of the state pass) is held divided by a scale G that

@@ -74,10 +74,15 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     StateDecay &X = *reinterpret_cast<StateDecay *>(sm + Lay::oDecay);   // DECAY only
     uint8_t *sK = sm + Lay::oK, *sV = sm + Lay::oV, *sOnes = sm + Lay::oOnes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // work item = (head, segment) over the segments this pass reduces (the
+    // causal split needs all but the last); its state goes to slot
+    // head * nseg + seg
     const int item = blockIdx.x;
-    const int head = item / p.nseg, seg = item - head * p.nseg;
-    const int tok0 = seg * p.seg_chunks * kC;
-    const int nloc = min(p.N - tok0, p.seg_chunks * kC);
+    const int nss = p.state_segs > 0 ? p.state_segs : p.nseg;
+    const int head = item / nss, seg = item - head * nss;
+    const int slot = head * p.nseg + seg;
+    int tok0, nloc;
+    segment_range(p, seg, tok0, nloc);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
     // reads only K and V: the consumer of S_seg waits for this whole grid
@@ -256,7 +261,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 if (lane == 0) X.n_part[wq] = ns;
             }
             named_bar(kBarA, kWG);
-            float *dst = S_seg + (size_t)item * D * DV;
+            float *dst = S_seg + (size_t)slot * D * DV;
 #pragma unroll 1
             for (int grp = 0; grp < DV / 16; ++grp) {
                 uint32_t rv[16];
@@ -273,7 +278,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             }
             const float n = DECAY ? G * ((X.n_part[0] + X.n_part[1]) + (X.n_part[2] + X.n_part[3]))
                                   : (float)nloc;
-            if (row < D) z_seg[(size_t)item * D + row] = fmaf(u2f(zv[0]), G, n);
+            if (row < D) z_seg[(size_t)slot * D + row] = fmaf(u2f(zv[0]), G, n);
         }
     }
     tc_fence_before();

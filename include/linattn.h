@@ -84,8 +84,8 @@ LA_API const char *la_status_string(la_status s);
 LA_API const char *la_version(void);
 
 /*
- * Workspace size in bytes for la_forward_causal with these sizes (0 when the
- * chosen kernels need none).  The workspace holds a small header (run-time
+ * Workspace size in bytes for la_forward_causal and la_forward_causal_decay
+ * with these sizes (0 when the chosen kernels need none).  The workspace holds a small header (run-time
  * status) and, when the heads alone cannot fill the GPU, the per-segment
  * states and their prefixes for the sequence-axis split ("Entrenamiento:
  * forma paralela": cumulative sums by a prefix scan).  The split depends on
@@ -133,9 +133,9 @@ LA_API la_status la_forward_causal(const void *q, const void *k, const void *v, 
  * array of H floats in [0, 1], 4-byte aligned, shared by the B batch rows;
  * its values are not checked (a value outside [0, 1] gives a meaningless
  * result, not an error).  Arguments, layouts, the initial / final state and
- * the workspace (size: la_causal_workspace_bytes; only its 256-byte status
- * header is used, and it may be NULL when that size is 0) as in
- * la_forward_causal.
+ * the workspace (size: la_causal_workspace_bytes; its status header and, for
+ * split sequences, the decayed segment states and their prefixes; NULL when
+ * that size is 0) as in la_forward_causal.
  * bf16 inputs with d, dv in {64, 128}: heads with gamma in [2^-1/2, 1] run on
  * the tensor cores, 128-token blocks as in la_forward_causal with key j of a
  * block of L tokens weighted by gamma^(L-1-j), the block's weights by

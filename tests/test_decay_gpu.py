@@ -192,6 +192,27 @@ def test_decay_limits(cuda_device):
     assert rel_max_err(y0, v.double().numpy()) <= 1e-6
 
 
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 256, 257])
+def test_causal_decay_edge_lengths(N, cuda_device):
+    """Block edges on the tensor cores: a single token, a block exactly full,
+    one token into the next block; with an initial and a final state."""
+    B, H, d, dv = 1, 3, 64, 128
+    gam = torch.tensor([0.75, 0.97, 1.0])
+    q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=0.3, seed=50 + N)
+    qp, kp, vp = random_qkv(B, H, 20, d, dv, dtype=torch.bfloat16, scale=0.3, seed=9)
+    _, S_in, z_in = oracle.causal_recurrent_decay(qp, kp, vp, gam, return_state=True)
+    dev = lambda t: torch.as_tensor(t, dtype=torch.float32).to(cuda_device)
+    y, S, z = la.forward_causal_decay(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                                      gam.to(cuda_device), S_in=dev(S_in), z_in=dev(z_in),
+                                      return_state=True, check_status=True)
+    torch.cuda.synchronize()
+    yo, So, zo = oracle.causal_recurrent_decay(q, k, v, gam, S_in=S_in, z_in=z_in,
+                                               return_state=True)
+    for name, g, w in (("y", y, yo), ("S", S, So), ("z", z, zo)):
+        err = rel_max_err(g, w)
+        assert err <= TOL_BF16, f"{name}: {err:.3e}"
+
+
 def test_decay_empty_sequence_copies_state(cuda_device):
     S_in = torch.randn(1, 2, 64, 64, device=cuda_device)
     z_in = torch.rand(1, 2, 64, device=cuda_device) + 1

@@ -289,13 +289,24 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v, flo
  * call); make that first call before any stream capture begins.  All calls
  * share the array and leave their partial sums in it: calls that can overlap
  * on the GPU (different streams, different host threads) race and must be
- * ordered by the caller.
+ * ordered by the caller.  A bounded wait that runs out at run time is
+ * recorded in the array's status word, which la_noalloc_status reads.
  */
 #define LA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 LA_API la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v,
                                               float *y, int B, int H, int N, int d, int dv,
                                               la_dtype dt, float eps, float *S_out, float *z_out,
                                               void *stream);
+
+/*
+ * Synchronise `stream` and report the run-time status that the last
+ * la_forward_noncausal_noalloc call on the current device recorded in the
+ * library's scratch array: LA_OK, or LA_ERR_TIMEOUT when one of its bounded
+ * waits ran out (its outputs are then undefined).  The next such call clears
+ * the record.  No counterpart on the pages; it exists because callers of the
+ * no-allocation entry point hold no pointer to its scratch.  Allocates nothing.
+ */
+LA_API la_status la_noalloc_status(void *stream);
 
 /*
  * Synchronise `stream` and report the run-time status recorded in a
@@ -320,6 +331,18 @@ LA_API la_status la_workspace_status(const void *workspace, size_t workspace_byt
  * (-1, 0) to turn the hook off.
  */
 LA_API void la_debug_set_fault(int drop_load_item, long long wait_limit_ns);
+
+/*
+ * Test hook (no counterpart on the pages): writes to out[i] (bf16) the
+ * feature residual that the tensor-core kernels feed to the MMAs for the bf16
+ * input x[i]: phi(x) - c rounded to bf16, phi(x) = elu(x) + 1 ("Mapas de
+ * características"); c = 1 gives elu(x) itself.  x and out are DEVICE arrays
+ * of n bfloat16 values (2-byte aligned, not overlapping); c must lie in
+ * [0, 1] (the kernels use bf16 values of c), else LA_ERR_INVALID_ARG.
+ * Enqueued on `stream`.
+ */
+LA_API la_status la_debug_feature_bf16(const void *x, void *out, long long n, float c,
+                                       void *stream);
 
 #ifdef __cplusplus
 }

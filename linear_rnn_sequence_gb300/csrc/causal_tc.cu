@@ -9,24 +9,28 @@
 // then S_prev += sum_{j in c} phi(k_j) v_j^T and z_prev += sum_{j in c} phi(k_j)
 // (the state recursion of "Forma recurrente e inferencia autorregresiva").
 //
-// Precision scheme.  With phi(x) = 1 + psi(x), psi = elu, every phi is close
-// to 1 for inputs of order 1/sqrt(d), so w_ij ~ d with small variations and
-// the output is a near-uniform average; bf16 operands holding phi itself
-// lose those variations.  The kernel therefore feeds only psi (small values)
-// to the tensor cores and carries the constant part exactly in fp32:
-//   w_ij            = d + alpha_i + beta_j + a_i . b_j     (a = bf16 psi(q), b = bf16 psi(k),
-//                                                          alpha_i = sum a_i, beta_j = sum b_j)
-//   S               = 1 u^T + R,  u = sum_j v_j,  R = sum_j b_j v_j^T
-//   z               = n 1 + zeta, n = token count, zeta = sum_j b_j
-//   phi(q_i)^T S    = (d + alpha_i) u + r + a_i R,          r = sum_j beta_j v_j = colsum(R)
-//   phi(q_i)^T z    = (d + alpha_i) n + rho + a_i . zeta,   rho = sum_j beta_j
+// Precision scheme.  Every feature is split per token as phi(x) = c + psi_c(x),
+// psi_c = phi - c, with c = 1 for inputs of order one or below (psi_1 = elu)
+// and c near the token's typical phi when its features are mostly strongly
+// negative (split_const in tc_common.cuh).  For inputs of order 1/sqrt(d)
+// every phi is close to 1, so w_ij ~ d with small variations and the output
+// is a near-uniform average; bf16 operands holding phi itself lose those
+// variations.  The kernel therefore feeds only the residuals (small values)
+// to the tensor cores and carries the constants exactly:
+//   w_ij            = d c_i c'_j + c_i beta_j + c'_j alpha_i + a_i . b_j
+//                       (a = bf16 psi_c(q), b = bf16 psi_c'(k), alpha_i = sum a_i,
+//                        beta_j = sum b_j; c_i of the query, c'_j of the key)
+//   S               = 1 u^T + R,  u = sum_j c'_j v_j,  R = sum_j b_j v_j^T
+//   z               = n 1 + zeta, n = sum_j c'_j,   zeta = sum_j b_j
+//   phi(q_i)^T S    = (d c_i + alpha_i) u + c_i r + a_i R,        r = sum_j beta_j v_j = colsum(R)
+//   phi(q_i)^T z    = (d c_i + alpha_i) n + c_i rho + a_i . zeta, rho = sum_j beta_j
 // The constant parts enter the MMAs through one extra K = 16 slice of the
-// psi(q) operand (carrying 1, alpha and d as bf16 hi/lo pairs) against small
-// tiles holding beta, u, r, n and rho, so the tensor core returns the full
-// weight w, numerator and inter-block denominator.  The intra-block weights
+// residual q operand (carrying c, alpha and d c as bf16 hi/lo pairs) against
+// small tiles holding beta, c', u, r, n and rho, so the tensor core returns
+// the full weight w, numerator and inter-block denominator.  The intra-block weights
 // w_ij (about d) are split into bf16 hi + lo parts for the P.V product, so
 // their rounding error is about 2^-17 of w.  All accumulation is fp32 (TMEM).
-// The result is the exact attention of the features 1 + bf16(psi(x)); the
+// The result is the exact attention of the features c + bf16(psi_c(x)); the
 // outputs are float32.
 //
 // Decay (DECAY = true; RetNet's S_t = gamma S_{t-1} + phi(k_t) v_t^T, z alike,
@@ -104,14 +108,15 @@ constexpr uint32_t kColR = 0, kColY = 128, kColG = 256, kColAq = 384, kColYz = 4
                    kColZ = 480, kColUV = 496;
 constexpr uint32_t kTmemCols = 512;
 
-// Augmentation step.  One extra K = 16 slice on the psi(q) operand carries
-// per-row constants, so the MMAs add the fp32 parts of the split form:
-//   A' row i  = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0...]      (TMEM, after psi(q))
-//   B' key j  = [beta_hi, beta_lo, 1, 1, 1, 0...]        -> G  = d + alpha_i + beta_j + a_i.b_j
+// Augmentation step.  One extra K = 16 slice on the residual q operand
+// carries per-row constants, so the MMAs add the exact parts of the split form:
+//   A' row i  = [c, c, alpha_hi, alpha_lo, d c, alpha_hi, d c, 0...]  (TMEM, after psi_c(q))
+//   B' key j  = [beta_hi, beta_lo, s_hi, s_hi, s_hi, s_lo, s_lo, 0...]   (s = c'_j, or its
+//               decayed weight)    -> G  = d c_i s_j + c_i beta_j + s_j alpha_i + a_i.b_j
 //   B'' col c = [r_hi, r_lo, u_hi, u_hi, u_hi, u_lo, u_lo, 0...]
-//                                                        -> Y  = (d + alpha_i) u + r + a_i R
+//                                  -> Y  = (d c_i + alpha_i) u + c_i r + a_i R
 //   Bz  col 0 = [rho_hi, rho_lo, n_hi, n_hi, n_hi, n_lo, n_lo, 0...]
-//                                                        -> Yz = (d + alpha_i) n + rho + a_i.zeta
+//                                  -> Yz = (d c_i + alpha_i) n + c_i rho + a_i.zeta
 // (x_hi = bf16(x), x_lo = bf16(x - x_hi): the pairs carry x to about 2^-17
 // of its value; the dropped alpha_lo * u_lo term is smaller still).  Each
 // B tile is [rows x 16] bf16, K-major without swizzle.
@@ -162,6 +167,7 @@ struct Small {
     alignas(16) float u[2][128];
     alignas(16) float zeta[128];       // last exported zeta (fp32), for the final state
     alignas(16) float rho_part[2][4];
+    alignas(16) float s_part[2][4];    // per-warp sums of the key weights s_j
     alignas(16) float e_inv[2][kC];    // output epilogue: 1 / max(den, eps) per row, per half
     alignas(16) float alpha_part[kC];  // psi(q) row sums of the second half
     alignas(16) float beta_part[kC];   // psi(k) row sums of the second half
@@ -181,7 +187,6 @@ static_assert(sizeof(Small) <= kSmallBytes, "small area");
 // Shared values of the decay kernel only (after Small; the plain kernel's
 // layout does not have them).
 struct DecaySmall {
-    alignas(16) float s_part[2][4];    // per-warp sums of the key weights s_j
     alignas(16) float gpow[2][kC + 2]; // [0][m] = gamma^m, [1][m] = gamma^-m
 };
 static_assert(sizeof(DecaySmall) <= 2 * 1024, "decay area");
@@ -234,7 +239,7 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
 // Per block c (one thread issues, in this order):
 //   G  = psi(Q) psi(K)^T + A' B'^T = w         after psi(q), psi(k) of block c
 //   R += psi(K)^T V, zeta += psi(K)^T 1,       after the previous state's export
-//   [u r] += V^T [1 beta_hi beta_lo]
+//   [. r u] += V^T [1 beta_hi beta_lo s_hi s_lo]
 //   Y  = psi(Q) R~ + A' B''^T,                 after the previous output epilogue
 //   Yz = psi(Q) zeta~ + A' Bz^T
 //   Y += P_hi V + P_lo V                       after the weight epilogue
@@ -369,10 +374,14 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         bool ok = wait_warp(&S.q_full, c & 1, g, 40);
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
-        float alpha = 0.f;
+        float alpha = 0.f, cq = 1.f;
         uint64_t alpha2 = f2pack(0.f, 0.f);
         if (ok) {
             tc_fence_after();   // the MMAs that read the previous psi(q) have completed
+            // the query's split constant, from its first eight features (both
+            // halves read them; nothing overwrites the Q tile before q_empty)
+            cq = split_const(*reinterpret_cast<const uint4 *>(sQ + sw128_off(row, 0)));
+            const SplitC kq = split_pairs(cq);
             // a real loop over 32-feature groups keeps the hot code small
 #pragma unroll 1
             for (int gq = 0; gq < D / 64; ++gq) {
@@ -390,7 +399,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                     const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk = psi_bf16x2(w[hw]);
+                        const uint32_t pk = feat_bf16x2(w[hw], kq);
                         alpha2 = acc_bf16x2(alpha2, pk);
                         v[f4 * 4 + hw] = pk;
                     }
@@ -405,11 +414,11 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         }
         // both halves of psi(q) are in TMEM, and alpha_part is written, past here
         if (group_any<kBarA, 2 * kWG>(!ok)) break;
-        if (h == 0) {   // A' = [1, 1, alpha_hi, alpha_lo, d, alpha_hi, d, 0, ...]
+        if (h == 0) {   // A' = [c, c, alpha_hi, alpha_lo, d c, alpha_hi, d c, 0, ...]
             alpha += S.alpha_part[row];
-            const float ah = bf16_round(alpha);
-            const uint32_t aug0[4] = {pack_bf16x2(1.f, 1.f), pack_bf16x2(ah, alpha - ah),
-                                      pack_bf16x2(dd, ah), pack_bf16x2(dd, 0.f)};
+            const float ah = bf16_round(alpha), dc = dd * cq;   // d c is exact in bf16
+            const uint32_t aug0[4] = {pack_bf16x2(cq, cq), pack_bf16x2(ah, alpha - ah),
+                                      pack_bf16x2(dc, ah), pack_bf16x2(dc, 0.f)};
             const uint32_t aug1[4] = {0u, 0u, 0u, 0u};
             tmem_st4(tb + lb + kColAq + D / 2, aug0);
             tmem_st4(tb + lb + kColAq + D / 2 + 4, aug1);
@@ -508,7 +517,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     const int N = nloc;   // tokens of this work item (segment)
     constexpr int kRGroups = DV / 32;     // 16-column groups of R (and Y) per half
 
-    // constant operand rows: [1|beta] row 0 = ones, rows 3..15 zero; zeta~ all zero
+    // operand rows: [1|beta|s] row 0 = ones, rows 5..15 zero (rows 1..4 are
+    // written per block by psi(k)); zeta~ all zero
     for (int e = wtid; e < 2 * 16 * kC; e += 2 * kWG) {
         const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
         *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
@@ -531,6 +541,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     };
     if (wtid > 0 && wtid < 16) aug_row(sZB, wtid, 0.f, 0.f);   // rows 1..15 of Bz stay zero
     mbar_arrive(&S.y_empty);   // Y is free for block 0
+
 
     // ---- initial state in split form S = 1 u^T + R, z = n 1 + zeta (u = first row
     //      of S, n = first entry of z; zero when absent); buffers [1] = "block -1"
@@ -572,14 +583,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             }
             const uint32_t zv[4] = {f2u(zeta0 * g0), 0u, 0u, 0u};
             tmem_st4(tb + lb + kColZ, zv);
-            if (DECAY) {   // columns [sum v | r_hi | r_lo | u_hi | u_lo | 0 0 0]
+            {   // columns [sum v | r_hi | r_lo | u_hi | u_lo | 0 0 0]
                 const uint32_t uv[4] = {0u, f2u(r0 * g0), 0u, f2u(u0 * g0)};
                 const uint32_t uw[4] = {0u, 0u, 0u, 0u};
                 tmem_st4(tb + lb + kColUV, uv);
                 tmem_st4(tb + lb + kColUV + 4, uw);
-            } else {       // columns [u | r_hi | r_lo | 0]
-                const uint32_t uv[4] = {f2u(u0), f2u(r0), 0u, 0u};
-                tmem_st4(tb + lb + kColUV, uv);
             }
             S.zeta[row] = zeta0;
             S.u[1][row] = u0;
@@ -619,6 +627,15 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
+        // the key's split constant from its first eight features (in h = 0's
+        // half; padding rows read zeros: c' = 1).  Both halves read them from
+        // the tile; h = 0 writes their residuals back only after the group
+        // barrier below, by which time h = 1 has read them.
+        uint4 first = make_uint4(0u, 0u, 0u, 0u);
+        if (ok) first = *reinterpret_cast<const uint4 *>(kt + sw128_off(row, 0));
+        const float ck = split_const(first);
+        const SplitC kk = split_pairs(ck);
+        uint4 held = make_uint4(0u, 0u, 0u, 0u);   // h = 0: residuals of features 0..7
         float beta = 0.f;
         uint64_t beta2 = f2pack(0.f, 0.f);
         if (ok) {
@@ -640,16 +657,20 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
                         const uint32_t pk =
-                            DECAY ? psi_scaled_bf16x2(w[hw], sc) : psi_bf16x2(w[hw]);
+                            DECAY ? feat_scaled_bf16x2(w[hw], kk, sc) : feat_bf16x2(w[hw], kk);
                         beta2 = acc_bf16x2(beta2, pk);
                         w[hw] = pk;
                     }
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
 #pragma unroll
-                for (int f = 0; f < kBatch; ++f)
-                    *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
-                                               sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
+                for (int f = 0; f < kBatch; ++f) {
+                    if (f0 + f == 0)
+                        held = raw[f];
+                    else
+                        *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
+                                                   sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
+                }
             }
             beta = f2sum(beta2);
             if (h == 1) S.beta_part[row] = beta;
@@ -657,29 +678,31 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         }
         if (group_any<kBarB, 2 * kWG>(!ok)) return false;
         if (h == 0) {
+            *reinterpret_cast<uint4 *>(kt + sw128_off(row, 0)) = held;
             beta += S.beta_part[row];
             const float bh = bf16_round(beta);
             uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
             *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
-            // key weight s_j / G as a bf16 pair (exactly 1, 0 without a decay)
-            float sh = 1.f, sl = 0.f;
-            if (DECAY) {
-                sh = bf16_round(sc);
-                sl = bf16_round(sc - sh);
-                *reinterpret_cast<__nv_bfloat16 *>(ubp + 48) = __float2bfloat16_rn(sh);
-                *reinterpret_cast<__nv_bfloat16 *>(ubp + 64) = __float2bfloat16_rn(sl);
-            }
+            // key weight s_j = sc c'_j as a bf16 pair: the key's constant part,
+            // times its decay weight over G with a decay (c'_j itself, a bf16
+            // value, without one); 0 for padding rows
+            const float sj = row < L ? sc * ck : 0.f;
+            const float sh = bf16_round(sj), sl = bf16_round(sj - sh);
+            // rows 3, 4 of [1|beta|s]: u += V^T s (row 0 stays 1: it also
+            // feeds zeta += psi_c(K)^T 1)
+            *reinterpret_cast<__nv_bfloat16 *>(ubp + 48) = __float2bfloat16_rn(sh);
+            *reinterpret_cast<__nv_bfloat16 *>(ubp + 64) = __float2bfloat16_rn(sl);
             // B' row of key j: [beta_hi, beta_lo, s_hi, s_hi, s_hi, s_lo, s_lo, 0]
-            // (beta is the sum of the scaled psi(k_j) with a decay)
+            // (beta is the sum of the residual features, scaled with a decay)
             *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) =
                 make_uint4(pack_bf16x2(bh, beta - bh), pack_bf16x2(sh, sh), pack_bf16x2(sh, sl),
                            pack_bf16x2(sl, 0.f));
             const float bsum = warp_sum_f(beta);
-            if (lane == 0) S.rho_part[cb][wq] = bsum;
-            if (DECAY) {
-                const float ssum = warp_sum_f(sh + sl);
-                if (lane == 0) X.s_part[cb][wq] = ssum;
+            const float ssum = warp_sum_f(sh + sl);
+            if (lane == 0) {
+                S.rho_part[cb][wq] = bsum;
+                S.s_part[cb][wq] = ssum;
             }
             fence_proxy_async();
             mbar_arrive(&S.phik_done[s]);
@@ -742,7 +765,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             uint32_t zv[4], uv[4], uw[4];
             tmem_ld4(tb + lb + kColZ, zv);
             tmem_ld4(tb + lb + kColUV, uv);
-            if (DECAY) tmem_ld4(tb + lb + kColUV + 4, uw);
+            tmem_ld4(tb + lb + kColUV + 4, uw);
             tmem_wait_ld();
             if (DECAY) {
 #pragma unroll
@@ -752,7 +775,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uw[m] = f2u(u2f(uw[m]) * G);
                 }
             }
-            const float u = DECAY ? u2f(uv[3]) + u2f(uw[0]) : u2f(uv[0]);
+            const float u = u2f(uv[3]) + u2f(uw[0]);
             if (row < D) {
                 S.zeta[row] = u2f(zv[0]);
                 *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
@@ -763,13 +786,16 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             if (wtid == 0) {
                 const float rsum = (S.rho_part[cb][0] + S.rho_part[cb][1]) +
                                    (S.rho_part[cb][2] + S.rho_part[cb][3]);
+                // n = sum of the keys' constants (the token count when every
+                // constant is 1)
+                const float ssum = (S.s_part[cb][0] + S.s_part[cb][1]) +
+                                   (S.s_part[cb][2] + S.s_part[cb][3]);
                 if (DECAY) {   // n and rho decay like the state: x <- gamma^L x + sum_j s_j x_j
                     const float gcur = X.gpow[0][L];
-                    S.n_s[cb] = fmaf(gcur, S.n_s[pb], G * ((X.s_part[cb][0] + X.s_part[cb][1]) +
-                                                           (X.s_part[cb][2] + X.s_part[cb][3])));
+                    S.n_s[cb] = fmaf(gcur, S.n_s[pb], G * ssum);
                     S.rho_s[cb] = fmaf(gcur, S.rho_s[pb], G * rsum);
                 } else {
-                    S.n_s[cb] = S.n_s[pb] + (float)L;
+                    S.n_s[cb] = S.n_s[pb] + ssum;
                     S.rho_s[cb] = S.rho_s[pb] + rsum;
                 }
                 aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
@@ -915,6 +941,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     segment_range(p, seg, tok0, nloc);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
+    // decay: heads whose gamma this kernel does not take are left entirely to
+    // the CUDA-core kernel that follows (the whole CTA leaves before any
+    // barrier, TMEM allocation or write, so their y, S_out and z_out, and an
+    // S_in aliased by S_out, are untouched here)
+    if (DECAY && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
     if (tid == 0) LA_TRACE_POINT(0, 15);
     // decay (one segment per head): powers of the head's gamma, read by both
     // row-worker groups (visible after the __syncthreads below)

@@ -13,7 +13,9 @@
 // the library).  Every call shares it; calls that can overlap on the GPU race
 // on it, so the caller must order them (one stream, or explicit waits).
 // Nothing in it has to start at zero: each call writes every partial it later
-// reads.
+// reads, and clears the run-time status word at its start.  That word (a
+// bounded wait that ran out) is read back with la_noalloc_status, since the
+// caller holds no pointer to the array.
 #include <mutex>
 
 #include "la_internal.h"
@@ -58,4 +60,15 @@ extern "C" la_status la_forward_noncausal_noalloc(const void *q, const void *k, 
     if (st != LA_OK) return st;
     return la_forward_noncausal(q, k, v, y, B, H, N, d, dv, dt, eps, S_out, z_out, scratch,
                                 la::kScratchBytes, stream);
+}
+
+extern "C" la_status la_noalloc_status(void *stream) {
+    void *scratch = nullptr;
+    const la_status st = la::scratch_address(&scratch);
+    if (st != LA_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    la::WsHeader h;
+    if (cudaMemcpy(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return h.error == 0 ? LA_OK : static_cast<la_status>(h.error);
 }

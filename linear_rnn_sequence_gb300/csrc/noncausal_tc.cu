@@ -16,21 +16,25 @@
 //      layout the MMA reads, z likewise, and sum_i z_i;
 //   3. noncausal_query_kernel: per (head, range of 128-query blocks), one bulk
 //      copy brings the head's operand image into shared memory, then for every
-//      block  psi(Q) [128 x d] (in place over the TMA tile) times S_hi and S_lo
-//      into a TMEM accumulator, psi(Q) times z_hi, z_lo into two more columns,
-//      and the epilogue
-//        y_i = (colsum(S) + psi(q_i)^T S) / max(sum z + psi(q_i)^T z, eps),
-//      using phi = 1 + psi, so phi(q)^T S = 1^T S + psi(q)^T S.
-// Precision: psi(q) and psi(k) enter the tensor cores as bf16 (the same
-// features 1 + bf16(psi(x)) as the causal path); S and z are fp32 sums split
+//      block  A = psi_c(Q) [128 x d] (the residual features phi(q) - c_i, in
+//      place over the TMA tile) times S_hi and S_lo into a TMEM accumulator,
+//      A times z_hi, z_lo into two more columns, and the epilogue
+//        y_i = (c_i colsum(S) + a_i^T S) / max(c_i sum z + a_i^T z, eps),
+//      using phi(q_i) = c_i 1 + a_i, so phi(q_i)^T S = c_i 1^T S + a_i^T S.
+// Precision: the residual features enter the tensor cores as bf16 (the same
+// features c + bf16(phi(x) - c), with the same per-token split constants, as
+// the causal path; split_const in tc_common.cuh); S and z are fp32 sums split
 // into bf16 hi + lo pairs, so the rounding of the state costs about 2^-17 of
 // its value; colsum(S) and sum z are fp32.  Outputs are float32.
 //
 // Query kernel warp roles (320 threads):
 //   warp 0      TMA producer (operand image once, then Q tiles, 3 stages)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..5  group A: psi(q) in place in shared memory, one token row per thread
-//   warps 6..9  group B (thread = TMEM lane): normaliser epilogue, 16-byte stores
+//   warps 2..5  group A: psi_c(q) in place in shared memory, one token row per thread
+//   warps 6..9  group B (thread = TMEM lane): normaliser epilogue, 16-byte stores;
+//               each thread takes its row's split constant from the row's first
+//               eight features in global memory (just read by the TMA, so an
+//               L2 hit), since the tile itself has been overwritten by then
 // Two TMEM accumulators (blocks c and c+1) let the epilogue of one block
 // overlap the MMA of the next.  Every wait is bounded in time; a wait that
 // runs out records LA_ERR_TIMEOUT in the workspace header and the CTA unwinds.
@@ -148,6 +152,8 @@ noncausal_prepare_kernel(const float *__restrict__ S_seg, const float *__restric
 // ------------------------------------------------------------------ query kernel
 struct QParams {
     float *y;
+    const __nv_bfloat16 *q;        // the queries themselves (split constants of the epilogue)
+    int D;
     const uint8_t *img;            // operand images, OpImage::stride bytes per head
     int N;
     int nq;                        // query ranges per head (work items = heads * nq)
@@ -163,6 +169,7 @@ struct QSmall {
     alignas(16) float colsum[128];     // colsum(S), fp32
     alignas(16) float cpart[128];      // second half of the column sums while they are formed
     alignas(16) float e_inv[kC];       // 1 / max(den, eps) per row of the current block
+    alignas(16) float cq[kC];          // split constant per row of the current block
     float zsum;
     uint64_t q_full[kQStages], q_empty[kQStages], psi_done[kQStages];
     uint64_t op_full, acc_full[2], acc_empty[2], drain;
@@ -310,6 +317,9 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
             const bool ok = wait_warp(&S.q_full[s], (c / kQStages) & 1, g, 74);
             if (ok) {
                 uint8_t *qt = sQ + s * Lay::kQ;
+                // the query's split constant, read before the row is overwritten
+                const SplitC kq = split_pairs(
+                    split_const(*reinterpret_cast<const uint4 *>(qt + sw128_off(row, 0))));
 #pragma unroll 1
                 for (int f0 = 0; f0 < D / 8; f0 += 8) {
                     uint4 raw[8];
@@ -322,7 +332,7 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
                         uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                         for (int h = 0; h < 4; ++h)
-                            w[h] = psi_bf16x2(w[h]);
+                            w[h] = feat_bf16x2(w[h], kq);
                         raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
 #pragma unroll
@@ -363,14 +373,22 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
         constexpr int kParts = 2 * (DV / 32);   // (16-lane half, 32-column block) pairs
         for (int c = 0; ok && c < nchunks; ++c) {
             const int b = c & 1;
+            // this row's first eight features (rows past the range: c = 1),
+            // loaded while the block's MMAs run
+            uint4 first = make_uint4(0u, 0u, 0u, 0u);
+            if (c * kC + row < nloc)
+                first = *reinterpret_cast<const uint4 *>(
+                    p.q + ((size_t)head * p.N + tok0 + c * kC + row) * p.D);
             ok = wait_warp(&S.acc_full[b], (c >> 1) & 1, g, 76);
             if (ok) {
                 tc_fence_after();
                 uint32_t dz[4];
                 tmem_ld4(tb + ((uint32_t)(wq * 32) << 16) + Lay::colDen + 16u * b, dz);
+                const float cr = split_const(first);
                 tmem_wait_ld();
                 __syncwarp();
-                S.e_inv[row] = 1.f / fmaxf(zsum + (u2f(dz[0]) + u2f(dz[1])), p.eps);
+                S.cq[row] = cr;
+                S.e_inv[row] = 1.f / fmaxf(fmaf(cr, zsum, u2f(dz[0]) + u2f(dz[1])), p.eps);
                 __syncwarp();
                 const int t0 = c * kC;
                 float *ychunk = p.y + ((size_t)head * p.N + tok0 + t0) * DV;
@@ -384,15 +402,16 @@ noncausal_query_kernel(const __grid_constant__ CUtensorMap qmap, const QParams p
                     const int half = part & 1, cblk = part >> 1;
                     const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
                     const float invA = S.e_inv[rA], invB = S.e_inv[rB];
+                    const float cA = S.cq[rA], cB = S.cq[rB];
                     const bool okA = t0 + rA < nloc, okB = t0 + rB < nloc;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int col = cblk * 32 + 8 * k + tcol;
                         const float2 cs = *reinterpret_cast<const float2 *>(S.colsum + col);
-                        const float2 oA = make_float2((u2f(vc[4 * k]) + cs.x) * invA,
-                                                      (u2f(vc[4 * k + 1]) + cs.y) * invA);
-                        const float2 oB = make_float2((u2f(vc[4 * k + 2]) + cs.x) * invB,
-                                                      (u2f(vc[4 * k + 3]) + cs.y) * invB);
+                        const float2 oA = make_float2(fmaf(cA, cs.x, u2f(vc[4 * k])) * invA,
+                                                      fmaf(cA, cs.y, u2f(vc[4 * k + 1])) * invA);
+                        const float2 oB = make_float2(fmaf(cB, cs.x, u2f(vc[4 * k + 2])) * invB,
+                                                      fmaf(cB, cs.y, u2f(vc[4 * k + 3])) * invB);
                         if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
                         if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
                     }
@@ -498,6 +517,8 @@ cudaError_t launch_nc(const FwdArgs &a) {
 
     QParams qp{};
     qp.y = a.y;
+    qp.q = static_cast<const __nv_bfloat16 *>(a.q);
+    qp.D = D;
     qp.img = img;
     qp.N = a.N;
     qp.eps = a.eps;

@@ -92,45 +92,6 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
     return r;
 }
 
-// psi(x) = elu(x) = x (x > 0), e^x - 1 (x <= 0) of both bf16 halves of w,
-// rounded back to bf16x2.  Written without a branch so lanes with inputs of
-// either sign stay converged: e^min(x,0) - 1 is 0 for x > 0, and for x <= 0
-// it is at least x (e^x >= 1 + x), so the maximum with x picks the right
-// branch.  e^x = 2^(x log2 e) with the flush-to-zero form (x <= 0 here, so a
-// flushed result only means e^x < 2^-126).  Where e^x - 1 and x are within
-// the exponential's rounding of each other (|x| < ~1e-3) either one is psi(x)
-// to well below the bf16 rounding the result gets.  The multiply and the -1
-// run on the packed pair.
-__device__ __forceinline__ uint32_t psi_bf16x2(uint32_t w) {
-    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
-    float t0, t1, e0, e1;
-    f2unpack(f2mul(f2pack(fminf(x0, 0.f), fminf(x1, 0.f)),
-                   f2pack(1.4426950408889634f, 1.4426950408889634f)), t0, t1);
-    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), f2pack(-1.f, -1.f)), e0, e1);
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(fmaxf(x1, e1)), "f"(fmaxf(x0, e0)));
-    return r;
-}
-
-// sc * psi(x) for both bf16 halves of w, rounded once to bf16x2 (the decayed
-// causal kernel weights key j by sc = gamma^(L-1-j) before the tensor cores
-// see it).
-__device__ __forceinline__ uint32_t psi_scaled_bf16x2(uint32_t w, float sc) {
-    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
-    float t0, t1, e0, e1;
-    f2unpack(f2mul(f2pack(fminf(x0, 0.f), fminf(x1, 0.f)),
-                   f2pack(1.4426950408889634f, 1.4426950408889634f)), t0, t1);
-    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), f2pack(-1.f, -1.f)), e0, e1);
-    f2unpack(f2mul(f2pack(fmaxf(x0, e0), fmaxf(x1, e1)), f2pack(sc, sc)), e0, e1);
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e1), "f"(e0));
-    return r;
-}
-
-// acc (two fp32 lanes) += the two bf16 halves of p.
-__device__ __forceinline__ uint64_t acc_bf16x2(uint64_t acc, uint32_t p) {
-    return f2add(acc, f2pack(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)));
-}
 __device__ __forceinline__ float f2sum(uint64_t v) {
     float a, b;
     f2unpack(v, a, b);
@@ -139,6 +100,98 @@ __device__ __forceinline__ float f2sum(uint64_t v) {
 
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ---- the features the tensor cores see ------------------------------------
+// phi(x) = elu(x) + 1 is split per token as phi(x) = c + (phi(x) - c): the
+// constant c is carried exactly (it is a bf16 value) and only the residual
+// phi(x) - c enters the MMAs as bf16.  For inputs of order one or below,
+// phi is close to 1 and c = 1 (the residual is then elu(x) itself); for a
+// token whose features are mostly strongly negative (phi << 1) a residual
+// taken against 1 would cancel almost all of phi, so c is then the mean of
+// phi over the token's first eight features.  The kernels compute the exact
+// attention of the features c + bf16(phi(x) - c).
+constexpr float kLog2e = 1.4426950408889634f;
+// e^x - 1 is replaced by x above this argument: for -2^-8 < x < 0 the two
+// differ by less than x^2 / 2, under half a bf16 unit of x, while the fp32
+// e^x - 1 loses relative accuracy there
+constexpr float kExpArgMax = -0.00390625f;
+
+// Split constant of a token from its first eight features (one 16-byte
+// chunk of the bf16 row): 1 when the mean of phi over them is at least 1/2,
+// else that mean rounded to bf16.  Every role that needs a token's constant
+// computes it from the same eight values with the same operations.  When
+// all eight inputs are at least ln(1/2), every phi is at least 1/2 and the
+// constant is 1 without any exponential; the warp takes the full rule only
+// when one of its rows needs it (a warp-wide vote: all lanes must call this
+// together), so a row's constant does not depend on its warp's other rows.
+constexpr float kLnHalf = -0.693147180559945f;
+__device__ __forceinline__ float split_const(uint4 raw) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float mn = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        mn = fminf(mn, fminf(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u)));
+    if (!__any_sync(0xffffffffu, !(mn >= kLnHalf))) return 1.f;
+    uint64_t acc = f2pack(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // phi(x) = max(x + 1, e^min(x, 0)), on packed pairs
+        const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
+        float t0, t1, a0, a1;
+        f2unpack(f2mul(f2pack(fminf(x0, 0.f), fminf(x1, 0.f)), f2pack(kLog2e, kLog2e)), t0, t1);
+        f2unpack(f2add(f2pack(x0, x1), f2pack(1.f, 1.f)), a0, a1);
+        acc = f2add(acc, f2pack(fmaxf(a0, ex2_ftz(t0)), fmaxf(a1, ex2_ftz(t1))));
+    }
+    const float m = f2sum(acc) * 0.125f;
+    return m >= 0.5f ? 1.f : bf16_round(m);
+}
+
+// The per-token constants as packed pairs: (1 - c, 1 - c) and (-c, -c).
+struct SplitC {
+    uint64_t omc2, nc2;
+};
+__device__ __forceinline__ SplitC split_pairs(float c) {
+    return {f2pack(1.f - c, 1.f - c), f2pack(-c, -c)};
+}
+
+// phi(x) - c of both bf16 halves of w, rounded to bf16x2:
+//   max(x + 1 - c, e^min(x, -2^-8) - c).
+// For x <= -2^-8 the exponential term is the larger (e^x >= 1 + x); for
+// x > -2^-8 it is e^-2^-8 - c, below x + 1 - c.  Branch-free, so lanes with
+// inputs of either sign stay converged.  e^x = 2^(x log2 e) in the
+// flush-to-zero form (a flushed result means e^x < 2^-126).  The multiply
+// and the adds run on the packed pair.  With c = 1 this is elu(x).
+__device__ __forceinline__ uint32_t feat_bf16x2(uint32_t w, const SplitC &k) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1, a0, a1;
+    f2unpack(f2mul(f2pack(fminf(x0, kExpArgMax), fminf(x1, kExpArgMax)),
+                   f2pack(kLog2e, kLog2e)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), k.nc2), e0, e1);
+    f2unpack(f2add(f2pack(x0, x1), k.omc2), a0, a1);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(fmaxf(a1, e1)), "f"(fmaxf(a0, e0)));
+    return r;
+}
+
+// sc * (phi(x) - c) for both bf16 halves of w, rounded once to bf16x2 (the
+// decayed kernels weight key j by sc = gamma^(L-1-j) / G before the tensor
+// cores see it).
+__device__ __forceinline__ uint32_t feat_scaled_bf16x2(uint32_t w, const SplitC &k, float sc) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1, a0, a1;
+    f2unpack(f2mul(f2pack(fminf(x0, kExpArgMax), fminf(x1, kExpArgMax)),
+                   f2pack(kLog2e, kLog2e)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), k.nc2), e0, e1);
+    f2unpack(f2add(f2pack(x0, x1), k.omc2), a0, a1);
+    f2unpack(f2mul(f2pack(fmaxf(a0, e0), fmaxf(a1, e1)), f2pack(sc, sc)), e0, e1);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e1), "f"(e0));
+    return r;
+}
+
+// acc (two fp32 lanes) += the two bf16 halves of p.
+__device__ __forceinline__ uint64_t acc_bf16x2(uint64_t acc, uint32_t p) {
+    return f2add(acc, f2pack(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)));
 }
 
 // Byte offset of element (row, col) in a [rows x 64] bf16 box with 128-byte

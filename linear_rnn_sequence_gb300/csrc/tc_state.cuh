@@ -18,9 +18,10 @@ namespace {
 //      S_s = sum phi(k_j) v_j^T, z_s = sum phi(k_j) from K and V (tensor cores);
 //   2. scan_states_kernel: per head, exclusive prefixes P_s = S_in + sum_{s'<s} S_s';
 //   3. causal_tc_kernel: every (head, segment) runs from its prefix.
-// The state pass reuses the split form of the main kernel: R = psi(K)^T V,
-// zeta = psi(K)^T 1 and u = V^T 1 accumulate in TMEM, and the plain state is
-// S = 1 u^T + R, z = n 1 + zeta.
+// The state pass reuses the split form of the main kernel (per-key split
+// constants c'_j, residual features b_j = bf16(phi(k_j) - c'_j)): R = B^T V,
+// zeta = B^T 1 and u = V^T c' accumulate in TMEM, and the plain state is
+// S = 1 u^T + R, z = n 1 + zeta with n = sum_j c'_j.
 // With a per-head decay (DECAY) the segment's state is the decayed sum
 // S_s = sum_j gamma^(end-1-j) phi(k_j) v_j^T (z alike), as the causal
 // kernel's: key j of a block of L tokens carries s_j = gamma^(L-1-j), the
@@ -34,13 +35,14 @@ template <int D, int DV, bool DECAY = false>
 struct StateLayout {
     static constexpr int kK = kC * D * 2;
     static constexpr int kV = kC * DV * 2;
-    // [16 x C] operand, row 0 = ones; with a decay one per stage, rows 1, 2 =
-    // the block's key weights s_j / G as bf16 hi, lo
+    // [16 x C] operand per stage: row 0 = ones (zeta += B^T 1), rows 1, 2 =
+    // the key weights as bf16 hi, lo (u += V^T s): s_j = c'_j, the key's split
+    // constant (0 for padding rows), times gamma^(L-1-j) / G with a decay
     static constexpr int kOnes = 16 * kC * 2;
     static constexpr int oK = 0;                   // 2 stages
     static constexpr int oV = oK + 2 * kK;         // 2 stages
-    static constexpr int oOnes = oV + 2 * kV;
-    static constexpr int oPad = oOnes + (DECAY ? 2 : 1) * kOnes;   // 16 KB the padded M = 128 operands may touch
+    static constexpr int oOnes = oV + 2 * kV;      // 2 stages
+    static constexpr int oPad = oOnes + 2 * kOnes; // 16 KB the padded M = 128 operands may touch
     static constexpr int oSmall = oPad + 16384;
     static constexpr int oDecay = oSmall + 2048;   // decay only: StateDecay
     static constexpr int bytes = oDecay + (DECAY ? 1024 : 0);
@@ -49,6 +51,7 @@ struct StateLayout {
 
 struct StateSmall {
     alignas(16) float u[128];
+    alignas(16) float n_part[4];      // per-warp sums of the keys' constants (decayed, over G)
     uint64_t kv_full[2], kv_empty[2], phik_done[2], init_done, st_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -57,7 +60,6 @@ static_assert(sizeof(StateSmall) <= 2048, "state small area");
 
 struct StateDecay {
     alignas(16) float gpow[kC + 1];   // gamma^m
-    alignas(16) float n_part[4];      // per-warp sums of the decayed token counts
 };
 static_assert(sizeof(StateDecay) <= 1024, "state decay area");
 
@@ -87,6 +89,9 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
     // reads only K and V: the consumer of S_seg waits for this whole grid
     griddep_launch_dependents();
+    // decay: heads left to the CUDA-core kernel need no segment states (the
+    // chunk kernel skips them too); the whole CTA leaves before any barrier
+    if (DECAY && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
 
     if (tid == 0) {
         S.abort_flag = 0;
@@ -130,7 +135,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                     if (last_kv[s] >= 0) drain_wait(&S.kv_full[s], (last_kv[s] >> 1) & 1, g.limit_ns);
         }
     } else if (warp == 1) {
-        if (lane == 0) {   // MMA: R += psi(K)^T V, zeta += psi(K)^T 1, u += V^T 1
+        if (lane == 0) {   // MMA: R += B^T V, zeta += B^T 1, u += V^T s (rows of the [1|s] operand)
             constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);
             constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);
             bool ok = mbar_wait(&S.init_done, 0, g, 61);
@@ -140,7 +145,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 63)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
-                const uint32_t ob = smem_u32(sOnes + (DECAY ? s * Lay::kOnes : 0));
+                const uint32_t ob = smem_u32(sOnes + s * Lay::kOnes);
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
@@ -158,8 +163,9 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     } else {
         const int wq = warp & 3, row = wq * 32 + lane, wtid = tid - 64;
         const uint32_t lb = (uint32_t)(wq * 32) << 16;
-        // ones operand(s) (row 0 = 1, rows 1..15 = 0) and a zeroed pad region
-        for (int e = wtid; e < (DECAY ? 2 : 1) * 16 * kC; e += kWG) {
+        // constant operands (row 0 = ones; rows 1, 2 are rewritten per block,
+        // rows 3..15 stay 0) and a zeroed pad region
+        for (int e = wtid; e < 2 * 16 * kC; e += kWG) {
             const int st = e / (16 * kC), n = (e / kC) % 16, k = e % kC;
             *reinterpret_cast<__nv_bfloat16 *>(sOnes + st * Lay::kOnes + (n >> 3) * 2048 +
                                                (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
@@ -182,7 +188,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         mbar_arrive(&S.init_done);
         bool ok = true;
         DecayScale ks(DECAY ? X.gpow[1] : 1.f);   // X.gpow[1] = gamma
-        float nrow = 0.f;   // decay: this token row's share of the decayed count, over G
+        float nrow = 0.f;   // this token row's share of n (with a decay: decayed, over G)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const int L = min(kC, nloc - c * kC);
@@ -215,6 +221,10 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 64);
             if (!ok) break;
             uint8_t *kt = sK + s * Lay::kK;
+            // the key's split constant from its first eight features (padding
+            // rows read zeros: c' = 1), read before the row is overwritten
+            const float ck = split_const(*reinterpret_cast<const uint4 *>(kt + sw128_off(row, 0)));
+            const SplitC kk = split_pairs(ck);
 #pragma unroll 1
             for (int f0 = 0; f0 < D / 8; f0 += 8) {
                 uint4 raw[8];
@@ -227,7 +237,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h)
-                        w[h] = DECAY ? psi_scaled_bf16x2(w[h], sc) : psi_bf16x2(w[h]);
+                        w[h] = DECAY ? feat_scaled_bf16x2(w[h], kk, sc) : feat_bf16x2(w[h], kk);
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
 #pragma unroll
@@ -235,8 +245,10 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                     *reinterpret_cast<uint4 *>(kt + ((f0 + f) >> 3) * (kC * 128) +
                                                sw128_off(row, ((f0 + f) & 7) * 8)) = raw[f];
             }
-            if (DECAY) {   // key weight s_j / G as a bf16 pair in rows 1, 2 of the ones operand
-                const float sh = bf16_round(sc), sl = bf16_round(sc - sh);
+            {   // rows 1, 2: the key weight s_j = c'_j sc as a bf16 pair (u += V^T s;
+                // sc = 1 without a decay); 0 on padding rows
+                const float sj = row < L ? sc * ck : 0.f;
+                const float sh = bf16_round(sj), sl = bf16_round(sj - sh);
                 uint8_t *op = sOnes + s * Lay::kOnes + (row >> 3) * 128 + (row & 7) * 2;
                 *reinterpret_cast<__nv_bfloat16 *>(op + 16) = __float2bfloat16_rn(sh);
                 *reinterpret_cast<__nv_bfloat16 *>(op + 32) = __float2bfloat16_rn(sl);
@@ -253,13 +265,11 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             tmem_ld4(tb + lb + kStColZ, zv);
             tmem_ld4(tb + lb + kStColU, uv);
             tmem_wait_ld();
-            // decay: the sums are held over G; u = v^T [s_hi + s_lo] (columns 1, 2)
+            // u = v^T [s_hi + s_lo] (columns 1, 2); with a decay the sums are held over G
             const float G = DECAY ? ks.G : 1.f;
-            S.u[row] = DECAY ? G * (u2f(uv[1]) + u2f(uv[2])) : u2f(uv[0]);
-            if (DECAY) {
-                const float ns = warp_sum_f(nrow);
-                if (lane == 0) X.n_part[wq] = ns;
-            }
+            S.u[row] = G * (u2f(uv[1]) + u2f(uv[2]));
+            const float ns = warp_sum_f(nrow);
+            if (lane == 0) S.n_part[wq] = ns;
             named_bar(kBarA, kWG);
             float *dst = S_seg + (size_t)slot * D * DV;
 #pragma unroll 1
@@ -276,8 +286,8 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                                         fmaf(u2f(rv[jj + 2]), G, S.u[grp * 16 + jj + 2]),
                                         fmaf(u2f(rv[jj + 3]), G, S.u[grp * 16 + jj + 3]));
             }
-            const float n = DECAY ? G * ((X.n_part[0] + X.n_part[1]) + (X.n_part[2] + X.n_part[3]))
-                                  : (float)nloc;
+            // n = sum of the keys' constants (nloc when every constant is 1)
+            const float n = G * ((S.n_part[0] + S.n_part[1]) + (S.n_part[2] + S.n_part[3]));
             if (row < D) z_seg[(size_t)slot * D + row] = fmaf(u2f(zv[0]), G, n);
         }
     }

@@ -87,6 +87,13 @@ def lib():
             L.la_workspace_status.restype = i
             L.la_debug_set_fault.argtypes = [i, ctypes.c_longlong]
             L.la_debug_set_fault.restype = None
+            L.la_debug_feature_bf16.argtypes = [vp, vp, ctypes.c_longlong, f, vp]
+            L.la_debug_feature_bf16.restype = i
+            L.la_forward_noncausal_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp,
+                                                       vp, vp]
+            L.la_forward_noncausal_noalloc.restype = i
+            L.la_noalloc_status.argtypes = [vp]
+            L.la_noalloc_status.restype = i
             _lib = L
     return _lib
 

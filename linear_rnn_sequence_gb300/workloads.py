@@ -139,10 +139,20 @@ def next_decode_inputs(w: Workload, g: torch.Generator, device=None):
     return q, k, v
 
 
-def random_qkv(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="cpu"):
-    """Ad-hoc seeded draw with the same recipe (for edge-case tests)."""
+def random_qkv(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="cpu",
+               shift=0.0):
+    """Ad-hoc seeded draw with the same recipe (for edge-case tests).
+
+    With ``shift`` the draws of q and k are moved by that amount in float32
+    before the cast (q, k ~ N(shift, scale^2), v ~ N(0, scale^2)), the inputs
+    whose features phi are all far below 1 when the shift is strongly negative.
+    """
     w = Workload("adhoc", "causal", B, H, N, d, dv, dtype, scale, seed)
-    return make_qkv(w, device=device)
+    if shift == 0.0:
+        return make_qkv(w, device=device)
+    q, k, v = make_qkv(w.with_(dtype=torch.float32), device=device)
+    sh = torch.tensor(shift, dtype=torch.float32)
+    return (q + sh).to(dtype), (k + sh).to(dtype), v.to(dtype)
 
 
 def random_qkv_dy(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device="cpu"):

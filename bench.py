@@ -52,7 +52,13 @@ def alg_flops_per_token_head(d, dv):
 
 
 def alg_bytes_per_token_head(w: Workload):
-    return (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4  # q, k, v read; y (fp32) written
+    """Algorithmic bytes: q, k, v read and y written once, all at the input dtype."""
+    return (2 * w.d + 2 * w.dv) * esize(w.dtype)
+
+
+def moved_bytes_per_token_head(w: Workload):
+    """The same with y written as float32, as the library writes it."""
+    return (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4
 
 
 def bwd_flops_per_token_head(d, dv):
@@ -77,6 +83,12 @@ def decay_flops_per_token_head(d, dv):
 
 
 def decode_bytes_per_head_step(w: Workload):
+    """fp32 S and z read and written; q, k, v read and y written at the input dtype."""
+    return 2 * (w.d * w.dv + w.d) * 4 + (2 * w.d + 2 * w.dv) * esize(w.dtype)
+
+
+def decode_moved_bytes_per_head_step(w: Workload):
+    """The same with y written as float32."""
     return 2 * (w.d * w.dv + w.d) * 4 + (2 * w.d + w.dv) * esize(w.dtype) + w.dv * 4
 
 
@@ -237,7 +249,15 @@ def time_steps(fn, steps, warmup, world, flush=None, min_warm_s=0.0):
     return max_over_ranks(total, world), per
 
 
-def roofline(bytes_per_launch, flops_per_launch, launch_ms, peaks, peak_kind, traffic=None):
+BYTES_BASIS = "q, k, v read and y written once at the input dtype (decode: plus fp32 S, z read and written)"
+
+
+def roofline(bytes_per_launch, flops_per_launch, launch_ms, peaks, peak_kind, traffic=None,
+             moved_bytes=None):
+    """Achieved rate and fraction of the measured peak for one launch.
+
+    ``frac`` is on the algorithmic bytes (BYTES_BASIS).  ``fp32_y`` repeats
+    the bytes figure with y counted as float32, the bytes the kernels move."""
     t = launch_ms * 1e-3
     gbs = bytes_per_launch / t / 1e9
     tflops = flops_per_launch / t / 1e12
@@ -252,13 +272,21 @@ def roofline(bytes_per_launch, flops_per_launch, launch_ms, peaks, peak_kind, tr
     r["traffic"] = traffic
     r["peak_source"] = peak_kind
     r["roof_fraction"] = max(t_bytes, t_flops) / t  # slower of the two roofs / measured time
+    r["bytes_basis"] = BYTES_BASIS
+    r["bytes_per_launch"] = bytes_per_launch
+    if moved_bytes is not None:
+        gbs = moved_bytes / t / 1e9
+        r["fp32_y"] = {"bytes_per_launch": moved_bytes, "achieved_gbs": gbs,
+                       "frac": gbs / peaks["hbm_gbs"]}
     return r
 
 
 # ----------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle as it stands, on a bounded sample
 # ----------------------------------------------------------------------------
-def cpu_baseline(w: Workload, budget_s=12.0):
+def cpu_baseline(w: Workload, budget_s=12.0, budget_1t_s=4.0):
+    """The oracle on the host cores (all of them, then one thread), in tokens/s
+    of the workload: B*N positions across all H heads."""
     import oracle
     cores = oracle.default_threads()
     sample = w.with_(B=1)
@@ -272,9 +300,20 @@ def cpu_baseline(w: Workload, budget_s=12.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
+    # one thread: whole heads of the same row, one after another; a position
+    # needs all H heads, so the rate is N / (H x seconds per head)
+    heads, t1 = 0, time.perf_counter()
+    while True:
+        h = heads % w.H
+        oracle.causal_recurrent(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], eps=w.eps, nthreads=1)
+        heads += 1
+        if time.perf_counter() - t1 >= budget_1t_s:
+            break
+    el1 = time.perf_counter() - t1
     return {"value": done_tokens / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} x (B=1, H={w.H}, N={w.N}, d={w.d}, dv={w.dv}) recurrent fp64, "
-                      f"{el:.1f} s"}
+                      f"{el:.1f} s; one thread: {heads} heads of that row, {el1:.1f} s",
+            "value_1thread": sample.N / (w.H * el1 / heads)}
 
 
 # ----------------------------------------------------------------------------
@@ -306,7 +345,8 @@ def run_ours(args, world, rank, local):
     bytes_launch = T * alg_bytes_per_token_head(w)
     flops_launch = T * alg_flops_per_token_head(w.d, w.dv)
     traffic = load_traffic(HEADLINE)
-    roof = roofline(bytes_launch, flops_launch, launch_ms, peaks, peak_kind, traffic)
+    roof = roofline(bytes_launch, flops_launch, launch_ms, peaks, peak_kind, traffic,
+                    moved_bytes=T * moved_bytes_per_token_head(w))
     status = la.workspace_status(ws)
 
     out = {
@@ -437,7 +477,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "l2": "flushed between launches (256 MB write)",
                      "roofline": roofline(T * alg_bytes_per_token_head(w),
                                           T * alg_flops_per_token_head(w.d, w.dv), ms, peaks,
-                                          peak_kind, load_traffic(w.name))}
+                                          peak_kind, load_traffic(w.name),
+                                          moved_bytes=T * moved_bytes_per_token_head(w))}
     del q, k, v, y, ws
 
     # long causal
@@ -453,7 +494,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "l2": "inputs larger than L2",
                      "roofline": roofline(T * alg_bytes_per_token_head(w),
                                           T * alg_flops_per_token_head(w.d, w.dv), ms, peaks,
-                                          peak_kind, load_traffic(w.name))}
+                                          peak_kind, load_traffic(w.name),
+                                          moved_bytes=T * moved_bytes_per_token_head(w))}
     del q, k, v, y, ws
     torch.cuda.empty_cache()
 
@@ -463,29 +505,34 @@ def run_modes(args, world, dev, peaks, peak_kind):
     _, S, z = la.forward_causal(q, k, v, return_state=True)
     del q, k, v
     torch.cuda.empty_cache()
-    nsteps = 256
+    # the workload's 4096 steps, each on one of 256 pre-drawn (q, k, v) sets in
+    # turn (drawing all 4096 would take 25 GB); the state evolves step by step
+    nsets, nsteps = 256, w.steps
     g = torch.Generator(device=dev).manual_seed(w.seed + 1)
     sc = torch.tensor(w.step_scale, device=dev)
-    qs = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
-    ks = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
-    vs = (torch.randn(nsteps, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
+    qs = (torch.randn(nsets, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    ks = (torch.randn(nsets, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    vs = (torch.randn(nsets, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
     yd = torch.empty(w.B, w.H, w.dv, device=dev)
     it = [0]
 
     def dstep():
-        i = it[0] % nsteps
+        i = it[0] % nsets
         it[0] += 1
         la.decode_step(qs[i], ks[i], vs[i], S, z, eps=w.eps, out=yd)
 
     total, per = time_steps(dstep, nsteps, args.warmup, world)
     ms = total / nsteps
     heads = w.BH
+    roof = roofline(heads * decode_bytes_per_head_step(w), heads * alg_flops_per_token_head(w.d, w.dv),
+                    sum(per) / len(per), peaks, peak_kind, load_traffic(w.name),
+                    moved_bytes=heads * decode_moved_bytes_per_head_step(w))
+    # per step over the whole run, launch gaps included (the per-launch figure
+    # above can read a little high: part of a step's write-back is still in L2)
+    roof["frac_per_step"] = heads * decode_bytes_per_head_step(w) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
     modes[w.name] = {"tokens_per_s": world * w.B / (ms * 1e-3), "ms_per_step": ms,
                      "steps_timed": nsteps, "l2": "state (512 MB) larger than L2",
-                     "roofline": roofline(heads * decode_bytes_per_head_step(w),
-                                          heads * alg_flops_per_token_head(w.d, w.dv),
-                                          sum(per) / len(per), peaks, peak_kind,
-                                          load_traffic(w.name))}
+                     "roofline": roof}
     del qs, ks, vs, S, z
     torch.cuda.empty_cache()
 
@@ -548,7 +595,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "kernels_per_call": launches_per_call("causal_decay", w),
                      "roofline": roofline(T * alg_bytes_per_token_head(w),
                                           T * decay_flops_per_token_head(w.d, w.dv), ms, peaks,
-                                          peak_kind, load_traffic(w.name))}
+                                          peak_kind, load_traffic(w.name),
+                                          moved_bytes=T * moved_bytes_per_token_head(w))}
     del q, k, v, y, ws
     torch.cuda.empty_cache()
 
@@ -569,7 +617,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "kernels_per_call": launches_per_call("causal_decay", w),
                      "roofline": roofline(T * alg_bytes_per_token_head(w),
                                           T * decay_flops_per_token_head(w.d, w.dv), ms, peaks,
-                                          peak_kind, load_traffic(w.name))}
+                                          peak_kind, load_traffic(w.name),
+                                          moved_bytes=T * moved_bytes_per_token_head(w))}
     del q, k, v, y, ws
     torch.cuda.empty_cache()
 
@@ -582,24 +631,26 @@ def run_modes(args, world, dev, peaks, peak_kind):
     torch.cuda.empty_cache()
     g = torch.Generator(device=dev).manual_seed(w.seed + 1)
     sc = torch.tensor(w.step_scale, device=dev)
-    qs = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
-    ks = (torch.randn(nsteps, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
-    vs = (torch.randn(nsteps, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
+    qs = (torch.randn(nsets, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    ks = (torch.randn(nsets, w.B, w.H, w.d, generator=g, device=dev) * sc).to(w.dtype)
+    vs = (torch.randn(nsets, w.B, w.H, w.dv, generator=g, device=dev) * sc).to(w.dtype)
     it[0] = 0
 
     def ddstep():
-        i = it[0] % nsteps
+        i = it[0] % nsets
         it[0] += 1
         la.decode_step_decay(qs[i], ks[i], vs[i], S, z, gam, eps=w.eps, out=yd)
 
+    nsteps = w.steps
     total, per = time_steps(ddstep, nsteps, args.warmup, world)
     ms = total / nsteps
+    roof = roofline(w.BH * decode_bytes_per_head_step(w), w.BH * decay_flops_per_token_head(w.d, w.dv),
+                    sum(per) / len(per), peaks, peak_kind, load_traffic(w.name),
+                    moved_bytes=w.BH * decode_moved_bytes_per_head_step(w))
+    roof["frac_per_step"] = w.BH * decode_bytes_per_head_step(w) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
     modes[w.name] = {"tokens_per_s": world * w.B / (ms * 1e-3), "ms_per_step": ms,
                      "steps_timed": nsteps, "l2": "state (512 MB) larger than L2",
-                     "roofline": roofline(w.BH * decode_bytes_per_head_step(w),
-                                          w.BH * decay_flops_per_token_head(w.d, w.dv),
-                                          sum(per) / len(per), peaks, peak_kind,
-                                          load_traffic(w.name))}
+                     "roofline": roof}
     del qs, ks, vs, S, z
     torch.cuda.empty_cache()
     return modes

@@ -119,33 +119,30 @@ def test_recurrent_matches_bruteforce(N, d, dv, scale, seed):
     assert _rel(oracle.quadratic(q, k, v, causal=False), _bruteforce(q, k, v, False)) < 1e-12
 
 
-def _torch_parallel_causal(q, k, v, eps=1e-6):
-    """Prefix-sum form with torch float64 library routines."""
-    q, k, v = (torch.from_numpy(x) for x in (q, k, v))
-    fq = torch.nn.functional.elu(q) + 1.0
-    fk = torch.nn.functional.elu(k) + 1.0
-    S = torch.einsum("bnd,bne->bnde", fk, v).cumsum(dim=1)
-    z = fk.cumsum(dim=1)
-    num = torch.einsum("bnd,bnde->bne", fq, S)
-    den = (fq * z).sum(-1, keepdim=True)
-    return (num / den.clamp_min(eps)).numpy()
+def _torch_phi(x):
+    """elu(x) + 1 from torch's expm1: x + 1 for x > 0, expm1(x) + 1 otherwise."""
+    return torch.where(x > 0, x, torch.special.expm1(torch.clamp(x, max=0.0))) + 1.0
 
 
-def _torch_noncausal(q, k, v, eps=1e-6):
-    q, k, v = (torch.from_numpy(x) for x in (q, k, v))
-    fq = torch.nn.functional.elu(q) + 1.0
-    fk = torch.nn.functional.elu(k) + 1.0
-    S = fk.transpose(-2, -1) @ v
-    z = fk.sum(-2)
-    return ((fq @ S) / (fq @ z.unsqueeze(-1)).clamp_min(eps)).numpy()
+def _torch_kernel_matrix(q, k, v, causal, eps=1e-6):
+    """The output as an explicit N x N kernel matrix, float64 torch routines:
+    A = Phi(Q) Phi(K)^T (lower triangle only when causal, by torch.tril), then
+    y = A V / max(A 1, eps) with batched matmuls.  No prefix sums and no state:
+    a different route to the same numbers than the oracle's recurrence."""
+    Q, K, V = (torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v))
+    A = torch.bmm(_torch_phi(Q), _torch_phi(K).transpose(1, 2))
+    if causal:
+        A = torch.tril(A)
+    den = torch.maximum(A.sum(dim=2, keepdim=True), torch.tensor(eps, dtype=A.dtype))
+    return (torch.bmm(A, V) / den).numpy()
 
 
 @pytest.mark.parametrize("B,N,d,dv,seed", [(2, 64, 16, 16, 7), (3, 50, 8, 12, 8), (1, 128, 32, 32, 9)])
 def test_library_cross_check(B, N, d, dv, seed):
     r = _rng(seed)
     q, k, v = (r.standard_normal((B, N, n)) for n in (d, d, dv))
-    assert _rel(oracle.causal_recurrent(q, k, v), _torch_parallel_causal(q, k, v)) < 1e-12
-    assert _rel(oracle.noncausal(q, k, v), _torch_noncausal(q, k, v)) < 1e-12
+    assert _rel(oracle.causal_recurrent(q, k, v), _torch_kernel_matrix(q, k, v, True)) < 1e-12
+    assert _rel(oracle.noncausal(q, k, v), _torch_kernel_matrix(q, k, v, False)) < 1e-12
 
 
 @pytest.mark.parametrize("C", [1, 3, 7, 64, 128, 300])

@@ -26,6 +26,14 @@ C loops in ``linattn_oracle.c``:
   causal form with respect to q, k, v (and the initial state), by the chain
   rule through the recurrence ("Linear Attention/es", "Entrenamiento: forma
   paralela" motivates it; the recurrence is "Forma recurrente ...").
+* ``causal_gated(q, k, v, gate, phi)`` -- the recurrent form with a
+  data-dependent gate per token (one value, or one per feature row of S) in
+  place of the decay ("Variantes y extensiones", gated linear attention), and
+  the feature map "elu1" or "identity" ("Mapas de características").
+* ``noncausal(..., phi=)`` and ``quadratic(..., phi=)`` take the same choice
+  of feature map.
+* ``random_features(x, W)`` -- the positive random-feature map
+  exp(W x - ||x||^2 / 2) / sqrt(m) of the same section (Performer), W given.
 
 Shapes: q, k ``[..., N, d]``; v ``[..., N, dv]``; leading dims are flattened
 into independent heads.  States: S ``[..., d, dv]``, z ``[..., d]``.
@@ -84,6 +92,14 @@ def _bind(lib):
     lib.oracle_causal_backward_decay.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, P, P, P,
                                                  P, P, i]
     lib.oracle_causal_backward_decay.restype = i
+    lib.oracle_causal_gated.argtypes = [P, P, P, P, i, i, i, i, dbl, i, P, i, P, P, P, P, i]
+    lib.oracle_causal_gated.restype = i
+    lib.oracle_noncausal_phi.argtypes = [P, P, P, P, i, i, i, i, dbl, i, P, P, i]
+    lib.oracle_noncausal_phi.restype = i
+    lib.oracle_quadratic_phi.argtypes = [P, P, P, P, i, i, i, i, dbl, i, i, i]
+    lib.oracle_quadratic_phi.restype = i
+    lib.oracle_random_features.argtypes = [P, P, P, ctypes.c_long, i, i]
+    lib.oracle_random_features.restype = i
     return lib
 
 
@@ -148,24 +164,30 @@ def causal_recurrent(q, k, v, eps: float = 1e-6, S_in=None, z_in=None,
     return (y, S, z) if return_state else y
 
 
+PHI_KINDS = {"elu1": 0, "identity": 1}
+
+
 def noncausal(q, k, v, eps: float = 1e-6, return_state: bool = False,
-              nthreads: int | None = None):
+              nthreads: int | None = None, phi: str = "elu1"):
     q, k, v, lead, BH, N, d, dv = _split(q, k, v)
     y = np.empty(lead + (N, dv))
     S = np.empty(lead + (d, dv)) if return_state else None
     z = np.empty(lead + (d,)) if return_state else None
-    rc = _load().oracle_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv, float(eps),
-                                  _ptr(S), _ptr(z), nthreads or default_threads())
+    rc = _load().oracle_noncausal_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                      float(eps), PHI_KINDS[phi], _ptr(S), _ptr(z),
+                                      nthreads or default_threads())
     if rc:
         raise RuntimeError("oracle_noncausal failed")
     return (y, S, z) if return_state else y
 
 
-def quadratic(q, k, v, causal: bool = True, eps: float = 1e-6, nthreads: int | None = None):
+def quadratic(q, k, v, causal: bool = True, eps: float = 1e-6, nthreads: int | None = None,
+              phi: str = "elu1"):
     q, k, v, lead, BH, N, d, dv = _split(q, k, v)
     y = np.empty(lead + (N, dv))
-    rc = _load().oracle_quadratic(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv, float(eps),
-                                  1 if causal else 0, nthreads or default_threads())
+    rc = _load().oracle_quadratic_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                      float(eps), 1 if causal else 0, PHI_KINDS[phi],
+                                      nthreads or default_threads())
     if rc:
         raise RuntimeError("oracle_quadratic failed")
     return y
@@ -262,3 +284,50 @@ def causal_recurrent_decay(q, k, v, gamma, eps: float = 1e-6, S_in=None, z_in=No
     if rc:
         raise RuntimeError("oracle_causal_recurrent_decay failed")
     return (y, S, z) if return_state else y
+
+
+def causal_gated(q, k, v, gate=None, phi: str = "elu1", eps: float = 1e-6, S_in=None,
+                 z_in=None, return_state: bool = False, nthreads: int | None = None):
+    """Recurrent form with a per-token gate and a choice of feature map.
+
+    ``gate``: None, shape [..., N] (one gate per token: S_t = g_t S_{t-1} +
+    phi(k_t) v_t^T) or [..., N, d] (one per token and feature row of S); the
+    leading dims are those of q.  ``phi``: "elu1" or "identity"."""
+    q, k, v, lead, BH, N, d, dv = _split(q, k, v)
+    g, gd = None, 1
+    if gate is not None:
+        g = _f64(gate)
+        if g.shape == lead + (N,):
+            gd = 1
+        elif g.shape == lead + (N, d):
+            gd = d
+        else:
+            raise ValueError(f"gate{g.shape} must be {lead + (N,)} or {lead + (N, d)}")
+        g = np.ascontiguousarray(g.reshape(BH, N, gd))
+    y = np.empty(lead + (N, dv))
+    S_in = None if S_in is None else _f64(S_in).reshape(BH, d, dv)
+    z_in = None if z_in is None else _f64(z_in).reshape(BH, d)
+    S = np.empty(lead + (d, dv)) if return_state else None
+    z = np.empty(lead + (d,)) if return_state else None
+    rc = _load().oracle_causal_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(y), BH, N, d, dv,
+                                     float(eps), PHI_KINDS[phi], _ptr(g), gd, _ptr(S_in),
+                                     _ptr(z_in), _ptr(S), _ptr(z), nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_causal_gated failed")
+    return (y, S, z) if return_state else y
+
+
+def random_features(x, W) -> np.ndarray:
+    """exp(W x - ||x||^2 / 2) / sqrt(m) for every row x of ``x`` ([..., d]);
+    W: [m, d].  Returns [..., m]."""
+    x, W = _f64(x), _f64(W)
+    d = x.shape[-1]
+    if W.ndim != 2 or W.shape[1] != d:
+        raise ValueError(f"W{W.shape} must be [m, {d}]")
+    m = W.shape[0]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    out = np.empty(x.shape[:-1] + (m,))
+    rc = _load().oracle_random_features(_ptr(x), _ptr(W), _ptr(out), rows, d, m)
+    if rc:
+        raise RuntimeError("oracle_random_features failed")
+    return out

@@ -47,6 +47,12 @@ static double phi(double x) { return x > 0.0 ? x + 1.0 : exp(x); }
 /* Denominator clamp used by the pages' examples: max(den, eps). */
 static double clamp_den(double den, double eps) { return den < eps ? eps : den; }
 
+/* [P1] "Mapas de características" lists the feature maps: kind 0 is the
+ * canonical elu(x) + 1 above; kind 1 is the identity map phi(x) = x, which
+ * "reduces the layer to a simple bilinear attention".  (The random-feature
+ * map changes the feature dimension and is oracle_random_features below.)  */
+static double feature(double x, int kind) { return kind == 1 ? x : phi(x); }
+
 void oracle_phi(const double *x, double *out, long n)
 {
     for (long i = 0; i < n; ++i) out[i] = phi(x[i]);
@@ -64,6 +70,9 @@ typedef struct {
     int BH, N, d, dv, causal, chunk;
     double eps;
     const double *gamma;       /* nullable: per-head decay (recurrent form only) */
+    const double *gate;        /* nullable: per-token gate [BH][N][gate_dim] (recurrent form) */
+    int gate_dim;              /* 1 (one gate per token) or d (one per token and feature) */
+    int phi_kind;              /* feature map, see feature() */
     int h_begin, h_end;
 } job_t;
 
@@ -74,9 +83,16 @@ typedef struct {
  * + phi(k_t) v_t^T, one gamma per head for the multi-scale retention the
  * section mentions) the state is first multiplied by gamma; z is decayed
  * the same way so that y_t stays a normalised average.                    */
+/* With a gate ([P1] "Variantes y extensiones": gated linear attention
+ * replaces the scalar decay by a data-dependent gate; the pages print no
+ * equation, so the reading is the decay's update with the decay taken per
+ * token): S_t = diag(g_t) S_{t-1} + phi(k_t) v_t^T and z_t = g_t * z_{t-1} +
+ * phi(k_t), g_t in [0, 1] given per token as one value (gate_dim = 1) or one
+ * per feature row of S (gate_dim = d, the per-channel gates of the Gated
+ * DeltaNet passage).                                                         */
 static void head_recurrent(const job_t *J, int h)
 {
-    const int N = J->N, d = J->d, dv = J->dv;
+    const int N = J->N, d = J->d, dv = J->dv, fkind = J->phi_kind;
     const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
     const double *v = J->v + (long)h * N * dv;
     double *y = J->y + (long)h * N * dv;
@@ -86,10 +102,18 @@ static void head_recurrent(const job_t *J, int h)
     if (J->S_in) memcpy(S, J->S_in + (long)h * d * dv, sizeof(double) * d * dv);
     if (J->z_in) memcpy(z, J->z_in + (long)h * d, sizeof(double) * d);
     for (int t = 0; t < N; ++t) {
-        for (int a = 0; a < d; ++a) fk[a] = phi(k[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) fk[a] = feature(k[(long)t * d + a], fkind);
         if (J->gamma) {
             const double g = J->gamma[h];
             for (int a = 0; a < d; ++a) {
+                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;
+                z[a] *= g;
+            }
+        }
+        if (J->gate) {
+            const double *gt = J->gate + ((long)h * N + t) * J->gate_dim;
+            for (int a = 0; a < d; ++a) {
+                const double g = gt[J->gate_dim == 1 ? 0 : a];
                 for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;
                 z[a] *= g;
             }
@@ -98,7 +122,7 @@ static void head_recurrent(const job_t *J, int h)
             for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fk[a] * v[(long)t * dv + b];
             z[a] += fk[a];
         }
-        for (int a = 0; a < d; ++a) fq[a] = phi(q[(long)t * d + a]);
+        for (int a = 0; a < d; ++a) fq[a] = feature(q[(long)t * d + a], fkind);
         double den = 0.0;
         for (int a = 0; a < d; ++a) den += fq[a] * z[a];
         den = clamp_den(den, J->eps);
@@ -118,7 +142,7 @@ static void head_recurrent(const job_t *J, int h)
  * y_i = phi(q_i)^T S / max(phi(q_i)^T z, eps).                             */
 static void head_noncausal(const job_t *J, int h)
 {
-    const int N = J->N, d = J->d, dv = J->dv;
+    const int N = J->N, d = J->d, dv = J->dv, fkind = J->phi_kind;
     const double *q = J->q + (long)h * N * d, *k = J->k + (long)h * N * d;
     const double *v = J->v + (long)h * N * dv;
     double *y = J->y + (long)h * N * dv;
@@ -126,14 +150,14 @@ static void head_noncausal(const job_t *J, int h)
     double *z = calloc((size_t)d, sizeof(double));
     double *f = malloc(sizeof(double) * d);
     for (int j = 0; j < N; ++j) {
-        for (int a = 0; a < d; ++a) f[a] = phi(k[(long)j * d + a]);
+        for (int a = 0; a < d; ++a) f[a] = feature(k[(long)j * d + a], fkind);
         for (int a = 0; a < d; ++a) {
             for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += f[a] * v[(long)j * dv + b];
             z[a] += f[a];
         }
     }
     for (int i = 0; i < N; ++i) {
-        for (int a = 0; a < d; ++a) f[a] = phi(q[(long)i * d + a]);
+        for (int a = 0; a < d; ++a) f[a] = feature(q[(long)i * d + a], fkind);
         double den = 0.0;
         for (int a = 0; a < d; ++a) den += f[a] * z[a];
         den = clamp_den(den, J->eps);
@@ -164,7 +188,8 @@ static void head_quadratic(const job_t *J, int h)
         for (int b = 0; b < dv; ++b) num[b] = 0.0;
         for (int j = 0; j <= jmax; ++j) {
             double w = 0.0;
-            for (int a = 0; a < d; ++a) w += phi(q[(long)i * d + a]) * phi(k[(long)j * d + a]);
+            for (int a = 0; a < d; ++a)
+                w += feature(q[(long)i * d + a], J->phi_kind) * feature(k[(long)j * d + a], J->phi_kind);
             den += w;
             for (int b = 0; b < dv; ++b) num[b] += w * v[(long)j * dv + b];
         }
@@ -315,6 +340,72 @@ int oracle_quadratic(const double *q, const double *k, const double *v, double *
     J.kind = 2; J.q = q; J.k = k; J.v = v; J.y = y; J.BH = BH; J.N = N; J.d = d; J.dv = dv;
     J.eps = eps; J.causal = causal;
     return run_jobs(J, nthreads);
+}
+
+/* Causal recurrent form with a gate per token (gate_dim = 1) or per token
+ * and feature (gate_dim = d), gate[BH][N][gate_dim] in [0, 1] (NULL: none),
+ * and feature map phi_kind (see feature()).                               */
+int oracle_causal_gated(const double *q, const double *k, const double *v, double *y,
+                        int BH, int N, int d, int dv, double eps, int phi_kind,
+                        const double *gate, int gate_dim, const double *S_in,
+                        const double *z_in, double *S_out, double *z_out, int nthreads)
+{
+    if (gate && gate_dim != 1 && gate_dim != d) return 1;
+    if (phi_kind != 0 && phi_kind != 1) return 1;
+    job_t J = {0};
+    J.kind = 0; J.q = q; J.k = k; J.v = v; J.y = y; J.S_in = S_in; J.z_in = z_in;
+    J.S_out = S_out; J.z_out = z_out; J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps;
+    J.gate = gate; J.gate_dim = gate ? gate_dim : 1; J.phi_kind = phi_kind;
+    return run_jobs(J, nthreads);
+}
+
+/* Non-causal matrix form with feature map phi_kind. */
+int oracle_noncausal_phi(const double *q, const double *k, const double *v, double *y,
+                         int BH, int N, int d, int dv, double eps, int phi_kind,
+                         double *S_out, double *z_out, int nthreads)
+{
+    if (phi_kind != 0 && phi_kind != 1) return 1;
+    job_t J = {0};
+    J.kind = 1; J.q = q; J.k = k; J.v = v; J.y = y; J.S_out = S_out; J.z_out = z_out;
+    J.BH = BH; J.N = N; J.d = d; J.dv = dv; J.eps = eps; J.phi_kind = phi_kind;
+    return run_jobs(J, nthreads);
+}
+
+/* Brute-force pairwise form with feature map phi_kind. */
+int oracle_quadratic_phi(const double *q, const double *k, const double *v, double *y,
+                         int BH, int N, int d, int dv, double eps, int causal, int phi_kind,
+                         int nthreads)
+{
+    if (phi_kind != 0 && phi_kind != 1) return 1;
+    job_t J = {0};
+    J.kind = 2; J.q = q; J.k = k; J.v = v; J.y = y; J.BH = BH; J.N = N; J.d = d; J.dv = dv;
+    J.eps = eps; J.causal = causal; J.phi_kind = phi_kind;
+    return run_jobs(J, nthreads);
+}
+
+/* [P1] "Mapas de características", random-feature maps (Performer): positive
+ * random features phi(x) proportional to exp(W x - ||x||^2 / 2), W holding
+ * the random projections as rows.  The constant of proportionality is read
+ * as 1 / sqrt(m) for m rows, so that phi(q) . phi(k) is the average over the
+ * m rows w of exp(w.q + w.k - (||q||^2 + ||k||^2) / 2); for Gaussian rows
+ * w ~ N(0, I) its expectation is exp(q . k), the softmax kernel the section
+ * says the map recovers in expectation.  x: [rows][d], W: [m][d] (given:
+ * the random numbers are an input), out: [rows][m].                          */
+int oracle_random_features(const double *x, const double *W, double *out, long rows, int d,
+                           int m)
+{
+    if (rows < 0 || d <= 0 || m <= 0) return 1;
+    const double scale = 1.0 / sqrt((double)m);
+    for (long r = 0; r < rows; ++r) {
+        double nrm = 0.0;
+        for (int a = 0; a < d; ++a) nrm += x[r * d + a] * x[r * d + a];
+        for (int f = 0; f < m; ++f) {
+            double wx = 0.0;
+            for (int a = 0; a < d; ++a) wx += W[(long)f * d + a] * x[r * d + a];
+            out[r * m + f] = scale * exp(wx - 0.5 * nrm);
+        }
+    }
+    return 0;
 }
 
 /* Blockwise causal form with block length `chunk` (>= 1). */

@@ -47,6 +47,15 @@ MUTANTS = {
                            "for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g * g;"),
     "bwd_decay_state_grad_unscaled": ("J->dS_in[(long)h * d * dv + i] = gam * S[i];",
                                       "J->dS_in[(long)h * d * dv + i] = S[i];"),
+    # gate and feature maps
+    "gate_skips_z": ("                const double g = gt[J->gate_dim == 1 ? 0 : a];\n                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;\n                z[a] *= g;",
+                     "                const double g = gt[J->gate_dim == 1 ? 0 : a];\n                for (int b = 0; b < dv; ++b) S[(long)a * dv + b] *= g;"),
+    "gate_first_feature_only": ("const double g = gt[J->gate_dim == 1 ? 0 : a];", "const double g = gt[0];"),
+    "gate_previous_token": ("const double *gt = J->gate + ((long)h * N + t) * J->gate_dim;",
+                            "const double *gt = J->gate + ((long)h * N + (t > 0 ? t - 1 : 0)) * J->gate_dim;"),
+    "identity_map_is_elu": ("return kind == 1 ? x : phi(x);", "return phi(x);"),
+    "random_features_no_norm_term": ("scale * exp(wx - 0.5 * nrm)", "scale * exp(wx)"),
+    "random_features_scale_1_over_m": ("1.0 / sqrt((double)m)", "1.0 / (double)m"),
     "bwd_decay_skips_reverse_z": ("                z[a] *= gam;\n            }\n        for (int a = 0; a < d; ++a) {\n            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a]",
                                   "            }\n        for (int a = 0; a < d; ++a) {\n            for (int b = 0; b < dv; ++b) S[(long)a * dv + b] += fq[a]"),
 }
@@ -107,6 +116,28 @@ def _pins_pass() -> bool:
         if not np.allclose(oracle.causal_recurrent_decay(q, k, v, [gam]),
                            brute_decay(q, k, v, gam), rtol=1e-11):
             return False
+    # gates and feature maps: hand examples, the closed form with products of
+    # gates (both gate shapes, both maps), the random features' closed form
+    from tests import gated_pins
+    with open(os.path.join(HERE, "golden", "gated_examples.json")) as f:
+        for c in json.load(f)["cases"]:
+            y = oracle.causal_gated(*(np.array(c[x], dtype=np.float64) for x in ("q", "k", "v")),
+                                    gate=np.array(c["gate"]), phi=c["phi"], eps=c["eps"])
+            if not np.allclose(y, np.array(c["y"]), rtol=1e-12):
+                return False
+    r = np.random.default_rng(6)
+    qg, kg = (np.abs(r.standard_normal((25, 3))) + 0.1 for _ in range(2))
+    vg = r.standard_normal((25, 2))
+    for kind in ("elu1", "identity"):
+        for shape in ((25,), (25, 3)):
+            g = r.uniform(0.1, 1.0, shape)
+            if not np.allclose(oracle.causal_gated(qg, kg, vg, gate=g, phi=kind),
+                               gated_pins.brute_gated(qg, kg, vg, g, kind), rtol=1e-11):
+                return False
+    W = r.standard_normal((16, 3))
+    if not np.allclose(oracle.random_features(qg, W), gated_pins.random_features_np(qg, W),
+                       rtol=1e-12):
+        return False
     return True
 
 

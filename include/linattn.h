@@ -77,6 +77,12 @@ typedef enum {
     LA_DTYPE_BF16 = 1         /* bfloat16 q, k, v                              */
 } la_dtype;
 
+/* The element-wise feature maps of "Mapas de características". */
+typedef enum {
+    LA_PHI_ELU1 = 0,          /* phi(x) = elu(x) + 1 (the canonical map)       */
+    LA_PHI_IDENTITY = 1       /* phi(x) = x (bilinear attention)               */
+} la_phi;
+
 /* Human-readable name of a status code (static string, never NULL). */
 LA_API const char *la_status_string(la_status s);
 
@@ -163,6 +169,78 @@ LA_API la_status la_forward_causal_decay(const void *q, const void *k, const voi
 LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *v, float *y,
                                       float *S, float *z, int B, int H, int d, int dv,
                                       la_dtype dt, float eps, const float *gamma, void *stream);
+
+/*
+ * Gated causal forward ("Linear Attention/es", "Variantes y extensiones":
+ * gated linear attention replaces RetNet's scalar decay by a data-dependent
+ * gate; the pages print no equation, and the update is read as the decay's
+ * with the decay taken per token):
+ *   S_t = diag(g_t) S_{t-1} + phi(k_t) v_t^T,  z_t = g_t * z_{t-1} + phi(k_t),
+ *   y_t = phi(q_t)^T S_t / max(phi(q_t)^T z_t, eps),
+ * g_t in [0, 1] given per token: gate is a DEVICE float32 array
+ * [B][H][N][gate_dim], 4-byte aligned, with gate_dim = 1 (one gate per token;
+ * row a of S and z[a] all scale by it) or gate_dim = d (one per token and
+ * feature row of S); gate = NULL means no gate (g_t = 1), which with phi =
+ * LA_PHI_IDENTITY gives the identity-map swap of "Mapas de características"
+ * (the layer becomes a bilinear attention).  The gate values are not
+ * checked.  phi: LA_PHI_ELU1 or LA_PHI_IDENTITY (else LA_ERR_UNSUPPORTED);
+ * with the identity map the denominator can be <= 0, and the clamp then gives
+ * num / eps.  Layouts, sizes, the initial / final state and the errors as in
+ * la_forward_causal; no workspace.  Every head runs on the CUDA cores, token
+ * by token in float32 (both input dtypes), one CTA per head.
+ */
+LA_API la_status la_forward_causal_gated(const void *q, const void *k, const void *v, float *y,
+                                         int B, int H, int N, int d, int dv, la_dtype dt,
+                                         float eps, la_phi phi, const float *gate, int gate_dim,
+                                         const float *S_in, const float *z_in, float *S_out,
+                                         float *z_out, void *stream);
+
+/*
+ * One gated decode step in place on (S, z):
+ *   S <- diag(g) S + phi(k) v^T,  z <- g * z + phi(k),  y = phi(q)^T S / max(phi(q)^T z, eps),
+ * gate a DEVICE float32 array [B][H][gate_dim] (gate_dim 1 or d; NULL: no
+ * gate), phi as in la_forward_causal_gated; the rest as in la_decode_step.
+ */
+LA_API la_status la_decode_step_gated(const void *q, const void *k, const void *v, float *y,
+                                      float *S, float *z, int B, int H, int d, int dv,
+                                      la_dtype dt, float eps, la_phi phi, const float *gate,
+                                      int gate_dim, void *stream);
+
+/*
+ * Workspace size in bytes for la_forward_noncausal_phi: that of
+ * la_forward_noncausal for LA_PHI_ELU1; for LA_PHI_IDENTITY the status
+ * header and the split-N partial sums of the CUDA-core path.  0 for
+ * unsupported arguments.
+ */
+LA_API size_t la_noncausal_phi_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt,
+                                               la_phi phi);
+
+/*
+ * Non-causal forward with a choice of element-wise feature map ("Mapas de
+ * características"): la_forward_noncausal for LA_PHI_ELU1; for
+ * LA_PHI_IDENTITY the same sums with phi(x) = x, on the CUDA cores in
+ * float32.  Workspace: la_noncausal_phi_workspace_bytes.
+ */
+LA_API la_status la_forward_noncausal_phi(const void *q, const void *k, const void *v, float *y,
+                                          int B, int H, int N, int d, int dv, la_dtype dt,
+                                          float eps, la_phi phi, float *S_out, float *z_out,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Positive random features ("Mapas de características", Performer: phi(x)
+ * proportional to exp(W x - ||x||^2 / 2), W random projections; the constant
+ * is taken as 1 / sqrt(m), so that phi(q) . phi(k) averages exp(q . k)
+ * estimates over the m rows of W):
+ *   phi_out[r][f] = exp(W[f] . x[r] - ||x[r]||^2 / 2) / sqrt(m)
+ * x: DEVICE [rows][d] of dtype dt (aligned to its element size); W: DEVICE
+ * float32 [m][d], drawn by the caller (the library draws no random numbers);
+ * phi_out: DEVICE float32 [rows][m], 4-byte aligned, overlapping neither.
+ * 1 <= d <= 128, 1 <= m <= 256, else LA_ERR_INVALID_ARG.  The features then
+ * go to the attention calls as float32 inputs with LA_PHI_IDENTITY and
+ * d = m (m in {32, 64, 128}).  Computed in float32 on the CUDA cores.
+ */
+LA_API la_status la_random_features(const void *x, float *phi_out, long long rows, int d, int m,
+                                    la_dtype dt, const float *W, void *stream);
 
 /*
  * Workspace size in bytes for la_backward_causal (0 for N == 0 or

@@ -248,6 +248,118 @@ la_status la_decode_step_decay(const void *q, const void *k, const void *v, floa
     return from_cuda(launch_decode_simt(a));
 }
 
+la_status la_forward_causal_gated(const void *q, const void *k, const void *v, float *y, int B,
+                                  int H, int N, int d, int dv, la_dtype dt, float eps, la_phi phi,
+                                  const float *gate, int gate_dim, const float *S_in,
+                                  const float *z_in, float *S_out, float *z_out, void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (phi != LA_PHI_ELU1 && phi != LA_PHI_IDENTITY) return LA_ERR_UNSUPPORTED;
+    if (gate && gate_dim != 1 && gate_dim != d) return LA_ERR_INVALID_ARG;
+    if (gate && (reinterpret_cast<uintptr_t>(gate) & 3u) != 0) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S_in, z_in, false)) != LA_OK) return st;
+    if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
+    const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
+    const size_t gb = gate ? T * gate_dim * 4 : 0;
+    if (overlap(y, T * dv * 4, S_in, sb) || overlap(y, T * dv * 4, z_in, zb) ||
+        overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb) ||
+        overlap(y, T * dv * 4, gate, gb) || overlap(S_out, sb, gate, gb) ||
+        overlap(z_out, zb, gate, gb))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {  // no tokens: the final state is the initial state
+        if (S_out) {
+            cudaError_t e = cudaSuccess;
+            if (!S_in) e = cudaMemsetAsync(S_out, 0, sb, s);
+            else if (S_in != S_out)
+                e = cudaMemcpyAsync(S_out, S_in, sb, cudaMemcpyDeviceToDevice, s);
+            if (e == cudaSuccess) {
+                if (!z_in) e = cudaMemsetAsync(z_out, 0, zb, s);
+                else if (z_in != z_out)
+                    e = cudaMemcpyAsync(z_out, z_in, zb, cudaMemcpyDeviceToDevice, s);
+            }
+            return from_cuda(e);
+        }
+        return LA_OK;
+    }
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out, nullptr, 0, s};
+    a.phi = (int)phi;
+    a.gate = gate;
+    a.gate_dim = gate ? gate_dim : 1;
+    return from_cuda(launch_causal_gated(a));
+}
+
+la_status la_decode_step_gated(const void *q, const void *k, const void *v, float *y, float *S,
+                               float *z, int B, int H, int d, int dv, la_dtype dt, float eps,
+                               la_phi phi, const float *gate, int gate_dim, void *stream) {
+    la_status st = check_common(q, k, v, y, B, H, 1, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (phi != LA_PHI_ELU1 && phi != LA_PHI_IDENTITY) return LA_ERR_UNSUPPORTED;
+    if (gate && gate_dim != 1 && gate_dim != d) return LA_ERR_INVALID_ARG;
+    if (gate && (reinterpret_cast<uintptr_t>(gate) & 3u) != 0) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S, z, true)) != LA_OK) return st;
+    const size_t yb = (size_t)B * H * dv * 4, sb = (size_t)B * H * d * dv * 4,
+                 zb = (size_t)B * H * d * 4, gb = gate ? (size_t)B * H * gate_dim * 4 : 0;
+    if (overlap(y, yb, S, sb) || overlap(y, yb, z, zb) || overlap(S, sb, z, zb) ||
+        overlap(gate, gb, S, sb) || overlap(gate, gb, z, zb) || overlap(gate, gb, y, yb))
+        return LA_ERR_INVALID_ARG;
+    DecodeArgs a{q, k, v, y, S, z, B, H, d, dv, dt, eps, static_cast<cudaStream_t>(stream)};
+    a.phi = (int)phi;
+    a.gate = gate;
+    a.gate_dim = gate ? gate_dim : 1;
+    return from_cuda(launch_decode_simt(a));
+}
+
+size_t la_noncausal_phi_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt,
+                                        la_phi phi) {
+    if (phi == LA_PHI_ELU1) return la_noncausal_workspace_bytes(B, H, N, d, dv, dt);
+    if (phi != LA_PHI_IDENTITY || B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    return noncausal_simt_workspace(B * H, N, d, dv);
+}
+
+la_status la_forward_noncausal_phi(const void *q, const void *k, const void *v, float *y, int B,
+                                   int H, int N, int d, int dv, la_dtype dt, float eps,
+                                   la_phi phi, float *S_out, float *z_out, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    if (phi == LA_PHI_ELU1)
+        return la_forward_noncausal(q, k, v, y, B, H, N, d, dv, dt, eps, S_out, z_out, workspace,
+                                    workspace_bytes, stream);
+    if (phi != LA_PHI_IDENTITY) return LA_ERR_UNSUPPORTED;
+    la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
+    if (st != LA_OK) return st;
+    if (N < 1) return LA_ERR_INVALID_ARG;
+    if ((st = check_state(S_out, z_out, false)) != LA_OK) return st;
+    const size_t T = (size_t)B * H * N, sb = (size_t)B * H * d * dv * 4, zb = (size_t)B * H * d * 4;
+    if (overlap(y, T * dv * 4, S_out, sb) || overlap(y, T * dv * 4, z_out, zb))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = la_noncausal_phi_workspace_bytes(B, H, N, d, dv, dt, phi);
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, nullptr, nullptr, S_out, z_out,
+              workspace, workspace_bytes, s};
+    a.phi = (int)phi;
+    return from_cuda(launch_noncausal_simt(a));
+}
+
+la_status la_random_features(const void *x, float *phi_out, long long rows, int d, int m,
+                             la_dtype dt, const float *W, void *stream) {
+    if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+    if (rows < 0 || d < 1 || d > 128 || m < 1 || m > 256) return LA_ERR_INVALID_ARG;
+    if (rows == 0) return LA_OK;
+    if (!x || !phi_out || !W) return LA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & (esize(dt) - 1)) != 0 ||
+        (reinterpret_cast<uintptr_t>(phi_out) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(W) & 3u) != 0)
+        return LA_ERR_INVALID_ARG;
+    const size_t ob = (size_t)rows * m * 4;
+    if (overlap(phi_out, ob, x, (size_t)rows * d * esize(dt)) ||
+        overlap(phi_out, ob, W, (size_t)m * d * 4))
+        return LA_ERR_INVALID_ARG;
+    return from_cuda(launch_random_features(x, phi_out, rows, d, m, dt, W,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 size_t la_causal_backward_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt) {
     if (B < 1 || H < 1 || N < 1 || !dim_ok(d) || !dim_ok(dv)) return 0;
     if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return 0;

@@ -4,7 +4,10 @@
 //   S <- S + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T S / max(phi(q)^T z, eps)
 // (update first, then read, as in "La formulación recurrente paso a paso").
 // With a per-head decay gamma (RetNet in "Variantes y extensiones":
-// S <- gamma S + phi(k) v^T, and z alike) the stored state is scaled first.
+// S <- gamma S + phi(k) v^T, and z alike) the stored state is scaled first;
+// with a gate (gated linear attention, same section) row a of S and z[a] are
+// scaled by the step's gate g (one value, or one per feature row).  The
+// feature map is elu + 1 or the identity ("Mapas de características").
 //
 // The step is bound by HBM: per head it reads and writes d*dv*4 bytes of S
 // and does 2*d*dv FMAs.  One CTA of 8 warps owns one head.  Warp w owns the
@@ -49,12 +52,14 @@ template <> struct FVec<4> {
 
 constexpr int kDecodeWarps = 8;
 
-template <int D, int DV, typename T, bool DECAY>
+// MODE: 0 plain, 1 per-head decay gamma[H], 2 gate[head][gate_dim]
+template <int D, int DV, typename T, int MODE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    float *__restrict__ y, float *__restrict__ S, float *__restrict__ z, float eps,
-                   const float *__restrict__ gamma, int H)
+                   const float *__restrict__ gamma, int H, int phi, int gate_dim)
 {
+    constexpr bool DECAY = MODE != 0;
     constexpr int NW = kDecodeWarps;
     constexpr int RPW = D / NW;   // rows of S per warp
     constexpr int VEC = DV / 32;  // columns per lane
@@ -67,7 +72,10 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long qk_off = (long)head * D, v_off = (long)head * DV;
     float *Sh = S + (long)head * D * DV;
-    const float g = DECAY ? gamma[head % H] : 1.f;
+    // the multiplier of row a of the stored state
+    const float *gh = MODE == 2 ? gamma + (long)head * gate_dim : nullptr;
+    const float g1 = MODE == 1 ? gamma[head % H] : (MODE == 2 ? gh[0] : 1.f);
+    auto gate_of = [&](int a) { return MODE == 2 && gate_dim > 1 ? gh[a] : g1; };
 
     // Issue the state loads first: they are the whole cost of the step.
     FVec<VEC> s[RPW];
@@ -77,11 +85,11 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     // phi(q), phi(k), v to shared; z update and the denominator phi(q)^T z_new.
     float dp = 0.f;
     for (int i = tid; i < D; i += NW * 32) {
-        const float fq = phi_f(to_f(q[qk_off + i]));
-        const float fk = phi_f(to_f(k[qk_off + i]));
+        const float fq = feature_f(to_f(q[qk_off + i]), phi);
+        const float fk = feature_f(to_f(k[qk_off + i]), phi);
         fq_s[i] = fq;
         fk_s[i] = fk;
-        const float zn = DECAY ? fmaf(g, z[qk_off + i], fk) : z[qk_off + i] + fk;
+        const float zn = DECAY ? fmaf(gate_of(i), z[qk_off + i], fk) : z[qk_off + i] + fk;
         z[qk_off + i] = zn;
         dp = fmaf(fq, zn, dp);
     }
@@ -96,7 +104,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         const int a = warp * RPW + r;
-        const float fk = fk_s[a], fq = fq_s[a];
+        const float fk = fk_s[a], fq = fq_s[a], g = DECAY ? gate_of(a) : 1.f;
 #pragma unroll
         for (int c = 0; c < VEC; ++c) {
             const float sn = fmaf(fk, vv[c], DECAY ? g * s[r].x[c] : s[r].x[c]);
@@ -117,19 +125,24 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     }
 }
 
-template <int D, int DV, typename T, bool DECAY>
+template <int D, int DV, typename T, int MODE>
 cudaError_t launch_typed(const DecodeArgs &a) {
-    decode_step_kernel<D, DV, T, DECAY><<<a.B * a.H, kDecodeWarps * 32, 0, a.stream>>>(
-        (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.S, a.z, a.eps, a.gamma, a.H);
+    decode_step_kernel<D, DV, T, MODE><<<a.B * a.H, kDecodeWarps * 32, 0, a.stream>>>(
+        (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.S, a.z, a.eps,
+        MODE == 2 ? a.gate : a.gamma, a.H, a.phi, a.gate_dim);
     return cudaGetLastError();
+}
+
+template <int D, int DV, typename T>
+cudaError_t launch_mode(const DecodeArgs &a) {
+    if (a.gate) return launch_typed<D, DV, T, 2>(a);
+    return a.gamma ? launch_typed<D, DV, T, 1>(a) : launch_typed<D, DV, T, 0>(a);
 }
 
 template <int D, int DV>
 cudaError_t launch_dv(const DecodeArgs &a) {
-    if (a.dt == LA_DTYPE_BF16)
-        return a.gamma ? launch_typed<D, DV, __nv_bfloat16, true>(a)
-                       : launch_typed<D, DV, __nv_bfloat16, false>(a);
-    return a.gamma ? launch_typed<D, DV, float, true>(a) : launch_typed<D, DV, float, false>(a);
+    return a.dt == LA_DTYPE_BF16 ? launch_mode<D, DV, __nv_bfloat16>(a)
+                                 : launch_mode<D, DV, float>(a);
 }
 
 template <int D>

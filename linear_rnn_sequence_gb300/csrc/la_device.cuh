@@ -12,6 +12,10 @@ namespace la {
 // underflows for x below about -87.
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
+// The feature map of a call: elu(x) + 1 (kind 0) or the identity (kind 1),
+// the two element-wise maps of "Mapas de características".
+__device__ __forceinline__ float feature_f(float x, int kind) { return kind ? x : phi_f(x); }
+
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {

@@ -27,6 +27,9 @@ struct FwdArgs {
     // decay only: heads whose gamma passes decay_on_tensor_cores were already
     // computed by the tensor-core kernel; the CUDA-core kernel skips them
     bool skip_tc_heads = false;
+    int phi = 0;                    // feature map: 0 elu + 1, 1 identity (CUDA-core kernels)
+    const float *gate = nullptr;    // per-token gate [B][H][N][gate_dim] (device), null: none
+    int gate_dim = 1;               // 1 or d
     int BH() const { return B * H; }
 };
 
@@ -46,6 +49,9 @@ struct DecodeArgs {
     float eps;
     cudaStream_t stream;
     const float *gamma = nullptr;   // per-head decay [H] (device), null: none
+    int phi = 0;                    // feature map: 0 elu + 1, 1 identity
+    const float *gate = nullptr;    // per-step gate [B][H][gate_dim] (device), null: none
+    int gate_dim = 1;               // 1 or d
 };
 
 // Gradients of the causal form; pointers are device pointers.
@@ -94,6 +100,11 @@ cudaError_t launch_causal_tc(const FwdArgs &a);
 bool noncausal_tc_supported(const FwdArgs &a);
 size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
 cudaError_t launch_noncausal_tc(const FwdArgs &a);
+
+// gated recurrence and feature maps (CUDA cores, fp32)
+cudaError_t launch_causal_gated(const FwdArgs &a);
+cudaError_t launch_random_features(const void *x, float *out, long long rows, int d, int m,
+                                   la_dtype dt, const float *W, cudaStream_t stream);
 
 // gradients of the causal form (CUDA cores, fp32)
 size_t causal_backward_workspace(int BH, int N, int d, int dv);

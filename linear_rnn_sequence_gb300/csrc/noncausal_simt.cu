@@ -1,4 +1,5 @@
-// noncausal_simt.cu -- non-causal linear attention on CUDA cores, fp32.
+// noncausal_simt.cu -- non-causal linear attention on CUDA cores, fp32, with
+// the feature map elu + 1 or the identity ("Mapas de características").
 //
 // "Linear Attention/es", "Reformulación con núcleos": S = sum_j phi(k_j) v_j^T
 // and z = sum_j phi(k_j) do not depend on the query, so they are reduced once
@@ -29,7 +30,7 @@ int num_splits(int BH, int N) {
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 state_partials_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, int DV, int nsplit,
-                      float *__restrict__ Sp, float *__restrict__ zp)
+                      float *__restrict__ Sp, float *__restrict__ zp, int phi)
 {
     constexpr int QS = D + 1, RPT = D / 8;
     __shared__ float Ks[kC * QS];
@@ -49,7 +50,7 @@ state_partials_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, i
         __syncthreads();
         for (int e = tid; e < kC * D; e += kThreads) {
             const int j = e / D, a = e % D;
-            Ks[j * QS + a] = j < L ? phi_f(to_f(kh[(long)(t0 + j) * D + a])) : 0.f;
+            Ks[j * QS + a] = j < L ? feature_f(to_f(kh[(long)(t0 + j) * D + a]), phi) : 0.f;
         }
         for (int e = tid; e < kC * kCols; e += kThreads) {
             const int j = e / kCols, c = e % kCols;
@@ -74,7 +75,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 queries_kernel(const T *__restrict__ q, float *__restrict__ y, int N, int DV, int nsplit,
                const float *__restrict__ Sp, const float *__restrict__ zp, float eps,
-               float *__restrict__ S_out, float *__restrict__ z_out)
+               float *__restrict__ S_out, float *__restrict__ z_out, int phi)
 {
     constexpr int QS = D + 1;
     extern __shared__ float sm[];
@@ -101,7 +102,7 @@ queries_kernel(const T *__restrict__ q, float *__restrict__ y, int N, int DV, in
     const T *qh = q + (long)head * N * D;
     for (int e = tid; e < kTile * D; e += kThreads) {
         const int i = e / D, a = e % D;
-        Qs[i * QS + a] = i < L ? phi_f(to_f(qh[(long)(t0 + i) * D + a])) : 0.f;
+        Qs[i * QS + a] = i < L ? feature_f(to_f(qh[(long)(t0 + i) * D + a]), phi) : 0.f;
     }
     __syncthreads();
     if (blockIdx.y == 0) {
@@ -140,7 +141,7 @@ cudaError_t launch_t(const FwdArgs &a) {
     float *Sp = reinterpret_cast<float *>(static_cast<char *>(a.ws) + sizeof(WsHeader));
     float *zp = Sp + (size_t)BH * ns * a.d * a.dv;
     state_partials_kernel<D, T><<<dim3(BH, ns, a.dv / kCols), kThreads, 0, a.stream>>>(
-        (const T *)a.k, (const T *)a.v, a.N, a.dv, ns, Sp, zp);
+        (const T *)a.k, (const T *)a.v, a.N, a.dv, ns, Sp, zp, a.phi);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = sizeof(float) * (D * kCols + D + kTile * (D + 1) + kTile);
@@ -148,7 +149,7 @@ cudaError_t launch_t(const FwdArgs &a) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<dim3(BH, (a.N + kTile - 1) / kTile, a.dv / kCols), kThreads, smem, a.stream>>>(
-        (const T *)a.q, a.y, a.N, a.dv, ns, Sp, zp, a.eps, a.S_out, a.z_out);
+        (const T *)a.q, a.y, a.N, a.dv, ns, Sp, zp, a.eps, a.S_out, a.z_out, a.phi);
     return cudaGetLastError();
 }
 

@@ -10,6 +10,8 @@ Names follow the C ABI:
 * ``forward_causal``    -> ``la_forward_causal``
 * ``forward_noncausal`` -> ``la_forward_noncausal``
 * ``decode_step``       -> ``la_decode_step``
+* ``forward_causal_gated``, ``decode_step_gated``, ``forward_noncausal_phi``,
+  ``random_features`` -> the gated and feature-map entry points
 """
 from __future__ import annotations
 
@@ -23,6 +25,7 @@ from . import _build
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+PHI = {"elu1": 0, "identity": 1}   # la_phi
 
 _lock = threading.Lock()
 _lib = None
@@ -94,6 +97,19 @@ def lib():
             L.la_forward_noncausal_noalloc.restype = i
             L.la_noalloc_status.argtypes = [vp]
             L.la_noalloc_status.restype = i
+            L.la_forward_causal_gated.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i,
+                                                  vp, vp, vp, vp, vp]
+            L.la_forward_causal_gated.restype = i
+            L.la_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
+                                               vp]
+            L.la_decode_step_gated.restype = i
+            L.la_noncausal_phi_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+            L.la_noncausal_phi_workspace_bytes.restype = sz
+            L.la_forward_noncausal_phi.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp,
+                                                   vp, sz, vp]
+            L.la_forward_noncausal_phi.restype = i
+            L.la_random_features.argtypes = [vp, vp, ctypes.c_longlong, i, i, i, vp, vp]
+            L.la_random_features.restype = i
             _lib = L
     return _lib
 
@@ -400,3 +416,94 @@ def workspace_header(workspace) -> tuple[int, int]:
 def set_fault(drop_load_item: int = -1, wait_limit_ns: int = 0) -> None:
     """Test hook: see la_debug_set_fault in include/linattn.h."""
     lib().la_debug_set_fault(int(drop_load_item), int(wait_limit_ns))
+
+def _gate_dim(gate, lead, d):
+    """gate_dim of a gate tensor whose leading shape is ``lead`` (1 or d)."""
+    if gate is None:
+        return 1
+    if gate.dtype != torch.float32:
+        raise TypeError("gate must be float32")
+    if tuple(gate.shape) == tuple(lead):
+        return 1
+    if tuple(gate.shape) == tuple(lead) + (d,):
+        return d
+    raise ValueError(f"gate shape {tuple(gate.shape)} must be {tuple(lead)} or {tuple(lead) + (d,)}")
+
+
+def forward_causal_gated(q, k, v, gate=None, phi="elu1", eps: float = 1e-6, S_in=None,
+                         z_in=None, return_state=False, out=None, S_out=None, z_out=None,
+                         stream=None):
+    """Gated causal attention (CUDA cores, fp32).  gate: None, [B,H,N] or [B,H,N,d]
+    float32; phi: "elu1" or "identity".  Returns y (and the final (S, z))."""
+    _check_cuda(q, k, v, gate, S_in, z_in, out, S_out, z_out)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v shapes / dtypes disagree")
+    gd = _gate_dim(gate, (B, H, N), d)
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    st = lib().la_forward_causal_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                       float(eps), PHI[phi], _ptr(gate), gd, _ptr(S_in),
+                                       _ptr(z_in), _ptr(S_out), _ptr(z_out),
+                                       _stream_handle(stream, q.device))
+    _raise(st, "la_forward_causal_gated")
+    return (y, S_out, z_out) if return_state else y
+
+
+def decode_step_gated(q, k, v, S, z, gate=None, phi="elu1", eps: float = 1e-6, out=None,
+                      stream=None):
+    """One gated decode step in place on (S, z); gate None, [B,H] or [B,H,d]."""
+    _check_cuda(q, k, v, S, z, gate, out)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    gd = _gate_dim(gate, (B, H), d)
+    y = out if out is not None else torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    st = lib().la_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), B, H,
+                                    d, dv, _dtype_code(q), float(eps), PHI[phi], _ptr(gate), gd,
+                                    _stream_handle(stream, q.device))
+    _raise(st, "la_decode_step_gated")
+    return y
+
+
+def forward_noncausal_phi(q, k, v, phi="identity", eps: float = 1e-6, return_state=False,
+                          out=None, workspace=None, stream=None):
+    """Non-causal attention with the feature map ``phi`` ("elu1" or "identity")."""
+    _check_cuda(q, k, v, out, workspace)
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    y = out if out is not None else torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    S_out = z_out = None
+    if return_state:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = int(lib().la_noncausal_phi_workspace_bytes(B, H, N, d, dv, dt, PHI[phi]))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().la_forward_noncausal_phi(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
+                                        float(eps), PHI[phi], _ptr(S_out), _ptr(z_out),
+                                        _ptr(workspace), wbytes, _stream_handle(stream, q.device))
+    _raise(st, "la_forward_noncausal_phi")
+    return (y, S_out, z_out) if return_state else y
+
+
+def random_features(x, W, out=None, stream=None):
+    """exp(W x - ||x||^2 / 2) / sqrt(m) for every row of x ([..., d], bf16 or fp32);
+    W: float32 [m, d] CUDA tensor.  Returns float32 [..., m]."""
+    _check_cuda(x, W, out)
+    d = x.shape[-1]
+    if W.dtype != torch.float32 or W.dim() != 2 or W.shape[1] != d:
+        raise ValueError("W must be float32 [m, d]")
+    m = W.shape[0]
+    rows = x.numel() // d
+    y = out if out is not None else torch.empty(tuple(x.shape[:-1]) + (m,), dtype=torch.float32,
+                                                device=x.device)
+    st = lib().la_random_features(_ptr(x), _ptr(y), rows, d, m, _dtype_code(x), _ptr(W),
+                                  _stream_handle(stream, x.device))
+    _raise(st, "la_random_features")
+    return y

@@ -15,7 +15,10 @@ causal one does and then, from the same generator, the upstream gradient dy
 as iid N(0, 1) float32 of shape ``[B, H, N, dv]`` (unscaled).  The decay
 workloads draw as their plain counterparts and use one fixed decay per head,
 gamma_h = 1 - 2^(-5 - 8 h / H): from 1 - 1/32 (a memory of about 32 tokens)
-to about 1 - 2^-13, a spread of time scales across the heads.
+to about 1 - 2^-13, a spread of time scales across the heads.  The gated
+workload draws as the causal one and then, from the same generator, one gate
+per token (and per feature when asked), g = 1 - 2^-(2 + 11 u) with u ~ U(0, 1)
+in float32: gates from 3/4 to 1 - 2^-13, spread evenly in their memory length.
 """
 from __future__ import annotations
 
@@ -78,6 +81,10 @@ WORKLOADS = {
     "decode_decay_bf16_b256h32d128": Workload("decode_decay_bf16_b256h32d128", "decode_decay",
                                               256, 32, 1024, 128, 128, torch.bfloat16, 1.0,
                                               steps=4096, step_scale=1.0 / math.sqrt(128)),
+    # gated causal (one gate per token and head), training / prefill shape.
+    "causal_gated_bf16_b8h16n8192d128": Workload("causal_gated_bf16_b8h16n8192d128",
+                                                 "causal_gated", 8, 16, 8192, 128, 128,
+                                                 torch.bfloat16, 1.0 / math.sqrt(128)),
     # recurrent decode from a 1024-token prefill.
     "decode_bf16_b256h32d128": Workload("decode_bf16_b256h32d128", "decode", 256, 32, 1024, 128,
                                         128, torch.bfloat16, 1.0, steps=4096,
@@ -159,3 +166,38 @@ def random_qkv_dy(B, H, N, d, dv, dtype=torch.float32, scale=1.0, seed=0, device
     """Ad-hoc seeded (q, k, v, dy) draw with the backward recipe."""
     w = Workload("adhoc", "backward", B, H, N, d, dv, dtype, scale, seed)
     return make_backward_inputs(w, device=device)
+
+
+def _gates(g: torch.Generator, shape, device) -> torch.Tensor:
+    u = torch.rand(shape, generator=g, dtype=torch.float32, device=g.device)
+    two = torch.tensor(2.0, dtype=torch.float32, device=u.device)
+    return (1.0 - torch.pow(two, -(2.0 + 11.0 * u))).to(device)
+
+
+def make_gated_inputs(w: Workload, gate_dim: int = 1, device="cpu", gen_device="cpu"):
+    """Draw (q, k, v, gate): q, k, v as ``make_qkv``, then the gates from the same
+    generator, [B, H, N] (gate_dim 1) or [B, H, N, d]."""
+    g = torch.Generator(device=gen_device)
+    g.manual_seed(w.seed)
+    q = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    k = _draw(g, (w.B, w.H, w.N, w.d), w.scale, w.dtype, device)
+    v = _draw(g, (w.B, w.H, w.N, w.dv), w.scale, w.dtype, device)
+    shape = (w.B, w.H, w.N) if gate_dim == 1 else (w.B, w.H, w.N, w.d)
+    return q, k, v, _gates(g, shape, device)
+
+
+def random_gated(B, H, N, d, dv, gate_dim=1, dtype=torch.float32, scale=1.0, seed=0,
+                 device="cpu", shift=0.0):
+    """Ad-hoc seeded (q, k, v, gate) draw with the gated recipe (``shift`` as in
+    ``random_qkv``)."""
+    w = Workload("adhoc", "causal_gated", B, H, N, d, dv, torch.float32, scale, seed)
+    q, k, v, gate = make_gated_inputs(w, gate_dim, device=device)
+    sh = torch.tensor(shift, dtype=torch.float32)
+    return (q + sh).to(dtype), (k + sh).to(dtype), v.to(dtype), gate
+
+
+def random_projection(m: int, d: int, seed: int = 0) -> torch.Tensor:
+    """W [m, d] with iid N(0, 1) rows (float32): the random projections of the
+    random-feature map."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((m, d), generator=g, dtype=torch.float32)

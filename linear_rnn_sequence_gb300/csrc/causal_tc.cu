@@ -18,8 +18,10 @@
 // variations.  The kernel therefore feeds only the residuals (small values)
 // to the tensor cores and carries the constants exactly:
 //   w_ij            = d c_i c'_j + c_i beta_j + c'_j alpha_i + a_i . b_j
-//                       (a = bf16 psi_c(q), b = bf16 psi_c'(k), alpha_i = sum a_i,
-//                        beta_j = sum b_j; c_i of the query, c'_j of the key)
+//                       (a = bf16 psi_c(q), b = bf16 psi_c'(k); alpha_i and beta_j
+//                        the sums of the residuals before rounding, which moves
+//                        w by about 1e-5 of itself, a constant per row or per key;
+//                        c_i of the query, c'_j of the key)
 //   S               = 1 u^T + R,  u = sum_j c'_j v_j,  R = sum_j b_j v_j^T
 //   z               = n 1 + zeta, n = sum_j c'_j,   zeta = sum_j b_j
 //   phi(q_i)^T S    = (d c_i + alpha_i) u + c_i r + a_i R,        r = sum_j beta_j v_j = colsum(R)
@@ -352,7 +354,7 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
 // Eight warps, two per TMEM lane quarter; the two threads of a token row
 // (halves h = 0, 1) share its work.  Block c: psi(q) of half the features
 // each -> TMEM (A operand); h = 0 then adds the augmentation slice A' (with
-// alpha_i = sum of the rounded psi(q_i) over both halves, and d).  Once
+// alpha_i = sum of psi(q_i) over both halves, before rounding, and d).  Once
 // G = w is ready, every other 16-column group each: w_ij (j <= i, else 0)
 // split into bf16 hi + lo pairs written back over G, and the partial row sums.
 template <int D, int DV, bool DECAY>
@@ -399,9 +401,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                     const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk = feat_bf16x2(w[hw], kq);
-                        alpha2 = acc_bf16x2(alpha2, pk);
-                        v[f4 * 4 + hw] = pk;
+                        v[f4 * 4 + hw] = feat_bf16x2_sum(w[hw], kq, alpha2);
                     }
                 }
                 tmem_st16(tb + lb + kColAq + grp * 16, v);
@@ -437,27 +437,36 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             // the weight relative to row i's common factor gamma^(i+1)
             const float gsc = DECAY ? X.gpow[1][min(kC, nloc - c * kC)] * ds.G : 1.f;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
-            // (hi + lo equals w to within about 2^-17 w)
-            float rowsum = 0.f;
+            // (hi + lo equals w to within about 2^-17 w), on packed fp32 pairs;
+            // groups wholly below the warp's rows keep every weight, the
+            // diagonal ones mask j > i
+            uint64_t rowsum2 = f2pack(0.f, 0.f);
+            const uint64_t gsc2 = f2pack(gsc, gsc);
             auto weights = [&](int grp, const uint32_t (&gc)[16]) {
                 uint32_t out[16];
                 if (grp > last_grp) {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) out[m] = 0u;
                 } else {
-                    // j - 16 grp <= lim is kept; whole groups below the warp's rows keep all
-                    const int lim = (wq * 32 >= grp * 16 + 15) ? 15 : row - grp * 16;
+                    const bool full = wq * 32 >= grp * 16 + 15;   // warp-uniform
+                    const int lim = full ? 15 : row - grp * 16;
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 2) {
-                        const float g0 = DECAY ? u2f(gc[jj]) * gsc : u2f(gc[jj]);
-                        const float g1 = DECAY ? u2f(gc[jj + 1]) * gsc : u2f(gc[jj + 1]);
-                        const float w0 = (jj <= lim) ? g0 : 0.f;
-                        const float w1 = (jj + 1 <= lim) ? g1 : 0.f;
+                        uint64_t w2 = f2pack(u2f(gc[jj]), u2f(gc[jj + 1]));
+                        if (DECAY) w2 = f2mul(w2, gsc2);
+                        if (!full) {
+                            float w0, w1;
+                            f2unpack(w2, w0, w1);
+                            w2 = f2pack(jj <= lim ? w0 : 0.f, jj + 1 <= lim ? w1 : 0.f);
+                        }
+                        float w0, w1;
+                        f2unpack(w2, w0, w1);
                         const uint32_t hi = pack_bf16x2(w0, w1);
-                        const uint32_t lo = pack_bf16x2(w0 - bf16_lo_f(hi), w1 - bf16_hi_f(hi));
-                        rowsum += w0 + w1;
+                        float l0, l1;
+                        f2unpack(f2sub(w2, f2pack(bf16_lo_f(hi), bf16_hi_f(hi))), l0, l1);
+                        rowsum2 = f2add(rowsum2, w2);
                         out[jj >> 1] = hi;
-                        out[8 + (jj >> 1)] = lo;
+                        out[8 + (jj >> 1)] = pack_bf16x2(l0, l1);
                     }
                 }
                 tmem_st16(tb + lb + kColG + grp * 16, out);
@@ -481,7 +490,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                 weights(g1, gB);
                 if (more && g2 <= last_grp) tmem_wait_ld();
             }
-            S.rowsum[cb][h][row] = rowsum;
+            S.rowsum[cb][h][row] = f2sum(rowsum2);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&S.h_ready[cb]);
@@ -614,7 +623,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     }
 
     // psi(k) in place (bf16) over this half's features; beta_j = sum of the
-    // rounded row over both halves; h = 0 writes the [1|beta] and B' rows.
+    // row (before rounding) over both halves; h = 0 writes the [1|beta] and B' rows.
     // Returns false when the group gave up (agreed at the group barrier).
     auto phi_k = [&](int c) -> bool {
         const int s = c & 1, cb = c & 1;
@@ -656,10 +665,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uint32_t w[4] = {raw[f].x, raw[f].y, raw[f].z, raw[f].w};
 #pragma unroll
                     for (int hw = 0; hw < 4; ++hw) {
-                        const uint32_t pk =
-                            DECAY ? feat_scaled_bf16x2(w[hw], kk, sc) : feat_bf16x2(w[hw], kk);
-                        beta2 = acc_bf16x2(beta2, pk);
-                        w[hw] = pk;
+                        w[hw] = DECAY ? feat_scaled_bf16x2_sum(w[hw], kk, sc, beta2)
+                                      : feat_bf16x2_sum(w[hw], kk, beta2);
                     }
                     raw[f] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -852,13 +859,14 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         auto outputs = [&](int part, const uint32_t (&vc)[32]) {
             const int half = part & 1, cblk = part >> 1;
             const int rA = wq * 32 + 16 * half + tq, rB = rA + 8;
-            const float invA = einv[rA], invB = einv[rB];
+            const uint64_t invA = f2pack(einv[rA], einv[rA]), invB = f2pack(einv[rB], einv[rB]);
             const bool okA = t0 + rA < N, okB = t0 + rB < N;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int col = cblk * 64 + 8 * k + tc;
-                const float2 oA = make_float2(u2f(vc[4 * k]) * invA, u2f(vc[4 * k + 1]) * invA);
-                const float2 oB = make_float2(u2f(vc[4 * k + 2]) * invB, u2f(vc[4 * k + 3]) * invB);
+                float2 oA, oB;
+                f2unpack(f2mul(f2pack(u2f(vc[4 * k]), u2f(vc[4 * k + 1])), invA), oA.x, oA.y);
+                f2unpack(f2mul(f2pack(u2f(vc[4 * k + 2]), u2f(vc[4 * k + 3])), invB), oB.x, oB.y);
                 if (okA) *reinterpret_cast<float2 *>(ychunk + (size_t)rA * DV + col) = oA;
                 if (okB) *reinterpret_cast<float2 *>(ychunk + (size_t)rB * DV + col) = oB;
             }

@@ -173,6 +173,25 @@ __device__ __forceinline__ uint32_t feat_bf16x2(uint32_t w, const SplitC &k) {
     return r;
 }
 
+// The same, also adding the two residuals (before their bf16 rounding) to
+// the packed row sum acc.  The row sums feed the constant parts of the
+// weights (c beta_j and c' alpha_i); taking them before the rounding moves a
+// weight by a constant per row or per key of about sqrt(d) 2^-9 |phi - c|,
+// some 1e-5 of the weight, and saves the unpacking of the rounded pair.
+__device__ __forceinline__ uint32_t feat_bf16x2_sum(uint32_t w, const SplitC &k, uint64_t &acc) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1, a0, a1;
+    f2unpack(f2mul(f2pack(fminf(x0, kExpArgMax), fminf(x1, kExpArgMax)),
+                   f2pack(kLog2e, kLog2e)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), k.nc2), e0, e1);
+    f2unpack(f2add(f2pack(x0, x1), k.omc2), a0, a1);
+    const float r0 = fmaxf(a0, e0), r1 = fmaxf(a1, e1);
+    acc = f2add(acc, f2pack(r0, r1));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(r1), "f"(r0));
+    return r;
+}
+
 // sc * (phi(x) - c) for both bf16 halves of w, rounded once to bf16x2 (the
 // decayed kernels weight key j by sc = gamma^(L-1-j) / G before the tensor
 // cores see it).
@@ -186,6 +205,30 @@ __device__ __forceinline__ uint32_t feat_scaled_bf16x2(uint32_t w, const SplitC 
     f2unpack(f2mul(f2pack(fmaxf(a0, e0), fmaxf(a1, e1)), f2pack(sc, sc)), e0, e1);
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e1), "f"(e0));
+    return r;
+}
+
+// sc * (phi(x) - c) as feat_scaled_bf16x2, also adding the scaled residuals
+// (before their bf16 rounding) to the packed row sum acc (see feat_bf16x2_sum).
+__device__ __forceinline__ uint32_t feat_scaled_bf16x2_sum(uint32_t w, const SplitC &k, float sc,
+                                                           uint64_t &acc) {
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+    float t0, t1, e0, e1, a0, a1;
+    f2unpack(f2mul(f2pack(fminf(x0, kExpArgMax), fminf(x1, kExpArgMax)),
+                   f2pack(kLog2e, kLog2e)), t0, t1);
+    f2unpack(f2add(f2pack(ex2_ftz(t0), ex2_ftz(t1)), k.nc2), e0, e1);
+    f2unpack(f2add(f2pack(x0, x1), k.omc2), a0, a1);
+    const uint64_t m = f2mul(f2pack(fmaxf(a0, e0), fmaxf(a1, e1)), f2pack(sc, sc));
+    acc = f2add(acc, m);
+    f2unpack(m, e0, e1);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e1), "f"(e0));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 

@@ -394,9 +394,10 @@ def launches_per_call(mode, w):
         return 3 if la.causal_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype) > 256 else 1
     tc = w.dtype == torch.bfloat16 and w.d in (64, 128) and w.dv in (64, 128)
     if mode == "noncausal":
-        # tensor-core path (bf16, d and dv in {64, 128}): segment states, their
-        # per-head sum, the query kernel; otherwise two CUDA-core kernels
-        return 3 if tc else 2
+        # tensor-core path (bf16, d and dv in {64, 128}): one fused kernel
+        # (partial states, their per-head sum, the queries); otherwise two
+        # CUDA-core kernels
+        return 1 if tc else 2
     if mode == "causal_decay":
         # tensor-core kernel for the heads it takes (preceded by the segment
         # states and their prefix scan when the sequence is split), then the

@@ -104,11 +104,12 @@ LA_API size_t la_causal_workspace_bytes(int B, int H, int N, int d, int dv, la_d
 /*
  * Workspace size in bytes for la_forward_noncausal with these sizes (0 for
  * N == 0 or unsupported sizes).  It holds the run-time status header and
- * the per-segment sums of S and z (bf16 inputs with d, dv in {64, 128}: also
- * one bf16 operand image of S and z per head; other cases: the split-N
- * partial sums).  Like the causal workspace it depends on the dtype and on
- * the current device's SM count; it must be device memory, 256-byte aligned,
- * and may be reused by later calls on the same stream.
+ * the partial sums of S and z over ranges of the sequence (bf16 inputs with
+ * d, dv in {64, 128}: also one arrival counter per head, which the call
+ * clears with the header; other cases: the split-N partial sums).  Like the
+ * causal workspace it depends on the dtype and on the current device's SM
+ * count; it must be device memory, 256-byte aligned, and may be reused by
+ * later calls on the same stream.
  */
 LA_API size_t la_noncausal_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt);
 

@@ -158,11 +158,15 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, floa
     const size_t need = la_noncausal_workspace_bytes(B, H, N, d, dv, dt);
     if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // a fresh run-time status for every call
-    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
     FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, nullptr, nullptr, S_out, z_out,
               workspace, workspace_bytes, s};
-    if (noncausal_tc_supported(a)) return from_cuda(launch_noncausal_tc(a));
+    const bool tc = noncausal_tc_supported(a);
+    // a fresh run-time status (and, on the tensor-core path, fresh per-head
+    // counters) for every call
+    if (cudaMemsetAsync(workspace, 0, tc ? noncausal_tc_clear_bytes(B * H) : sizeof(WsHeader), s) !=
+        cudaSuccess)
+        return LA_ERR_CUDA;
+    if (tc) return from_cuda(launch_noncausal_tc(a));
     return from_cuda(launch_noncausal_simt(a));
 }
 

@@ -99,6 +99,7 @@ int causal_tc_launches(int BH, int N);   // kernels one causal call launches
 cudaError_t launch_causal_tc(const FwdArgs &a);
 bool noncausal_tc_supported(const FwdArgs &a);
 size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
+size_t noncausal_tc_clear_bytes(int BH);   // workspace bytes to zero before each call
 cudaError_t launch_noncausal_tc(const FwdArgs &a);
 
 // gated recurrence and feature maps (CUDA cores, fp32)

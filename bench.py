@@ -222,7 +222,9 @@ def time_steps(fn, steps, warmup, world, flush=None, min_warm_s=0.0):
     """
     stream = torch.cuda.current_stream()
     t_warm = time.perf_counter()
-    for _ in range(warmup):
+    for _ in range(warmup):   # the warm-up repeats the timed loop's pattern, flush included
+        if flush is not None:
+            flush()
         fn()
     torch.cuda.synchronize()
     while time.perf_counter() - t_warm < min_warm_s:
@@ -712,10 +714,11 @@ def run_reference(args, world, rank):
 def profile_case(args):
     """A few launches of one kernel on one workload, for ncu captures.
 
-    --profile-case causal|long|noncausal|decode|backward|causal_decay|long_decay|decode_decay
+    --profile-case causal|long|noncausal|decode|backward|causal_decay|long_decay|decode_decay|gated
     picks the workload (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 /
     B256 H32 d128 decode / gradients at B8 H16 N8192 d128 / the decay variants of
-    the causal, long and decode workloads); --batch overrides B for a smaller capture.
+    the causal, long and decode workloads / the gated causal form at B8 H16 N8192
+    d128); --batch overrides B for a smaller capture.
     """
     from linear_rnn_sequence_gb300 import linattn as la
     names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
@@ -723,7 +726,8 @@ def profile_case(args):
              "backward": "causal_backward_bf16_b8h16n8192d128",
              "causal_decay": "causal_decay_bf16_b8h16n8192d128",
              "long_decay": "causal_decay_bf16_b1h32n131072d64",
-             "decode_decay": "decode_decay_bf16_b256h32d128"}
+             "decode_decay": "decode_decay_bf16_b256h32d128",
+             "gated": "causal_gated_bf16_b8h16n8192d128"}
     w = WORKLOADS[names[args.profile_case]]
     if args.batch:
         w = w.with_(B=args.batch)
@@ -742,6 +746,10 @@ def profile_case(args):
         else:
             gam = head_decays(w.H).to(dev)
             fn = lambda: la.decode_step_decay(q, k, v, S, z, gam, eps=w.eps, out=y)
+    elif args.profile_case == "gated":
+        q, k, v, gate = make_gated_inputs(w, device=dev, gen_device=dev)
+        y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
+        fn = lambda: la.forward_causal_gated(q, k, v, gate=gate, eps=w.eps, out=y)
     elif w.mode == "causal_decay":
         q, k, v = make_qkv(w, device=dev, gen_device=dev)
         y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
@@ -788,7 +796,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward",
-                                               "causal_decay", "long_decay", "decode_decay"])
+                                               "causal_decay", "long_decay", "decode_decay",
+                                               "gated"])
     ap.add_argument("--batch", type=int, default=0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

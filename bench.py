@@ -581,25 +581,25 @@ def run_modes(args, world, dev, peaks, peak_kind):
     del q, k, v, dy, outs, ws
     torch.cuda.empty_cache()
 
-    # gated causal (one gate per token and head; CUDA cores, fp32)
+    # gated causal (one gate per token and head, all in [3/4, 1): every head on
+    # the tensor cores, after the per-block tables of gate products)
     w = WORKLOADS["causal_gated_bf16_b8h16n8192d128"]
     q, k, v, gate = make_gated_inputs(w, device=dev, gen_device=dev)
     y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
-    total, per = time_steps(lambda: la.forward_causal_gated(q, k, v, gate=gate, eps=w.eps, out=y),
-                            max(3, min(args.steps, 10)), args.warmup, world)
+    ws = la.alloc_workspace(la.causal_gated_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
+    total, per = time_steps(lambda: la.forward_causal_gated(q, k, v, gate=gate, eps=w.eps, out=y,
+                                                            workspace=ws),
+                            steps, args.warmup, world)
     T = w.BH * w.N
     ms = sum(per) / len(per)
-    alg_flops = T * decay_flops_per_token_head(w.d, w.dv)
-    alg_bytes = T * (alg_bytes_per_token_head(w) + 4)   # plus the fp32 gate
-    tflops = alg_flops / (ms * 1e-3) / 1e12
+    gate_bytes = T * 4   # the fp32 gates, read once
     modes[w.name] = {"tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
-                     "l2": "inputs larger than L2",
-                     "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
-                                  "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
-                                  "traffic": None,
-                                  "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
-                                  "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
-    del q, k, v, gate, y
+                     "l2": "inputs larger than L2", "kernels_per_call": 3,
+                     "roofline": roofline(T * alg_bytes_per_token_head(w) + gate_bytes,
+                                          T * decay_flops_per_token_head(w.d, w.dv), ms, peaks,
+                                          peak_kind, load_traffic(w.name),
+                                          moved_bytes=T * moved_bytes_per_token_head(w) + gate_bytes)}
+    del q, k, v, gate, y, ws
     torch.cuda.empty_cache()
 
     # causal with a per-head decay (every head of this workload has

@@ -172,6 +172,19 @@ LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *
                                       la_dtype dt, float eps, const float *gamma, void *stream);
 
 /*
+ * Workspace size in bytes for la_forward_causal_gated with a gate of
+ * gate_dim values per token (1 or d); 0 for unsupported arguments.  For bf16
+ * inputs with d, dv in {64, 128}, gate_dim = 1 and LA_PHI_ELU1 (the
+ * tensor-core path) it holds the run-time status header, one flag per head
+ * and per-128-token-block tables of gate products, 1,056 bytes per block and
+ * head; otherwise the header alone (256 bytes), which also serves a call
+ * without a gate.  Device memory, 256-byte aligned, reusable by later calls on
+ * the same stream.
+ */
+LA_API size_t la_causal_gated_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt,
+                                              la_phi phi, int gate_dim);
+
+/*
  * Gated causal forward ("Linear Attention/es", "Variantes y extensiones":
  * gated linear attention replaces RetNet's scalar decay by a data-dependent
  * gate; the pages print no equation, and the update is read as the decay's
@@ -183,18 +196,28 @@ LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *
  * row a of S and z[a] all scale by it) or gate_dim = d (one per token and
  * feature row of S); gate = NULL means no gate (g_t = 1), which with phi =
  * LA_PHI_IDENTITY gives the identity-map swap of "Mapas de características"
- * (the layer becomes a bilinear attention).  The gate values are not
- * checked.  phi: LA_PHI_ELU1 or LA_PHI_IDENTITY (else LA_ERR_UNSUPPORTED);
- * with the identity map the denominator can be <= 0, and the clamp then gives
- * num / eps.  Layouts, sizes, the initial / final state and the errors as in
- * la_forward_causal; no workspace.  Every head runs on the CUDA cores, token
- * by token in float32 (both input dtypes), one CTA per head.
+ * (the layer becomes a bilinear attention).  phi: LA_PHI_ELU1 or
+ * LA_PHI_IDENTITY (else LA_ERR_UNSUPPORTED); with the identity map the
+ * denominator can be <= 0, and the clamp then gives num / eps.  Layouts,
+ * sizes, the initial / final state and the errors as in la_forward_causal.
+ * Workspace: la_causal_gated_workspace_bytes (header size when gate is NULL),
+ * overlapping no other buffer.
+ *
+ * Where it applies (bf16, d and dv in {64, 128}, gate_dim = 1, LA_PHI_ELU1),
+ * the heads whose gates all lie in [2^-1/2, 1] run on the tensor cores, as
+ * the decayed form of la_forward_causal_decay does, with the bf16 tolerance;
+ * the device decides per head from the gate values, and the other heads
+ * (closed gates, NaN, ...) run on the CUDA cores.  Everything else runs on
+ * the CUDA cores, token by token in float32, one CTA per head.  A wait of the
+ * tensor-core path that runs out records LA_ERR_TIMEOUT in the workspace
+ * header (la_workspace_status).
  */
 LA_API la_status la_forward_causal_gated(const void *q, const void *k, const void *v, float *y,
                                          int B, int H, int N, int d, int dv, la_dtype dt,
                                          float eps, la_phi phi, const float *gate, int gate_dim,
                                          const float *S_in, const float *z_in, float *S_out,
-                                         float *z_out, void *stream);
+                                         float *z_out, void *workspace, size_t workspace_bytes,
+                                         void *stream);
 
 /*
  * One gated decode step in place on (S, z):

@@ -252,10 +252,25 @@ la_status la_decode_step_decay(const void *q, const void *k, const void *v, floa
     return from_cuda(launch_decode_simt(a));
 }
 
+size_t la_causal_gated_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt,
+                                       la_phi phi, int gate_dim) {
+    if (B < 1 || H < 1 || N < 0 || !dim_ok(d) || !dim_ok(dv)) return 0;
+    if (dt != LA_DTYPE_F32 && dt != LA_DTYPE_BF16) return 0;
+    if (gate_dim != 1 && gate_dim != d) return 0;
+    FwdArgs a{};
+    a.B = B; a.H = H; a.N = N; a.d = d; a.dv = dv; a.dt = dt;
+    a.phi = (int)phi;
+    a.gate = reinterpret_cast<const float *>(&a);   // a gate is given (its address is not used)
+    a.gate_dim = gate_dim;
+    if (N > 0 && gated_tc_supported(a)) return gated_tc_workspace(B * H, N);
+    return sizeof(WsHeader);
+}
+
 la_status la_forward_causal_gated(const void *q, const void *k, const void *v, float *y, int B,
                                   int H, int N, int d, int dv, la_dtype dt, float eps, la_phi phi,
                                   const float *gate, int gate_dim, const float *S_in,
-                                  const float *z_in, float *S_out, float *z_out, void *stream) {
+                                  const float *z_in, float *S_out, float *z_out, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
     la_status st = check_common(q, k, v, y, B, H, N, d, dv, dt, eps);
     if (st != LA_OK) return st;
     if (phi != LA_PHI_ELU1 && phi != LA_PHI_IDENTITY) return LA_ERR_UNSUPPORTED;
@@ -270,7 +285,15 @@ la_status la_forward_causal_gated(const void *q, const void *k, const void *v, f
         overlap(y, T * dv * 4, gate, gb) || overlap(S_out, sb, gate, gb) ||
         overlap(z_out, zb, gate, gb))
         return LA_ERR_INVALID_ARG;
+    const size_t need = gate ? la_causal_gated_workspace_bytes(B, H, N, d, dv, dt, phi, gate_dim)
+                             : sizeof(WsHeader);
+    if ((st = check_ws(workspace, workspace_bytes, need)) != LA_OK) return st;
+    if (overlap(workspace, need, y, T * dv * 4) || overlap(workspace, need, gate, gb) ||
+        overlap(workspace, need, S_out, sb) || overlap(workspace, need, z_out, zb))
+        return LA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // a fresh run-time status for every call (the tensor-core path also clears its flags)
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), s) != cudaSuccess) return LA_ERR_CUDA;
     if (N == 0) {  // no tokens: the final state is the initial state
         if (S_out) {
             cudaError_t e = cudaSuccess;
@@ -286,7 +309,8 @@ la_status la_forward_causal_gated(const void *q, const void *k, const void *v, f
         }
         return LA_OK;
     }
-    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out, nullptr, 0, s};
+    FwdArgs a{q, k, v, y, B, H, N, d, dv, dt, eps, S_in, z_in, S_out, z_out, workspace,
+              workspace_bytes, s};
     a.phi = (int)phi;
     a.gate = gate;
     a.gate_dim = gate ? gate_dim : 1;

@@ -132,7 +132,7 @@ __device__ __forceinline__ uint32_t k16_off(int n, int k) {
 
 constexpr int kSmallBytes = 6 * 1024;   // the Small area of every layout
 
-template <int D, int DV, bool DECAY = false>
+template <int D, int DV, int DK = 0>
 struct Layout {
     static constexpr int kQ = kC * D * 2;           // one Q stage
     static constexpr int kK = kC * D * 2;
@@ -155,7 +155,7 @@ struct Layout {
     static constexpr int oSmall = oZB + kZB;
     static constexpr int kSmall = kSmallBytes;
     static constexpr int oDecay = oSmall + kSmall;  // decay kernel only: DecaySmall
-    static constexpr int kDecay = DECAY ? 2 * 1024 : 0;
+    static constexpr int kDecay = DK ? 2 * 1024 : 0;
     static constexpr int bytes = oDecay + kDecay;
     // request enough that only one CTA fits per SM (TMEM: 512 columns each)
     static constexpr int request = (bytes + 1024) > 120 * 1024 ? bytes + 1024 : 120 * 1024;
@@ -195,6 +195,39 @@ static_assert(sizeof(DecaySmall) <= 2 * 1024, "decay area");
 __device__ __forceinline__ DecaySmall &decay_area(Small &S) {
     return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
 }
+
+// Per-token gates: one table per 128-token block, [P_0 .. P_128 | pad | 1/P_0 .. 1/P_128 | pad]
+// with P_m = g_t0 g_t0+1 ... g_t0+m-1 the product of the block's first m gates.
+constexpr int kGateInv = kC + 4;          // offset of the inverses
+constexpr int kGateTab = 2 * kGateInv;    // floats per block
+// Gates the kernel takes: [2^-1/2, 1], so that the products over a block stay
+// at or above 2^-64, the range the fixed decay is held to.
+constexpr float kGateMin = 0.70710677f;
+
+// The decay factors of a block, from a fixed decay (DK = 1: the per-head table
+// of gamma powers in shared memory) or from per-token gates (DK = 2: the
+// block's table of gate products in global memory).  For block c of L tokens:
+//   pw(c, m)  = the decay over its first m tokens (gamma^m, or P_m)
+//   ipw(c, m) = 1 / pw(c, m)
+//   key_weight(c, L, j) = the decay after key j to the block's end, pw(c, L) / pw(c, j + 1)
+template <int DK>
+struct DecayPow {
+    const float (*gpow)[kC + 2];   // DK = 1
+    const float *tab;              // DK = 2: the table of the work item's first block
+    __device__ __forceinline__ float pw(int c, int m) const {
+        return DK == 2 ? __ldg(tab + (size_t)c * kGateTab + m) : gpow[0][m];
+    }
+    __device__ __forceinline__ float ipw(int c, int m) const {
+        return DK == 2 ? __ldg(tab + (size_t)c * kGateTab + kGateInv + m) : gpow[1][m];
+    }
+    __device__ __forceinline__ float key_weight(int c, int L, int j) const {
+        return DK == 2 ? pw(c, L) * ipw(c, j + 1) : gpow[0][L - 1 - j];
+    }
+    // what DecayScale starts from (any value but 1 gives the restart value 3/4)
+    __device__ __forceinline__ float first() const {
+        return DK == 1 ? gpow[0][1] : (DK == 2 ? 0.5f : 1.f);
+    }
+};
 
 // ------------------------------------------------------------------ producer
 template <int D, int DV>
@@ -357,22 +390,31 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
 // alpha_i = sum of psi(q_i) over both halves, before rounding, and d).  Once
 // G = w is ready, every other 16-column group each: w_ij (j <= i, else 0)
 // split into bf16 hi + lo pairs written back over G, and the partial row sums.
-template <int D, int DV, bool DECAY>
+template <int D, int DV, int DK>
 __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
-                                             int nchunks, int nloc, const Guard &g) {
+                                             int nchunks, int nloc, const Guard &g,
+                                             const float *gtab) {
+    constexpr bool DECAY = DK != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpA) >> 2;
-    DecaySmall &X = decay_area(S);   // touched only with DECAY
-    // state scale G of block c (gpow[0][1] = gamma; the plain layout has no table)
-    DecayScale ds(DECAY ? X.gpow[0][1] : 1.f);
+    const DecayPow<DK> P{decay_area(S).gpow, gtab};   // touched only with a decay or gates
+    // state scale G of block c (the plain layout has no table)
+    DecayScale ds(P.first());
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const float dd = (float)D;
     // groups entirely above this warp's rows are all zero (causal mask)
     const int last_grp = (wq * 32 + 31) >> 4;
     for (int c = 0; c < nchunks; ++c) {
         const int cb = c & 1;
-        if (DECAY) ds.step(X.gpow[0][min(kC, nloc - c * kC)]);
+        // the block's decay over its L tokens, and (gsc below) its inverse
+        float pL = 1.f, ipL = 1.f;
+        if (DECAY) {
+            const int L = min(kC, nloc - c * kC);
+            pL = P.pw(c, L);
+            ipL = P.ipw(c, L);
+            ds.step(pL);
+        }
         bool ok = wait_warp(&S.q_full, c & 1, g, 40);
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
@@ -435,7 +477,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             // decay: the weight tile holds gamma^(L-1-j) w_ij / G (keys
             // pre-scaled), so multiplying by gamma^-L G gives gamma^-(j+1) w_ij,
             // the weight relative to row i's common factor gamma^(i+1)
-            const float gsc = DECAY ? X.gpow[1][min(kC, nloc - c * kC)] * ds.G : 1.f;
+            const float gsc = DECAY ? ipL * ds.G : 1.f;
             // one 16-column group: w_ij for j <= i (else 0) -> bf16 hi, lo pairs
             // (hi + lo equals w to within about 2^-17 w), on packed fp32 pairs;
             // groups wholly below the warp's rows keep every weight, the
@@ -505,22 +547,23 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
 // Eight warps, two per TMEM lane quarter, the two threads of a row (halves
 // h = 0, 1) sharing its work: psi(k) in place over half of the features,
 // the state export of half of R's columns, half of the output columns.
-template <int D, int DV, bool DECAY>
+template <int D, int DV, int DK>
 __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
                                              uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
                                              uint8_t *sYB, uint8_t *sZB,
                                              const TcParams &p, int head, int slot,
                                              int tok0, int nloc, bool last_seg, int nchunks,
-                                             const Guard &g) {
+                                             const Guard &g, const float *gtab) {
     using Lay = Layout<D, DV>;
+    constexpr bool DECAY = DK != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
     const int h = (warp - kWarpB) >> 2;
-    DecaySmall &X = decay_area(S);   // touched only with DECAY
+    const DecayPow<DK> P{decay_area(S).gpow, gtab};   // touched only with a decay or gates
     // scales of the block whose keys phi_k prepares and of the state in TMEM
     // (the export's block); the plain layout has no table
-    DecayScale ks(DECAY ? X.gpow[0][1] : 1.f);
-    DecayScale xs(DECAY ? X.gpow[0][1] : 1.f);
+    DecayScale ks(P.first());
+    DecayScale xs(P.first());
     const int wtid = tid - kWarpB * 32;   // 0..255
     const uint32_t lb = (uint32_t)(wq * 32) << 16;
     const int N = nloc;   // tokens of this work item (segment)
@@ -561,9 +604,9 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const float *zin = p.z_in ? p.z_in + (size_t)slot * D : nullptr;
         // decay: the initial state enters TMEM divided by G0, and already
         // multiplied by gamma^L of block 0 when the scale restarts there
-        if (DECAY) xs.step(X.gpow[0][min(kC, N)]);
-        const float g0 =
-            DECAY ? (xs.renorm ? X.gpow[0][min(kC, N)] : 1.f) / xs.G0 : 1.f;
+        const float p0 = DECAY ? P.pw(0, min(kC, N)) : 1.f;
+        if (DECAY) xs.step(p0);
+        const float g0 = DECAY ? (xs.renorm ? p0 : 1.f) / xs.G0 : 1.f;
 #pragma unroll
         for (int gq = 0; gq < kRGroups; ++gq) {
             const int grp = h * kRGroups + gq;
@@ -631,8 +674,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // s_j = gamma^(L-1-j), its share of the state after the block
         // (padding rows: 0)
         const int L = min(kC, N - c * kC);
-        if (DECAY) ks.step(X.gpow[0][L]);
-        const float sc = DECAY ? (row < L ? X.gpow[0][L - 1 - row] / ks.G : 0.f) : 1.f;
+        float sc = 1.f;
+        if (DECAY) {   // s_j / G, with s_j = (decay of the whole block) / (decay up to key j)
+            ks.step(P.pw(c, L));
+            sc = row < L ? P.key_weight(c, L, row) / ks.G : 0.f;
+        }
         const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
@@ -728,10 +774,11 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // the scale restarts at block c+1, the state is multiplied by gamma^L
         // of block c+1 over G0 and written back before that block's update
         const float G = DECAY ? xs.G : 1.f;
+        const float gcur = DECAY ? P.pw(c, L) : 1.f;   // the decay of block c
         bool rescale = false;
         float gnext = 1.f;
         if (DECAY && c + 1 < nchunks) {
-            const float gL = X.gpow[0][min(kC, N - (c + 1) * kC)];
+            const float gL = P.pw(c + 1, min(kC, N - (c + 1) * kC));
             xs.step(gL);
             rescale = xs.renorm;
             gnext = gL / xs.G0;
@@ -798,7 +845,6 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 const float ssum = (S.s_part[cb][0] + S.s_part[cb][1]) +
                                    (S.s_part[cb][2] + S.s_part[cb][3]);
                 if (DECAY) {   // n and rho decay like the state: x <- gamma^L x + sum_j s_j x_j
-                    const float gcur = X.gpow[0][L];
                     S.n_s[cb] = fmaf(gcur, S.n_s[pb], G * ssum);
                     S.rho_s[cb] = fmaf(gcur, S.rho_s[pb], G * rsum);
                 } else {
@@ -836,15 +882,16 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     // Half h takes the 16-lane half h of its quarter (parts h, h + 2, ...).
     auto epilogue = [&](int c) -> bool {
         const int t0 = c * kC, cb = c & 1;
+        // decay: row i's numerator and denominator are both carried divided by
+        // gamma^(i+1) (the decay from the block's start through token i), so
+        // the clamp max(den, eps) becomes max(den', eps gamma^-(i+1))
+        const float eps_row = DECAY ? p.eps * P.ipw(c, row + 1) : p.eps;
         if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 8);
         tc_fence_after();
         uint32_t yz[4];
         tmem_ld4(tb + lb + kColYz, yz);
-        // decay: row i's numerator and denominator are both carried divided by
-        // gamma^(i+1), so the clamp max(den, eps) becomes max(den', eps gamma^-(i+1))
-        const float eps_row = DECAY ? p.eps * X.gpow[1][row + 1] : p.eps;
         tmem_wait_ld();
         S.e_inv[h][row] =
             1.f / fmaxf(u2f(yz[0]) + (S.rowsum[cb][0][row] + S.rowsum[cb][1][row]), eps_row);
@@ -924,13 +971,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int DV, bool DECAY>
+template <int D, int DV, int DK>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap,
                  const TcParams p)
 {
-    using Lay = Layout<D, DV, DECAY>;
+    using Lay = Layout<D, DV, DK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -953,11 +1000,17 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // the CUDA-core kernel that follows (the whole CTA leaves before any
     // barrier, TMEM allocation or write, so their y, S_out and z_out, and an
     // S_in aliased by S_out, are untouched here)
-    if (DECAY && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
+    if (DK == 1 && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
+    // gates: likewise for heads with a gate outside [2^-1/2, 1]
+    const float *gtab = nullptr;
+    if (DK == 2) {
+        if (p.gate_skip[head] != 0u) return;
+        gtab = p.gate_tab + ((size_t)head * p.gate_blocks + tok0 / kC) * kGateTab;
+    }
     if (tid == 0) LA_TRACE_POINT(0, 15);
     // decay (one segment per head): powers of the head's gamma, read by both
     // row-worker groups (visible after the __syncthreads below)
-    if (DECAY && tid < kC + 2) {
+    if (DK == 1 && tid < kC + 2) {
         DecaySmall &X = decay_area(S);
         const float gam = p.gamma[head % p.H];
         X.gpow[0][tid] = powf(gam, (float)tid);
@@ -1009,10 +1062,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     } else if (warp == 1) {
         if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
     } else if (warp < kWarpB) {
-        group_a_role<D, DV, DECAY>(S, tb, sQ, nchunks, nloc, g);
+        group_a_role<D, DV, DK>(S, tb, sQ, nchunks, nloc, g, gtab);
     } else {
-        group_b_role<D, DV, DECAY>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, slot, tok0,
-                                   nloc, seg == p.nseg - 1, nchunks, g);
+        group_b_role<D, DV, DK>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, slot, tok0,
+                                nloc, seg == p.nseg - 1, nchunks, g, gtab);
     }
     tc_fence_before();
     __syncthreads();
@@ -1092,9 +1145,58 @@ size_t segment_workspace(int BH, int N, int d, int dv) {
     return sizeof(WsHeader) + 2 * sizeof(float) * (size_t)BH * nseg * ((size_t)d * dv + d);
 }
 
-template <int D, int DV, bool DECAY>
+// Per-token gates: the per-block tables of gate products (kGateTab floats per
+// block, see DecayPow) and the per-head flag of a gate outside [2^-1/2, 1]
+// (the flags start at zero).  One warp per (head, block): lane l takes the
+// block's gates 4l .. 4l+3, multiplies them in order, and a warp scan
+// multiplies in the products of the lanes below it.
+constexpr int kGateWarps = 4;
+__global__ void __launch_bounds__(kGateWarps * 32)
+gate_tables_kernel(const float *__restrict__ gate, int N, int nblocks, float *__restrict__ tab,
+                   unsigned int *__restrict__ skip)
+{
+    const int lane = threadIdx.x & 31;
+    const int blk = blockIdx.x * kGateWarps + (threadIdx.x >> 5), head = blockIdx.y;
+    if (blk >= nblocks) return;
+    const int t0 = blk * kC + 4 * lane;
+    float gv[4];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int t = t0 + k;
+        gv[k] = t < N ? gate[(size_t)head * N + t] : 1.f;
+        bad |= !(gv[k] >= kGateMin && gv[k] <= 1.f);   // NaN counts as outside
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&skip[head], 1u);
+    float loc[4];
+    loc[0] = gv[0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) loc[k] = loc[k - 1] * gv[k];
+    float x = loc[3];   // inclusive scan of the lanes' products
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x *= y;
+    }
+    float ex = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) ex = 1.f;
+    float *tb = tab + ((size_t)head * nblocks + blk) * kGateTab;
+    if (lane == 0) {
+        tb[0] = 1.f;
+        tb[kGateInv] = 1.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float P = ex * loc[k];
+        tb[4 * lane + k + 1] = P;
+        tb[kGateInv + 4 * lane + k + 1] = 1.f / P;
+    }
+}
+
+template <int D, int DV, int DK>
 cudaError_t launch_dv(const FwdArgs &a) {
-    using Lay = Layout<D, DV, DECAY>;
+    constexpr bool DECAY = DK == 1;
+    using Lay = Layout<D, DV, DK>;
     CUtensorMap qm, km, vm;
     const int BH = a.BH();
     if (!encode_3d(&qm, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
@@ -1113,7 +1215,17 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.z_in = a.z_in;
     p.S_out = a.S_out;
     p.z_out = a.z_out;
-    choose_segments(BH, a.N, p.nseg, p.seg_chunks);
+    if (DK == 2) {   // gates: one work item per head (no state pass for them)
+        p.nseg = 1;
+        p.seg_chunks = (a.N + kC - 1) / kC;
+        p.gate_blocks = p.seg_chunks;
+        p.gate_tab = reinterpret_cast<const float *>(static_cast<const char *>(a.ws) +
+                                                     gated_tables_offset(BH));
+        p.gate_skip = reinterpret_cast<const unsigned int *>(static_cast<const char *>(a.ws) +
+                                                             sizeof(WsHeader));
+    } else {
+        choose_segments(BH, a.N, p.nseg, p.seg_chunks);
+    }
     if (DECAY) {
         p.gamma = a.gamma;
         p.H = a.H;
@@ -1125,7 +1237,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
     p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
-    if (p.nseg > 1) {
+    if (DK != 2 && p.nseg > 1) {
         // states of every segment but each head's last, then their exclusive
         // prefixes, which become the initial states of the (head, segment) items
         const size_t nS = (size_t)D * DV, cnt = (size_t)items;
@@ -1151,7 +1263,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
         p.S_in = S_pre;
         p.z_in = z_pre;
     }
-    auto kern = causal_tc_kernel<D, DV, DECAY>;
+    auto kern = causal_tc_kernel<D, DV, DK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::request);
     if (e != cudaSuccess) return e;
@@ -1176,17 +1288,44 @@ int causal_tc_launches(int BH, int N) {
     return nseg > 1 ? 3 : 1;
 }
 
-template <bool DECAY>
+template <int DK>
 cudaError_t launch_tc_dims(const FwdArgs &a) {
-    if (a.d == 64 && a.dv == 64) return launch_dv<64, 64, DECAY>(a);
-    if (a.d == 64 && a.dv == 128) return launch_dv<64, 128, DECAY>(a);
-    if (a.d == 128 && a.dv == 64) return launch_dv<128, 64, DECAY>(a);
-    if (a.d == 128 && a.dv == 128) return launch_dv<128, 128, DECAY>(a);
+    if (a.d == 64 && a.dv == 64) return launch_dv<64, 64, DK>(a);
+    if (a.d == 64 && a.dv == 128) return launch_dv<64, 128, DK>(a);
+    if (a.d == 128 && a.dv == 64) return launch_dv<128, 64, DK>(a);
+    if (a.d == 128 && a.dv == 128) return launch_dv<128, 128, DK>(a);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_causal_tc(const FwdArgs &a) {
-    return a.gamma ? launch_tc_dims<true>(a) : launch_tc_dims<false>(a);
+    return a.gamma ? launch_tc_dims<1>(a) : launch_tc_dims<0>(a);
+}
+
+bool gated_tc_supported(const FwdArgs &a) {
+    return causal_tc_supported(a) && a.gate != nullptr && a.gate_dim == 1 && a.phi == LA_PHI_ELU1;
+}
+
+size_t gated_tables_offset(int BH) {
+    return sizeof(WsHeader) + ((size_t)BH * sizeof(unsigned int) + 255) / 256 * 256;
+}
+
+size_t gated_tc_workspace(int BH, int N) {
+    const size_t nb = (size_t)(N + kC - 1) / kC;
+    return gated_tables_offset(BH) + sizeof(float) * (size_t)BH * nb * kGateTab;
+}
+
+size_t gated_tc_clear_bytes(int BH) { return gated_tables_offset(BH); }
+
+cudaError_t launch_gated_tc(const FwdArgs &a) {
+    const int BH = a.BH(), nb = (a.N + kC - 1) / kC;
+    char *ws = static_cast<char *>(a.ws);
+    gate_tables_kernel<<<dim3((nb + kGateWarps - 1) / kGateWarps, BH), kGateWarps * 32, 0,
+                         a.stream>>>(a.gate, a.N, nb,
+                                     reinterpret_cast<float *>(ws + gated_tables_offset(BH)),
+                                     reinterpret_cast<unsigned int *>(ws + sizeof(WsHeader)));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_tc_dims<2>(a);
 }
 
 }  // namespace la

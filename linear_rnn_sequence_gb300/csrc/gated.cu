@@ -50,9 +50,13 @@ causal_gated_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
                     float *__restrict__ y, int N, float eps, int phi,
                     const float *__restrict__ gate, int gate_dim,
                     const float *__restrict__ S_in, const float *__restrict__ z_in,
-                    float *__restrict__ S_out, float *__restrict__ z_out)
+                    float *__restrict__ S_out, float *__restrict__ z_out,
+                    const unsigned int *__restrict__ tc_skip)
 {
     constexpr int NT = GatedCfg<D, DV>::kNT, NW = NT / 32;
+    // heads the tensor-core kernel took are left alone (before any read or
+    // write, so an S_in aliased by S_out stays intact for the other heads)
+    if (tc_skip && tc_skip[blockIdx.x] == 0u) return;
     using CT = WarpRows<NT, DV, D>;   // warp: CT::RPW value columns; lane: CT::CPL features
     static_assert(NT >= D, "one thread per feature");
     extern __shared__ float4 smem4[];
@@ -161,7 +165,7 @@ cudaError_t launch_typed(const FwdArgs &a) {
     if (e != cudaSuccess) return e;
     kern<<<a.BH(), GatedCfg<D, DV>::kNT, smem, a.stream>>>(
         (const T *)a.q, (const T *)a.k, (const T *)a.v, a.y, a.N, a.eps, a.phi, a.gate,
-        a.gate_dim, a.S_in, a.z_in, a.S_out, a.z_out);
+        a.gate_dim, a.S_in, a.z_in, a.S_out, a.z_out, a.gate_skip);
     return cudaGetLastError();
 }
 
@@ -229,6 +233,21 @@ random_features_kernel(const T *__restrict__ x, float *__restrict__ out, long lo
 }  // namespace
 
 cudaError_t launch_causal_gated(const FwdArgs &a) {
+    if (gated_tc_supported(a)) {
+        // the tensor cores take the heads whose gates all lie in [2^-1/2, 1];
+        // this kernel follows for the others
+        cudaError_t e = cudaMemsetAsync(a.ws, 0, gated_tc_clear_bytes(a.BH()), a.stream);
+        if (e == cudaSuccess) e = launch_gated_tc(a);
+        if (e != cudaSuccess) return e;
+        FwdArgs b = a;
+        b.gate_skip = reinterpret_cast<const unsigned int *>(static_cast<const char *>(a.ws) +
+                                                             sizeof(WsHeader));
+        return launch_causal_gated_simt(b);
+    }
+    return launch_causal_gated_simt(a);
+}
+
+cudaError_t launch_causal_gated_simt(const FwdArgs &a) {
     switch (a.d) {
     case 32: return launch_d<32>(a);
     case 64: return launch_d<64>(a);

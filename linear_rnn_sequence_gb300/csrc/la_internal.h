@@ -30,6 +30,9 @@ struct FwdArgs {
     int phi = 0;                    // feature map: 0 elu + 1, 1 identity (CUDA-core kernels)
     const float *gate = nullptr;    // per-token gate [B][H][N][gate_dim] (device), null: none
     int gate_dim = 1;               // 1 or d
+    // gates: per-head flags of the gated tensor-core path (0: that kernel took
+    // the head, and the CUDA-core kernel skips it); null: every head here
+    const unsigned int *gate_skip = nullptr;
     int BH() const { return B * H; }
 };
 
@@ -97,13 +100,21 @@ bool causal_tc_supported(const FwdArgs &a);
 size_t causal_tc_workspace(int BH, int N, int d, int dv);
 int causal_tc_launches(int BH, int N);   // kernels one causal call launches
 cudaError_t launch_causal_tc(const FwdArgs &a);
+// the gated form on the tensor cores (gate_dim 1, elu + 1, bf16, d and dv in
+// {64, 128}): workspace = header | per-head flags | per-block gate tables
+bool gated_tc_supported(const FwdArgs &a);
+size_t gated_tables_offset(int BH);
+size_t gated_tc_workspace(int BH, int N);
+size_t gated_tc_clear_bytes(int BH);   // header and flags, cleared before each call
+cudaError_t launch_gated_tc(const FwdArgs &a);
 bool noncausal_tc_supported(const FwdArgs &a);
 size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
 size_t noncausal_tc_clear_bytes(int BH);   // workspace bytes to zero before each call
 cudaError_t launch_noncausal_tc(const FwdArgs &a);
 
 // gated recurrence and feature maps (CUDA cores, fp32)
-cudaError_t launch_causal_gated(const FwdArgs &a);
+cudaError_t launch_causal_gated(const FwdArgs &a);        // tensor cores where they apply
+cudaError_t launch_causal_gated_simt(const FwdArgs &a);   // CUDA cores (skips a.gate_skip's heads)
 cudaError_t launch_random_features(const void *x, float *out, long long rows, int d, int m,
                                    la_dtype dt, const float *W, cudaStream_t stream);
 

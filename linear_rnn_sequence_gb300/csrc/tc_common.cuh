@@ -37,6 +37,12 @@ struct TcParams {
     int drop_item;                 // test hook: this item's first K/V copy is never issued (-1: off)
     const float *gamma;            // per-head decay [H] (causal kernel with DECAY only)
     int H;
+    // per-token gates (causal kernel with gates only): per-block tables of the
+    // gate products, gate_blocks blocks per head, and a per-head flag that is
+    // nonzero when a gate lies outside the kernel's range
+    const float *gate_tab;
+    const unsigned int *gate_skip;
+    int gate_blocks;
     int state_segs;                // segments per head the state pass reduces (0: all)
 };
 

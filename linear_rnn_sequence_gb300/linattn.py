@@ -98,8 +98,10 @@ def lib():
             L.la_noalloc_status.argtypes = [vp]
             L.la_noalloc_status.restype = i
             L.la_forward_causal_gated.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i,
-                                                  vp, vp, vp, vp, vp]
+                                                  vp, vp, vp, vp, vp, sz, vp]
             L.la_forward_causal_gated.restype = i
+            L.la_causal_gated_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+            L.la_causal_gated_workspace_bytes.restype = sz
             L.la_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i,
                                                vp]
             L.la_decode_step_gated.restype = i
@@ -430,12 +432,21 @@ def _gate_dim(gate, lead, d):
     raise ValueError(f"gate shape {tuple(gate.shape)} must be {tuple(lead)} or {tuple(lead) + (d,)}")
 
 
+def causal_gated_workspace_bytes(B, H, N, d, dv, dtype=torch.bfloat16, phi="elu1",
+                                 gate_dim=1) -> int:
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(lib().la_causal_gated_workspace_bytes(B, H, N, d, dv, code, PHI[phi], gate_dim))
+
+
 def forward_causal_gated(q, k, v, gate=None, phi="elu1", eps: float = 1e-6, S_in=None,
                          z_in=None, return_state=False, out=None, S_out=None, z_out=None,
-                         stream=None):
-    """Gated causal attention (CUDA cores, fp32).  gate: None, [B,H,N] or [B,H,N,d]
-    float32; phi: "elu1" or "identity".  Returns y (and the final (S, z))."""
-    _check_cuda(q, k, v, gate, S_in, z_in, out, S_out, z_out)
+                         workspace=None, stream=None, check_status=False):
+    """Gated causal attention.  gate: None, [B,H,N] or [B,H,N,d] float32; phi:
+    "elu1" or "identity".  bf16 inputs with d, dv in {64, 128}, one gate per
+    token and elu + 1 run on the tensor cores (heads whose gates all lie in
+    [2^-1/2, 1]); everything else in fp32 on the CUDA cores.  Returns y (and the
+    final (S, z)); ``check_status`` as for :func:`forward_causal`."""
+    _check_cuda(q, k, v, gate, S_in, z_in, out, S_out, z_out, workspace)
     B, H, N, d = q.shape
     dv = v.shape[-1]
     dt = _dtype_code(q)
@@ -446,11 +457,20 @@ def forward_causal_gated(q, k, v, gate=None, phi="elu1", eps: float = 1e-6, S_in
     if return_state and S_out is None:
         S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=q.device)
         z_out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    need = (causal_gated_workspace_bytes(B, H, N, d, dv, q.dtype, phi, gd) if gate is not None
+            else 256)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
     st = lib().la_forward_causal_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(y), B, H, N, d, dv, dt,
                                        float(eps), PHI[phi], _ptr(gate), gd, _ptr(S_in),
-                                       _ptr(z_in), _ptr(S_out), _ptr(z_out),
+                                       _ptr(z_in), _ptr(S_out), _ptr(z_out), _ptr(workspace),
+                                       workspace.numel() if workspace is not None else 0,
                                        _stream_handle(stream, q.device))
     _raise(st, "la_forward_causal_gated")
+    if check_status and workspace is not None:
+        err, where = workspace_header(workspace)
+        if err != LA_OK:
+            raise LinAttnError(err, f"la_forward_causal_gated (run time, wait site {where})")
     return (y, S_out, z_out) if return_state else y
 
 

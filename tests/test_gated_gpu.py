@@ -2,9 +2,13 @@
 fp64 oracle ("Linear Attention/es", "Variantes y extensiones": gated linear
 attention; "Mapas de características": identity and random-feature maps).
 
-la_forward_causal_gated, la_decode_step_gated and la_forward_noncausal_phi run
-in float32 on the CUDA cores for both input dtypes (bf16 inputs are exact in
-float32), so the float32 bound, 1e-4 of RMS, applies to all of them.  The
+la_decode_step_gated and la_forward_noncausal_phi with the identity map run in
+float32 on the CUDA cores for both input dtypes (bf16 inputs are exact in
+float32), so the float32 bound, 1e-4 of RMS, applies to them, and to
+la_forward_causal_gated wherever it runs on the CUDA cores.  With bf16 inputs,
+d and dv in {64, 128}, one gate per token and elu + 1, la_forward_causal_gated
+runs on the tensor cores (tests/test_gated_tc_gpu.py), and the bf16 bound,
+2e-2 of RMS, applies.  The
 identity map's denominator can cross zero; those cases draw q and k around
 +1.5 so that it stays away from the clamp, except the clamp case itself.
 """
@@ -16,9 +20,16 @@ import oracle
 from linear_rnn_sequence_gb300 import linattn as la
 from linear_rnn_sequence_gb300.workloads import (WORKLOADS, head_decays, make_gated_inputs,
                                                  random_gated, random_projection, random_qkv)
-from metrics import TOL_F32, rel_max_err
+from metrics import TOL_BF16, TOL_F32, rel_max_err
 
 pytestmark = pytest.mark.gpu
+
+
+def gated_tol(dt, d, dv, gate_dim, phi, gated=True):
+    """The bound of the path la_forward_causal_gated takes for these arguments."""
+    tc = (dt == torch.bfloat16 and d in (64, 128) and dv in (64, 128) and gate_dim == 1
+          and phi == "elu1" and gated)
+    return TOL_BF16 if tc else TOL_F32
 
 
 def _check(got, want, tol=TOL_F32, what=""):
@@ -61,7 +72,8 @@ def test_causal_gated_matches_oracle(case, gate_dim, phi, cuda_device):
                                       S_in=dev(S_in), z_in=dev(z_in), return_state=True)
     torch.cuda.synchronize()
     want = oracle.causal_gated(q, k, v, gate=g, phi=phi, S_in=S_in, z_in=z_in, return_state=True)
-    _check((y, S, z), want, what=f"{gate_dim} {phi}")
+    _check((y, S, z), want, tol=gated_tol(dt, d, dv, gd, phi, g is not None),
+           what=f"{gate_dim} {phi}")
 
 
 def test_gated_with_constant_gates_equals_decay(cuda_device):
@@ -182,7 +194,8 @@ def test_random_feature_attention_end_to_end(cuda_device):
 
 def test_gated_workload_sampled_heads(cuda_device):
     """The gated training-shape workload in the launch configuration the
-    benchmark times; whole heads checked (heads are independent)."""
+    benchmark times (its gates lie in [3/4, 1): every head on the tensor
+    cores); whole heads checked (heads are independent)."""
     w = WORKLOADS["causal_gated_bf16_b8h16n8192d128"]
     q, k, v, g = make_gated_inputs(w)
     y = la.forward_causal_gated(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
@@ -191,7 +204,7 @@ def test_gated_workload_sampled_heads(cuda_device):
     flat = lambda t: t.reshape(w.BH, w.N, *t.shape[3:])
     for h in (0, 77, 127):
         want = oracle.causal_gated(flat(q)[h], flat(k)[h], flat(v)[h], gate=flat(g)[h])
-        assert rel_max_err(flat(y)[h], want) <= TOL_F32, f"head {h}"
+        assert rel_max_err(flat(y)[h], want) <= TOL_BF16, f"head {h}"   # tensor cores
 
 
 def test_gated_empty_sequence_copies_state(cuda_device):

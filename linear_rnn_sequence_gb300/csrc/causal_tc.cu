@@ -405,16 +405,24 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
     const float dd = (float)D;
     // groups entirely above this warp's rows are all zero (causal mask)
     const int last_grp = (wq * 32 + 31) >> 4;
+    // the block's decay over its L tokens and its inverse (gsc below); with
+    // gates they come from global memory and are loaded one block ahead
+    float pL_next = 1.f, ipL_next = 1.f;
+    auto fetch = [&](int c) {
+        if (DK == 2 && c < nchunks) {
+            const int L = min(kC, nloc - c * kC);
+            pL_next = P.pw(c, L);
+            ipL_next = P.ipw(c, L);
+        }
+    };
+    fetch(0);
     for (int c = 0; c < nchunks; ++c) {
         const int cb = c & 1;
-        // the block's decay over its L tokens, and (gsc below) its inverse
-        float pL = 1.f, ipL = 1.f;
-        if (DECAY) {
-            const int L = min(kC, nloc - c * kC);
-            pL = P.pw(c, L);
-            ipL = P.ipw(c, L);
-            ds.step(pL);
-        }
+        const int Lc = min(kC, nloc - c * kC);
+        const float pL = DK == 2 ? pL_next : (DECAY ? P.pw(c, Lc) : 1.f);
+        const float ipL = DK == 2 ? ipL_next : (DECAY ? P.ipw(c, Lc) : 1.f);
+        fetch(c + 1);
+        if (DECAY) ds.step(pL);
         bool ok = wait_warp(&S.q_full, c & 1, g, 40);
         if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
@@ -668,6 +676,25 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     // psi(k) in place (bf16) over this half's features; beta_j = sum of the
     // row (before rounding) over both halves; h = 0 writes the [1|beta] and B' rows.
     // Returns false when the group gave up (agreed at the group barrier).
+    // Decay factors.  With gates they come from global memory and each is
+    // loaded one call ahead: phi_k's block decay and key weight, the export's
+    // decays of blocks c and c + 1, the epilogue's 1 / (decay through token i).
+    float kf_pL = 1.f, kf_kw = 1.f, ex_cur = 1.f, ex_next = 1.f, ep_ipw = 1.f;
+    auto kfetch = [&](int c) {
+        if (DK == 2 && c < nchunks) {
+            const int L = min(kC, N - c * kC);
+            kf_pL = P.pw(c, L);
+            kf_kw = row < L ? P.key_weight(c, L, row) : 0.f;
+        }
+    };
+    auto bdecay = [&](int c) { return (DECAY && c < nchunks) ? P.pw(c, min(kC, N - c * kC)) : 1.f; };
+    if (DK == 2) {
+        kfetch(0);
+        ex_cur = bdecay(0);
+        ex_next = bdecay(1);
+        ep_ipw = P.ipw(0, row + 1);
+    }
+
     auto phi_k = [&](int c) -> bool {
         const int s = c & 1, cb = c & 1;
         // decay: key j of a block of L tokens enters with weight
@@ -676,9 +703,10 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const int L = min(kC, N - c * kC);
         float sc = 1.f;
         if (DECAY) {   // s_j / G, with s_j = (decay of the whole block) / (decay up to key j)
-            ks.step(P.pw(c, L));
-            sc = row < L ? P.key_weight(c, L, row) / ks.G : 0.f;
+            ks.step(DK == 2 ? kf_pL : P.pw(c, L));
+            sc = (DK == 2 ? kf_kw : (row < L ? P.key_weight(c, L, row) : 0.f)) / ks.G;
         }
+        kfetch(c + 1);
         const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
@@ -774,11 +802,16 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // the scale restarts at block c+1, the state is multiplied by gamma^L
         // of block c+1 over G0 and written back before that block's update
         const float G = DECAY ? xs.G : 1.f;
-        const float gcur = DECAY ? P.pw(c, L) : 1.f;   // the decay of block c
+        // the decays of blocks c and c + 1
+        const float gcur = DK == 2 ? ex_cur : bdecay(c);
+        const float gL = DK == 2 ? ex_next : bdecay(c + 1);
+        if (DK == 2) {
+            ex_cur = ex_next;
+            ex_next = bdecay(c + 2);
+        }
         bool rescale = false;
         float gnext = 1.f;
         if (DECAY && c + 1 < nchunks) {
-            const float gL = P.pw(c + 1, min(kC, N - (c + 1) * kC));
             xs.step(gL);
             rescale = xs.renorm;
             gnext = gL / xs.G0;
@@ -885,7 +918,8 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // decay: row i's numerator and denominator are both carried divided by
         // gamma^(i+1) (the decay from the block's start through token i), so
         // the clamp max(den, eps) becomes max(den', eps gamma^-(i+1))
-        const float eps_row = DECAY ? p.eps * P.ipw(c, row + 1) : p.eps;
+        const float eps_row = DECAY ? p.eps * (DK == 2 ? ep_ipw : P.ipw(c, row + 1)) : p.eps;
+        if (DK == 2 && c + 1 < nchunks) ep_ipw = P.ipw(c + 1, row + 1);
         if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 8);

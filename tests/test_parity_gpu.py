@@ -245,12 +245,14 @@ def test_causal_host_buffer_too_small_is_rejected(cuda_device):
 
 
 # The tensor-core causal path for every (d, dv) pair, ragged tails, one-block
-# sequences and the sequence split (few heads, long sequences), with and
-# without an initial state.
+# sequences, the sequence split (few heads, long sequences) and one CTA per
+# head for 64 to 128 heads, with and without an initial state.
 @pytest.mark.parametrize("B,H,N,d,dv,with_state", [
     (1, 1, 1, 64, 64, False), (1, 2, 127, 64, 128, True), (1, 2, 129, 128, 64, False),
     (2, 3, 1000, 64, 128, False), (1, 3, 2049, 128, 64, True), (1, 1, 20000, 64, 64, True),
     (1, 2, 9001, 128, 128, False), (96, 1, 300, 64, 128, False),
+    (1, 96, 600, 64, 64, True), (1, 128, 1031, 128, 128, False), (4, 25, 2049, 64, 128, True),
+    (2, 64, 777, 128, 64, True),
 ])
 def test_causal_tc_shapes(B, H, N, d, dv, with_state, cuda_device):
     q, k, v = random_qkv(B, H, N, d, dv, dtype=torch.bfloat16, scale=d ** -0.5, seed=N + dv)

@@ -229,8 +229,16 @@ struct DecayPow {
     }
 };
 
+// Where each instantiation keeps the slow path of its bounded waits (the W of
+// mbar_wait), per feature width and decay mode, as measured on the workloads:
+// the d = 128 plain kernel inline, the others partly or wholly out of line.
+template <int D, int DK>
+struct WaitPolicy {
+    static constexpr int value = D == 128 ? (DK == 0 ? 0 : (DK == 1 ? 2 : 1)) : (DK == 0 ? 2 : 1);
+};
+
 // ------------------------------------------------------------------ producer
-template <int D, int DV>
+template <int D, int DV, int W>
 __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
                                               const CUtensorMap *qmap, const CUtensorMap *kmap,
                                               const CUtensorMap *vmap, int head, int tok0,
@@ -243,7 +251,7 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
         // block 0's copies read only q, k, v; every later wait may depend on
         // the initial state, which the previous kernel (if any) writes
         if (c == 1) griddep_wait();
-        if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 11)) break;
+        if (c >= 2 && !mbar_wait<W>(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 11)) break;
         mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
         if (!(drop_first && c == 0)) {   // test hook: a copy that never arrives
 #pragma unroll
@@ -255,7 +263,7 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
             last_kv[s] = c;
         }
         LA_TRACE_POINT(c, 13);
-        if (c > 0 && !mbar_wait(&S.q_empty, (c - 1) & 1, g, 10)) break;
+        if (c > 0 && !mbar_wait<W>(&S.q_empty, (c - 1) & 1, g, 10)) break;
         mbar_arrive_expect_tx(&S.q_full, qbytes);
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx)
@@ -280,7 +288,7 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
 //   Y += P_hi V + P_lo V                       after the weight epilogue
 // The export of the state after block c waits for both st_full and aq_free:
 // the second says Y and Yz no longer read the operands it overwrites.
-template <int D, int DV>
+template <int D, int DV, int W>
 __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
                                          uint8_t *sRt, uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
                                          uint8_t *sYB, uint8_t *sZB, int nchunks,
@@ -298,9 +306,9 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
     const uint64_t zaug = smem_desc(smem_u32(sZB), 128, 256, kSwizzleNone);
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
-        if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 20)) break;
-        if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 21)) break;
-        if (!mbar_wait(&S.phiq_done, c & 1, g, 22)) break;
+        if (!mbar_wait<W>(&S.kv_full[s], (c >> 1) & 1, g, 20)) break;
+        if (!mbar_wait<W>(&S.phik_done[s], (c >> 1) & 1, g, 21)) break;
+        if (!mbar_wait<W>(&S.phiq_done, c & 1, g, 22)) break;
         LA_TRACE_POINT(c, 10);
         tc_fence_after();
         const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
@@ -318,7 +326,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         // state update first: it only has to wait for the export of the
         // previous state (out of TMEM), and fills the tensor pipe while the
         // output epilogue of the previous block still reads Y
-        if (!mbar_wait(&S.rt_ready, c & 1, g, 23)) break;
+        if (!mbar_wait<W>(&S.rt_ready, c & 1, g, 23)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
@@ -331,7 +339,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         }
         mma_commit(&S.st_full);
         LA_TRACE_POINT(c, 24);
-        if (!mbar_wait(&S.y_empty, c & 1, g, 24)) break;
+        if (!mbar_wait<W>(&S.y_empty, c & 1, g, 24)) break;
         LA_TRACE_POINT(c, 11);
         tc_fence_after();
 #pragma unroll
@@ -347,7 +355,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         // psi(q) and the exported state operands (R~, zeta~, B'', Bz) are free
         mma_commit(&S.aq_free);
         LA_TRACE_POINT(c, 25);
-        if (!mbar_wait(&S.h_ready[c & 1], (c >> 1) & 1, g, 25)) break;
+        if (!mbar_wait<W>(&S.h_ready[c & 1], (c >> 1) & 1, g, 25)) break;
         LA_TRACE_POINT(c, 12);
         tc_fence_after();
 #pragma unroll
@@ -394,6 +402,7 @@ template <int D, int DV, int DK>
 __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
                                              int nchunks, int nloc, const Guard &g,
                                              const float *gtab) {
+    constexpr int kW = WaitPolicy<D, DK>::value;
     constexpr bool DECAY = DK != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3, row = wq * 32 + lane;
@@ -423,8 +432,8 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         const float ipL = DK == 2 ? ipL_next : (DECAY ? P.ipw(c, Lc) : 1.f);
         fetch(c + 1);
         if (DECAY) ds.step(pL);
-        bool ok = wait_warp(&S.q_full, c & 1, g, 40);
-        if (ok && c > 0) ok = wait_warp(&S.aq_free, (c - 1) & 1, g, 41);
+        bool ok = wait_warp<kW>(&S.q_full, c & 1, g, 40);
+        if (ok && c > 0) ok = wait_warp<kW>(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
         float alpha = 0.f, cq = 1.f;
         uint64_t alpha2 = f2pack(0.f, 0.f);
@@ -478,7 +487,7 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
             if (lane == 0) LA_TRACE_POINT(c, 16 + wq);
             if (lane == 0 && wq == 3) LA_TRACE_POINT(c, 1);
         }
-        ok = wait_warp(&S.g_full, c & 1, g, 43);
+        ok = wait_warp<kW>(&S.g_full, c & 1, g, 43);
         if (ok) {
             tc_fence_after();
             if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 2);
@@ -562,6 +571,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                                              const TcParams &p, int head, int slot,
                                              int tok0, int nloc, bool last_seg, int nchunks,
                                              const Guard &g, const float *gtab) {
+    constexpr int kW = WaitPolicy<D, DK>::value;
     using Lay = Layout<D, DV>;
     constexpr bool DECAY = DK != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -707,7 +717,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             sc = (DK == 2 ? kf_kw : (row < L ? P.key_weight(c, L, row) : 0.f)) / ks.G;
         }
         kfetch(c + 1);
-        const bool ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 50);
+        const bool ok = wait_warp<kW>(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
         uint8_t *kt = sK + s * Lay::kK;
         // the key's split constant from its first eight features (in h = 0's
@@ -816,7 +826,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             rescale = xs.renorm;
             gnext = gL / xs.G0;
         }
-        if (!wait_warp(&S.st_full, c & 1, g, 51) || !wait_warp(&S.aq_free, c & 1, g, 54))
+        if (!wait_warp<kW>(&S.st_full, c & 1, g, 51) || !wait_warp<kW>(&S.aq_free, c & 1, g, 54))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 4);
         tc_fence_after();
@@ -920,7 +930,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         // the clamp max(den, eps) becomes max(den', eps gamma^-(i+1))
         const float eps_row = DECAY ? p.eps * (DK == 2 ? ep_ipw : P.ipw(c, row + 1)) : p.eps;
         if (DK == 2 && c + 1 < nchunks) ep_ipw = P.ipw(c + 1, row + 1);
-        if (!wait_warp(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp(&S.y_full, c & 1, g, 53))
+        if (!wait_warp<kW>(&S.h_ready[cb], (c >> 1) & 1, g, 52) || !wait_warp<kW>(&S.y_full, c & 1, g, 53))
             return false;
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 8);
         tc_fence_after();
@@ -1091,10 +1101,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     // the initial state; the producer waits after issuing block 0's copies.
     if (warp != 0) griddep_wait();
     if (warp == 0) {
-        if (lane == 0) producer_role<D, DV>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, tok0, nchunks,
+        if (lane == 0) producer_role<D, DV, WaitPolicy<D, DK>::value>(S, sQ, sK, sV, &qmap, &kmap, &vmap, head, tok0, nchunks,
                                            item == p.drop_item, g);
     } else if (warp == 1) {
-        if (lane == 0) mma_role<D, DV>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, nchunks, g);
+        if (lane == 0)
+            mma_role<D, DV, WaitPolicy<D, DK>::value>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB,
+                                                      nchunks, g);
     } else if (warp < kWarpB) {
         group_a_role<D, DV, DK>(S, tb, sQ, nchunks, nloc, g, gtab);
     } else {

@@ -260,9 +260,10 @@ __device__ __forceinline__ float warp_sum_f(float x) {
 }
 
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the result.
+template <int W = 0>
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, const Guard &g,
                                           unsigned int where) {
-    const bool ok = mbar_wait(bar, parity, g, where);
+    const bool ok = mbar_wait<W>(bar, parity, g, where);
     return __all_sync(0xffffffffu, ok);
 }
 

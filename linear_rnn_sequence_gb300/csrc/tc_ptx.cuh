@@ -67,17 +67,48 @@ __device__ __forceinline__ void guard_fail(const Guard &g, unsigned int code, un
     if (g.err_where) atomicCAS(g.err_where, 0u, where);
 }
 
-// Bounded wait: returns false (and raises the CTA's abort flag) if the phase
-// does not complete within the guard's time limit or another wait gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Guard &g,
-                                          unsigned int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ void guard_fail_ool(const Guard g, unsigned int code,
+                                                   unsigned int where) {
+    guard_fail(g, code, where);
+}
+
+// The polling loop of a bounded wait (see mbar_wait), out of line.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, const Guard g,
+                                                   unsigned int where) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*g.abort) return false;
         if (globaltimer_ns() - t0 > g.limit_ns) {
             guard_fail(g, 4u /* LA_ERR_TIMEOUT */, where);
+            return false;
+        }
+    }
+}
+
+// Bounded wait: returns false (and raises the CTA's abort flag) if the phase
+// does not complete within the guard's time limit or another wait gave up.
+// The first try_wait already suspends the thread for up to its time hint, so
+// the polling loop only runs for waits of a millisecond or more.  W says where
+// that slow path lives: 0 inline at every wait site; 1 the whole loop out of
+// line; 2 only the failure report out of line.  Out-of-line code keeps the
+// many wait sites of a kernel small in the instruction cache, at the price of
+// a call that the register allocator must allow for; which one pays differs
+// between kernels and is measured per instantiation.
+template <int W = 0>
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Guard &g,
+                                          unsigned int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (W == 1) return mbar_wait_slow(bar, parity, g, where);
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*g.abort) return false;
+        if (globaltimer_ns() - t0 > g.limit_ns) {
+            if (W == 2)
+                guard_fail_ool(g, 4u /* LA_ERR_TIMEOUT */, where);
+            else
+                guard_fail(g, 4u /* LA_ERR_TIMEOUT */, where);
             return false;
         }
     }

@@ -63,11 +63,19 @@ struct StateDecay {
 };
 static_assert(sizeof(StateDecay) <= 1024, "state decay area");
 
+// Where the state pass keeps the slow path of its bounded waits (the W of
+// mbar_wait), as measured on the long-sequence workloads (d = 64).
+template <int D, bool DECAY>
+struct StateWaitPolicy {
+    static constexpr int value = D == 64 ? (DECAY ? 1 : 2) : 0;
+};
+
 template <int D, int DV, bool DECAY = false>
 __global__ void __launch_bounds__(kStateThreads)
 causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const TcParams p, float *__restrict__ S_seg, float *__restrict__ z_seg)
 {
+    constexpr int kW = StateWaitPolicy<D, DECAY>::value;
     using Lay = StateLayout<D, DV, DECAY>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -122,7 +130,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             int last_kv[2] = {-1, -1};
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1, t0 = tok0 + c * kC;
-                if (c >= 2 && !mbar_wait(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 60)) break;
+                if (c >= 2 && !mbar_wait<kW>(&S.kv_empty[s], ((c >> 1) - 1) & 1, g, 60)) break;
                 mbar_arrive_expect_tx(&S.kv_full[s], kvbytes);
                 for (int bx = 0; bx < D / 64; ++bx)
                     tma_load_3d(sK + s * Lay::kK + bx * kC * 128, &kmap, &S.kv_full[s], bx * 64, t0, head);
@@ -138,11 +146,11 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         if (lane == 0) {   // MMA: R += B^T V, zeta += B^T 1, u += V^T s (rows of the [1|s] operand)
             constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);
             constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);
-            bool ok = mbar_wait(&S.init_done, 0, g, 61);
+            bool ok = mbar_wait<kW>(&S.init_done, 0, g, 61);
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int s = c & 1;
-                if (!mbar_wait(&S.kv_full[s], (c >> 1) & 1, g, 62)) break;
-                if (!mbar_wait(&S.phik_done[s], (c >> 1) & 1, g, 63)) break;
+                if (!mbar_wait<kW>(&S.kv_full[s], (c >> 1) & 1, g, 62)) break;
+                if (!mbar_wait<kW>(&S.phik_done[s], (c >> 1) & 1, g, 63)) break;
                 tc_fence_after();
                 const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
                 const uint32_t ob = smem_u32(sOnes + s * Lay::kOnes);
@@ -199,7 +207,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 nrow *= gL * Gp / ks.G;   // the count is carried over the new scale too
                 if (ks.renorm && c > 0) {
                     // the previous block's MMAs must be done before the sums are rescaled
-                    ok = wait_warp(&S.kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1, g, 66);
+                    ok = wait_warp<kW>(&S.kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1, g, 66);
                     if (!ok) break;
                     tc_fence_after();
                     const float f = gL * Gp / ks.G0;
@@ -218,7 +226,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                 }
                 sc = row < L ? X.gpow[L - 1 - row] / ks.G : 0.f;
             }
-            ok = wait_warp(&S.kv_full[s], (c >> 1) & 1, g, 64);
+            ok = wait_warp<kW>(&S.kv_full[s], (c >> 1) & 1, g, 64);
             if (!ok) break;
             uint8_t *kt = sK + s * Lay::kK;
             // the key's split constant from its first eight features (padding
@@ -258,7 +266,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             if (DECAY) tc_fence_before();   // after a rescale of the TMEM sums
             mbar_arrive(&S.phik_done[s]);
         }
-        ok = ok && wait_warp(&S.st_done, 0, g, 65);
+        ok = ok && wait_warp<kW>(&S.st_done, 0, g, 65);
         if (ok) {   // plain state of the segment: S = 1 u^T + R, z = n 1 + zeta
             tc_fence_after();
             uint32_t zv[4], uv[4];

@@ -175,11 +175,13 @@ LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *
  * Workspace size in bytes for la_forward_causal_gated with a gate of
  * gate_dim values per token (1 or d); 0 for unsupported arguments.  For bf16
  * inputs with d, dv in {64, 128}, gate_dim = 1 and LA_PHI_ELU1 (the
- * tensor-core path) it holds the run-time status header, one flag per head
- * and per-128-token-block tables of gate products, 1,056 bytes per block and
- * head; otherwise the header alone (256 bytes), which also serves a call
- * without a gate.  Device memory, 256-byte aligned, reusable by later calls on
- * the same stream.
+ * tensor-core path) it holds the run-time status header, one flag per head,
+ * per-128-token-block tables of gate products (1,056 bytes per block and
+ * head) and, when few heads make the call split the sequence into segments,
+ * the segments' states and products of gates, so it depends on the current
+ * device's SM count; otherwise the header alone (256 bytes), which also serves
+ * a call without a gate.  Device memory, 256-byte aligned, reusable by later
+ * calls on the same stream.
  */
 LA_API size_t la_causal_gated_workspace_bytes(int B, int H, int N, int d, int dv, la_dtype dt,
                                               la_phi phi, int gate_dim);

@@ -262,7 +262,7 @@ size_t la_causal_gated_workspace_bytes(int B, int H, int N, int d, int dv, la_dt
     a.phi = (int)phi;
     a.gate = reinterpret_cast<const float *>(&a);   // a gate is given (its address is not used)
     a.gate_dim = gate_dim;
-    if (N > 0 && gated_tc_supported(a)) return gated_tc_workspace(B * H, N);
+    if (N > 0 && gated_tc_supported(a)) return gated_tc_workspace(B * H, N, d, dv);
     return sizeof(WsHeader);
 }
 

@@ -196,13 +196,6 @@ __device__ __forceinline__ DecaySmall &decay_area(Small &S) {
     return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
 }
 
-// Per-token gates: one table per 128-token block, [P_0 .. P_128 | pad | 1/P_0 .. 1/P_128 | pad]
-// with P_m = g_t0 g_t0+1 ... g_t0+m-1 the product of the block's first m gates.
-constexpr int kGateInv = kC + 4;          // offset of the inverses
-constexpr int kGateTab = 2 * kGateInv;    // floats per block
-// Gates the kernel takes: [2^-1/2, 1], so that the products over a block stay
-// at or above 2^-64, the range the fixed decay is held to.
-constexpr float kGateMin = 0.70710677f;
 
 // The decay factors of a block, from a fixed decay (DK = 1: the per-head table
 // of gamma powers in shared memory) or from per-token gates (DK = 2: the
@@ -1123,17 +1116,19 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
 
 // ------------------------------------------------------------------ segment prefix scan
 // Exclusive prefix over the segments of each head, in a fixed order:
-// P_0 = S_in (or 0), P_s = f P_{s-1} + S_{s-1}; the same for z.  f = 1, or
-// with a per-head decay gamma^(segment length): every segment but the last
-// has the same length (seg_len), and the last one's state is neither used
-// nor computed.  One thread per state element (grid: heads x element
+// P_0 = S_in (or 0), P_s = f_{s-1} P_{s-1} + S_{s-1}; the same for z.  f = 1,
+// or with a per-head decay gamma^(segment length) (every segment but the last
+// has the same length, seg_len, and the last one's state is neither used nor
+// computed), or with gates the segment's product of gates (seg_decay, from
+// the state pass).  One thread per state element (grid: heads x element
 // blocks); the segment loop issues its loads ahead of the running sum.
 constexpr int kScanThreads = 128;
 __global__ void __launch_bounds__(kScanThreads)
 scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_seg,
                    float *__restrict__ S_pre, float *__restrict__ z_pre,
                    const float *__restrict__ S_in, const float *__restrict__ z_in, int nseg,
-                   int D, int DV, const float *__restrict__ gamma, int H, int seg_len)
+                   int D, int DV, const float *__restrict__ gamma, int H, int seg_len,
+                   const float *__restrict__ seg_decay)
 {
     griddep_launch_dependents();
     griddep_wait();   // S_seg, z_seg come from the state pass
@@ -1152,6 +1147,15 @@ scan_states_kernel(const float *__restrict__ S_seg, const float *__restrict__ z_
     const float f = gamma ? powf(gamma[head % H], (float)seg_len) : 1.f;
     const size_t base = (size_t)head * nseg * stride + o;
     int sg = 0;
+    if (seg_decay) {   // gates: a factor per segment
+        const float *fs = seg_decay + (size_t)head * nseg;
+        for (; sg < nseg - 1; ++sg) {
+            dst[base + sg * stride] = acc;
+            acc = fmaf(__ldg(fs + sg), acc, src[base + sg * stride]);
+        }
+        dst[base + (size_t)(nseg - 1) * stride] = acc;
+        return;
+    }
     for (; sg + 4 <= nseg - 1; sg += 4) {
         const float s0 = src[base + (sg + 0) * stride], s1 = src[base + (sg + 1) * stride];
         const float s2 = src[base + (sg + 2) * stride], s3 = src[base + (sg + 3) * stride];
@@ -1261,16 +1265,16 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.z_in = a.z_in;
     p.S_out = a.S_out;
     p.z_out = a.z_out;
-    if (DK == 2) {   // gates: one work item per head (no state pass for them)
-        p.nseg = 1;
-        p.seg_chunks = (a.N + kC - 1) / kC;
-        p.gate_blocks = p.seg_chunks;
+    choose_segments(BH, a.N, p.nseg, p.seg_chunks);
+    // the segment states: after the header, or with gates after their tables
+    size_t split_base = sizeof(WsHeader);
+    if (DK == 2) {
+        p.gate_blocks = (a.N + kC - 1) / kC;
         p.gate_tab = reinterpret_cast<const float *>(static_cast<const char *>(a.ws) +
                                                      gated_tables_offset(BH));
         p.gate_skip = reinterpret_cast<const unsigned int *>(static_cast<const char *>(a.ws) +
                                                              sizeof(WsHeader));
-    } else {
-        choose_segments(BH, a.N, p.nseg, p.seg_chunks);
+        split_base = gated_split_offset(BH, a.N);
     }
     if (DECAY) {
         p.gamma = a.gamma;
@@ -1283,17 +1287,18 @@ cudaError_t launch_dv(const FwdArgs &a) {
     p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
     p.drop_item = debug_fault().drop_load_item;
     const int items = BH * p.nseg;
-    if (DK != 2 && p.nseg > 1) {
+    if (p.nseg > 1) {
         // states of every segment but each head's last, then their exclusive
         // prefixes, which become the initial states of the (head, segment) items
         const size_t nS = (size_t)D * DV, cnt = (size_t)items;
         p.state_segs = p.nseg - 1;
-        float *S_seg = reinterpret_cast<float *>(static_cast<char *>(a.ws) + sizeof(WsHeader));
+        float *S_seg = reinterpret_cast<float *>(static_cast<char *>(a.ws) + split_base);
         float *z_seg = S_seg + cnt * nS;
         float *S_pre = z_seg + cnt * D;
         float *z_pre = S_pre + cnt * nS;
-        using SL = StateLayout<D, DV, DECAY>;
-        auto skern = causal_state_kernel<D, DV, DECAY>;
+        if (DK == 2) p.seg_decay = z_pre + cnt * D;   // the segments' products of gates
+        using SL = StateLayout<D, DV, DK == 1>;
+        auto skern = causal_state_kernel<D, DV, DK>;
         cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::request);
         if (e != cudaSuccess) return e;
@@ -1304,7 +1309,7 @@ cudaError_t launch_dv(const FwdArgs &a) {
         e = launch_overlapped(scan_states_kernel, sgrid, dim3(kScanThreads), 0, a.stream,
                               (const float *)S_seg, (const float *)z_seg, S_pre, z_pre, a.S_in,
                               a.z_in, p.nseg, D, DV, DECAY ? a.gamma : (const float *)nullptr,
-                              a.H, p.seg_chunks * kC);
+                              a.H, p.seg_chunks * kC, (const float *)p.seg_decay);
         if (e != cudaSuccess) return e;
         p.S_in = S_pre;
         p.z_in = z_pre;
@@ -1355,9 +1360,20 @@ size_t gated_tables_offset(int BH) {
     return sizeof(WsHeader) + ((size_t)BH * sizeof(unsigned int) + 255) / 256 * 256;
 }
 
-size_t gated_tc_workspace(int BH, int N) {
+size_t gated_split_offset(int BH, int N) {
     const size_t nb = (size_t)(N + kC - 1) / kC;
-    return gated_tables_offset(BH) + sizeof(float) * (size_t)BH * nb * kGateTab;
+    return (gated_tables_offset(BH) + sizeof(float) * (size_t)BH * nb * kGateTab + 255) / 256 * 256;
+}
+
+// header | flags | tables | (sequence split: S_seg, z_seg, S_pre, z_pre, the
+// segments' products of gates)
+size_t gated_tc_workspace(int BH, int N, int d, int dv) {
+    int nseg, seg_chunks;
+    choose_segments(BH, N, nseg, seg_chunks);
+    size_t bytes = gated_split_offset(BH, N);
+    if (nseg > 1)
+        bytes += sizeof(float) * (size_t)BH * nseg * (2 * ((size_t)d * dv + d) + 1);
+    return bytes;
 }
 
 size_t gated_tc_clear_bytes(int BH) { return gated_tables_offset(BH); }

@@ -101,10 +101,12 @@ size_t causal_tc_workspace(int BH, int N, int d, int dv);
 int causal_tc_launches(int BH, int N);   // kernels one causal call launches
 cudaError_t launch_causal_tc(const FwdArgs &a);
 // the gated form on the tensor cores (gate_dim 1, elu + 1, bf16, d and dv in
-// {64, 128}): workspace = header | per-head flags | per-block gate tables
+// {64, 128}): workspace = header | per-head flags | per-block gate tables |
+// the sequence split's segment states
 bool gated_tc_supported(const FwdArgs &a);
 size_t gated_tables_offset(int BH);
-size_t gated_tc_workspace(int BH, int N);
+size_t gated_split_offset(int BH, int N);
+size_t gated_tc_workspace(int BH, int N, int d, int dv);
 size_t gated_tc_clear_bytes(int BH);   // header and flags, cleared before each call
 cudaError_t launch_gated_tc(const FwdArgs &a);
 bool noncausal_tc_supported(const FwdArgs &a);

@@ -43,8 +43,17 @@ struct TcParams {
     const float *gate_tab;
     const unsigned int *gate_skip;
     int gate_blocks;
+    float *seg_decay;              // gates with a sequence split: each segment's product of gates
     int state_segs;                // segments per head the state pass reduces (0: all)
 };
+
+// Per-token gates: one table per 128-token block, [P_0 .. P_128 | pad | 1/P_0 .. 1/P_128 | pad]
+// with P_m = g_t0 g_t0+1 ... g_t0+m-1 the product of the block's first m gates.
+constexpr int kGateInv = kC + 4;          // offset of the inverses
+constexpr int kGateTab = 2 * kGateInv;    // floats per block
+// Gates the tensor-core kernels take: [2^-1/2, 1], so that the products over a
+// block stay at or above 2^-64, the range the fixed decay is held to.
+constexpr float kGateMin = 0.70710677f;
 
 // Token range of segment seg of a head (segments of seg_chunks blocks).
 __device__ __forceinline__ void segment_range(const TcParams &p, int seg, int &tok0, int &nloc) {

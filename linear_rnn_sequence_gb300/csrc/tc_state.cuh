@@ -27,7 +27,10 @@ namespace {
 // kernel's: key j of a block of L tokens carries s_j = gamma^(L-1-j), the
 // TMEM sums are held divided by a running scale G that shrinks by gamma^L per
 // block (keys enter multiplied by s_j / G; the export multiplies by G), and
-// they are rescaled in TMEM only when G would fall below 2^-48.
+// they are rescaled in TMEM only when G would fall below 2^-48.  With
+// per-token gates (DK = 2) gamma^m becomes the product of the block's first m
+// gates, read from the per-block tables of the gated path, and the pass also
+// records each segment's product of gates for the prefix scan.
 constexpr int kStateThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 psi(k) / export
 constexpr uint32_t kStColR = 0, kStColZ = 128, kStColU = 144, kStTmemCols = 256;
 
@@ -70,13 +73,14 @@ struct StateWaitPolicy {
     static constexpr int value = D == 64 ? (DECAY ? 1 : 2) : 0;
 };
 
-template <int D, int DV, bool DECAY = false>
+template <int D, int DV, int DK = 0>
 __global__ void __launch_bounds__(kStateThreads)
 causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const TcParams p, float *__restrict__ S_seg, float *__restrict__ z_seg)
 {
+    constexpr bool DECAY = DK != 0;   // a fixed decay (1) or gates (2)
     constexpr int kW = StateWaitPolicy<D, DECAY>::value;
-    using Lay = StateLayout<D, DV, DECAY>;
+    using Lay = StateLayout<D, DV, DK == 1>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -99,7 +103,13 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     griddep_launch_dependents();
     // decay: heads left to the CUDA-core kernel need no segment states (the
     // chunk kernel skips them too); the whole CTA leaves before any barrier
-    if (DECAY && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
+    if (DK == 1 && !decay_on_tensor_cores(p.gamma[head % p.H])) return;
+    if (DK == 2 && p.gate_skip[head] != 0u) return;
+    // gates: this segment's first block's table of gate products
+    const float *gtab =
+        DK == 2 ? p.gate_tab + ((size_t)head * p.gate_blocks + tok0 / kC) * kGateTab : nullptr;
+    // the block's decay over its first m tokens
+    auto pw = [&](int c, int m) { return DK == 2 ? __ldg(gtab + (size_t)c * kGateTab + m) : X.gpow[m]; };
 
     if (tid == 0) {
         S.abort_flag = 0;
@@ -114,7 +124,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
     }
-    if (DECAY && tid < kC + 1) X.gpow[tid] = powf(p.gamma[head % p.H], (float)tid);
+    if (DK == 1 && tid < kC + 1) X.gpow[tid] = powf(p.gamma[head % p.H], (float)tid);
     if (warp == 1) {
         tmem_alloc(&S.tmem_base, kStTmemCols);
         tmem_relinquish();
@@ -195,15 +205,17 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         tc_fence_before();
         mbar_arrive(&S.init_done);
         bool ok = true;
-        DecayScale ks(DECAY ? X.gpow[1] : 1.f);   // X.gpow[1] = gamma
+        DecayScale ks(DK == 1 ? X.gpow[1] : (DK == 2 ? 0.5f : 1.f));   // X.gpow[1] = gamma
+        float segf = 1.f;   // gates: the segment's product of gates (thread wtid 0)
         float nrow = 0.f;   // this token row's share of n (with a decay: decayed, over G)
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const int L = min(kC, nloc - c * kC);
             float sc = 1.f;
             if (DECAY) {
-                const float Gp = ks.G, gL = X.gpow[L];
+                const float Gp = ks.G, gL = pw(c, L);
                 ks.step(gL);
+                segf *= gL;
                 nrow *= gL * Gp / ks.G;   // the count is carried over the new scale too
                 if (ks.renorm && c > 0) {
                     // the previous block's MMAs must be done before the sums are rescaled
@@ -224,7 +236,9 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
                     }
                     tmem_wait_st();
                 }
-                sc = row < L ? X.gpow[L - 1 - row] / ks.G : 0.f;
+                const float kw = DK == 2 ? gL * __ldg(gtab + (size_t)c * kGateTab + kGateInv + row + 1)
+                                         : X.gpow[L - 1 - row];
+                sc = row < L ? kw / ks.G : 0.f;
             }
             ok = wait_warp<kW>(&S.kv_full[s], (c >> 1) & 1, g, 64);
             if (!ok) break;
@@ -297,6 +311,7 @@ causal_state_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
             // n = sum of the keys' constants (nloc when every constant is 1)
             const float n = G * ((S.n_part[0] + S.n_part[1]) + (S.n_part[2] + S.n_part[3]));
             if (row < D) z_seg[(size_t)slot * D + row] = fmaf(u2f(zv[0]), G, n);
+            if (DK == 2 && wtid == 0) p.seg_decay[slot] = segf;
         }
     }
     tc_fence_before();

@@ -69,6 +69,21 @@ def test_gated_tc_shapes(d, dv, N, cuda_device):
     _check(got, want, TOL_BF16, f"d{d} dv{dv} N{N}")
 
 
+# Few heads and long sequences: the sequence is split into segments (a state
+# pass over the segments with their products of gates, a prefix scan, then the
+# chunk kernel from each segment's prefix).
+@pytest.mark.parametrize("B,H,N,d,dv", [(1, 2, 20000, 64, 64), (1, 3, 5000, 128, 128),
+                                        (2, 2, 3000, 64, 128)])
+def test_gated_tc_split_sequences(B, H, N, d, dv, cuda_device):
+    q, k, v, g = random_gated(B, H, N, d, dv, 1, dtype=torch.bfloat16, scale=d ** -0.5, seed=N + d)
+    gen = torch.Generator().manual_seed(N + 1)
+    S_in = torch.randn(B, H, d, dv, generator=gen) * 0.5
+    z_in = torch.rand(B, H, d, generator=gen) * 5 + 1
+    got = _run(q, k, v, g, cuda_device, S_in=S_in, z_in=z_in)
+    want = oracle.causal_gated(q, k, v, gate=g, S_in=S_in, z_in=z_in, return_state=True)
+    _check(got, want, TOL_BF16, f"B{B} H{H} N{N} d{d} dv{dv}")
+
+
 def test_gated_tc_constant_gates_are_the_decay(cuda_device):
     """Gates equal to a per-head gamma at every token give the decayed form."""
     B, H, N, d, dv = 2, 4, 700, 64, 64

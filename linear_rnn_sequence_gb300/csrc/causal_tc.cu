@@ -143,10 +143,19 @@ struct Layout {
     static constexpr int kGB = kC * 16 * 2;         // B' (G augmentation), [C x 16]
     static constexpr int kYB = DV * 16 * 2;         // B'' (Y augmentation), [dv x 16]
     static constexpr int kZB = 16 * 16 * 2;         // Bz (Yz augmentation), [16 x 16]
+    // d = dv = 64 ("ext"): each K stage is followed by an extension box whose
+    // first columns hold the keys' weights and residual row sums, and each V
+    // stage by a ones box, so one MMA per 16 tokens updates R, zeta, u and r
+    // together (the accumulator is [R | zeta ...] over dv + 64 columns, with
+    // rows 64..67 holding s_hi, s_lo, beta_hi, beta_lo times V).  The [1|beta]
+    // operand area is then free and serves as scratch (ExtScratch).
+    static constexpr bool kExt = D == 64 && DV == 64;
+    static constexpr int kKs = kExt ? 2 * kK : kK;  // K stage stride
+    static constexpr int kVs = kExt ? 2 * kV : kV;  // V stage stride
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQ;              // 2 stages
-    static constexpr int oV = oK + 2 * kK;          // 2 stages
-    static constexpr int oRt = oV + 2 * kV;
+    static constexpr int oV = oK + 2 * kKs;         // 2 stages
+    static constexpr int oRt = oV + 2 * kVs;
     static constexpr int oUVB = oRt + kRt;          // 2 stages
     static constexpr int oZt = oUVB + 2 * kUVB;
     static constexpr int oGB = oZt + kZt;           // 2 stages
@@ -196,6 +205,15 @@ __device__ __forceinline__ DecaySmall &decay_area(Small &S) {
     return *reinterpret_cast<DecaySmall *>(reinterpret_cast<uint8_t *>(&S) + kSmallBytes);
 }
 
+
+// Scratch of the ext layout (d = dv = 64) in the otherwise unused [1|beta]
+// operand area: rows 64..67 of the state accumulator over the dv columns, and
+// the initial state's r.
+struct ExtScratch {
+    alignas(16) float uv[4][128];
+    alignas(16) float r0[128];
+};
+static_assert(sizeof(ExtScratch) <= 2 * 16 * kC * 2, "ext scratch fits the operand area");
 
 // The decay factors of a block, from a fixed decay (DK = 1: the per-head table
 // of gamma powers in shared memory) or from per-token gates (DK = 2: the
@@ -249,10 +267,10 @@ __device__ __forceinline__ void producer_role(Small &S, uint8_t *sQ, uint8_t *sK
         if (!(drop_first && c == 0)) {   // test hook: a copy that never arrives
 #pragma unroll
             for (int bx = 0; bx < D / 64; ++bx)
-                tma_load_3d(sK + s * Lay::kK + bx * kC * 128, kmap, &S.kv_full[s], bx * 64, t0, head);
+                tma_load_3d(sK + s * Lay::kKs + bx * kC * 128, kmap, &S.kv_full[s], bx * 64, t0, head);
 #pragma unroll
             for (int bx = 0; bx < DV / 64; ++bx)
-                tma_load_3d(sV + s * Lay::kV + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
+                tma_load_3d(sV + s * Lay::kVs + bx * kC * 128, vmap, &S.kv_full[s], bx * 64, t0, head);
             last_kv[s] = c;
         }
         LA_TRACE_POINT(c, 13);
@@ -293,6 +311,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
     constexpr uint32_t iYz = idesc_bf16(128, 16, 0, 0);  // A in TMEM, B = zeta~ no swizzle
     constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);   // A = psi(k)^T MN-major, B = V MN-major
     constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);   // A MN-major, B = [1|beta] no swizzle
+    constexpr uint32_t iE = idesc_bf16(128, DV + 64, 1, 1);   // ext: A, B MN-major, N = dv + 64
     constexpr uint32_t aAug = kColAq + D / 2;            // A' columns
     const uint32_t rb = smem_u32(sRt), zb = smem_u32(sZt);
     const uint64_t yaug = smem_desc(smem_u32(sYB), 128, 256, kSwizzleNone);
@@ -304,7 +323,7 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
         if (!mbar_wait<W>(&S.phiq_done, c & 1, g, 22)) break;
         LA_TRACE_POINT(c, 10);
         tc_fence_after();
-        const uint32_t kb = smem_u32(sK + s * Lay::kK), vb = smem_u32(sV + s * Lay::kV);
+        const uint32_t kb = smem_u32(sK + s * Lay::kKs), vb = smem_u32(sV + s * Lay::kVs);
         const uint32_t ub = smem_u32(sUVB + s * Lay::kUVB);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -326,9 +345,13 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
             const uint64_t ad = smem_desc(kb + ks * 2048, kC * 128, 1024, kSwizzle128B);
             const uint64_t vd = smem_desc(vb + ks * 2048, kC * 128, 1024, kSwizzle128B);
             const uint64_t ud = smem_desc(ub + ks * 256, 128, 2048, kSwizzleNone);
-            mma_ss(tb + kColR, ad, vd, iR, 1);
-            mma_ss(tb + kColZ, ad, ud, iZ, 1);
-            mma_ss(tb + kColUV, vd, ud, iZ, 1);
+            if (Lay::kExt) {   // [psi(K)^T ; weights^T] [V | 1]: R, zeta, u, r at once
+                mma_ss(tb + kColR, ad, vd, iE, 1);
+            } else {
+                mma_ss(tb + kColR, ad, vd, iR, 1);
+                mma_ss(tb + kColZ, ad, ud, iZ, 1);
+                mma_ss(tb + kColUV, vd, ud, iZ, 1);
+            }
         }
         mma_commit(&S.st_full);
         LA_TRACE_POINT(c, 24);
@@ -558,7 +581,8 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
 // h = 0, 1) sharing its work: psi(k) in place over half of the features,
 // the state export of half of R's columns, half of the output columns.
 template <int D, int DV, int DK>
-__device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sRt,
+__device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK, uint8_t *sV,
+                                             uint8_t *sRt,
                                              uint8_t *sUVB, uint8_t *sZt, uint8_t *sGB,
                                              uint8_t *sYB, uint8_t *sZB,
                                              const TcParams &p, int head, int slot,
@@ -580,14 +604,28 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
     const int N = nloc;   // tokens of this work item (segment)
     constexpr int kRGroups = DV / 32;     // 16-column groups of R (and Y) per half
 
-    // operand rows: [1|beta|s] row 0 = ones, rows 5..15 zero (rows 1..4 are
-    // written per block by psi(k)); zeta~ all zero
-    for (int e = wtid; e < 2 * 16 * kC; e += 2 * kWG) {
-        const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
-        *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
-                                           (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
-            __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
+    ExtScratch &XS = *reinterpret_cast<ExtScratch *>(sUVB);   // ext only
+    if (Lay::kExt) {
+        // extension boxes zero (the first 16 bytes of a key's row are written
+        // per block), ones boxes: first column 1, the rest 0
+        for (int e = wtid; e < 2 * kC * 8; e += 2 * kWG) {
+            const int st = e / (kC * 8), r = (e / 8) % kC, ch = e % 8;
+            *reinterpret_cast<uint4 *>(sK + st * Lay::kKs + Lay::kK + sw128_off(r, ch * 8)) =
+                make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(sV + st * Lay::kVs + Lay::kV + sw128_off(r, ch * 8)) =
+                ch == 0 ? make_uint4(pack_bf16x2(1.f, 0.f), 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    } else {
+        // operand rows: [1|beta|s] row 0 = ones, rows 5..15 zero (rows 1..4 are
+        // written per block by psi(k))
+        for (int e = wtid; e < 2 * 16 * kC; e += 2 * kWG) {
+            const int s = e / (16 * kC), rem = e % (16 * kC), n = rem / kC, k = rem % kC;
+            *reinterpret_cast<__nv_bfloat16 *>(sUVB + s * Lay::kUVB + (n >> 3) * 2048 +
+                                               (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) =
+                __float2bfloat16_rn(n == 0 ? 1.f : 0.f);
+        }
     }
+    // zeta~ all zero
     for (int e = wtid; e < 16 * D; e += 2 * kWG)
         *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(e / D, e % D, D)) = __float2bfloat16_rn(0.f);
     // B' rows: slots 8..15 are zero for good (slots 0..7 are written per block)
@@ -618,6 +656,22 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         const float p0 = DECAY ? P.pw(0, min(kC, N)) : 1.f;
         if (DECAY) xs.step(p0);
         const float g0 = DECAY ? (xs.renorm ? p0 : 1.f) / xs.G0 : 1.f;
+        // u = the first row of S, r = the column sums of R = S - 1 u^T (per dv
+        // column: thread row takes column row)
+        float u0 = 0.f, r0 = 0.f;
+        if (h == 0 && Sin && row < DV) {
+            u0 = Sin[row];
+            // independent loads, issued 16 at a time ahead of the sums
+#pragma unroll 16
+            for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
+        }
+        if (Lay::kExt) {   // rows 64 and 66 of the accumulator start from u and r
+            if (h == 0 && row < DV) {
+                S.u[1][row] = u0;
+                XS.r0[row] = r0;
+            }
+            named_bar(kBarB, 2 * kWG);
+        }
 #pragma unroll
         for (int gq = 0; gq < kRGroups; ++gq) {
             const int grp = h * kRGroups + gq;
@@ -625,7 +679,10 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int b = grp * 16 + jj;
-                v[jj] = f2u((Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f);
+                float x = (Sin && row < D) ? Sin[(size_t)row * DV + b] - Sin[b] : 0.f;
+                if (Lay::kExt && row == 64) x = S.u[1][b];
+                if (Lay::kExt && row == 66) x = XS.r0[b];
+                v[jj] = f2u(x);
             }
             if (row < D) export_row_bf16<D, DV>(sRt, row, grp, v);
             if (DECAY) {
@@ -637,16 +694,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         float zeta0 = 0.f;
         if (h == 0) {
             zeta0 = (zin && row < D) ? zin[row] - zin[0] : 0.f;
-            float u0 = 0.f, r0 = 0.f;
-            if (Sin && row < DV) {
-                u0 = Sin[row];
-                // independent loads, issued 16 at a time ahead of the sums
-#pragma unroll 16
-                for (int a = 1; a < D; ++a) r0 += Sin[(size_t)a * DV + row] - u0;
-            }
             const uint32_t zv[4] = {f2u(zeta0 * g0), 0u, 0u, 0u};
-            tmem_st4(tb + lb + kColZ, zv);
-            {   // columns [sum v | r_hi | r_lo | u_hi | u_lo | 0 0 0]
+            if (Lay::kExt) {
+                tmem_st4(tb + lb + kColR + DV, zv);   // the ones column
+            } else {
+                tmem_st4(tb + lb + kColZ, zv);
+                // columns [sum v | r_hi | r_lo | u_hi | u_lo | 0 0 0]
                 const uint32_t uv[4] = {0u, f2u(r0 * g0), 0u, f2u(u0 * g0)};
                 const uint32_t uw[4] = {0u, 0u, 0u, 0u};
                 tmem_st4(tb + lb + kColUV, uv);
@@ -712,7 +765,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         kfetch(c + 1);
         const bool ok = wait_warp<kW>(&S.kv_full[s], (c >> 1) & 1, g, 50);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 6);
-        uint8_t *kt = sK + s * Lay::kK;
+        uint8_t *kt = sK + s * Lay::kKs;
         // the key's split constant from its first eight features (in h = 0's
         // half; padding rows read zeros: c' = 1).  Both halves read them from
         // the tile; h = 0 writes their residuals back only after the group
@@ -765,18 +818,25 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             *reinterpret_cast<uint4 *>(kt + sw128_off(row, 0)) = held;
             beta += S.beta_part[row];
             const float bh = bf16_round(beta);
-            uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
-            *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
             // key weight s_j = sc c'_j as a bf16 pair: the key's constant part,
             // times its decay weight over G with a decay (c'_j itself, a bf16
             // value, without one); 0 for padding rows
             const float sj = row < L ? sc * ck : 0.f;
             const float sh = bf16_round(sj), sl = bf16_round(sj - sh);
-            // rows 3, 4 of [1|beta|s]: u += V^T s (row 0 stays 1: it also
-            // feeds zeta += psi_c(K)^T 1)
-            *reinterpret_cast<__nv_bfloat16 *>(ubp + 48) = __float2bfloat16_rn(sh);
-            *reinterpret_cast<__nv_bfloat16 *>(ubp + 64) = __float2bfloat16_rn(sl);
+            if (Lay::kExt) {
+                // the key's row of the extension box: [s_hi, s_lo, beta_hi, beta_lo, 0 ...]
+                // (rows 64..67 of the state MMA's A: u and r accumulate there)
+                *reinterpret_cast<uint4 *>(kt + Lay::kK + sw128_off(row, 0)) =
+                    make_uint4(pack_bf16x2(sh, sl), pack_bf16x2(bh, beta - bh), 0u, 0u);
+            } else {
+                uint8_t *ubp = sUVB + s * Lay::kUVB + (row >> 3) * 128 + (row & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 16) = __float2bfloat16_rn(bh);
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 32) = __float2bfloat16_rn(beta - bh);
+                // rows 3, 4 of [1|beta|s]: u += V^T s (row 0 stays 1: it also
+                // feeds zeta += psi_c(K)^T 1)
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 48) = __float2bfloat16_rn(sh);
+                *reinterpret_cast<__nv_bfloat16 *>(ubp + 64) = __float2bfloat16_rn(sl);
+            }
             // B' row of key j: [beta_hi, beta_lo, s_hi, s_hi, s_hi, s_lo, s_lo, 0]
             // (beta is the sum of the residual features, scaled with a decay)
             *reinterpret_cast<uint4 *>(sGB + s * Lay::kGB + k16_off(row, 0)) =
@@ -840,6 +900,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             if (row < D) {
                 export_row_bf16<D, DV>(sRt, row, grp, rv0);
                 export_row_bf16<D, DV>(sRt, row, grp + 1, rv1);
+            } else if (Lay::kExt && row < 68) {   // rows 64..67: the u and r parts
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    XS.uv[row - 64][grp * 16 + m] = u2f(rv0[m]);
+                    XS.uv[row - 64][(grp + 1) * 16 + m] = u2f(rv1[m]);
+                }
             }
             if (rescale) {
 #pragma unroll
@@ -851,11 +917,16 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                 tmem_st16(tb + lb + kColR + (grp + 1) * 16, rv1);
             }
         }
+        if (Lay::kExt) named_bar(kBarB, 2 * kWG);   // the u and r parts are in the scratch
         if (h == 0) {
-            uint32_t zv[4], uv[4], uw[4];
-            tmem_ld4(tb + lb + kColZ, zv);
-            tmem_ld4(tb + lb + kColUV, uv);
-            tmem_ld4(tb + lb + kColUV + 4, uw);
+            uint32_t zv[4], uv[4] = {0u, 0u, 0u, 0u}, uw[4] = {0u, 0u, 0u, 0u};
+            if (Lay::kExt) {
+                tmem_ld4(tb + lb + kColR + DV, zv);   // zeta in the ones column
+            } else {
+                tmem_ld4(tb + lb + kColZ, zv);
+                tmem_ld4(tb + lb + kColUV, uv);
+                tmem_ld4(tb + lb + kColUV + 4, uw);
+            }
             tmem_wait_ld();
             if (DECAY) {
 #pragma unroll
@@ -865,14 +936,18 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uw[m] = f2u(u2f(uw[m]) * G);
                 }
             }
-            const float u = u2f(uv[3]) + u2f(uw[0]);
+            // u and r per dv column (thread row takes column row)
+            const float u = Lay::kExt ? (row < DV ? XS.uv[0][row] + XS.uv[1][row] : 0.f)
+                                      : u2f(uv[3]) + u2f(uw[0]);
+            const float rr = Lay::kExt ? (row < DV ? XS.uv[2][row] + XS.uv[3][row] : 0.f)
+                                       : u2f(uv[1]) + u2f(uv[2]);
             if (row < D) {
                 S.zeta[row] = u2f(zv[0]);
                 *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
                     __float2bfloat16_rn(u2f(zv[0]));
             }
             S.u[cb][row] = u;
-            if (row < DV) aug_row(sYB, row, u2f(uv[1]) + u2f(uv[2]), u);
+            if (row < DV) aug_row(sYB, row, rr, u);
             if (wtid == 0) {
                 const float rsum = (S.rho_part[cb][0] + S.rho_part[cb][1]) +
                                    (S.rho_part[cb][2] + S.rho_part[cb][3]);
@@ -896,9 +971,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     uv[m] = f2u(u2f(uv[m]) * gnext);
                     uw[m] = f2u(u2f(uw[m]) * gnext);
                 }
-                tmem_st4(tb + lb + kColZ, zv);
-                tmem_st4(tb + lb + kColUV, uv);
-                tmem_st4(tb + lb + kColUV + 4, uw);
+                if (Lay::kExt) {
+                    tmem_st4(tb + lb + kColR + DV, zv);
+                } else {
+                    tmem_st4(tb + lb + kColZ, zv);
+                    tmem_st4(tb + lb + kColUV, uv);
+                    tmem_st4(tb + lb + kColUV + 4, uw);
+                }
             }
         }
         if (rescale) tmem_wait_st();
@@ -1103,7 +1182,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant
     } else if (warp < kWarpB) {
         group_a_role<D, DV, DK>(S, tb, sQ, nchunks, nloc, g, gtab);
     } else {
-        group_b_role<D, DV, DK>(S, tb, sK, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, slot, tok0,
+        group_b_role<D, DV, DK>(S, tb, sK, sV, sRt, sUVB, sZt, sGB, sYB, sZB, p, head, slot, tok0,
                                 nloc, seg == p.nseg - 1, nchunks, g, gtab);
     }
     tc_fence_before();

@@ -137,11 +137,15 @@ struct Layout {
     static constexpr int kQ = kC * D * 2;           // one Q stage
     static constexpr int kK = kC * D * 2;
     static constexpr int kV = kC * DV * 2;
-    static constexpr int kRt = D * DV * 2;          // bf16 R operand, 128B-swizzled MN-major
+    static constexpr bool kExtY = D == 64 && DV == 64;   // as kExt below
+    // bf16 R operand, 128B-swizzled MN-major; ext: a zeta box follows (column 0
+    // = zeta~), so [R~ | zeta box] is one N = dv + 64 operand
+    static constexpr int kRt = D * DV * 2 + (kExtY ? D * 128 : 0);
     static constexpr int kUVB = 16 * kC * 2;        // [1|beta_hi|beta_lo] operand, [16 x C]
     static constexpr int kZt = 16 * D * 2;          // zeta operand, [16 x d]
     static constexpr int kGB = kC * 16 * 2;         // B' (G augmentation), [C x 16]
-    static constexpr int kYB = DV * 16 * 2;         // B'' (Y augmentation), [dv x 16]
+    // B'' (Y augmentation), [dv x 16]; ext: row dv is Bz's row (rows dv+1..dv+15 zero)
+    static constexpr int kYB = (DV + (kExtY ? 16 : 0)) * 16 * 2;
     static constexpr int kZB = 16 * 16 * 2;         // Bz (Yz augmentation), [16 x 16]
     // d = dv = 64 ("ext"): each K stage is followed by an extension box whose
     // first columns hold the keys' weights and residual row sums, and each V
@@ -309,6 +313,8 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
     constexpr uint32_t iY = idesc_bf16(128, DV, 0, 1);   // A in TMEM, B MN-major (R~ or V)
     constexpr uint32_t iYk = idesc_bf16(128, DV, 0, 0);  // A in TMEM, B'' K-major
     constexpr uint32_t iYz = idesc_bf16(128, 16, 0, 0);  // A in TMEM, B = zeta~ no swizzle
+    constexpr uint32_t iYe = idesc_bf16(128, DV + 64, 0, 1);   // ext: B = [R~ | zeta box]
+    constexpr uint32_t iYke = idesc_bf16(128, DV + 16, 0, 0);  // ext: B = [B'' ; Bz row]
     constexpr uint32_t iR = idesc_bf16(128, DV, 1, 1);   // A = psi(k)^T MN-major, B = V MN-major
     constexpr uint32_t iZ = idesc_bf16(128, 16, 1, 0);   // A MN-major, B = [1|beta] no swizzle
     constexpr uint32_t iE = idesc_bf16(128, DV + 64, 1, 1);   // ext: A, B MN-major, N = dv + 64
@@ -361,13 +367,21 @@ __device__ __forceinline__ void mma_role(Small &S, uint32_t tb, uint8_t *sK, uin
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const uint64_t bd = smem_desc(rb + ks * 2048, D * 128, 1024, kSwizzle128B);
-            mma_ts(tb + kColY, tb + kColAq + ks * 8, bd, iY, ks > 0);
-            const uint64_t zd = smem_desc(zb + ks * 256, 128, D * 16, kSwizzleNone);
-            mma_ts(tb + kColYz, tb + kColAq + ks * 8, zd, iYz, ks > 0);
+            if (Lay::kExt) {   // [Y | den ...] = psi(Q) [R~ | zeta~]
+                mma_ts(tb + kColY, tb + kColAq + ks * 8, bd, iYe, ks > 0);
+            } else {
+                mma_ts(tb + kColY, tb + kColAq + ks * 8, bd, iY, ks > 0);
+                const uint64_t zd = smem_desc(zb + ks * 256, 128, D * 16, kSwizzleNone);
+                mma_ts(tb + kColYz, tb + kColAq + ks * 8, zd, iYz, ks > 0);
+            }
         }
         // + (d + alpha_i) u + r and + (d + alpha_i) n + rho
-        mma_ts(tb + kColY, tb + aAug, yaug, iYk, 1);
-        mma_ts(tb + kColYz, tb + aAug, zaug, iYz, 1);
+        if (Lay::kExt) {
+            mma_ts(tb + kColY, tb + aAug, yaug, iYke, 1);
+        } else {
+            mma_ts(tb + kColY, tb + aAug, yaug, iYk, 1);
+            mma_ts(tb + kColYz, tb + aAug, zaug, iYz, 1);
+        }
         // psi(q) and the exported state operands (R~, zeta~, B'', Bz) are free
         mma_commit(&S.aq_free);
         LA_TRACE_POINT(c, 25);
@@ -641,6 +655,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         *reinterpret_cast<uint4 *>(tile + k16_off(n, 8)) = make_uint4(0u, 0u, 0u, 0u);
     };
     if (wtid > 0 && wtid < 16) aug_row(sZB, wtid, 0.f, 0.f);   // rows 1..15 of Bz stay zero
+    if (Lay::kExt) {
+        // the zeta box (column 0 written per export) and B'' rows dv+1..dv+15 zero
+        for (int e = wtid; e < D * 8; e += 2 * kWG)
+            *reinterpret_cast<uint4 *>(sRt + D * DV * 2 + sw128_off(e / 8, (e % 8) * 8)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        if (wtid > 0 && wtid < 16) aug_row(sYB, DV + wtid, 0.f, 0.f);
+    }
     mbar_arrive(&S.y_empty);   // Y is free for block 0
 
 
@@ -710,8 +731,13 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             if (row < DV) aug_row(sYB, row, r0, u0);
         }
         named_bar(kBarB, 2 * kWG);  // zero rows of zeta~ written before row 0 below
-        if (h == 0 && row < D)
-            *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
+        if (h == 0 && row < D) {
+            if (Lay::kExt)
+                *reinterpret_cast<__nv_bfloat16 *>(sRt + D * DV * 2 + sw128_off(row, 0)) =
+                    __float2bfloat16_rn(zeta0);
+            else
+                *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) = __float2bfloat16_rn(zeta0);
+        }
         if (wtid == 0) {
             float rho0 = 0.f;
             if (zin) {
@@ -721,7 +747,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
             }
             S.n_s[1] = zin ? zin[0] : 0.f;
             S.rho_s[1] = rho0;
-            aug_row(sZB, 0, rho0, S.n_s[1]);
+            aug_row(Lay::kExt ? sYB : sZB, Lay::kExt ? DV : 0, rho0, S.n_s[1]);
         }
         tmem_wait_st();
         fence_proxy_async();
@@ -943,8 +969,12 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                                        : u2f(uv[1]) + u2f(uv[2]);
             if (row < D) {
                 S.zeta[row] = u2f(zv[0]);
-                *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
-                    __float2bfloat16_rn(u2f(zv[0]));
+                if (Lay::kExt)
+                    *reinterpret_cast<__nv_bfloat16 *>(sRt + D * DV * 2 + sw128_off(row, 0)) =
+                        __float2bfloat16_rn(u2f(zv[0]));
+                else
+                    *reinterpret_cast<__nv_bfloat16 *>(sZt + zt_off(0, row, D)) =
+                        __float2bfloat16_rn(u2f(zv[0]));
             }
             S.u[cb][row] = u;
             if (row < DV) aug_row(sYB, row, rr, u);
@@ -962,7 +992,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
                     S.n_s[cb] = S.n_s[pb] + ssum;
                     S.rho_s[cb] = S.rho_s[pb] + rsum;
                 }
-                aug_row(sZB, 0, S.rho_s[cb], S.n_s[cb]);
+                aug_row(Lay::kExt ? sYB : sZB, Lay::kExt ? DV : 0, S.rho_s[cb], S.n_s[cb]);
             }
             if (rescale) {
 #pragma unroll
@@ -1007,7 +1037,7 @@ __device__ __forceinline__ void group_b_role(Small &S, uint32_t tb, uint8_t *sK,
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 8);
         tc_fence_after();
         uint32_t yz[4];
-        tmem_ld4(tb + lb + kColYz, yz);
+        tmem_ld4(tb + lb + (Lay::kExt ? kColY + DV : kColYz), yz);   // den (ext: the column after Y)
         tmem_wait_ld();
         S.e_inv[h][row] =
             1.f / fmaxf(u2f(yz[0]) + (S.rowsum[cb][0][row] + S.rowsum[cb][1][row]), eps_row);

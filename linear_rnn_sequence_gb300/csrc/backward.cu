@@ -281,13 +281,20 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const int my_row = r0 + RT::row_of(lane);
     const bool writer = RT::writer(lane);
 
-    float R[RT::RPW][RT::CPL], Sh[RT::RPW][RT::CPL];
+    // R and Sh as packed pairs of rows: Rp[i][c] = (R[2i][c], R[2i+1][c])
+    constexpr int RP = RT::RPW / 2;
+    uint64_t Rp[RP][RT::CPL], Shp[RP][RT::CPL];
     const float *pre = prefix + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int r = 0; r < RT::RPW; ++r) {
-        ldn(pre + (r0 + r) * DV + c0, R[r]);
+    for (int i = 0; i < RP; ++i) {
+        float ra[RT::CPL], rb[RT::CPL];
+        ldn(pre + (r0 + 2 * i) * DV + c0, ra);
+        ldn(pre + (r0 + 2 * i + 1) * DV + c0, rb);
 #pragma unroll
-        for (int c = 0; c < RT::CPL; ++c) Sh[r][c] = 0.f;
+        for (int c = 0; c < RT::CPL; ++c) {
+            Rp[i][c] = pk2(ra[c], rb[c]);
+            Shp[i][c] = pk2(0.f, 0.f);
+        }
     }
     float zeta_run = tid < D ? pre[C::kOffZ + tid] : 0.f;   // thread a < D: zeta[a]
     if (tid >= D && tid < D + DV) sUrun[tid - D] = pre[C::kOffU + tid - D];
@@ -389,7 +396,9 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         for (int e = tid; e < L * DV; e += NT) sG[e] *= sDinv[e / DV];
         __syncthreads();
         // the recurrence: R_t = R_{t-1} + psi(k_t) v_t^T, hR_t = R_t g_t;
-        // and the segment's sum of phi(q_t) g_t^T
+        // and the segment's sum of phi(q_t) g_t^T.  Each FMA updates a pair of
+        // rows (packed), with the same operations per element as the scalar form.
+        const uint64_t gm2 = pk2(gm, gm);
         auto token_loop = [&](auto scaled_tag) {
             constexpr bool SC = decltype(scaled_tag)::value;
             // two tokens per iteration overlap one token's reduce-scatter with the
@@ -411,26 +420,34 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 #pragma unroll
                     for (int r = 0; r < RT::RPW; ++r) fq[r] *= w;
                 }
+                uint64_t xb[RT::CPL], gb[RT::CPL];   // each column value in both lanes
 #pragma unroll
-                for (int r = 0; r < RT::RPW; ++r) {
-                    acc[r] = 0.f;
+                for (int c = 0; c < RT::CPL; ++c) {
+                    xb[c] = pk2(x[c], x[c]);
+                    gb[c] = pk2(g[c], g[c]);
+                }
+#pragma unroll
+                for (int i = 0; i < RP; ++i) {
+                    const uint64_t pkp = pk2(pk[2 * i], pk[2 * i + 1]);
+                    uint64_t accp = pk2(0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < RT::CPL; ++c) {
-                        R[r][c] = fmaf(pk[r], x[c], (DECAY && !SC) ? gm * R[r][c] : R[r][c]);
-                        acc[r] = fmaf(R[r][c], g[c], acc[r]);
-                        if constexpr (SEG) Sh[r][c] = fmaf(fq[r], g[c], Sh[r][c]);
+                        Rp[i][c] = fma2(pkp, xb[c], (DECAY && !SC) ? mul2(gm2, Rp[i][c]) : Rp[i][c]);
+                        accp = fma2(Rp[i][c], gb[c], accp);
+                        if constexpr (SEG) Shp[i][c] = fma2(pk2(fq[2 * i], fq[2 * i + 1]), gb[c], Shp[i][c]);
                     }
+                    unpk2(accp, acc[2 * i], acc[2 * i + 1]);
                 }
                 float hsum = reduce_scatter<RT::RPW>(acc, lane);
                 if constexpr (SC) hsum *= sGp[t + 1];
                 if (writer) sH[t * D + my_row] = hsum;
             }
             if constexpr (SC) {
-                const float pL = sGp[L];
+                const uint64_t pL = pk2(sGp[L], sGp[L]);
 #pragma unroll
-                for (int r = 0; r < RT::RPW; ++r)
+                for (int i = 0; i < RP; ++i)
 #pragma unroll
-                    for (int c = 0; c < RT::CPL; ++c) R[r][c] *= pL;
+                    for (int c = 0; c < RT::CPL; ++c) Rp[i][c] = mul2(Rp[i][c], pL);
             }
         };
         if (scaled) token_loop(std::true_type{});
@@ -468,9 +485,10 @@ bwd_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     if constexpr (SEG) {
         float *out = rev_local + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-        for (int r = 0; r < RT::RPW; ++r)
+        for (int i = 0; i < RP; ++i)
 #pragma unroll
-            for (int c = 0; c < RT::CPL; ++c) out[(r0 + r) * DV + c0 + c] = Sh[r][c];
+            for (int c = 0; c < RT::CPL; ++c)
+                unpk2(Shp[i][c], out[(r0 + 2 * i) * DV + c0 + c], out[(r0 + 2 * i + 1) * DV + c0 + c]);
         if (tid < D) out[C::kOffZ + tid] = zh;
         for (int e = tid; e < DV + 4; e += NT) out[C::kOffU + e] = 0.f;   // unused slots
     }
@@ -518,10 +536,18 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     const int my_row = r0 + RT::row_of(lane);
     const bool wr1 = RT::writer(lane);
 
-    float S1[RT::RPW][RT::CPL];
+    // Sh as packed pairs of rows: S1p[i][c] = (Sh[2i][c], Sh[2i+1][c])
+    constexpr int RP = RT::RPW / 2;
+    uint64_t S1p[RP][RT::CPL];
     const float *suf = suffix + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int r = 0; r < RT::RPW; ++r) ldn(suf + (r0 + r) * DV + c0, S1[r]);
+    for (int i = 0; i < RP; ++i) {
+        float ra[RT::CPL], rb[RT::CPL];
+        ldn(suf + (r0 + 2 * i) * DV + c0, ra);
+        ldn(suf + (r0 + 2 * i + 1) * DV + c0, rb);
+#pragma unroll
+        for (int c = 0; c < RT::CPL; ++c) S1p[i][c] = pk2(ra[c], rb[c]);
+    }
     float zh = tid < D ? suf[C::kOffZ + tid] : 0.f;   // thread a < D carries zh[a]
     const float gm = DECAY ? gamma[sg.h % H] : 1.f;
     // gamma >= 1/4: Sh carried rescaled within a chunk, as in bwd_dq_kernel
@@ -573,6 +599,7 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 sDK[t * D + tid] = zh;
             }
         __syncthreads();
+        const uint64_t gm2 = pk2(gm, gm);
         auto token_loop = [&](auto scaled_tag) {
             constexpr bool SC = decltype(scaled_tag)::value;
             int slot = 0;
@@ -594,17 +621,33 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
 #pragma unroll
                     for (int r = 0; r < RT::RPW; ++r) fq[r] *= ip;
                 }
+                // each FMA updates a pair of rows (packed); pv keeps the even and
+                // odd rows' partial sums in its two lanes until the end
+                uint64_t gb[RT::CPL], xb[RT::CPL], pvp[RT::CPL];
 #pragma unroll
-                for (int cc = 0; cc < RT::CPL; ++cc) pv[cc] = 0.f;
+                for (int cc = 0; cc < RT::CPL; ++cc) {
+                    gb[cc] = pk2(g[cc], g[cc]);
+                    xb[cc] = pk2(x[cc], x[cc]);
+                    pvp[cc] = pk2(0.f, 0.f);
+                }
 #pragma unroll
-                for (int r = 0; r < RT::RPW; ++r) {
-                    acc[r] = 0.f;
+                for (int i = 0; i < RP; ++i) {
+                    const uint64_t fqp = pk2(fq[2 * i], fq[2 * i + 1]);
+                    const uint64_t fkp = pk2(fk[2 * i], fk[2 * i + 1]);
+                    uint64_t accp = pk2(0.f, 0.f);
 #pragma unroll
                     for (int cc = 0; cc < RT::CPL; ++cc) {
-                        S1[r][cc] = fmaf(fq[r], g[cc], (DECAY && !SC) ? gm * S1[r][cc] : S1[r][cc]);
-                        acc[r] = fmaf(S1[r][cc], x[cc], acc[r]);
-                        pv[cc] = fmaf(S1[r][cc], fk[r], pv[cc]);
+                        S1p[i][cc] = fma2(fqp, gb[cc], (DECAY && !SC) ? mul2(gm2, S1p[i][cc]) : S1p[i][cc]);
+                        accp = fma2(S1p[i][cc], xb[cc], accp);
+                        pvp[cc] = fma2(S1p[i][cc], fkp, pvp[cc]);
                     }
+                    unpk2(accp, acc[2 * i], acc[2 * i + 1]);
+                }
+#pragma unroll
+                for (int cc = 0; cc < RT::CPL; ++cc) {
+                    float a0, a1;
+                    unpk2(pvp[cc], a0, a1);
+                    pv[cc] = a0 + a1;
                 }
                 float dfk = reduce_scatter<RT::RPW>(acc, lane);
                 if constexpr (SC) {
@@ -631,11 +674,11 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
                 }
             }
             if constexpr (SC) {
-                const float pL = sGp[L];
+                const uint64_t pL = pk2(sGp[L], sGp[L]);
 #pragma unroll
-                for (int r = 0; r < RT::RPW; ++r)
+                for (int i = 0; i < RP; ++i)
 #pragma unroll
-                    for (int cc = 0; cc < RT::CPL; ++cc) S1[r][cc] *= pL;
+                    for (int cc = 0; cc < RT::CPL; ++cc) S1p[i][cc] = mul2(S1p[i][cc], pL);
             }
         };
         if (scaled) token_loop(std::true_type{});
@@ -647,9 +690,14 @@ bwd_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__res
     if (sg.p == 0 && grad_S) {
         float *gS = grad_S + (size_t)sg.h * D * DV;
 #pragma unroll
-        for (int r = 0; r < RT::RPW; ++r)
+        for (int i = 0; i < RP; ++i)
 #pragma unroll
-            for (int cc = 0; cc < RT::CPL; ++cc) gS[(r0 + r) * DV + c0 + cc] = gm * S1[r][cc];
+            for (int cc = 0; cc < RT::CPL; ++cc) {
+                float a0, a1;
+                unpk2(S1p[i][cc], a0, a1);
+                gS[(r0 + 2 * i) * DV + c0 + cc] = gm * a0;
+                gS[(r0 + 2 * i + 1) * DV + c0 + cc] = gm * a1;
+            }
         if (tid < D) grad_z[(size_t)sg.h * D + tid] = gm * zh;
     }
 }

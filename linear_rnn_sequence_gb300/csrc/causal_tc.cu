@@ -429,7 +429,7 @@ __device__ __forceinline__ uint32_t zt_off(int n, int k, int D) {
 // G = w is ready, every other 16-column group each: w_ij (j <= i, else 0)
 // split into bf16 hi + lo pairs written back over G, and the partial row sums.
 template <int D, int DV, int DK>
-__device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_t *sQ,
+__device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, uint8_t *sQ,
                                              int nchunks, int nloc, const Guard &g,
                                              const float *gtab) {
     constexpr int kW = WaitPolicy<D, DK>::value;
@@ -462,15 +462,28 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
         const float ipL = DK == 2 ? ipL_next : (DECAY ? P.ipw(c, Lc) : 1.f);
         fetch(c + 1);
         if (DECAY) ds.step(pL);
+        // Gated kernel: psi(q) is formed as soon as the Q tile has landed, in
+        // place over the tile, while the previous block's Y MMAs may still read
+        // the TMEM operand, and copied into TMEM once they have completed (h = 0
+        // keeps its first eight features' residuals in registers: both halves
+        // read those features for the split constant).  That takes psi(q) off
+        // the chain to the next G.  The plain and fixed-decay kernels form
+        // psi(q) straight into TMEM after that wait: there, the idle time it
+        // leaves goes to group B's output epilogue, and the early form was
+        // measured 7% slower; the gated kernel gains 3%.
+        constexpr bool kEarly = DK == 2;
         bool ok = wait_warp<kW>(&S.q_full, c & 1, g, 40);
-        if (ok && c > 0) ok = wait_warp<kW>(&S.aq_free, (c - 1) & 1, g, 41);
+        if (!kEarly && ok && c > 0) ok = wait_warp<kW>(&S.aq_free, (c - 1) & 1, g, 41);
         if (lane == 0 && wq == 3 && h == 0) LA_TRACE_POINT(c, 0);
         float alpha = 0.f, cq = 1.f;
         uint64_t alpha2 = f2pack(0.f, 0.f);
+        uint4 held = make_uint4(0u, 0u, 0u, 0u);
+        auto q_chunk = [&](int f) {
+            return reinterpret_cast<uint4 *>(sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
+        };
         if (ok) {
-            tc_fence_after();   // the MMAs that read the previous psi(q) have completed
-            // the query's split constant, from its first eight features (both
-            // halves read them; nothing overwrites the Q tile before q_empty)
+            if (!kEarly) tc_fence_after();   // the MMAs that read the previous psi(q) have completed
+            // the query's split constant, from its first eight features
             cq = split_const(*reinterpret_cast<const uint4 *>(sQ + sw128_off(row, 0)));
             const SplitC kq = split_pairs(cq);
             // a real loop over 32-feature groups keeps the hot code small
@@ -479,25 +492,48 @@ __device__ __forceinline__ void group_a_role(Small &S, uint32_t tb, const uint8_
                 const int grp = h * (D / 64) + gq;   // 32 features -> 16 TMEM columns
                 uint4 raw[4];
 #pragma unroll
-                for (int f4 = 0; f4 < 4; ++f4) {
-                    const int f = grp * 4 + f4;
-                    raw[f4] = *reinterpret_cast<const uint4 *>(
-                        sQ + (f >> 3) * (kC * 128) + sw128_off(row, (f & 7) * 8));
-                }
+                for (int f4 = 0; f4 < 4; ++f4) raw[f4] = *q_chunk(grp * 4 + f4);
                 uint32_t v[16];
 #pragma unroll
                 for (int f4 = 0; f4 < 4; ++f4) {
                     const uint32_t w[4] = {raw[f4].x, raw[f4].y, raw[f4].z, raw[f4].w};
 #pragma unroll
-                    for (int hw = 0; hw < 4; ++hw) {
-                        v[f4 * 4 + hw] = feat_bf16x2_sum(w[hw], kq, alpha2);
+                    for (int hw = 0; hw < 4; ++hw) v[f4 * 4 + hw] = feat_bf16x2_sum(w[hw], kq, alpha2);
+                }
+                if (kEarly) {
+#pragma unroll
+                    for (int f4 = 0; f4 < 4; ++f4) {
+                        const uint4 o = make_uint4(v[f4 * 4], v[f4 * 4 + 1], v[f4 * 4 + 2], v[f4 * 4 + 3]);
+                        if (grp == 0 && f4 == 0) held = o; else *q_chunk(grp * 4 + f4) = o;
                     }
+                } else {
+                    tmem_st16(tb + lb + kColAq + grp * 16, v);
+                }
+            }
+            if (!kEarly) mbar_arrive(&S.q_empty);
+            alpha = f2sum(alpha2);
+            if (h == 1) S.alpha_part[row] = alpha;
+            if (!kEarly) {
+                tmem_wait_st();
+                tc_fence_before();
+            }
+        }
+        if (kEarly && ok && c > 0) ok = wait_warp<kW>(&S.aq_free, (c - 1) & 1, g, 41);
+        if (kEarly && ok) {
+            tc_fence_after();   // the MMAs that read the previous psi(q) have completed
+#pragma unroll 1
+            for (int gq = 0; gq < D / 64; ++gq) {
+                const int grp = h * (D / 64) + gq;
+                uint32_t v[16];
+#pragma unroll
+                for (int f4 = 0; f4 < 4; ++f4) {
+                    const uint4 x = (grp == 0 && f4 == 0) ? held : *q_chunk(grp * 4 + f4);
+                    v[f4 * 4 + 0] = x.x; v[f4 * 4 + 1] = x.y; v[f4 * 4 + 2] = x.z; v[f4 * 4 + 3] = x.w;
                 }
                 tmem_st16(tb + lb + kColAq + grp * 16, v);
             }
+            fence_proxy_async();   // the in-place writes precede the next copy into the tile
             mbar_arrive(&S.q_empty);
-            alpha = f2sum(alpha2);
-            if (h == 1) S.alpha_part[row] = alpha;
             tmem_wait_st();
             tc_fence_before();
         }

@@ -74,13 +74,17 @@ causal_gated_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const bool writer = CT::writer(lane);
     const Feature feat{phi};
 
-    // S[a0 + j][b0 + i] in S2[i][j]; S_in is read in full before S_out is written
-    float S2[CT::RPW][CT::CPL];
+    // S[a0 + j][b0 + i] in S2p[i / 2][j], packed pairs of value columns
+    // (2i', 2i' + 1); S_in is read in full before S_out is written
+    constexpr int RP = CT::RPW / 2;
+    uint64_t S2p[RP][CT::CPL];
     const float *Sh_in = S_in ? S_in + (size_t)head * D * DV : nullptr;
 #pragma unroll
-    for (int i = 0; i < CT::RPW; ++i)
+    for (int i = 0; i < RP; ++i)
 #pragma unroll
-        for (int j = 0; j < CT::CPL; ++j) S2[i][j] = Sh_in ? Sh_in[(a0 + j) * DV + b0 + i] : 0.f;
+        for (int j = 0; j < CT::CPL; ++j)
+            S2p[i][j] = Sh_in ? pk2(Sh_in[(a0 + j) * DV + b0 + 2 * i], Sh_in[(a0 + j) * DV + b0 + 2 * i + 1])
+                              : pk2(0.f, 0.f);
     float z = (tid < D && z_in) ? z_in[(size_t)head * D + tid] : 0.f;   // thread a < D: z[a]
 
     const T *qh = q + (size_t)head * N * D, *kh = k + (size_t)head * N * D;
@@ -131,14 +135,25 @@ causal_gated_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             ldn(sFq + t * D + a0, fq);
             ldn(sG + t * D + a0, gf);
             ldn(sV + t * DV + b0, vv);   // warp-uniform
+            // each FMA updates a pair of value columns (packed), with the same
+            // operations per element as the scalar form
+            uint64_t fkb[CT::CPL], fqb[CT::CPL], gfb[CT::CPL];   // both lanes alike
 #pragma unroll
-            for (int i = 0; i < CT::RPW; ++i) {
-                acc[i] = 0.f;
+            for (int j = 0; j < CT::CPL; ++j) {
+                fkb[j] = pk2(fk[j], fk[j]);
+                fqb[j] = pk2(fq[j], fq[j]);
+                gfb[j] = pk2(gf[j], gf[j]);
+            }
+#pragma unroll
+            for (int i = 0; i < RP; ++i) {
+                const uint64_t vp = pk2(vv[2 * i], vv[2 * i + 1]);
+                uint64_t accp = pk2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < CT::CPL; ++j) {
-                    S2[i][j] = fmaf(fk[j], vv[i], gf[j] * S2[i][j]);
-                    acc[i] = fmaf(S2[i][j], fq[j], acc[i]);
+                    S2p[i][j] = fma2(fkb[j], vp, mul2(gfb[j], S2p[i][j]));
+                    accp = fma2(S2p[i][j], fqb[j], accp);
                 }
+                unpk2(accp, acc[2 * i], acc[2 * i + 1]);
             }
             const float num = reduce_scatter<CT::RPW>(acc, lane);
             if (writer) sY[t * DV + my_col] = num * sDinv[t];
@@ -149,9 +164,10 @@ causal_gated_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     if (S_out) {
         float *So = S_out + (size_t)head * D * DV;
 #pragma unroll
-        for (int i = 0; i < CT::RPW; ++i)
+        for (int i = 0; i < RP; ++i)
 #pragma unroll
-            for (int j = 0; j < CT::CPL; ++j) So[(a0 + j) * DV + b0 + i] = S2[i][j];
+            for (int j = 0; j < CT::CPL; ++j)
+                unpk2(S2p[i][j], So[(a0 + j) * DV + b0 + 2 * i], So[(a0 + j) * DV + b0 + 2 * i + 1]);
     }
     if (z_out && tid < D) z_out[(size_t)head * D + tid] = z;
 }

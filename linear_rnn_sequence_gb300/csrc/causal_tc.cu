@@ -1442,14 +1442,22 @@ cudaError_t launch_dv(const FwdArgs &a) {
         float *S_pre = z_seg + cnt * D;
         float *z_pre = S_pre + cnt * nS;
         if (DK == 2) p.seg_decay = z_pre + cnt * D;   // the segments' products of gates
-        using SL = StateLayout<D, DV, DK == 1>;
-        auto skern = causal_state_kernel<D, DV, DK>;
-        cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SL::request);
+        cudaError_t e;
+        if (DK == 0 && D == 64) {
+            // phase 1 of the fused non-causal kernel: one MMA per 16 tokens and
+            // up to four K/V stages, which streams at the SM's share of HBM
+            e = launch_segment_states_nc(a, p.nseg, p.seg_chunks, S_seg, z_seg);
+        } else {
+            using SL = StateLayout<D, DV, DK == 1>;
+            auto skern = causal_state_kernel<D, DV, DK>;
+            e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SL::request);
+            if (e != cudaSuccess) return e;
+            skern<<<BH * p.state_segs, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg,
+                                                                                 z_seg);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
-        skern<<<BH * p.state_segs, kStateThreads, SL::request, a.stream>>>(km, vm, p, S_seg,
-                                                                             z_seg);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const dim3 sgrid(BH, (D * DV + D + kScanThreads - 1) / kScanThreads);
         e = launch_overlapped(scan_states_kernel, sgrid, dim3(kScanThreads), 0, a.stream,
                               (const float *)S_seg, (const float *)z_seg, S_pre, z_pre, a.S_in,

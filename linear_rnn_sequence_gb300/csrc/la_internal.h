@@ -113,6 +113,10 @@ bool noncausal_tc_supported(const FwdArgs &a);
 size_t noncausal_tc_workspace(int BH, int N, int d, int dv);
 size_t noncausal_tc_clear_bytes(int BH);   // workspace bytes to zero before each call
 cudaError_t launch_noncausal_tc(const FwdArgs &a);
+// States of every segment but each head's last for the causal sequence split
+// (d = 64, bf16, no decay), into slot head * nseg + segment of S_seg, z_seg.
+cudaError_t launch_segment_states_nc(const FwdArgs &a, int nseg, int seg_chunks, float *S_seg,
+                                     float *z_seg);
 
 // gated recurrence and feature maps (CUDA cores, fp32)
 cudaError_t launch_causal_gated(const FwdArgs &a);        // tensor cores where they apply

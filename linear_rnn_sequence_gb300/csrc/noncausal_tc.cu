@@ -31,7 +31,9 @@
 //            using phi(q_i) = c_i 1 + a_i.
 // With more than one range per head the items wait for one another, so the
 // launch is cooperative (every item resident at once); with one range per
-// head nothing waits.
+// head nothing waits.  In its state-only mode the kernel runs phase 1 alone:
+// the causal path's sequence split uses it for the states of its segments
+// (d = 64, no decay), each (head, segment) item exporting its own sums.
 //
 // Precision: the residual features enter the tensor cores as bf16 (the same
 // features c + bf16(phi(x) - c) as the causal path, split_const in
@@ -177,6 +179,8 @@ struct FParams {
     int range_chunks;              // 128-token blocks per range (the last one may be shorter)
     float eps;
     float *S_part, *z_part;        // workspace: [BH][nranges][d][dv], [BH][nranges][d]
+    int slot_stride;               // item (head, range) exports to slot head * slot_stride + range
+    int state_only;                // 1: phase 1 and its export only (the causal path's segment states)
     unsigned int *counters;        // workspace: [BH] partials published (zero at the call's start)
     float *S_out, *z_out;
     unsigned int *err;
@@ -215,6 +219,9 @@ noncausal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     const int nloc = min(p.N - tok0, p.range_chunks * kC);
     const int nchunks = (nloc + kC - 1) / kC;
     const Guard g{&S.abort_flag, p.err, p.err_where, p.limit_ns};
+    // segment states: the item reads only K and V, and the prefix scan that
+    // consumes them waits for this whole grid, so it may be scheduled now
+    if (p.state_only) griddep_launch_dependents();
 
     if (tid == 0) {
         S.abort_flag = 0;
@@ -445,7 +452,8 @@ noncausal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                     if (lane == 0) S.n_part[wq] = ns;
                 }
                 named_bar(kBarA, kWG);
-                float *dst = p.S_part + (size_t)item * D * DV;
+                const size_t slot = (size_t)head * p.slot_stride + rng;
+                float *dst = p.S_part + slot * D * DV;
 #pragma unroll 1
                 for (int grp = 0; grp < DV / 16; ++grp) {
                     uint32_t rv[16];
@@ -461,7 +469,7 @@ noncausal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                                             u2f(rv[jj + 3]) + S.u[grp * 16 + jj + 3]);
                 }
                 const float n = (S.n_part[0] + S.n_part[1]) + (S.n_part[2] + S.n_part[3]);
-                if (row < D) p.z_part[(size_t)item * D + row] = u2f(zv[0]) + n;
+                if (row < D) p.z_part[slot * D + row] = u2f(zv[0]) + n;
                 __threadfence();   // the partial is visible GPU-wide before it is published
             }
         }
@@ -485,9 +493,10 @@ noncausal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     };
     // The item publishes its partial before it issues the Q copies: a release
     // waits for the thread's earlier memory operations, copies included.
-    const bool meet = !S.abort_flag && p.nranges > 1;
+    const bool so = p.state_only != 0;   // the item ends with its exported partial
+    const bool meet = !so && !S.abort_flag && p.nranges > 1;
     if (meet && tid == 0) red_release_gpu_add(&p.counters[head], 1u);
-    if (!S.abort_flag && warp == 0 && lane == 0)
+    if (!so && !S.abort_flag && warp == 0 && lane == 0)
         for (int c = 0; c < min(nchunks, Lay::kQS); ++c) load_q(c);
 
     // ======================================================== meet
@@ -506,7 +515,7 @@ noncausal_fused_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 
     // ======================================================== image of the head's state
-    const bool run2 = !S.abort_flag;
+    const bool run2 = !so && !S.abort_flag;
     if (run2) {
         if (tid < kImgThreads) {   // S: thread t keeps column t % dv, rows t / dv + k (256 / dv)
             constexpr int kRowStep = kImgThreads / DV;
@@ -855,6 +864,8 @@ cudaError_t launch_fused(const FwdArgs &a) {
     p.counters = reinterpret_cast<unsigned int *>(ws + sizeof(WsHeader));
     p.S_part = reinterpret_cast<float *>(ws + sizeof(WsHeader) + counters_bytes(BH));
     p.z_part = p.S_part + (size_t)BH * p.nranges * D * DV;
+    p.slot_stride = p.nranges;
+    p.state_only = 0;
     p.S_out = a.S_out;
     p.z_out = a.z_out;
     p.err = &hdr->error;
@@ -895,6 +906,56 @@ size_t noncausal_tc_workspace(int BH, int N, int d, int dv) {
 }
 
 size_t noncausal_tc_clear_bytes(int BH) { return sizeof(WsHeader) + counters_bytes(BH); }
+
+// The causal path's sequence split (d = 64, no decay): the states of every
+// segment but each head's last, by phase 1 of the fused kernel alone.  Item
+// (head, segment) reduces its segment's K and V and exports the plain state
+// to slot head * nseg + segment of S_seg, z_seg; nothing waits across items.
+template <int D, int DV>
+cudaError_t launch_states(const FwdArgs &a, int nseg, int seg_chunks, float *S_seg, float *z_seg) {
+    using Lay = FLayout<D, DV>;
+    const int BH = a.BH();
+    CUtensorMap qm, km, vm;
+    if (!encode_3d(&qm, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&km, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&vm, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, DV, a.N, BH, 64, kC,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    WsHeader *hdr = static_cast<WsHeader *>(a.ws);
+    const long long lim = debug_fault().wait_limit_ns;
+    FParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.N = a.N;
+    p.eps = a.eps;
+    p.nranges = nseg - 1;
+    p.range_chunks = seg_chunks;
+    p.slot_stride = nseg;
+    p.state_only = 1;
+    p.S_part = S_seg;
+    p.z_part = z_seg;
+    p.err = &hdr->error;
+    p.err_where = &hdr->error_where;
+    p.limit_ns = lim > 0 ? (unsigned long long)lim : 1000000000ull;
+    p.drop_item = -1;
+    auto kern = noncausal_fused_kernel<D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay::request);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<BH * p.nranges, kFThreads, Lay::request, a.stream>>>(qm, km, vm, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_states_nc(const FwdArgs &a, int nseg, int seg_chunks, float *S_seg,
+                                     float *z_seg) {
+    if (a.d == 64 && a.dv == 64) return launch_states<64, 64>(a, nseg, seg_chunks, S_seg, z_seg);
+    if (a.d == 64 && a.dv == 128) return launch_states<64, 128>(a, nseg, seg_chunks, S_seg, z_seg);
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_noncausal_tc(const FwdArgs &a) {
     if (a.d == 64 && a.dv == 64) return launch_fused<64, 64>(a);

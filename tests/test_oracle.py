@@ -4,10 +4,11 @@
 * closed forms of phi;
 * a brute-force pairwise evaluation written here in numpy (phi as x+1 / e^x,
   not elu+1), for the causal and non-causal forms;
-* torch float64 library routines (F.elu, einsum, cumsum): the parallel
-  prefix-sum form that the "Linear Transformer" page says equals the
-  recurrent one ("Comprobar la equivalencia entre cálculo recurrente y
-  cálculo causal vectorizado");
+* torch float64 library routines (expm1, batched matmul, tril): the output
+  as an explicit masked N x N kernel matrix, a route with no prefix sums and
+  no state, which the "Linear Transformer" page says gives the recurrent
+  result ("Comprobar la equivalencia entre cálculo recurrente y cálculo
+  causal vectorizado");
 * the blockwise form at several block lengths ("Linear Attention/es",
   "Entrenamiento: forma paralela");
 * invariants that follow from the equations.

@@ -142,11 +142,14 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r0 = warp * RT::RPW, c0 = lane * RT::CPL;
     const float gm = DECAY ? gamma[sg.h % H] : 1.f;
-    float R[RT::RPW][RT::CPL];
+    const uint64_t gm2 = pk2(gm, gm);
+    // R as packed pairs of rows: Rp[i][c] = (R[2i][c], R[2i+1][c])
+    constexpr int RP = RT::RPW / 2;
+    uint64_t Rp[RP][RT::CPL];
 #pragma unroll
-    for (int r = 0; r < RT::RPW; ++r)
+    for (int i = 0; i < RP; ++i)
 #pragma unroll
-        for (int c = 0; c < RT::CPL; ++c) R[r][c] = 0.f;
+        for (int c = 0; c < RT::CPL; ++c) Rp[i][c] = pk2(0.f, 0.f);
     float zeta = 0.f, u = 0.f;
     ChunkLoad<D, T, NT> lk;
     ChunkLoad<DV, T, NT> lv;
@@ -175,17 +178,20 @@ bwd_kv_states_kernel(const T *__restrict__ k, const T *__restrict__ v, int N, in
             ldn(sPk + t * D + r0, pk);
             ldn(sV + t * DV + c0, x);
 #pragma unroll
-            for (int r = 0; r < RT::RPW; ++r)
+            for (int i = 0; i < RP; ++i) {
+                const uint64_t pkp = pk2(pk[2 * i], pk[2 * i + 1]);
 #pragma unroll
                 for (int c = 0; c < RT::CPL; ++c)
-                    R[r][c] = fmaf(pk[r], x[c], DECAY ? gm * R[r][c] : R[r][c]);
+                    Rp[i][c] = fma2(pkp, pk2(x[c], x[c]), DECAY ? mul2(gm2, Rp[i][c]) : Rp[i][c]);
+            }
         }
     }
     float *out = states + ((size_t)sg.h * P + sg.p) * C::kE;
 #pragma unroll
-    for (int r = 0; r < RT::RPW; ++r)
+    for (int i = 0; i < RP; ++i)
 #pragma unroll
-        for (int c = 0; c < RT::CPL; ++c) out[(r0 + r) * DV + c0 + c] = R[r][c];
+        for (int c = 0; c < RT::CPL; ++c)
+            unpk2(Rp[i][c], out[(r0 + 2 * i) * DV + c0 + c], out[(r0 + 2 * i + 1) * DV + c0 + c]);
     if (tid < D) out[C::kOffZ + tid] = zeta;
     else if (tid < D + DV) out[C::kOffU + tid - D] = u;
     if (tid < 4) {

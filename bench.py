@@ -558,7 +558,7 @@ def run_modes(args, world, dev, peaks, peak_kind):
                      "l2": "inputs larger than L2",
                      "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
                                   "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
-                                  "traffic": None,
+                                  "traffic": load_traffic("causal_backward_bf16_b8h16n8192d128"),
                                   "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
                                   "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
     # the same gradients for the decayed forward (per-head gamma)
@@ -575,7 +575,8 @@ def run_modes(args, world, dev, peaks, peak_kind):
         "tokens_per_s": world * w.B * w.N / (ms * 1e-3), "ms_per_call": ms,
         "l2": "inputs larger than L2",
         "roofline": {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
-                     "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": None,
+                     "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS,
+                     "traffic": load_traffic("causal_backward_decay_bf16_b8h16n8192d128"),
                      "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz",
                      "hbm_roof_fraction": alg_bytes / (peaks["hbm_gbs"] * 1e9) / (ms * 1e-3)}}
     del q, k, v, dy, outs, ws
@@ -714,16 +715,18 @@ def run_reference(args, world, rank):
 def profile_case(args):
     """A few launches of one kernel on one workload, for ncu captures.
 
-    --profile-case causal|long|noncausal|decode|backward|causal_decay|long_decay|decode_decay|gated
-    picks the workload (B8 H16 N8192 d128 / B1 H32 N131072 d64 / B4 H8 N4096 d64 /
-    B256 H32 d128 decode / gradients at B8 H16 N8192 d128 / the decay variants of
-    the causal, long and decode workloads / the gated causal form at B8 H16 N8192
-    d128); --batch overrides B for a smaller capture.
+    --profile-case causal|long|noncausal|decode|backward|backward_decay|causal_decay|
+    long_decay|decode_decay|gated picks the workload (B8 H16 N8192 d128 / B1 H32
+    N131072 d64 / B4 H8 N4096 d64 / B256 H32 d128 decode / gradients at B8 H16 N8192
+    d128, without and with the per-head decays / the decay variants of the causal,
+    long and decode workloads / the gated causal form at B8 H16 N8192 d128);
+    --batch overrides B for a smaller capture.
     """
     from linear_rnn_sequence_gb300 import linattn as la
     names = {"causal": HEADLINE, "long": "causal_bf16_b1h32n131072d64",
              "noncausal": "noncausal_bf16_b4h8n4096d64", "decode": "decode_bf16_b256h32d128",
              "backward": "causal_backward_bf16_b8h16n8192d128",
+             "backward_decay": "causal_backward_bf16_b8h16n8192d128",
              "causal_decay": "causal_decay_bf16_b8h16n8192d128",
              "long_decay": "causal_decay_bf16_b1h32n131072d64",
              "decode_decay": "decode_decay_bf16_b256h32d128",
@@ -763,7 +766,8 @@ def profile_case(args):
                 torch.empty(w.B, w.H, w.N, w.dv, device=dev))
         ws = la.alloc_workspace(
             la.causal_backward_workspace_bytes(w.B, w.H, w.N, w.d, w.dv, w.dtype), dev)
-        fn = lambda: la.backward_causal(q, k, v, dy, eps=w.eps, out=outs, workspace=ws)
+        gam = head_decays(w.H).to(dev) if args.profile_case == "backward_decay" else None
+        fn = lambda: la.backward_causal(q, k, v, dy, eps=w.eps, out=outs, workspace=ws, gamma=gam)
     else:
         q, k, v = make_qkv(w, device=dev, gen_device=dev)
         y = torch.empty(w.B, w.H, w.N, w.dv, device=dev)
@@ -796,6 +800,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["causal", "long", "noncausal", "decode", "backward",
+                                               "backward_decay",
                                                "causal_decay", "long_decay", "decode_decay",
                                                "gated"])
     ap.add_argument("--batch", type=int, default=0)

@@ -14,8 +14,10 @@ namespace {
 // ("Linear Attention/es", "Entrenamiento: forma paralela": the cumulative sums
 // can be formed with a prefix scan).  Three launches, with no waits between
 // CTAs:
-//   1. causal_state_kernel: per (head, segment), the segment's own state
-//      S_s = sum phi(k_j) v_j^T, z_s = sum phi(k_j) from K and V (tensor cores);
+//   1. per (head, segment), the segment's own state S_s = sum phi(k_j) v_j^T,
+//      z_s = sum phi(k_j) from K and V (tensor cores): causal_state_kernel
+//      below, or at d = 64 without a decay phase 1 of the fused non-causal
+//      kernel (noncausal_tc.cu), which issues one MMA per 16 tokens;
 //   2. scan_states_kernel: per head, exclusive prefixes P_s = S_in + sum_{s'<s} S_s';
 //   3. causal_tc_kernel: every (head, segment) runs from its prefix.
 // The state pass reuses the split form of the main kernel (per-key split
